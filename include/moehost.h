@@ -1,0 +1,222 @@
+/*
+ * moehost.h -- C ABI of the GB300 (sm_103a) library for the mixture-of-experts
+ * layer of a decode step whose experts do not all fit in HBM.
+ *
+ * Method (from "DeepSeek-V4.1-Flash on One GB300 Without the Second GPU: What the
+ * Sidecar Is Worth", section 1, The idea): the router picks the top-k experts per
+ * token; cold experts live in pinned host memory; one kernel per layer copies only
+ * the routed cold experts into a shared HBM slot scratch and remaps their ids; one
+ * grouped SwiGLU expert call then runs over all experts as if they were resident;
+ * outputs are combined with the router weights; between steps a residency manager
+ * promotes often-picked cold experts and demotes quiet hot ones.
+ *
+ * Conventions
+ *  - Every call returns an int status: MOE_OK (0) or a negative MOE_ERR_* code.
+ *    A call that returns an error has launched nothing.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued on it; nothing synchronises except
+ *    residency_update on an acting step (it reads the pick counters on the host),
+ *    moe_get_status, moe_layer_get_loc and moe_layer_get_counts.
+ *  - Errors found by a kernel after launch (non-finite logits, an expert id out of
+ *    range) are written to the layer's device status word (first error wins);
+ *    moe_get_status reads it.
+ *  - Ownership: the caller owns every buffer it passes (device memory, and host
+ *    blobs that are pinned and mapped, e.g. cudaHostAlloc or torch pin_memory).
+ *    The library borrows raw pointers for the life of the layer and owns only its
+ *    handles and small internal tables (placement map, phys-id pointer table, pick
+ *    counters, status word), freed by the destroy calls.
+ *  - Shapes: H and I multiples of 128; 1 <= k <= 32; k <= E <= 1024.
+ *
+ * Expert blob format (one contiguous blob per expert, every plane 16-byte aligned):
+ *   w13 nibbles [2I][H/2] | w13 scales [2I][H/32] | w2 nibbles [H][I/2] | w2 scales [H][I/32]
+ *   MXFP4: E2M1 elements, E8M0 scale per 32-element block along the reduction
+ *   dimension ("A 475 GB Model Across Two Workstations, With the Table on Disk",
+ *   Abstract: routed experts ship in MXFP4).  w13 rows 0..I-1 are the gate
+ *   projection, rows I..2I-1 the up projection (the fused w13/w2 planes of "Milo
+ *   and James Try Inference Engineering", offload flag table).  Inside a row,
+ *   elements sit in 64-byte groups of 128: element e (0..31) of block j (0..3) of
+ *   a group is in byte 16*(e/8) + 4*j + (e%8)/2 of the group, low nibble when e is
+ *   even.  Scale byte b of a row is the exponent of elements 32b..32b+31.
+ *
+ * Placement: loc[e] in [0, n_hot) is an HBM slot; loc[e] = n_hot + c is cold slot
+ * c, whose bytes live in host blob c and are copied to scratch slot c when routed.
+ * The physical id of a pick is loc of its expert.
+ */
+#ifndef MOEHOST_H
+#define MOEHOST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)
+#define MOE_ERR_CUDA (-2)
+#define MOE_ERR_NONFINITE (-3)
+#define MOE_ERR_BAD_EXPERT (-4)
+#define MOE_ERR_TIMEOUT (-5)
+#define MOE_ERR_NOMEM (-6)
+#define MOE_ERR_INJECTED (-7)
+
+/* Layer parameters.
+ *  E, k        experts and picks per token ("Milo and James Try Inference
+ *              Engineering", the mixture-of-experts paragraph: 384 experts, 6 per
+ *              token).
+ *  H, I        hidden and expert intermediate sizes.
+ *  n_hot       experts resident in HBM; n_cold = E - n_hot in pinned host memory
+ *              ("DeepSeek-V4.1-Flash on One GB300 ...", section 1: 255 / 129).
+ *  renorm      0: pick weight = softmax probability; 1: divided by the sum over
+ *              the k picks.
+ *  swap_every  residency_update acts on every swap_every-th call (0 = never).
+ *  max_swaps   at most this many swaps per acting update (<= 64).
+ *  hysteresis  a cold expert is promoted over a hot one only when its window
+ *              count exceeds hysteresis times the hot one's (same page, section 3:
+ *              3.0 is the published default). */
+typedef struct moe_params {
+    int E, k, H, I, n_hot, n_cold;
+    int renorm;
+    int swap_every;
+    int max_swaps;
+    float hysteresis;
+} moe_params;
+
+typedef struct moe_scratch moe_scratch;
+typedef struct moe_layer moe_layer;
+
+/* Bytes of one expert blob for (H, I): 3*H*I/2 nibble bytes + 3*H*I/32 scale
+ * bytes.  Returns 0 if H or I is not a positive multiple of 128. */
+size_t moe_expert_bytes(int H, int I);
+
+/* Shared cold-slot scratch ("DeepSeek-V4.1-Flash on One GB300 ...", section 1:
+ * one scratch area with a slot per cold expert, shared by all layers because they
+ * run one after another).  slot_dev: caller-owned device memory of
+ * n_slots * expert_bytes bytes, 256-byte aligned; slot c starts at
+ * slot_dev + c * expert_bytes.  All layers that share it must run their
+ * cold_gather and moe_grouped_ffn calls in stream order.
+ * Errors: MOE_ERR_INVALID_ARG (null, n_slots < 0, misaligned, not device memory). */
+int moe_scratch_create(int n_slots, size_t expert_bytes, void* slot_dev, moe_scratch** out);
+int moe_scratch_destroy(moe_scratch* s);
+
+/* One MoE layer.  hot_blobs_dev[h] (h < n_hot): device pointer of HBM slot h's
+ * blob.  cold_blobs_host[c] (c < n_cold): host pointer of cold slot c's blob,
+ * pinned and mapped.  init_loc: host array [E], a bijection onto [0, E).  The
+ * scratch must have at least n_cold slots of moe_expert_bytes(H, I) bytes.
+ * Validates shapes, 16-byte alignment, memory kinds (cudaPointerGetAttributes)
+ * and the map.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_NOMEM. */
+int moe_layer_create(const moe_params* p, moe_scratch* scratch, void* const* hot_blobs_dev,
+                     void* const* cold_blobs_host, const int32_t* init_loc, moe_layer** out);
+int moe_layer_destroy(moe_layer* L);
+
+/* Router: top-k, softmax weights and token-to-expert bucketing for T tokens
+ * ("Milo and James Try Inference Engineering", the mixture-of-experts paragraph;
+ * "DeepSeek-V4.1-Flash on One GB300 ...", section 1: the copy kernel looks at
+ * which experts the router picked).
+ *  logits   device fp32 [T][E] row-major.
+ *  topk_ids device int32 [T][k]: expert e is picked iff fewer than k experts have
+ *           a larger logit or an equal logit and a lower index; listed by that
+ *           rank (descending logit, ties to the lower index).
+ *  topk_w   device fp32 [T][k]: softmax probability of each pick over all E
+ *           (renorm: divided by the sum over the picks).
+ *  counts   device int32 [E]; offsets device int32 [E+1] (exclusive prefix);
+ *  entries  device int32 [T*k]: pick ids t*k+j grouped by expert, ascending.
+ * Also adds the picks to the layer's window counters used by residency_update.
+ * A token with a non-finite logit gets ids 0..k-1 and weights 0, and the status
+ * word becomes MOE_ERR_NONFINITE.  T = 0 is valid (offsets become all zero).
+ * Errors: MOE_ERR_INVALID_ARG (null pointer with T > 0, T < 0), MOE_ERR_CUDA. */
+int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float* topk_w, int32_t* counts,
+              int32_t* offsets, int32_t* entries, void* stream);
+
+/* Cold dedupe, id remap and gather ("DeepSeek-V4.1-Flash on One GB300 ...",
+ * section 1: one small kernel copies just the routed cold experts into their
+ * slots; section 3: that copy was 2.60 ms of a 10.49 ms step).
+ *  topk_ids      device int32 [T][k].
+ *  phys_ids      device int32 [T][k] out: loc of each pick's expert (-1 for an id
+ *                outside [0, E), which also sets MOE_ERR_BAD_EXPERT in the status).
+ *  cold_list     device int32 [min(n_cold, T*k)] out: distinct cold slots picked,
+ *                ascending.
+ *  n_cold_picked device int32 [1] out.
+ * Every listed slot of the scratch is overwritten with the bytes of its host blob,
+ * read zero-copy with 16-byte loads; unlisted slots are left as they were.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids, int32_t* cold_list,
+                int32_t* n_cold_picked, void* stream);
+
+/* Device workspace bytes moe_grouped_ffn needs for T tokens. */
+int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes);
+
+/* Grouped SwiGLU expert FFN over all picks ("DeepSeek-V4.1-Flash on One GB300
+ * ...", section 1: the layer runs all experts in a single call).  For pick
+ * i = t*k + j with expert blob B = blob of physical id phys_ids[i]:
+ *   g = W_gate x_t, u = W_up x_t, h = SiLU(g) * u, y_i = W2 h.
+ *  x        device bf16 [T][H].
+ *  phys_ids device int32 [T][k] (from cold_gather); counts/offsets/entries from
+ *           moe_route.
+ *  y        device fp32 [T*k][H] out, row i = pick i.
+ *  workspace device memory of at least moe_ffn_workspace_bytes(L, T) bytes,
+ *           256-byte aligned; its contents are overwritten.
+ * Each distinct expert's weights are streamed once per call.  Errors:
+ * MOE_ERR_INVALID_ARG (null, T < 0, workspace too small), MOE_ERR_CUDA. */
+int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
+                    const int32_t* offsets, const int32_t* entries, float* y, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* Combine ("DeepSeek-V4.1-Flash on One GB300 ...", section 4: contributions are
+ * summed; the order only moves the last decimal places).  out[t] = sum over
+ * j = 0..k-1, in that order, of topk_w[t][j] * y[t*k+j], in fp32.
+ *  y device fp32 [T*k][H]; topk_w device fp32 [T][k];
+ *  out device [T][H]: bf16 (round to nearest even) when out_fp32 = 0, else fp32.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* out, int out_fp32, void* stream);
+
+/* Adaptive residency ("DeepSeek-V4.1-Flash on One GB300 ...", section 1: between
+ * steps a manager swaps often-picked experts into the hot set and quiet ones out;
+ * section 3: hysteresis 3.0 as the published default).  Call once per step.  On
+ * every swap_every-th call it synchronises `stream`, reads the window counters,
+ * pairs cold experts picked at least once (count desc, id asc) with hot experts
+ * (count asc, id asc), swaps pair i while count(cold) > hysteresis * count(hot)
+ * (at most max_swaps, stopping at the first pair that fails), exchanges the two
+ * experts' bytes in place between the HBM slot and the host blob, rewrites the
+ * placement map and clears the counters.  Other calls only count the step.
+ *  n_swaps_out host int32 [1] out (0 on non-acting calls).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_INJECTED (test hook). */
+int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream);
+
+/* Copies the placement map to host int32 [E] (synchronous). */
+int moe_layer_get_loc(moe_layer* L, int32_t* loc_host);
+
+/* Copies the window pick counters to host int32 [E] (synchronous). */
+int moe_layer_get_counts(moe_layer* L, int32_t* counts_host);
+
+/* Reads the layer's device status word (synchronous); 0 = no error so far. */
+int moe_get_status(moe_layer* L, int* status);
+
+/* Clears the device status word (synchronous). */
+int moe_clear_status(moe_layer* L);
+
+/* Text for a status code. */
+const char* moe_strerror(int code);
+
+/* Test hook for host-side fault injection: what = 1 makes the next acting
+ * residency_update fail with MOE_ERR_INJECTED before any copy or map change (as a
+ * failed host copy would); what = 0 clears it.  Never set in normal use. */
+int moe_layer_inject_fault(moe_layer* L, int what);
+
+/* Host-link probe: copies `bytes` (a multiple of 16) from mapped pinned host
+ * memory `src_host` to device memory `dst_dev` with the same zero-copy 16-byte
+ * load loop as cold_gather, on `ctas` CTAs (0 = one per SM).  Used to measure
+ * the link peak the cold gather is reported against. */
+int moe_link_probe(const void* src_host, void* dst_dev, size_t bytes, int ctas, void* stream);
+
+/* Lane-layout check of the E2M1 pair conversion used by the FFN kernels: writes
+ * for every byte b (0..255) the two f16 values it decodes to (low nibble first)
+ * as uint32 [256] to out_dev (device). */
+int moe_debug_e2m1_pairs(uint32_t* out_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEHOST_H */

@@ -1,0 +1,176 @@
+"""moe_decode_host_gb300: MoE decode layer with host-resident cold experts on GB300.
+
+Thin Python binding of the C ABI in include/moehost.h (libmoehost.so).  The entry
+points keep the C names -- moe_route, cold_gather, moe_grouped_ffn, moe_combine,
+residency_update -- and only marshal arguments: torch (or raw) pointers in,
+status codes out as MoeError.  PyTorch is used for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from ._lib import (LIB_PATH, MOE_ERR_BAD_EXPERT, MOE_ERR_CUDA, MOE_ERR_INJECTED, MOE_ERR_INVALID_ARG,
+                   MOE_ERR_NOMEM, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT, MOE_OK, MoeError, check, lib, moe_params,
+                   ptr, stream_handle)
+
+__all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_bytes", "moe_route", "cold_gather",
+           "moe_grouped_ffn", "moe_combine", "residency_update", "link_probe", "debug_e2m1_pairs", "run_step",
+           "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
+           "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED"]
+
+
+def expert_bytes(H: int, I: int) -> int:
+    return int(lib.moe_expert_bytes(H, I))
+
+
+class Scratch:
+    """Shared cold-slot scratch over caller-owned device memory (slot c at c*expert_bytes)."""
+
+    def __init__(self, n_slots: int, nbytes_per_expert: int, slot_dev):
+        h = ctypes.c_void_p()
+        check(lib.moe_scratch_create(n_slots, nbytes_per_expert, ptr(slot_dev), ctypes.byref(h)),
+              "moe_scratch_create")
+        self.handle = h
+        self.memory = slot_dev
+
+    def close(self):
+        if self.handle:
+            lib.moe_scratch_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Layer:
+    """One MoE layer handle (moe_layer_create)."""
+
+    def __init__(self, *, E, k, H, I, n_hot, n_cold, scratch, hot_ptrs, cold_ptrs, init_loc, renorm=0,
+                 swap_every=16, max_swaps=8, hysteresis=3.0):
+        self.p = moe_params(E, k, H, I, n_hot, n_cold, renorm, swap_every, max_swaps, hysteresis)
+        hot = (ctypes.c_void_p * max(1, n_hot))(*[ptr(x) for x in hot_ptrs])
+        cold = (ctypes.c_void_p * max(1, n_cold))(*[ptr(x) for x in cold_ptrs])
+        loc = np.ascontiguousarray(init_loc, dtype=np.int32)
+        h = ctypes.c_void_p()
+        check(lib.moe_layer_create(ctypes.byref(self.p), scratch.handle if scratch else None,
+                                   hot if n_hot else None, cold if n_cold else None, loc.ctypes.data,
+                                   ctypes.byref(h)), "moe_layer_create")
+        self.handle = h
+        self.scratch = scratch
+        self.E, self.k, self.H, self.I = E, k, H, I
+        self.n_hot, self.n_cold = n_hot, n_cold
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def ffn_workspace_bytes(self, T: int) -> int:
+        n = ctypes.c_size_t()
+        check(lib.moe_ffn_workspace_bytes(self.handle, T, ctypes.byref(n)), "moe_ffn_workspace_bytes")
+        return int(n.value)
+
+    def get_loc(self) -> np.ndarray:
+        out = np.zeros(self.E, np.int32)
+        check(lib.moe_layer_get_loc(self.handle, out.ctypes.data), "moe_layer_get_loc")
+        return out
+
+    def get_counts(self) -> np.ndarray:
+        out = np.zeros(self.E, np.int32)
+        check(lib.moe_layer_get_counts(self.handle, out.ctypes.data), "moe_layer_get_counts")
+        return out
+
+    def status(self) -> int:
+        s = ctypes.c_int()
+        check(lib.moe_get_status(self.handle, ctypes.byref(s)), "moe_get_status")
+        return int(s.value)
+
+    def clear_status(self):
+        check(lib.moe_clear_status(self.handle), "moe_clear_status")
+
+    def inject_fault(self, what: int):
+        check(lib.moe_layer_inject_fault(self.handle, what), "moe_layer_inject_fault")
+
+
+def moe_route(layer: Layer, logits, T, topk_ids, topk_w, counts, offsets, entries, stream=None):
+    check(lib.moe_route(layer.handle, ptr(logits), T, ptr(topk_ids), ptr(topk_w), ptr(counts), ptr(offsets),
+                        ptr(entries), stream_handle(stream)), "moe_route")
+
+
+def cold_gather(layer: Layer, topk_ids, T, phys_ids, cold_list, n_cold_picked, stream=None):
+    check(lib.cold_gather(layer.handle, ptr(topk_ids), T, ptr(phys_ids), ptr(cold_list), ptr(n_cold_picked),
+                          stream_handle(stream)), "cold_gather")
+
+
+def moe_grouped_ffn(layer: Layer, x, T, phys_ids, counts, offsets, entries, y, workspace, workspace_bytes=None,
+                    stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    check(lib.moe_grouped_ffn(layer.handle, ptr(x), T, ptr(phys_ids), ptr(counts), ptr(offsets), ptr(entries),
+                              ptr(y), ptr(workspace), workspace_bytes, stream_handle(stream)), "moe_grouped_ffn")
+
+
+def moe_combine(y, topk_w, T, k, H, out, out_fp32=False, stream=None):
+    check(lib.moe_combine(ptr(y), ptr(topk_w), T, k, H, ptr(out), 1 if out_fp32 else 0, stream_handle(stream)),
+          "moe_combine")
+
+
+def residency_update(layer: Layer, stream=None) -> int:
+    n = ctypes.c_int32()
+    check(lib.residency_update(layer.handle, ctypes.byref(n), stream_handle(stream)), "residency_update")
+    return int(n.value)
+
+
+def link_probe(src_host, dst_dev, nbytes, ctas=0, stream=None):
+    check(lib.moe_link_probe(ptr(src_host), ptr(dst_dev), nbytes, ctas, stream_handle(stream)), "moe_link_probe")
+
+
+def debug_e2m1_pairs(out_dev, stream=None):
+    check(lib.moe_debug_e2m1_pairs(ptr(out_dev), stream_handle(stream)), "moe_debug_e2m1_pairs")
+
+
+class StepBuffers:
+    """Device buffers of one decode step for T tokens (torch allocations)."""
+
+    def __init__(self, layer: Layer, T: int, device="cuda", out_fp32=False):
+        import torch
+        k, E, H = layer.k, layer.E, layer.H
+        n = max(1, T * k)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.T = T
+        self.topk_ids = torch.empty((max(1, T), k), **i32)
+        self.topk_w = torch.empty((max(1, T), k), dtype=torch.float32, device=device)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.entries = torch.empty(n, **i32)
+        self.phys_ids = torch.empty(n, **i32)
+        self.cold_list = torch.empty(max(1, min(max(layer.n_cold, 1), n)), **i32)
+        self.n_cold_picked = torch.zeros(1, **i32)
+        self.y = torch.empty((n, H), dtype=torch.float32, device=device)
+        ws = layer.ffn_workspace_bytes(T)
+        self.workspace = torch.empty(max(256, ws), dtype=torch.uint8, device=device)
+        self.out_fp32 = out_fp32
+        self.out = torch.empty((max(1, T), H), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=device)
+
+
+def run_step(layer: Layer, buf: StepBuffers, logits, x, stream=None, residency=True) -> int:
+    """One pass of the layer: route, cold gather, grouped FFN, combine, then the
+    residency step.  Returns the number of swaps made (0 on non-acting steps)."""
+    T = buf.T
+    moe_route(layer, logits, T, buf.topk_ids, buf.topk_w, buf.counts, buf.offsets, buf.entries, stream)
+    cold_gather(layer, buf.topk_ids, T, buf.phys_ids, buf.cold_list, buf.n_cold_picked, stream)
+    moe_grouped_ffn(layer, x, T, buf.phys_ids, buf.counts, buf.offsets, buf.entries, buf.y, buf.workspace,
+                    stream=stream)
+    moe_combine(buf.y, buf.topk_w, T, layer.k, layer.H, buf.out, buf.out_fp32, stream)
+    return residency_update(layer, stream) if residency else 0

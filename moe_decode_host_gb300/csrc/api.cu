@@ -1,0 +1,382 @@
+// Host side of the C ABI declared in moehost.h: argument checks, layer state,
+// launches, and the residency manager.
+//
+// Residency ("DeepSeek-V4.1-Flash on One GB300 Without the Second GPU", section 1:
+// between steps a manager swaps often-picked experts into the hot set and quiet
+// ones out; section 3: a hysteresis threshold of 3.0 is the published default and
+// halved the swap count without slowing the step).  The pick counters of the
+// window are accumulated on the device by moe_route; on an acting step the host
+// reads them, builds the swap list, exchanges the bytes with one kernel and
+// rewrites the placement map.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.cuh"
+
+using namespace moe;
+
+struct moe_scratch {
+    int n_slots;
+    size_t expert_bytes;
+    uint8_t* base;
+};
+
+struct moe_layer {
+    moe_params p;
+    moe_scratch* scratch;
+    BlobLayout lay;
+    int sm_count;
+    std::vector<uint8_t*> hot;        // device blobs of the HBM slots
+    std::vector<uint8_t*> cold_dev;   // device-mapped pointers of the host blobs
+    std::vector<int32_t> loc;         // host mirror of the placement map
+    int32_t* d_loc = nullptr;         // [E]
+    const uint8_t** d_ptr = nullptr;  // [n_hot + n_cold] phys id -> blob base
+    const uint8_t** d_cold_src = nullptr;  // [n_cold] host blobs (device-mapped)
+    int32_t* d_window = nullptr;      // [E] picks in the current window
+    int* d_status = nullptr;
+    int32_t* h_counts = nullptr;      // pinned [E]
+    int32_t* h_loc = nullptr;         // pinned [E]
+    long steps = 0;
+    int fault = 0;
+};
+
+namespace {
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Returns the device pointer of pinned, mapped host memory, or nullptr.
+void* mapped_host_ptr(void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost) return nullptr;
+    void* d = nullptr;
+    if (cudaHostGetDevicePointer(&d, p, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return d;
+}
+
+cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+void free_layer(moe_layer* L) {
+    if (!L) return;
+    cudaFree(L->d_loc);
+    cudaFree(L->d_ptr);
+    cudaFree(L->d_cold_src);
+    cudaFree(L->d_window);
+    cudaFree(L->d_status);
+    cudaFreeHost(L->h_counts);
+    cudaFreeHost(L->h_loc);
+    delete L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_expert_bytes(int H, int I) {
+    if (H <= 0 || I <= 0 || H % 128 || I % 128) return 0;
+    return blob_layout(H, I).total;
+}
+
+int moe_scratch_create(int n_slots, size_t expert_bytes, void* slot_dev, moe_scratch** out) {
+    if (!out || n_slots < 0 || expert_bytes == 0 || expert_bytes % 16) return MOE_ERR_INVALID_ARG;
+    if (n_slots > 0 && (!slot_dev || !aligned(slot_dev, 256) || !is_device_ptr(slot_dev))) return MOE_ERR_INVALID_ARG;
+    moe_scratch* s = new (std::nothrow) moe_scratch;
+    if (!s) return MOE_ERR_NOMEM;
+    s->n_slots = n_slots;
+    s->expert_bytes = expert_bytes;
+    s->base = static_cast<uint8_t*>(slot_dev);
+    *out = s;
+    return MOE_OK;
+}
+
+int moe_scratch_destroy(moe_scratch* s) {
+    delete s;
+    return MOE_OK;
+}
+
+int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* hot_blobs_dev,
+                     void* const* cold_blobs_host, const int32_t* init_loc, moe_layer** out) {
+    if (!pp || !out || !init_loc) return MOE_ERR_INVALID_ARG;
+    const moe_params p = *pp;
+    if (p.E < 1 || p.E > 1024 || p.k < 1 || p.k > 32 || p.k > p.E) return MOE_ERR_INVALID_ARG;
+    if (moe_expert_bytes(p.H, p.I) == 0) return MOE_ERR_INVALID_ARG;
+    if (p.n_hot < 0 || p.n_cold < 0 || p.n_hot + p.n_cold != p.E || p.n_cold > 4096) return MOE_ERR_INVALID_ARG;
+    if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
+    if (p.swap_every < 0 || p.max_swaps < 0 || p.max_swaps > kMaxSwaps) return MOE_ERR_INVALID_ARG;
+    if (!(p.hysteresis >= 0.0f) || p.hysteresis > 1e30f) return MOE_ERR_INVALID_ARG;
+    const size_t eb = moe_expert_bytes(p.H, p.I);
+    if (p.n_cold > 0 && (!scratch || scratch->expert_bytes != eb || scratch->n_slots < p.n_cold))
+        return MOE_ERR_INVALID_ARG;
+    if (p.n_hot > 0 && !hot_blobs_dev) return MOE_ERR_INVALID_ARG;
+    if (p.n_cold > 0 && !cold_blobs_host) return MOE_ERR_INVALID_ARG;
+    // placement map: a bijection onto [0, E)
+    std::vector<char> seen(p.E, 0);
+    for (int e = 0; e < p.E; ++e) {
+        const int v = init_loc[e];
+        if (v < 0 || v >= p.E || seen[v]) return MOE_ERR_INVALID_ARG;
+        seen[v] = 1;
+    }
+    moe_layer* L = new (std::nothrow) moe_layer;
+    if (!L) return MOE_ERR_NOMEM;
+    L->p = p;
+    L->scratch = scratch;
+    L->lay = blob_layout(p.H, p.I);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&L->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        delete L;
+        return MOE_ERR_CUDA;
+    }
+    L->hot.resize(p.n_hot);
+    for (int h = 0; h < p.n_hot; ++h) {
+        void* b = hot_blobs_dev[h];
+        if (!b || !aligned(b, 16) || !is_device_ptr(b)) {
+            delete L;
+            return MOE_ERR_INVALID_ARG;
+        }
+        L->hot[h] = static_cast<uint8_t*>(b);
+    }
+    L->cold_dev.resize(p.n_cold);
+    for (int c = 0; c < p.n_cold; ++c) {
+        void* b = cold_blobs_host[c];
+        void* d = b ? mapped_host_ptr(b) : nullptr;
+        if (!d || !aligned(b, 16) || !aligned(d, 16)) {
+            delete L;
+            return MOE_ERR_INVALID_ARG;
+        }
+        L->cold_dev[c] = static_cast<uint8_t*>(d);
+    }
+    L->loc.assign(init_loc, init_loc + p.E);
+    std::vector<const uint8_t*> ptr(p.E);
+    for (int h = 0; h < p.n_hot; ++h) ptr[h] = L->hot[h];
+    for (int c = 0; c < p.n_cold; ++c) ptr[p.n_hot + c] = scratch->base + (size_t)c * eb;
+    cudaError_t err = cudaSuccess;
+    err = err ? err : cudaMalloc(&L->d_loc, sizeof(int32_t) * p.E);
+    err = err ? err : cudaMalloc(&L->d_ptr, sizeof(uint8_t*) * p.E);
+    err = err ? err : cudaMalloc(&L->d_cold_src, sizeof(uint8_t*) * (p.n_cold > 0 ? p.n_cold : 1));
+    err = err ? err : cudaMalloc(&L->d_window, sizeof(int32_t) * p.E);
+    err = err ? err : cudaMalloc(&L->d_status, sizeof(int));
+    err = err ? err : cudaHostAlloc(&L->h_counts, sizeof(int32_t) * p.E, cudaHostAllocDefault);
+    err = err ? err : cudaHostAlloc(&L->h_loc, sizeof(int32_t) * p.E, cudaHostAllocDefault);
+    err = err ? err : cudaMemcpy(L->d_loc, init_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice);
+    err = err ? err : cudaMemcpy(L->d_ptr, ptr.data(), sizeof(uint8_t*) * p.E, cudaMemcpyHostToDevice);
+    if (p.n_cold > 0)
+        err = err ? err
+                  : cudaMemcpy(L->d_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold, cudaMemcpyHostToDevice);
+    err = err ? err : cudaMemset(L->d_window, 0, sizeof(int32_t) * p.E);
+    err = err ? err : cudaMemset(L->d_status, 0, sizeof(int));
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        free_layer(L);
+        return err == cudaErrorMemoryAllocation ? MOE_ERR_NOMEM : MOE_ERR_CUDA;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+int moe_layer_destroy(moe_layer* L) {
+    if (!L) return MOE_ERR_INVALID_ARG;
+    free_layer(L);
+    return MOE_OK;
+}
+
+int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float* topk_w, int32_t* counts,
+              int32_t* offsets, int32_t* entries, void* stream) {
+    if (!L || T < 0 || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_ids || !topk_w || !entries)) return MOE_ERR_INVALID_ARG;
+    if ((long)T * L->p.k > (1L << 30)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_route(logits, T, L->p.E, L->p.k, L->p.renorm, topk_ids, topk_w, counts, offsets,
+                                    entries, L->d_window, L->d_status, S(stream)));
+}
+
+int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids, int32_t* cold_list,
+                int32_t* n_cold_picked, void* stream) {
+    if (!L || T < 0 || !n_cold_picked) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !phys_ids)) return MOE_ERR_INVALID_ARG;
+    if (L->p.n_cold > 0 && T > 0 && !cold_list) return MOE_ERR_INVALID_ARG;
+    const int ctas = 2 * L->sm_count;
+    return cuda_status(launch_cold_gather(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold,
+                                          L->d_cold_src, L->scratch ? L->scratch->base : nullptr,
+                                          L->lay.total, phys_ids, cold_list, n_cold_picked, L->d_status, ctas,
+                                          S(stream)));
+}
+
+int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes) {
+    if (!L || T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I);
+    return MOE_OK;
+}
+
+int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
+                    const int32_t* offsets, const int32_t* entries, float* y, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (!L || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !phys_ids || !counts || !offsets || !entries || !y || !workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I)) return MOE_ERR_INVALID_ARG;
+    FfnArgs a;
+    memset(&a, 0, sizeof a);
+    a.ptr = L->d_ptr;
+    a.n_phys = L->p.E;
+    a.phys_ids = phys_ids;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.entries = entries;
+    a.E = L->p.E;
+    a.k = L->p.k;
+    a.H = L->p.H;
+    a.I = L->p.I;
+    a.T = T;
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.y = y;
+    a.status = L->d_status;
+    a.w13s = L->lay.w13s;
+    a.w2n = L->lay.w2n;
+    a.w2s = L->lay.w2s;
+    return cuda_status(launch_ffn_decode(a, workspace, L->sm_count, S(stream)));
+}
+
+int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* out, int out_fp32, void* stream) {
+    if (T < 0 || k < 1 || k > 32 || H <= 0 || H % 4) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !topk_w || !out || !aligned(y, 16) || !aligned(out, out_fp32 ? 16 : 8)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(y, topk_w, T, k, H, out, out_fp32, S(stream)));
+}
+
+int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
+    if (!L || !n_swaps_out) return MOE_ERR_INVALID_ARG;
+    *n_swaps_out = 0;
+    const moe_params& p = L->p;
+    L->steps += 1;
+    if (p.swap_every <= 0 || (L->steps % p.swap_every) != 0) return MOE_OK;
+    if (L->fault == 1) {
+        L->fault = 0;
+        return MOE_ERR_INJECTED;
+    }
+    cudaStream_t st = S(stream);
+    cudaError_t err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    const int32_t* cnt = L->h_counts;
+    // candidates: picked cold experts (count desc, id asc), hot experts (count asc, id asc)
+    std::vector<int> cold, hot;
+    for (int e = 0; e < p.E; ++e) {
+        if (L->loc[e] >= p.n_hot) {
+            if (cnt[e] >= 1) cold.push_back(e);
+        } else {
+            hot.push_back(e);
+        }
+    }
+    std::sort(cold.begin(), cold.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] > cnt[b] : a < b; });
+    std::sort(hot.begin(), hot.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] < cnt[b] : a < b; });
+    const size_t lim = std::min({(size_t)p.max_swaps, cold.size(), hot.size()});
+    SwapList sw;
+    sw.n = 0;
+    std::vector<int32_t> loc = L->loc;
+    for (size_t i = 0; i < lim; ++i) {
+        const int a = cold[i], b = hot[i];
+        if (!((double)cnt[a] > (double)p.hysteresis * (double)cnt[b])) break;
+        const int slot_h = loc[b];             // HBM slot of the demoted expert
+        const int slot_c = loc[a] - p.n_hot;   // cold slot of the promoted expert
+        sw.hot[sw.n] = L->hot[slot_h];
+        sw.host[sw.n] = L->cold_dev[slot_c];
+        ++sw.n;
+        std::swap(loc[a], loc[b]);
+    }
+    if (sw.n > 0) {
+        err = launch_swap(sw, L->lay.total, L->sm_count, st);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        std::memcpy(L->h_loc, loc.data(), sizeof(int32_t) * p.E);
+        err = cudaMemcpyAsync(L->d_loc, L->h_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice, st);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        L->loc = loc;
+    }
+    err = cudaMemsetAsync(L->d_window, 0, sizeof(int32_t) * p.E, st);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    *n_swaps_out = sw.n;
+    return MOE_OK;
+}
+
+int moe_layer_get_loc(moe_layer* L, int32_t* loc_host) {
+    if (!L || !loc_host) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemcpy(loc_host, L->d_loc, sizeof(int32_t) * L->p.E, cudaMemcpyDeviceToHost));
+}
+
+int moe_layer_get_counts(moe_layer* L, int32_t* counts_host) {
+    if (!L || !counts_host) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemcpy(counts_host, L->d_window, sizeof(int32_t) * L->p.E, cudaMemcpyDeviceToHost));
+}
+
+int moe_get_status(moe_layer* L, int* status) {
+    if (!L || !status) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemcpy(status, L->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+}
+
+int moe_clear_status(moe_layer* L) {
+    if (!L) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemset(L->d_status, 0, sizeof(int)));
+}
+
+const char* moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_NONFINITE: return "non-finite router logit";
+        case MOE_ERR_BAD_EXPERT: return "expert id out of range";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_NOMEM: return "out of memory";
+        case MOE_ERR_INJECTED: return "injected fault (test hook)";
+        default: return "unknown status";
+    }
+}
+
+int moe_layer_inject_fault(moe_layer* L, int what) {
+    if (!L || what < 0 || what > 1) return MOE_ERR_INVALID_ARG;
+    L->fault = what;
+    return MOE_OK;
+}
+
+int moe_link_probe(const void* src_host, void* dst_dev, size_t bytes, int ctas, void* stream) {
+    if (!src_host || !dst_dev || bytes == 0 || bytes % 16 || ctas < 0) return MOE_ERR_INVALID_ARG;
+    void* d = mapped_host_ptr(const_cast<void*>(src_host));
+    if (!d || !aligned(d, 16) || !aligned(dst_dev, 16) || !is_device_ptr(dst_dev)) return MOE_ERR_INVALID_ARG;
+    if (ctas == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        ctas = sms;
+    }
+    return cuda_status(launch_link_probe(static_cast<const uint8_t*>(d), static_cast<uint8_t*>(dst_dev), bytes, ctas,
+                                         S(stream)));
+}
+
+int moe_debug_e2m1_pairs(uint32_t* out_dev, void* stream) {
+    if (!out_dev) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_debug_e2m1(out_dev, S(stream)));
+}
+
+}  // extern "C"

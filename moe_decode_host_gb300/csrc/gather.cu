@@ -1,0 +1,124 @@
+// Cold dedupe, id remap and gather.
+//
+// "DeepSeek-V4.1-Flash on One GB300 Without the Second GPU", section 1 (The
+// idea): cold experts sit in pinned host memory that the GPU reads directly; one
+// small kernel per layer looks at the router's picks and copies just the cold
+// ones among them into their scratch slots.  Section 3 measured that copy at
+// 2.60 ms of a 10.49 ms step, so the copy is the host-link-bound part of the path.
+//
+// Every CTA rebuilds the (tiny) set of picked cold slots in shared memory, then
+// the grid streams the listed host blobs into their slots with 16-byte zero-copy
+// loads, several in flight per thread to cover the link latency.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kGatherThreads = 256;
+constexpr int kUnroll = 8;          // 16-byte loads in flight per thread
+constexpr int kMaxColdSlots = 4096;  // n_cold bound checked at layer creation
+
+__device__ __forceinline__ uint4 ld_host_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA.
+__device__ __forceinline__ void copy_range(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t c0,
+                                           size_t c1) {
+    const size_t stride = (size_t)kGatherThreads * kUnroll;
+    size_t base = c0 + threadIdx.x;
+    for (; base + (size_t)kGatherThreads * (kUnroll - 1) < c1; base += stride) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_host_v4(src + base + (size_t)u * kGatherThreads);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) dst[base + (size_t)u * kGatherThreads] = v[u];
+    }
+    for (; base < c1; base += kGatherThreads) dst[base] = ld_host_v4(src + base);
+}
+
+__global__ void __launch_bounds__(kGatherThreads) cold_gather_kernel(
+    const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
+    const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes,
+    int32_t* __restrict__ phys, int32_t* __restrict__ cold_list, int32_t* __restrict__ n_picked, int* status) {
+    __shared__ unsigned char flag[kMaxColdSlots];
+    __shared__ int32_t list[kMaxColdSlots];
+    __shared__ int s_cnt;
+    for (int c = threadIdx.x; c < n_cold; c += blockDim.x) flag[c] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_picks; i += blockDim.x) {
+        int id = __ldg(ids + i);
+        int p = -1;
+        if (id >= 0 && id < E) {
+            p = __ldg(loc + id);
+            if (p >= n_hot) flag[p - n_hot] = 1;
+        } else if (blockIdx.x == 0) {
+            set_status(status, MOE_ERR_BAD_EXPERT);
+        }
+        if (blockIdx.x == 0) phys[i] = p;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int cnt = 0;
+        for (int base = 0; base < n_cold; base += 32) {
+            int c = base + lane;
+            bool f = (c < n_cold) && flag[c];
+            unsigned m = __ballot_sync(0xffffffffu, f);
+            if (f) list[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+            cnt += __popc(m);
+        }
+        if (lane == 0) s_cnt = cnt;
+    }
+    __syncthreads();
+    const int cnt = s_cnt;
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < cnt; i += blockDim.x) cold_list[i] = list[i];
+        if (threadIdx.x == 0) *n_picked = cnt;
+    }
+    if (cnt == 0) return;
+    // work items: each picked slot is cut into `seg` contiguous pieces
+    const size_t chunks = blob_bytes / 16;
+    int seg = (int)gridDim.x / cnt;
+    if (seg < 1) seg = 1;
+    const int items = cnt * seg;
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const int c = list[it / seg];
+        const int s = it % seg;
+        const size_t c0 = chunks * (size_t)s / (size_t)seg;
+        const size_t c1 = chunks * (size_t)(s + 1) / (size_t)seg;
+        copy_range(reinterpret_cast<const uint4*>(cold_src[c]),
+                   reinterpret_cast<uint4*>(slot_base + (size_t)c * blob_bytes), c0, c1);
+    }
+}
+
+__global__ void __launch_bounds__(kGatherThreads) link_probe_kernel(const uint8_t* __restrict__ src,
+                                                                    uint8_t* __restrict__ dst, size_t bytes) {
+    const size_t chunks = bytes / 16;
+    const size_t c0 = chunks * (size_t)blockIdx.x / gridDim.x;
+    const size_t c1 = chunks * (size_t)(blockIdx.x + 1) / gridDim.x;
+    copy_range(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), c0, c1);
+}
+
+}  // namespace
+
+cudaError_t launch_cold_gather(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                               const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes,
+                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, int ctas,
+                               cudaStream_t st) {
+    if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
+    cold_gather_kernel<<<ctas, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, cold_src, slot_base,
+                                                        blob_bytes, phys, cold_list, n_picked, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st) {
+    link_probe_kernel<<<ctas, kGatherThreads, 0, st>>>(src, dst, bytes);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

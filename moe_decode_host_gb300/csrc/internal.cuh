@@ -1,0 +1,84 @@
+// Internal declarations shared by the library's translation units (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moehost.h"
+
+namespace moe {
+
+constexpr int kMaxSwaps = 64;
+
+// Blob plane offsets for (H, I); see the blob format in moehost.h.
+struct BlobLayout {
+    size_t w13n, w13s, w2n, w2s, total;
+};
+
+inline BlobLayout blob_layout(int H, int I) {
+    BlobLayout b;
+    size_t a = (size_t)2 * I * (H / 2);
+    size_t s = (size_t)2 * I * (H / 32);
+    size_t c = (size_t)H * (I / 2);
+    size_t d = (size_t)H * (I / 32);
+    b.w13n = 0;
+    b.w13s = a;
+    b.w2n = a + s;
+    b.w2s = a + s + c;
+    b.total = a + s + c + d;
+    return b;
+}
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- launchers (implemented in the .cu files) -------------------------------
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
+                         int32_t* counts, int32_t* offsets, int32_t* entries, int32_t* window, int* status,
+                         cudaStream_t st);
+
+cudaError_t launch_cold_gather(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                               const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes,
+                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, int ctas,
+                               cudaStream_t st);
+
+cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
+
+struct FfnArgs {
+    const uint8_t* const* ptr;  // phys id -> blob base (device)
+    int n_phys;
+    const int32_t* phys_ids;  // [T*k]
+    const int32_t* counts;    // [E]
+    const int32_t* offsets;   // [E+1]
+    const int32_t* entries;   // [T*k]
+    int E, k, H, I, T;
+    const __nv_bfloat16* x;  // [T][H]
+    __half* x16;             // workspace [T][H]
+    int32_t* xexp;           // workspace [T]
+    unsigned* hamax;         // workspace [T*k]
+    float* h;                // workspace [T*k][I]
+    float* y;                // [T*k][H]
+    int* status;
+    size_t w13s, w2n, w2s;   // plane offsets in a blob
+};
+
+size_t ffn_decode_workspace(int T, int k, int H, int I);
+cudaError_t launch_ffn_decode(FfnArgs a, void* workspace, int sm_count, cudaStream_t st);
+
+cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
+                           cudaStream_t st);
+
+struct SwapList {
+    int n;
+    uint8_t* hot[kMaxSwaps];   // device blob of the HBM slot
+    uint8_t* host[kMaxSwaps];  // device-mapped pointer of the host blob
+};
+cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st);
+
+cudaError_t launch_debug_e2m1(uint32_t* out, cudaStream_t st);
+
+}  // namespace moe

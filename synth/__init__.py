@@ -132,6 +132,31 @@ def gen_blobs(n: int, H: int, I: int, seed: int, device="cpu", out: torch.Tensor
     return out
 
 
+def fill_layer(hot: torch.Tensor, cold: torch.Tensor, loc: np.ndarray, H: int, I: int, seed: int,
+               device="cpu") -> None:
+    """Draws every expert's blob (expert ids in ascending order, one generator) and
+    writes it where the placement map puts it: hot[loc[e]] when loc[e] < n_hot,
+    else cold[loc[e] - n_hot].  hot/cold may live on any device (cold is usually
+    pinned host memory)."""
+    n_hot = hot.shape[0]
+    sec = blob_sections(H, I)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    tmp = torch.empty(sec["total"], dtype=torch.uint8, device=device)
+    for e in range(len(loc)):
+        for name in ("w13n", "w13s", "w2n", "w2s"):
+            off, size = sec[name]
+            if name.endswith("n"):
+                tmp[off:off + size] = _random_nibble_bytes(size, gen, device)
+            else:
+                tmp[off:off + size] = _random_scale_bytes(size, gen, device)
+        p = int(loc[e])
+        if p < n_hot:
+            hot[p].copy_(tmp)
+        else:
+            cold[p - n_hot].copy_(tmp)
+
+
 def gen_x(T: int, H: int, seed: int, device="cpu") -> torch.Tensor:
     """Activations bf16(N(0,1)) of shape [T, H]."""
     gen = torch.Generator(device="cpu")

@@ -1,0 +1,56 @@
+"""Set-up helpers for the GPU tests: layers built from the seeded generator,
+device buffers, and readers that fetch an expert's current bytes wherever the
+placement map says it lives (so the oracle sees exactly what the GPU used)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+
+
+class LayerFixture:
+    def __init__(self, *, H, I, E, n_hot, n_cold, k, seed, loc=None, swap_every=0, max_swaps=8,
+                 hysteresis=3.0, renorm=0, scratch=None, slots=None, gen_device="cuda"):
+        import moe_decode_host_gb300 as m
+
+        self.m = m
+        self.H, self.I, self.E, self.n_hot, self.n_cold, self.k = H, I, E, n_hot, n_cold, k
+        self.eb = m.expert_bytes(H, I)
+        dev = torch.device("cuda")
+        self.loc0 = np.arange(E, dtype=np.int32) if loc is None else np.asarray(loc, np.int32)
+        self.hot = torch.empty((max(1, n_hot), self.eb), dtype=torch.uint8, device=dev)
+        self.cold = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8).pin_memory()
+        synth.fill_layer(self.hot, self.cold, self.loc0, H, I, seed, device=gen_device)
+        if scratch is None:
+            self.slots = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8, device=dev)
+            self.scratch = m.Scratch(n_cold, self.eb, self.slots) if n_cold > 0 else None
+        else:
+            self.slots, self.scratch = slots, scratch
+        self.layer = m.Layer(E=E, k=k, H=H, I=I, n_hot=n_hot, n_cold=n_cold, scratch=self.scratch,
+                             hot_ptrs=[self.hot[h] for h in range(n_hot)],
+                             cold_ptrs=[self.cold[c] for c in range(n_cold)], init_loc=self.loc0,
+                             renorm=renorm, swap_every=swap_every, max_swaps=max_swaps, hysteresis=hysteresis)
+
+    def expert_bytes_now(self, e: int, loc=None) -> np.ndarray:
+        """Current bytes of expert e (from its HBM slot or its host blob)."""
+        loc = self.layer.get_loc() if loc is None else loc
+        p = int(loc[e])
+        if p < self.n_hot:
+            return self.hot[p].cpu().numpy()
+        return self.cold[p - self.n_hot].numpy().copy()
+
+    def all_blobs_now(self) -> list:
+        loc = self.layer.get_loc()
+        return [self.expert_bytes_now(e, loc) for e in range(self.E)]
+
+
+def bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def rel_l2(got, want) -> float:
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))

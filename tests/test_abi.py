@@ -1,0 +1,88 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every function that
+include/moehost.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moehost.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def mlib():
+    from moe_decode_host_gb300 import build as b
+
+    b.build()
+    import moe_decode_host_gb300 as m
+
+    return m
+
+
+def test_header_declares_the_five_entry_points():
+    names = _declared_functions()
+    for n in ("moe_route", "cold_gather", "moe_grouped_ffn", "moe_combine", "residency_update"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(mlib):
+    lib = ctypes.CDLL(mlib.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_argument_checks(mlib):
+    lib = mlib.lib
+    assert lib.moe_expert_bytes(100, 128) == 0
+    assert lib.moe_expert_bytes(4096, 3072) == 20054016
+    assert lib.moe_expert_bytes(256, 512) == 208896
+    out = ctypes.c_void_p()
+    assert lib.moe_scratch_create(-1, 208896, None, ctypes.byref(out)) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_scratch_create(4, 208896, None, ctypes.byref(out)) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(None, None, -1, 2, 256, None, 0, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(None, None, 4, 0, 256, None, 0, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(None, None, 1, None, None, None, None, None, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.cold_gather(None, None, 1, None, None, None, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_grouped_ffn(None, None, 1, None, None, None, None, None, None, 0, None) == \
+        mlib.MOE_ERR_INVALID_ARG
+    n = ctypes.c_int32()
+    assert lib.residency_update(None, ctypes.byref(n), None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_destroy(None) == mlib.MOE_ERR_INVALID_ARG
+    p = mlib.moe_params(16, 2, 256, 512, 12, 4, 0, 16, 8, 3.0)
+    loc = (ctypes.c_int32 * 16)(*range(16))
+    bad = mlib.moe_params(16, 0, 256, 512, 12, 4, 0, 16, 8, 3.0)
+    assert lib.moe_layer_create(ctypes.byref(bad), None, None, None, loc, ctypes.byref(out)) == \
+        mlib.MOE_ERR_INVALID_ARG
+    bad = mlib.moe_params(16, 2, 200, 512, 12, 4, 0, 16, 8, 3.0)
+    assert lib.moe_layer_create(ctypes.byref(bad), None, None, None, loc, ctypes.byref(out)) == \
+        mlib.MOE_ERR_INVALID_ARG
+    bad = mlib.moe_params(16, 2, 256, 512, 12, 5, 0, 16, 8, 3.0)
+    assert lib.moe_layer_create(ctypes.byref(bad), None, None, None, loc, ctypes.byref(out)) == \
+        mlib.MOE_ERR_INVALID_ARG
+    # cold experts but no scratch
+    assert lib.moe_layer_create(ctypes.byref(p), None, None, None, loc, ctypes.byref(out)) == \
+        mlib.MOE_ERR_INVALID_ARG
+    # a map that is not a bijection
+    dup = (ctypes.c_int32 * 16)(*([0] + list(range(1, 15)) + [0]))
+    assert lib.moe_layer_create(ctypes.byref(p), None, None, None, dup, ctypes.byref(out)) == \
+        mlib.MOE_ERR_INVALID_ARG
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -99):
+        assert lib.moe_strerror(code)
+
+
+def test_package_has_no_oracle_dependency():
+    pkg = os.path.join(ROOT, "moe_decode_host_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "moe_oracle" not in src, f
