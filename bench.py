@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--experts", type=int, default=None, help="override E (profiling on a smaller layer)")
+    ap.add_argument("--hot", type=int, default=None, help="override n_hot (with --experts)")
+    ap.add_argument("--no-link-probe", action="store_true")
     return ap.parse_args()
 
 
@@ -65,6 +68,10 @@ def workload(args):
         c["s"] = args.skew
     if args.layers is not None:
         c["layers"] = args.layers
+    if args.experts is not None:
+        c["E"] = args.experts
+        c["n_hot"] = args.hot if args.hot is not None else min(c["n_hot"], args.experts)
+        c["n_cold"] = c["E"] - c["n_hot"]
     c["name"] = args.config
     return c
 
@@ -325,7 +332,10 @@ def run_ours(args):
     c = workload(args)
     c["no_res"] = args.no_residency
     hbm_peak, peak_kind = _peaks()
-    link_peak, link_detail = measure_link_peak(dev)
+    if args.no_link_probe:
+        link_peak, link_detail = None, {"skipped": True}
+    else:
+        link_peak, link_detail = measure_link_peak(dev)
     layers, scratch, slots = build_layers(c, dev)
     P = args.pool
     pool = gen_pool(c, layers, P, dev)
@@ -415,8 +425,9 @@ def run_ours(args):
     hot_bytes = (distinct - ncold_h) * eb
     ffn_gbs = float(ffn_bytes.sum() / (ffn_ms.sum() * 1e-3) / 1e9)
     gather_gbs = float(gather_bytes.sum() / max(1e-9, gat_ms.sum() * 1e-3) / 1e9) if gather_bytes.sum() else 0.0
-    tstar_nom = np.maximum(hot_bytes / (HBM_NOMINAL_GBS * 1e9), gather_bytes / (link_peak * 1e9))
-    tstar_meas = np.maximum(hot_bytes / (hbm_peak * 1e9), gather_bytes / (link_peak * 1e9))
+    lp = link_peak if link_peak else float("inf")
+    tstar_nom = np.maximum(hot_bytes / (HBM_NOMINAL_GBS * 1e9), gather_bytes / (lp * 1e9))
+    tstar_meas = np.maximum(hot_bytes / (hbm_peak * 1e9), gather_bytes / (lp * 1e9))
     step_ms = elapsed_ms / K
     value = world * K * T / (elapsed_ms * 1e-3)
     # dominant kernel by measured time
@@ -428,7 +439,8 @@ def run_ours(args):
                 "peak_kind": peak_kind}
     else:
         roof = {"kernel": "cold_gather (zero-copy host reads)", "bound": "link", "achieved": gather_gbs,
-                "peak": link_peak, "unit": "GB/s", "frac": gather_gbs / link_peak, "traffic": None,
+                "peak": link_peak, "unit": "GB/s", "frac": gather_gbs / link_peak if link_peak else None,
+                "traffic": None,
                 "peak_kind": "measured in this run (max of pinned cudaMemcpyAsync and zero-copy probe)"}
     line = {"metric": "MoE layer tokens/s (decode)", "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -436,15 +448,16 @@ def run_ours(args):
             "roofline": roof,
             "kernels": {n: {"ms_mean": float(np.mean(per[n])), "share": tot[n] / max(1e-9, sum(tot.values()))}
                         for n in names},
-            "step_roofline": {"tstar_ms_nominal_hbm": float(tstar_nom.sum() / K),
-                              "frac_nominal": float(tstar_nom.sum() / K / step_ms),
-                              "tstar_ms_measured_hbm": float(tstar_meas.sum() / K),
-                              "frac_measured": float(tstar_meas.sum() / K / step_ms),
+            "step_roofline": {"tstar_ms_nominal_hbm": float(1e3 * tstar_nom.sum() / K),
+                              "frac_nominal": float(1e3 * tstar_nom.sum() / K / step_ms),
+                              "tstar_ms_measured_hbm": float(1e3 * tstar_meas.sum() / K),
+                              "frac_measured": float(1e3 * tstar_meas.sum() / K / step_ms),
                               "hbm_peak_gbs": hbm_peak, "link_peak_gbs": link_peak, "link_probe": link_detail},
             "ffn_hbm_gbs": ffn_gbs, "gather_link_gbs": gather_gbs,
             "distinct_experts_per_layer_step": float(distinct.mean()),
             "cold_experts_per_layer_step": float(ncold_h.mean()), "swaps": int(total_swaps),
-            "clocks": clk, "gpu_launches": int(launches)}
+            "clocks": clk, "gpu_launches": int(launches),
+            "device_status": [int(L["layer"].status()) for L in layers]}
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, c, layers, pool, bufs, dev, dist, world)
     if rank == 0 and not args.no_cpu:

@@ -140,9 +140,19 @@ int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float
  *  n_cold_picked device int32 [1] out.
  * Every listed slot of the scratch is overwritten with the bytes of its host blob,
  * read zero-copy with 16-byte loads; unlisted slots are left as they were.
+ * phys_ids, cold_list and n_cold_picked are ready in `stream` order.  The byte
+ * copy itself runs on the layer's own copy stream, forked from `stream` at this
+ * call, so that moe_grouped_ffn can work on the experts in HBM while the link
+ * streams the cold ones; moe_grouped_ffn and residency_update on this layer join
+ * it, and so does moe_gather_join.  A layer sharing the scratch must not call
+ * cold_gather before this layer's copy has been joined into `stream`.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
 int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids, int32_t* cold_list,
                 int32_t* n_cold_picked, void* stream);
+
+/* Makes `stream` wait for the layer's cold copy in flight (no-op when none).
+ * Needed only to read the scratch slots without calling moe_grouped_ffn. */
+int moe_gather_join(moe_layer* L, void* stream);
 
 /* Device workspace bytes moe_grouped_ffn needs for T tokens. */
 int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes);
@@ -193,8 +203,15 @@ int moe_layer_get_counts(moe_layer* L, int32_t* counts_host);
 /* Reads the layer's device status word (synchronous); 0 = no error so far. */
 int moe_get_status(moe_layer* L, int* status);
 
-/* Clears the device status word (synchronous). */
+/* Clears the device status word and the diagnostic record (synchronous). */
 int moe_clear_status(moe_layer* L);
+
+/* Copies the diagnostic record of the first device-side wait that ran out of
+ * time (set together with MOE_ERR_TIMEOUT) to host int32 [16]: [0] 1 when set,
+ * [1] block, [2] warp, [3] wait kind (1 stage full, 2 stage empty), [4] ring slot,
+ * [5] parity waited for, [6] stage index, [7] task << 8 | token columns,
+ * [8] 1 if the other parity had completed.  All zero when nothing timed out. */
+int moe_get_diag(moe_layer* L, int32_t* diag_host);
 
 /* Text for a status code. */
 const char* moe_strerror(int code);

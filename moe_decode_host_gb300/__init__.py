@@ -16,7 +16,7 @@ from ._lib import (LIB_PATH, MOE_ERR_BAD_EXPERT, MOE_ERR_CUDA, MOE_ERR_INJECTED,
                    ptr, stream_handle)
 
 __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_bytes", "moe_route", "cold_gather",
-           "moe_grouped_ffn", "moe_combine", "residency_update", "link_probe", "debug_e2m1_pairs", "run_step",
+           "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
            "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED"]
 
@@ -96,6 +96,11 @@ class Layer:
         check(lib.moe_get_status(self.handle, ctypes.byref(s)), "moe_get_status")
         return int(s.value)
 
+    def diag(self) -> np.ndarray:
+        out = np.zeros(16, np.int32)
+        check(lib.moe_get_diag(self.handle, out.ctypes.data), "moe_get_diag")
+        return out
+
     def clear_status(self):
         check(lib.moe_clear_status(self.handle), "moe_clear_status")
 
@@ -111,6 +116,10 @@ def moe_route(layer: Layer, logits, T, topk_ids, topk_w, counts, offsets, entrie
 def cold_gather(layer: Layer, topk_ids, T, phys_ids, cold_list, n_cold_picked, stream=None):
     check(lib.cold_gather(layer.handle, ptr(topk_ids), T, ptr(phys_ids), ptr(cold_list), ptr(n_cold_picked),
                           stream_handle(stream)), "cold_gather")
+
+
+def moe_gather_join(layer: Layer, stream=None):
+    check(lib.moe_gather_join(layer.handle, stream_handle(stream)), "moe_gather_join")
 
 
 def moe_grouped_ffn(layer: Layer, x, T, phys_ids, counts, offsets, entries, y, workspace, workspace_bytes=None,

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libmoehost.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build the CUDA library first "
-        "(python -m moe_decode_host_gb300.build, or __graft_entry__.build())")
+        "(python moe_decode_host_gb300/build.py, or __graft_entry__.build())")
 
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -48,6 +48,7 @@ _SIGS = {
     "moe_layer_destroy": (_I, [_P]),
     "moe_route": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "cold_gather": (_I, [_P, _P, _I, _P, _P, _P, _P]),
+    "moe_gather_join": (_I, [_P, _P]),
     "moe_ffn_workspace_bytes": (_I, [_P, _I, ctypes.POINTER(_Z)]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _I, _P]),
@@ -56,6 +57,7 @@ _SIGS = {
     "moe_layer_get_counts": (_I, [_P, _P]),
     "moe_get_status": (_I, [_P, ctypes.POINTER(_I)]),
     "moe_clear_status": (_I, [_P]),
+    "moe_get_diag": (_I, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [_I]),
     "moe_layer_inject_fault": (_I, [_P, _I]),
     "moe_link_probe": (_I, [_P, _P, _Z, _I, _P]),

@@ -37,8 +37,14 @@ struct moe_layer {
     const uint8_t** d_cold_src = nullptr;  // [n_cold] host blobs (device-mapped)
     int32_t* d_window = nullptr;      // [E] picks in the current window
     int* d_status = nullptr;
+    int* d_diag = nullptr;            // [16] record of the first device-side wait that timed out
     int32_t* h_counts = nullptr;      // pinned [E]
     int32_t* h_loc = nullptr;         // pinned [E]
+    TmapPair* d_tmaps = nullptr;      // [E] TMA descriptors per physical id
+    cudaStream_t copy_stream = nullptr;  // cold slot copies run here, joined by moe_grouped_ffn
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    bool copy_pending = false;
+    int copy_ctas = 0;
     long steps = 0;
     int fault = 0;
 };
@@ -76,13 +82,58 @@ void* mapped_host_ptr(void* p) {
 
 cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2D u8 view [rows][row_bytes] at base; box = 128 bytes x 32 rows, 128-byte swizzle.
+bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {128, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Makes `st` wait for the layer's cold copy in flight, if any.
+cudaError_t join_copy(moe_layer* L, cudaStream_t st) {
+    if (!L->copy_pending) return cudaSuccess;
+    L->copy_pending = false;
+    return cudaStreamWaitEvent(st, L->ev_join, 0);
+}
+
 void free_layer(moe_layer* L) {
     if (!L) return;
+    if (L->copy_stream) cudaStreamSynchronize(L->copy_stream);
+    if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
+    if (L->ev_fork) cudaEventDestroy(L->ev_fork);
+    if (L->ev_join) cudaEventDestroy(L->ev_join);
+    cudaFree(L->d_tmaps);
     cudaFree(L->d_loc);
     cudaFree(L->d_ptr);
     cudaFree(L->d_cold_src);
     cudaFree(L->d_window);
     cudaFree(L->d_status);
+    cudaFree(L->d_diag);
     cudaFreeHost(L->h_counts);
     cudaFreeHost(L->h_loc);
     delete L;
@@ -177,6 +228,8 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     err = err ? err : cudaMalloc(&L->d_cold_src, sizeof(uint8_t*) * (p.n_cold > 0 ? p.n_cold : 1));
     err = err ? err : cudaMalloc(&L->d_window, sizeof(int32_t) * p.E);
     err = err ? err : cudaMalloc(&L->d_status, sizeof(int));
+    err = err ? err : cudaMalloc(&L->d_diag, sizeof(int) * 16);
+    err = err ? err : cudaMemset(L->d_diag, 0, sizeof(int) * 16);
     err = err ? err : cudaHostAlloc(&L->h_counts, sizeof(int32_t) * p.E, cudaHostAllocDefault);
     err = err ? err : cudaHostAlloc(&L->h_loc, sizeof(int32_t) * p.E, cudaHostAllocDefault);
     err = err ? err : cudaMemcpy(L->d_loc, init_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice);
@@ -186,6 +239,22 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
                   : cudaMemcpy(L->d_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold, cudaMemcpyHostToDevice);
     err = err ? err : cudaMemset(L->d_window, 0, sizeof(int32_t) * p.E);
     err = err ? err : cudaMemset(L->d_status, 0, sizeof(int));
+    err = err ? err : cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking);
+    err = err ? err : cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
+    err = err ? err : cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
+    if (err == cudaSuccess) {
+        std::vector<TmapPair> maps(p.E);
+        for (int i = 0; i < p.E; ++i) {
+            if (!encode_plane(&maps[i].w13n, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||
+                !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H)) {
+                free_layer(L);
+                return MOE_ERR_CUDA;
+            }
+        }
+        err = cudaMalloc(&L->d_tmaps, sizeof(TmapPair) * p.E);
+        err = err ? err : cudaMemcpy(L->d_tmaps, maps.data(), sizeof(TmapPair) * p.E, cudaMemcpyHostToDevice);
+    }
+    L->copy_ctas = L->sm_count / 2 > 0 ? L->sm_count / 2 : 1;
     if (err != cudaSuccess) {
         cudaGetLastError();
         free_layer(L);
@@ -215,11 +284,25 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
     if (!L || T < 0 || !n_cold_picked) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!topk_ids || !phys_ids)) return MOE_ERR_INVALID_ARG;
     if (L->p.n_cold > 0 && T > 0 && !cold_list) return MOE_ERR_INVALID_ARG;
-    const int ctas = 2 * L->sm_count;
-    return cuda_status(launch_cold_gather(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold,
-                                          L->d_cold_src, L->scratch ? L->scratch->base : nullptr,
-                                          L->lay.total, phys_ids, cold_list, n_cold_picked, L->d_status, ctas,
-                                          S(stream)));
+    cudaStream_t st = S(stream);
+    cudaError_t err = launch_cold_remap(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, phys_ids,
+                                        cold_list, n_cold_picked, L->d_status, st);
+    if (err != cudaSuccess || L->p.n_cold == 0 || T == 0) return cuda_status(err);
+    // the byte copy forks onto the layer's copy stream so that the FFN over the
+    // experts already in HBM can run while the link streams the cold ones
+    err = cudaEventRecord(L->ev_fork, st);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
+    if (err == cudaSuccess)
+        err = launch_cold_copy(cold_list, n_cold_picked, L->d_cold_src, L->scratch->base, L->lay.total, L->copy_ctas,
+                               L->copy_stream);
+    if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
+    if (err == cudaSuccess) L->copy_pending = true;
+    return cuda_status(err);
+}
+
+int moe_gather_join(moe_layer* L, void* stream) {
+    if (!L) return MOE_ERR_INVALID_ARG;
+    return cuda_status(join_copy(L, S(stream)));
 }
 
 int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes) {
@@ -239,6 +322,9 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     FfnArgs a;
     memset(&a, 0, sizeof a);
     a.ptr = L->d_ptr;
+    a.tmaps = L->d_tmaps;
+    a.loc = L->d_loc;
+    a.n_hot = L->p.n_hot;
     a.n_phys = L->p.E;
     a.phys_ids = phys_ids;
     a.counts = counts;
@@ -252,10 +338,25 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     a.x = static_cast<const __nv_bfloat16*>(x);
     a.y = y;
     a.status = L->d_status;
+    a.diag = L->d_diag;
     a.w13s = L->lay.w13s;
     a.w2n = L->lay.w2n;
     a.w2s = L->lay.w2s;
-    return cuda_status(launch_ffn_decode(a, workspace, L->sm_count, S(stream)));
+    cudaStream_t st = S(stream);
+    cudaError_t err = launch_ffn_prep(a, workspace, st);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    if (L->copy_pending) {
+        // experts in HBM first, while the cold copy is in flight; then the cold ones
+        err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        if (err == cudaSuccess) err = join_copy(L, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 2, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 2, L->sm_count, st);
+    } else {
+        err = launch_ffn_phase(a, 0, 0, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 0, L->sm_count, st);
+    }
+    return cuda_status(err);
 }
 
 int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* out, int out_fp32, void* stream) {
@@ -276,7 +377,9 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
         return MOE_ERR_INJECTED;
     }
     cudaStream_t st = S(stream);
-    cudaError_t err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
+    cudaError_t err = join_copy(L, st);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     const int32_t* cnt = L->h_counts;
@@ -336,7 +439,14 @@ int moe_get_status(moe_layer* L, int* status) {
 
 int moe_clear_status(moe_layer* L) {
     if (!L) return MOE_ERR_INVALID_ARG;
-    return cuda_status(cudaMemset(L->d_status, 0, sizeof(int)));
+    cudaError_t e = cudaMemset(L->d_status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(L->d_diag, 0, sizeof(int) * 16);
+    return cuda_status(e);
+}
+
+int moe_get_diag(moe_layer* L, int32_t* diag_host) {
+    if (!L || !diag_host) return MOE_ERR_INVALID_ARG;
+    return cuda_status(cudaMemcpy(diag_host, L->d_diag, sizeof(int32_t) * 16, cudaMemcpyDeviceToHost));
 }
 
 const char* moe_strerror(int code) {

@@ -53,25 +53,25 @@ __global__ void __launch_bounds__(kSwapThreads) swap_kernel(SwapList s, size_t b
         uint4* b = reinterpret_cast<uint4*>(s.host[i]);
         const size_t c0 = chunks * (size_t)part / (size_t)seg;
         const size_t c1 = chunks * (size_t)(part + 1) / (size_t)seg;
-        size_t base = c0 + threadIdx.x;
         const size_t stride = (size_t)kSwapThreads * kSwapUnroll;
-        for (; base + (size_t)kSwapThreads * (kSwapUnroll - 1) < c1; base += stride) {
+        for (size_t base = c0 + threadIdx.x; base < c1; base += stride) {
             uint4 va[kSwapUnroll], vb[kSwapUnroll];
 #pragma unroll
             for (int u = 0; u < kSwapUnroll; ++u) {
-                va[u] = a[base + (size_t)u * kSwapThreads];
-                vb[u] = b[base + (size_t)u * kSwapThreads];
+                const size_t ci = base + (size_t)u * kSwapThreads;
+                if (ci < c1) {
+                    va[u] = a[ci];
+                    vb[u] = b[ci];
+                }
             }
 #pragma unroll
             for (int u = 0; u < kSwapUnroll; ++u) {
-                a[base + (size_t)u * kSwapThreads] = vb[u];
-                b[base + (size_t)u * kSwapThreads] = va[u];
+                const size_t ci = base + (size_t)u * kSwapThreads;
+                if (ci < c1) {
+                    a[ci] = vb[u];
+                    b[ci] = va[u];
+                }
             }
-        }
-        for (; base < c1; base += kSwapThreads) {
-            uint4 va = a[base], vb = b[base];
-            a[base] = vb;
-            b[base] = va;
         }
     }
 }

@@ -1,4 +1,5 @@
-// Grouped SwiGLU expert FFN, decode path (up to 32 tokens per expert and pass).
+// Grouped SwiGLU expert FFN, decode path (tokens per expert handled 8, 16 or 32
+// at a time).
 //
 // "DeepSeek-V4.1-Flash on One GB300 Without the Second GPU", section 1: after the
 // cold copy, the layer runs all experts in one call, as if they were resident.
@@ -6,36 +7,196 @@
 // I=3072) are streamed once from HBM (or from its scratch slot) and applied to
 // the few tokens routed to it, so the kernel is bound by HBM bandwidth.
 //
-// Per warp: 16-row m16 tiles of E2M1 weights are dequantised in registers (one
-// e2m1x2 -> f16x2 conversion per byte) and fed to mma.sync m16n8k16 as an exact
-// f16 x f16 -> fp32 dot-product engine; the E8M0 scale of each 32-element block
-// is applied in fp32 to that block's partial sums.  The blob layout puts, in every
-// 64-byte group, the 8 elements of each of 4 blocks that one lane of a quad needs
-// into that lane's 16-byte load, so every mma step sees a single block.
-// Activations are staged as f16 with an exact per-row power-of-two prescale.
-// Four warps split the reduction dimension and reduce through shared memory in a
-// fixed order, so results do not depend on timing.
+// Structure (one persistent CTA per SM):
+//  - a producer warp streams 128-byte-wide slices of the weight rows of each task
+//    (an expert and 32 output rows) into a ring of shared-memory stages with 2D
+//    TMA loads (128-byte swizzle), signalling mbarriers;
+//  - eight consumer warps dequantise the E2M1 nibbles in registers (one
+//    e2m1x2 -> f16x2 conversion per byte) and feed mma.sync m16n8k16 as an exact
+//    f16 x f16 -> fp32 dot-product engine; each 32-element block's E8M0 scale is
+//    applied in fp32 to that block's partial sums.  Warps split the rows and the
+//    reduction dimension; partial sums meet in shared memory in a fixed order.
+// The blob layout puts, in every 64-byte group of a row, the 8 elements of each of
+// 4 blocks that one lane of a quad needs into that lane's 16 bytes, so every mma
+// step sees a single block.  Activations are staged as f16 with an exact
+// power-of-two prescale per row.  Every wait is bounded by a deadline; a wait
+// that runs out sets MOE_ERR_TIMEOUT in the status word and the CTA drains its
+// copies and returns.
+#include <cuda.h>
+
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kConsumers = 8;
+constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxE = 1024;
+constexpr int kSliceBytes = 128;  // bytes of one row per stage (256 elements)
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
-__device__ __forceinline__ uint4 ld_weights(const uint8_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+template <int P>
+struct Cfg;
+// phase 0: task = 32 output rows -> 32 gate + 32 up weight rows per stage; each warp
+// holds a gate tile and the matching up tile (16 rows); 2 row tiles x 4 K-splits
+template <>
+struct Cfg<0> {
+    static constexpr int kRows = 64, kNTile = 2, kRT = 2, kKS = 4, kTaskRows = 32;
+};
+// phase 1: task = 32 rows of w2; one 16-row tile per warp; 2 row tiles x 4 K-splits
+template <>
+struct Cfg<1> {
+    static constexpr int kRows = 32, kNTile = 1, kRT = 2, kKS = 4, kTaskRows = 32;
+};
+constexpr int kActStride = 576;  // bytes per activation column slice in a stage (512 + 64 pad)
+constexpr int kStageBudget = 160 * 1024;
+
+template <int P, int NT>
+struct Layout {
+    static constexpr int kWBytes = Cfg<P>::kRows * 128;
+    static constexpr int kABytes = 8 * NT * kActStride;
+    static constexpr int kStageBytes = ((kWBytes + kABytes) + 1023) & ~1023;
+    static constexpr int kStages = (kStageBudget / kStageBytes) < 64 ? (kStageBudget / kStageBytes) : 64;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the barrier phase with the given parity; false when the deadline
+// passed (status set, abort raised, the place recorded in diag) or another warp
+// raised abort.  where: 1 = stage full (consumer), 2 = stage empty (producer).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity, volatile int* abort, int* status, int* diag,
+                                       int where, int slot, int stage, int extra) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (unsigned it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort = 1;
+                if (diag && atomicCAS(diag, 0, 1) == 0) {
+                    diag[1] = blockIdx.x;
+                    diag[2] = (int)(threadIdx.x >> 5);
+                    diag[3] = where;
+                    diag[4] = slot;
+                    diag[5] = (int)parity;
+                    diag[6] = stage;
+                    diag[7] = extra;
+                    diag[8] = mbar_try_wait(bar, parity ^ 1u) ? 1 : 0;
+                    __threadfence();
+                }
+                set_status(status, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Waits until the producer has stamped `slot` with global stage `g` (it stamps a
+// slot only after the slot's previous stage was released), so that the following
+// parity wait on the slot's full barrier cannot match an older phase.
+__device__ __noinline__ bool seq_wait(volatile int* seq, int g, volatile int* abort, int* status, int* diag,
+                                      int slot) {
+    if (*seq == g) return true;
+    const uint64_t t0 = globaltimer();
+    for (unsigned it = 1;; ++it) {
+        if (*seq == g) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort = 1;
+                if (diag && atomicCAS(diag, 0, 1) == 0) {
+                    diag[1] = blockIdx.x;
+                    diag[2] = (int)(threadIdx.x >> 5);
+                    diag[3] = 3;
+                    diag[4] = slot;
+                    diag[5] = *seq;
+                    diag[6] = g;
+                    __threadfence();
+                }
+                set_status(status, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used when draining copies in flight before exit (ignores abort).
+__device__ __noinline__ void mbar_drain(uint64_t* bar, unsigned parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
     uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
+}
+
+// Four E8M0 exponent bytes (byte j = block j) -> 2^(e_j - 127) as fp32, exactly
+// (e = 0 gives the subnormal 2^-127, e = 255 gives NaN): two ue8m0x2 -> bf16x2
+// conversions, then the bf16 halves are widened to fp32.
+__device__ __forceinline__ void e8m0x4_to_f32(uint32_t w, float (&s)[4]) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "mov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %0, h0;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %1, h1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+    s[0] = __uint_as_float(lo << 16);
+    s[1] = __uint_as_float(lo & 0xffff0000u);
+    s[2] = __uint_as_float(hi << 16);
+    s[3] = __uint_as_float(hi & 0xffff0000u);
 }
 
 // 8 E2M1 nibbles (byte b holds elements 2b, 2b+1) -> 4 f16x2 (r[b] = {elem 2b, elem 2b+1}).
@@ -48,13 +209,6 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
         "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
         : "r"(w));
-}
-
-// E8M0 exponent byte -> 2^(e-127) as fp32 (e = 0 gives the subnormal 2^-127,
-// e = 255 gives NaN).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
-    uint32_t bits = (e == 0u) ? 0x00400000u : ((e == 255u) ? 0x7fc00000u : (e << 23));
-    return __uint_as_float(bits);
 }
 
 // 2^p for p in [-126, 127].
@@ -72,7 +226,7 @@ __device__ __forceinline__ int prescale_exp(float amax) {
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -83,98 +237,71 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-// B operand from prescaled f16 activations: column pointer per n-tile (nullptr = empty column).
+// Fragment row g (0..7) of an m16 tile is weight row perm8(g) (and +8): with the
+// 128-byte swizzle this keeps the two rows a quarter-warp reads in disjoint banks.
+__device__ __forceinline__ int perm8(int g) { return (g >> 1) | ((g & 1) << 2); }
+
+// B operand from the stage's activation slices: column n (token or pick) of the
+// stage lives at act + n * kActStride, 256 prescaled f16 values; missing columns read
+// as zero.
 template <int NT>
-struct X16Loader {
-    const __half* col[NT];
-    __device__ __forceinline__ void load(int nt, int kidx, uint32_t& b0, uint32_t& b1) const {
-        if (col[nt]) {
-            uint2 v = __ldg(reinterpret_cast<const uint2*>(col[nt] + kidx));
-            b0 = v.x;
-            b1 = v.y;
-        } else {
-            b0 = 0u;
-            b1 = 0u;
-        }
+struct SmemB {
+    const uint8_t* col[NT];  // this lane's column in each n-tile, or nullptr
+    __device__ __forceinline__ uint4 load(int nt, int byte_off) const {
+        if (col[nt]) return *reinterpret_cast<const uint4*>(col[nt] + byte_off);
+        return make_uint4(0u, 0u, 0u, 0u);
     }
 };
 
-// B operand from fp32 intermediate h, scaled by 2^-p per column and rounded to f16.
-template <int NT>
-struct HLoader {
-    const float* col[NT];
-    float scale[NT];
-    __device__ __forceinline__ void load(int nt, int kidx, uint32_t& b0, uint32_t& b1) const {
-        if (col[nt]) {
-            float4 v = __ldg(reinterpret_cast<const float4*>(col[nt] + kidx));
-            __half2 lo = __floats2half2_rn(v.x * scale[nt], v.y * scale[nt]);
-            __half2 hi = __floats2half2_rn(v.z * scale[nt], v.w * scale[nt]);
-            b0 = *reinterpret_cast<uint32_t*>(&lo);
-            b1 = *reinterpret_cast<uint32_t*>(&hi);
-        } else {
-            b0 = 0u;
-            b1 = 0u;
-        }
-    }
-};
-
-// acc[i][nt] (m16 x n8 C fragments) += W_i[rows, groups g0..g1) x B, for NTILE weight
-// tiles whose rows g and g+8 (g = lane/4) start at rp[i][0], rp[i][1] (nibble rows)
-// and sp[i][0], sp[i][1] (scale rows).
-template <int NTILE, int NT, class BL>
-__device__ __forceinline__ void kloop(const uint8_t* const (&rp)[NTILE][2], const uint8_t* const (&sp)[NTILE][2],
-                                      int g0, int g1, const BL& bl, float (&acc)[NTILE][NT][4]) {
+// One stage: acc[i][nt] += W_i[rows of this lane, groups G0..G0+ng) x B.
+// srow[i][r]: shared-memory row (within the stage) of tile i, fragment row r (g or g+8).
+// sc[gl][i][r]: the 4 scale bytes of group gl for that row (prefetched).
+template <int NTILE, int NT>
+__device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow)[NTILE][2],
+                                          const uint32_t (&sc)[2][NTILE][2], int ng, const SmemB<NT>& bl,
+                                          float (&acc)[NTILE][NT][4]) {
     const int q = threadIdx.x & 3;
-    uint4 wcur[NTILE][2], wnxt[NTILE][2];
-    uint32_t scur[NTILE][2], snxt[NTILE][2];
-    if (g0 < g1) {
+#pragma unroll
+    for (int gl = 0; gl < 2; ++gl) {
+        if (gl >= ng) break;
+        uint4 wv[NTILE][2];
 #pragma unroll
         for (int i = 0; i < NTILE; ++i)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                wcur[i][r] = ld_weights(rp[i][r] + (size_t)g0 * 64 + q * 16);
-                scur[i][r] = ld_u32(sp[i][r] + (size_t)g0 * 4);
+                const int row = srow[i][r];
+                const int chunk = (gl * 4 + q) ^ (row & 7);
+                wv[i][r] = *reinterpret_cast<const uint4*>(stage + row * kSliceBytes + chunk * 16);
             }
-    }
-    for (int G = g0; G < g1; ++G) {
-        if (G + 1 < g1) {
+        float scf[NTILE][2][4];
 #pragma unroll
-            for (int i = 0; i < NTILE; ++i)
+        for (int i = 0; i < NTILE; ++i)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    wnxt[i][r] = ld_weights(rp[i][r] + (size_t)(G + 1) * 64 + q * 16);
-                    snxt[i][r] = ld_u32(sp[i][r] + (size_t)(G + 1) * 4);
-                }
-        }
+            for (int r = 0; r < 2; ++r) e8m0x4_to_f32(sc[gl][i][r], scf[i][r]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t af[NTILE][2][4];
 #pragma unroll
             for (int i = 0; i < NTILE; ++i)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(word_of(wcur[i][r], j), af[i][r]);
+                for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(word_of(wv[i][r], j), af[i][r]);
+            uint4 bv[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) bv[nt] = bl.load(nt, gl * 256 + 64 * j + 16 * q);
             float d[NTILE][NT][4];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    uint32_t b0, b1;
-                    bl.load(nt, G * 128 + 32 * j + 8 * q + 4 * t, b0, b1);
-#pragma unroll
-                    for (int i = 0; i < NTILE; ++i) {
-                        if (t == 0)
-                            mma_f16(d[i][nt], af[i][0][0], af[i][1][0], af[i][0][1], af[i][1][1], b0, b1, 0.f, 0.f,
-                                    0.f, 0.f);
-                        else
-                            mma_f16(d[i][nt], af[i][0][2], af[i][1][2], af[i][0][3], af[i][1][3], b0, b1,
-                                    d[i][nt][0], d[i][nt][1], d[i][nt][2], d[i][nt][3]);
-                    }
+                for (int i = 0; i < NTILE; ++i) {
+                    mma_f16(d[i][nt], af[i][0][0], af[i][1][0], af[i][0][1], af[i][1][1], bv[nt].x, bv[nt].y, 0.f,
+                            0.f, 0.f, 0.f);
+                    mma_f16(d[i][nt], af[i][0][2], af[i][1][2], af[i][0][3], af[i][1][3], bv[nt].z, bv[nt].w,
+                            d[i][nt][0], d[i][nt][1], d[i][nt][2], d[i][nt][3]);
                 }
-            }
 #pragma unroll
             for (int i = 0; i < NTILE; ++i) {
-                const float s0 = e8m0_to_f32((scur[i][0] >> (8 * j)) & 0xffu);
-                const float s1 = e8m0_to_f32((scur[i][1] >> (8 * j)) & 0xffu);
+                const float s0 = scf[i][0][j];
+                const float s1 = scf[i][1][j];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     acc[i][nt][0] = fmaf(s0, d[i][nt][0], acc[i][nt][0]);
@@ -184,217 +311,390 @@ __device__ __forceinline__ void kloop(const uint8_t* const (&rp)[NTILE][2], cons
                 }
             }
         }
-        if (G + 1 < g1) {
-#pragma unroll
-            for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    wcur[i][r] = wnxt[i][r];
-                    scur[i][r] = snxt[i][r];
-                }
-        }
     }
 }
 
-struct Smem {
+struct alignas(16) SmemHead {
+    uint64_t full[64];
+    uint64_t empty[64];
+    int seq[64];  // global stage number last issued into each slot
     int list[kMaxE];
     int D;
-    float red[kWarps][2][4][4][32];
+    int abort;
 };
 
-// Sums the four warps' fragments in warp order into acc of warp 0.
-template <int NT>
-__device__ __forceinline__ void reduce_warps(Smem& sm, float (&acc)[2][NT][4]) {
+// Task t of this CTA: expert list[t / tiles], rows (t % tiles) * 64.
+struct TaskInfo {
+    int e, rt, cnt, off, phys;
+    bool valid;
+};
+
+__device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& hd, int task, int tiles) {
+    TaskInfo ti;
+    ti.e = hd.list[task / tiles];
+    ti.rt = task % tiles;
+    ti.cnt = __ldg(a.counts + ti.e);
+    ti.off = __ldg(a.offsets + ti.e);
+    ti.phys = __ldg(a.phys_ids + __ldg(a.entries + ti.off));
+    ti.valid = ti.phys >= 0 && ti.phys < a.n_phys;
+    return ti;
+}
+
+template <int P, int NT>
+__global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo, int hi, int sel) {
+    using C = Cfg<P>;
+    using L = Layout<P, NT>;
+    constexpr int NTILE = C::kNTile;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    SmemHead& hd = *reinterpret_cast<SmemHead*>(stages + L::kStages * L::kStageBytes);
+    float* red = reinterpret_cast<float*>(&hd + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sm.red[warp][i][nt][c][lane] = acc[i][nt][c];
-    __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float s = sm.red[0][i][nt][c][lane];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) s += sm.red[w][i][nt][c][lane];
-                    acc[i][nt][c] = s;
-                }
-    }
-    __syncthreads();
-}
-
-// Phase 0: h[pick][r] = SiLU(gate_r . x) * (up_r . x) for a 16-row tile.
-template <int NT>
-__device__ void gate_up_tile(const FfnArgs& a, Smem& sm, const uint8_t* blob, bool valid, int r0, int off,
-                             int tokbase, int ncols) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
     const int H = a.H, I = a.I;
-    float acc[2][NT][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
-    if (valid) {
-        const size_t nrow = (size_t)H / 2, srow = (size_t)H / 32;
-        const uint8_t* nb = blob;
-        const uint8_t* sb = blob + a.w13s;
-        const uint8_t* rp[2][2] = {{nb + (size_t)(r0 + g) * nrow, nb + (size_t)(r0 + g + 8) * nrow},
-                                   {nb + (size_t)(I + r0 + g) * nrow, nb + (size_t)(I + r0 + g + 8) * nrow}};
-        const uint8_t* sp[2][2] = {{sb + (size_t)(r0 + g) * srow, sb + (size_t)(r0 + g + 8) * srow},
-                                   {sb + (size_t)(I + r0 + g) * srow, sb + (size_t)(I + r0 + g + 8) * srow}};
-        X16Loader<NT> bl;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int n = nt * 8 + g;
-            if (n < ncols) {
-                const int pick = __ldg(a.entries + off + tokbase + n);
-                bl.col[nt] = a.x16 + (size_t)(pick / a.k) * H;
-            } else {
-                bl.col[nt] = nullptr;
-            }
-        }
-        const int ng = H / 128;
-        kloop<2, NT>(rp, sp, warp * ng / kWarps, (warp + 1) * ng / kWarps, bl, acc);
-    }
-    reduce_warps<NT>(sm, acc);
-    if (warp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int col = nt * 8 + 2 * q + (c & 1);
-                if (col < ncols) {
-                    const int pick = __ldg(a.entries + off + tokbase + col);
-                    const int tok = pick / a.k;
-                    const float sc = pow2i(__ldg(a.xexp + tok));
-                    const float gv = acc[0][nt][c] * sc;
-                    const float uv = acc[1][nt][c] * sc;
-                    const float hv = gv / (1.0f + expf(-gv)) * uv;
-                    const int row = r0 + g + ((c >> 1) << 3);
-                    a.h[(size_t)pick * I + row] = hv;
-                    atomicMax(a.hamax + pick, __float_as_uint(fabsf(hv)));
-                }
-            }
-    }
-}
+    const int K = P == 0 ? H : I;
+    const int ngroups = K / 128;
+    const int nst = (ngroups + 1) / 2;
+    const int tiles = (P == 0 ? I : H) / C::kTaskRows;
+    const __half* act = P == 0 ? a.x16 : a.h16;  // prescaled f16 activations
+    const int act_len = K;
 
-// Phase 1: y[pick][r] = W2_r . h[pick] for a 32-row tile.
-template <int NT>
-__device__ void down_tile(const FfnArgs& a, Smem& sm, const uint8_t* blob, bool valid, int r0, int off, int tokbase,
-                          int ncols) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    const int H = a.H, I = a.I;
-    float acc[2][NT][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
-    if (valid) {
-        const size_t nrow = (size_t)I / 2, srow = (size_t)I / 32;
-        const uint8_t* nb = blob + a.w2n;
-        const uint8_t* sb = blob + a.w2s;
-        const uint8_t* rp[2][2] = {{nb + (size_t)(r0 + g) * nrow, nb + (size_t)(r0 + g + 8) * nrow},
-                                   {nb + (size_t)(r0 + 16 + g) * nrow, nb + (size_t)(r0 + 24 + g) * nrow}};
-        const uint8_t* sp[2][2] = {{sb + (size_t)(r0 + g) * srow, sb + (size_t)(r0 + g + 8) * srow},
-                                   {sb + (size_t)(r0 + 16 + g) * srow, sb + (size_t)(r0 + 24 + g) * srow}};
-        HLoader<NT> bl;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int n = nt * 8 + g;
-            if (n < ncols) {
-                const int pick = __ldg(a.entries + off + tokbase + n);
-                bl.col[nt] = a.h + (size_t)pick * I;
-                bl.scale[nt] = pow2i(-prescale_exp(__uint_as_float(__ldcg(a.hamax + pick))));
-            } else {
-                bl.col[nt] = nullptr;
-                bl.scale[nt] = 0.f;
-            }
-        }
-        const int ng = I / 128;
-        kloop<2, NT>(rp, sp, warp * ng / kWarps, (warp + 1) * ng / kWarps, bl, acc);
-    }
-    reduce_warps<NT>(sm, acc);
+    // active experts in this launch's token-count range and placement class, ascending
     if (warp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int col = nt * 8 + 2 * q + (c & 1);
-                if (col < ncols) {
-                    const int pick = __ldg(a.entries + off + tokbase + col);
-                    const float sc = pow2i(prescale_exp(__uint_as_float(__ldcg(a.hamax + pick))));
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int row = r0 + 16 * i + g + ((c >> 1) << 3);
-                        a.y[(size_t)pick * H + row] = acc[i][nt][c] * sc;
-                    }
-                }
-            }
-    }
-}
-
-// One kernel per (phase, token-tile width NT): it serves the experts whose token
-// count lies in (lo, hi]; wider buckets are walked in groups of 32 tokens.
-template <int PHASE, int NT>
-__global__ void __launch_bounds__(kThreads) ffn_decode_kernel(FfnArgs a, int lo, int hi) {
-    __shared__ Smem sm;
-    // active experts in this kernel's count range, ascending
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
         int cnt = 0;
         for (int base = 0; base < a.E; base += 32) {
             const int e = base + lane;
-            const int c = (e < a.E) ? __ldg(a.counts + e) : 0;
-            const bool act = c > lo && c <= hi;
-            const unsigned m = __ballot_sync(0xffffffffu, act);
-            if (act) sm.list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
+            bool act_e = false;
+            if (e < a.E) {
+                const int c = __ldg(a.counts + e);
+                act_e = c > lo && c <= hi;
+                if (act_e && sel != 0) {
+                    const bool hot = __ldg(a.loc + e) < a.n_hot;
+                    act_e = (sel == 1) ? hot : !hot;
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, act_e);
+            if (act_e) hd.list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
             cnt += __popc(m);
         }
-        if (lane == 0) sm.D = cnt;
+        if (lane == 0) {
+            hd.D = cnt;
+            hd.abort = 0;
+            for (int s = 0; s < L::kStages; ++s) {
+                mbar_init(&hd.full[s], 1);
+                mbar_init(&hd.empty[s], C::kRT);
+                hd.seq[s] = -1;
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
     }
     __syncthreads();
-    const int tiles = PHASE == 0 ? a.I / 16 : a.H / 32;
-    const int ntask = sm.D * tiles;
-    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
-        const int e = sm.list[task / tiles];
-        const int rt = task % tiles;
-        const int cnt = __ldg(a.counts + e);
-        const int off = __ldg(a.offsets + e);
-        const int phys = __ldg(a.phys_ids + __ldg(a.entries + off));
-        const bool valid = phys >= 0 && phys < a.n_phys;
-        if (!valid && rt == 0 && threadIdx.x == 0) set_status(a.status, MOE_ERR_BAD_EXPERT);
-        const uint8_t* blob = valid ? a.ptr[phys] : nullptr;
-        for (int tb = 0; tb < cnt; tb += 8 * NT) {
-            const int ncols = min(8 * NT, cnt - tb);
-            if (PHASE == 0) gate_up_tile<NT>(a, sm, blob, valid, rt * 16, off, tb, ncols);
-            else down_tile<NT>(a, sm, blob, valid, rt * 32, off, tb, ncols);
+    const int ntask = hd.D * tiles;
+    volatile int* abort = &hd.abort;
+
+    if (warp == kConsumers) {
+        // ---------------- producer (whole warp) ----------------
+        int slot = 0;
+        unsigned phase = 0;
+        int gstage = 0;  // global stage number in this CTA's stream
+        bool ok = true;
+        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+            const TaskInfo ti = task_info(a, hd, task, tiles);
+            if (!ti.valid) continue;
+            const CUtensorMap* map = P == 0 ? &a.tmaps[ti.phys].w13n : &a.tmaps[ti.phys].w2n;
+            // descriptors live in global memory and a layer's table may reuse the address
+            // of a destroyed one: acquire the current contents for the async proxy
+            if (lane == 0) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+            const int r0 = ti.rt * C::kTaskRows;
+            for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
+                const int ncols = min(8 * NT, ti.cnt - tb);
+                // this lane's activation row (one column of the tile), if any
+                const __half* arow = nullptr;
+                if (lane < ncols) {
+                    const int pick = __ldg(a.entries + ti.off + tb + lane);
+                    arow = act + (size_t)(P == 0 ? pick / a.k : pick) * act_len;
+                }
+                for (int s = 0; s < nst; ++s) {
+                    bool got = true;
+                    if (lane == 0)
+                        got = mbar_wait(&hd.empty[slot], phase ^ 1u, abort, a.status, a.diag, 2, slot, s,
+                                        (task << 8) | ncols);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    const int kelems = min(256, K - s * 256);  // 256, or 128 at an odd tail
+                    const unsigned abytes = (unsigned)kelems * 2u;
+                    uint8_t* dst = stages + slot * L::kStageBytes;
+                    if (lane == 0) {
+                        *reinterpret_cast<volatile int*>(&hd.seq[slot]) = gstage;
+                        mbar_arrive_expect_tx(&hd.full[slot], (unsigned)L::kWBytes + abytes * (unsigned)ncols);
+                        if (P == 0) {
+                            tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+                            tma_load_2d(dst + C::kTaskRows * kSliceBytes, map, s * kSliceBytes, I + r0,
+                                        &hd.full[slot]);
+                        } else {
+                            tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+                        }
+                    }
+                    __syncwarp();
+                    if (arow)
+                        bulk_load(dst + L::kWBytes + lane * kActStride, arow + (size_t)s * 256, abytes,
+                                  &hd.full[slot]);
+                    ++gstage;
+                    if (++slot == L::kStages) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
         }
+        // drain: every issued copy has landed before the CTA may exit
+        if (lane == 0) {
+            for (int s = 0; s < L::kStages; ++s) {
+                // slot s was last filled in the current phase if it lies before the next
+                // slot to fill, else in the previous one (or never)
+                const unsigned par = (s < slot) ? phase : (phase ^ 1u);
+                mbar_drain(&hd.full[s], par);
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int rt = warp % C::kRT;  // row tile
+    const int ks = warp / C::kRT;  // reduction split
+    const int g = lane >> 2, q = lane & 3;
+    const int pg = perm8(g);
+    const size_t srs = (size_t)K / 32;  // scale bytes per row
+    int slot = 0;
+    unsigned phase = 0;
+    int gstage = 0;
+    bool done = false;
+    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
+        const TaskInfo ti = task_info(a, hd, task, tiles);
+        const int r0 = ti.rt * C::kTaskRows;
+        if (!ti.valid) {
+            // zero outputs for an expert whose physical id is out of range
+            if (ti.rt == 0 && threadIdx.x == 0) set_status(a.status, MOE_ERR_BAD_EXPERT);
+            for (int c = threadIdx.x; c < ti.cnt * C::kTaskRows; c += 32 * kConsumers) {
+                const int pick = __ldg(a.entries + ti.off + c / C::kTaskRows);
+                const int row = r0 + c % C::kTaskRows;
+                if (P == 0) a.h[(size_t)pick * I + row] = 0.f;
+                else a.y[(size_t)pick * H + row] = 0.f;
+            }
+            continue;
+        }
+        const uint8_t* blob = a.ptr[ti.phys];
+        const uint8_t* sb = blob + (P == 0 ? a.w13s : a.w2s);
+        // rows of this lane: shared-memory rows within a stage and global rows
+        int srow[NTILE][2];
+        int grow[NTILE][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int lr = 16 * rt + pg + 8 * r;  // local output row
+            srow[0][r] = lr;
+            grow[0][r] = r0 + lr;
+            if (NTILE == 2) {
+                srow[NTILE - 1][r] = C::kTaskRows + lr;
+                grow[NTILE - 1][r] = I + r0 + lr;
+            }
+        }
+        // warm L1 with the scale lines of this warp's rows in the next task
+        {
+            const int nxt = task + gridDim.x;
+            if (nxt < ntask && q == 0) {
+                const TaskInfo tn = task_info(a, hd, nxt, tiles);
+                if (tn.valid) {
+                    const uint8_t* nsb = a.ptr[tn.phys] + (P == 0 ? a.w13s : a.w2s);
+                    const int nr0 = tn.rt * C::kTaskRows;
+#pragma unroll
+                    for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            for (size_t o = 0; o < srs; o += 128)
+                                prefetch_l1(nsb + (size_t)(grow[i][r] - r0 + nr0) * srs + o);
+                }
+            }
+        }
+        for (int tb = 0; tb < ti.cnt; tb += 8 * NT) {
+            const int ncols = min(8 * NT, ti.cnt - tb);
+            float acc[NTILE][NT][4];
+#pragma unroll
+            for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
+            // scale words of this warp's first stage, then one own stage ahead
+            uint32_t sc[2][NTILE][2], scn[2][NTILE][2];
+            auto load_sc = [&](int s, uint32_t(&dst)[2][NTILE][2]) {
+                const int G0 = 2 * s;
+                const int ng = min(2, ngroups - G0);
+#pragma unroll
+                for (int gl = 0; gl < 2; ++gl)
+#pragma unroll
+                    for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            dst[gl][i][r] = (gl < ng) ? ld_u32(sb + (size_t)grow[i][r] * srs + (size_t)(G0 + gl) * 4)
+                                                      : 0u;
+            };
+            if (ks < nst) load_sc(ks, sc);
+            bool ok = true;
+            for (int s = 0; s < nst; ++s) {
+                if ((s % C::kKS) == ks) {
+                    if (s + C::kKS < nst) load_sc(s + C::kKS, scn);
+                    if (!seq_wait(&hd.seq[slot], gstage, abort, a.status, a.diag, slot) ||
+                        !mbar_wait(&hd.full[slot], phase, abort, a.status, a.diag, 1, slot, s, (task << 8) | ncols)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* stage = stages + slot * L::kStageBytes;
+                    SmemB<NT> bl;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int n = nt * 8 + g;
+                        bl.col[nt] = n < ncols ? stage + L::kWBytes + n * kActStride : nullptr;
+                    }
+                    stage_mma<NTILE, NT>(stage, srow, sc, min(2, ngroups - 2 * s), bl, acc);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&hd.empty[slot]);
+#pragma unroll
+                    for (int gl = 0; gl < 2; ++gl)
+#pragma unroll
+                        for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) sc[gl][i][r] = scn[gl][i][r];
+                }
+                ++gstage;
+                if (++slot == L::kStages) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            // partial sums of the K-splits meet in shared memory (fixed order)
+            constexpr int kFrag = NTILE * NT * 4 * 32;
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
+            if (ks > 0) {
+                float* dst = red + (size_t)((ks - 1) * C::kRT + rt) * kFrag;
+#pragma unroll
+                for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[((i * NT + nt) * 4 + c) * 32 + lane] = acc[i][nt][c];
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
+            if (ks == 0 && ok) {
+#pragma unroll
+                for (int i = 0; i < NTILE; ++i)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int k2 = 1; k2 < C::kKS; ++k2)
+                                acc[i][nt][c] += red[(size_t)((k2 - 1) * C::kRT + rt) * kFrag +
+                                                     ((i * NT + nt) * 4 + c) * 32 + lane];
+                // epilogue
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = nt * 8 + 2 * q + (c & 1);
+                        if (col >= ncols) continue;
+                        const int pick = __ldg(a.entries + ti.off + tb + col);
+                        const int orow = r0 + 16 * rt + pg + ((c >> 1) << 3);  // output row
+                        if constexpr (P == 0) {
+                            const float sx = pow2i(__ldg(a.xexp + pick / a.k));
+                            const float gv = acc[0][nt][c] * sx;
+                            const float uv = acc[NTILE - 1][nt][c] * sx;
+                            const float hv = gv / (1.0f + expf(-gv)) * uv;
+                            a.h[(size_t)pick * I + orow] = hv;
+                            atomicMax(a.hamax + pick, __float_as_uint(fabsf(hv)));
+                        } else {
+                            a.y[(size_t)pick * H + orow] = acc[0][nt][c] * pow2i(__ldg(a.hexp + pick));
+                        }
+                    }
+            }
+            // all consumer warps take the same decision to stop (a timed-out wait anywhere)
+            unsigned stop;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, 1, %2, p;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(stop)
+                : "r"((unsigned)(!ok || *abort)), "n"(32 * kConsumers)
+                : "memory");
+            if (stop) {
+                done = true;
+                break;
+            }
+        }
+        if (done) break;
     }
 }
 
-// One warp per token: per-token power-of-two prescale, f16 copy of x, and the
+// One CTA per pick of the selected class: per-pick power-of-two prescale of h
+// (from the amax the gate/up phase accumulated) and its f16 copy for the down
+// projection.
+__global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h, const unsigned* __restrict__ hamax,
+                                                    const int32_t* __restrict__ phys_ids, int n_hot, int n_phys,
+                                                    int sel, int I, __half* __restrict__ h16,
+                                                    int32_t* __restrict__ hexp) {
+    const int p = blockIdx.x;
+    const int ph = __ldg(phys_ids + p);
+    const bool hot = ph >= 0 && ph < n_hot;
+    const bool valid = ph >= 0 && ph < n_phys;
+    if (sel == 1 && !hot) return;
+    if (sel == 2 && (hot || !valid)) return;
+    const int e = prescale_exp(__uint_as_float(__ldcg(hamax + p)));
+    const float sc = pow2i(-e);
+    const float4* src = reinterpret_cast<const float4*>(h + (size_t)p * I);
+    uint2* dst = reinterpret_cast<uint2*>(h16 + (size_t)p * I);
+    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
+        float4 v = __ldcg(src + c);
+        __half2 lo = __floats2half2_rn(v.x * sc, v.y * sc);
+        __half2 hi = __floats2half2_rn(v.z * sc, v.w * sc);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        dst[c] = o;
+    }
+    if (threadIdx.x == 0) hexp[p] = e;
+}
+
+// One CTA per token: per-token power-of-two prescale, f16 copy of x, and the
 // per-pick amax slots of h cleared.
 __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int k,
                                                     __half* __restrict__ x16, int32_t* __restrict__ xexp,
                                                     unsigned* __restrict__ hamax) {
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (t >= T) return;
+    __shared__ float wmax[8];
+    const int t = blockIdx.x;
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * H);
+    const int nch = H / 8;
+    constexpr int kPer = 4;  // up to 4 chunks of 8 per thread kept in registers (H <= 8192)
+    uint4 v[kPer];
     float amax = 0.f;
-    for (int c = lane; c < H / 8; c += 32) {
-        uint4 v = __ldg(row + c);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int c = threadIdx.x + u * 256;
+        if (c < nch) {
+            v[u] = __ldg(row + c);
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 f = __bfloat1622float2(p[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) {
+        uint4 w = __ldg(row + c);
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float2 f = __bfloat1622float2(p[i]);
@@ -403,12 +703,15 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
     const int p = prescale_exp(amax);
     const float s = pow2i(-p);
-    uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * H);
-    for (int c = lane; c < H / 8; c += 32) {
-        uint4 v = __ldg(row + c);
-        const __nv_bfloat162* pi = reinterpret_cast<const __nv_bfloat162*>(&v);
+    auto conv = [&](const uint4& in) {
+        const __nv_bfloat162* pi = reinterpret_cast<const __nv_bfloat162*>(&in);
         uint4 o;
         __half2* po = reinterpret_cast<__half2*>(&o);
 #pragma unroll
@@ -416,10 +719,16 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
             float2 f = __bfloat1622float2(pi[i]);
             po[i] = __floats2half2_rn(f.x * s, f.y * s);
         }
-        out[c] = o;
+        return o;
+    };
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int c = threadIdx.x + u * 256;
+        if (c < nch) out[c] = conv(v[u]);
     }
-    if (lane == 0) xexp[t] = p;
-    if (lane < k) hamax[(size_t)t * k + lane] = 0u;
+    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) out[c] = conv(__ldg(row + c));
+    if (threadIdx.x == 0) xexp[t] = p;
+    if (threadIdx.x < k) hamax[(size_t)t * k + threadIdx.x] = 0u;
 }
 
 __global__ void debug_e2m1_kernel(uint32_t* out) {
@@ -432,7 +741,7 @@ __global__ void debug_e2m1_kernel(uint32_t* out) {
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t x16, xexp, hamax, h, total;
+    size_t x16, xexp, hamax, h, h16, hexp, total;
 };
 
 WsLayout ws_layout(int T, int k, int H, int I) {
@@ -446,68 +755,83 @@ WsLayout ws_layout(int T, int k, int H, int I) {
     o = align256(o + (size_t)T * k * sizeof(unsigned));
     w.h = o;
     o = align256(o + (size_t)T * k * I * sizeof(float));
+    w.h16 = o;
+    o = align256(o + (size_t)T * k * I * sizeof(__half));
+    w.hexp = o;
+    o = align256(o + (size_t)T * k * sizeof(int32_t));
     w.total = o;
     return w;
 }
 
-int occupancy(const void* fn) {
-    static const void* keys[8];
-    static int vals[8];
-    for (int i = 0; i < 8; ++i)
-        if (keys[i] == fn) return vals[i];
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = 1;
+template <int P, int NT>
+size_t smem_bytes() {
+    using C = Cfg<P>;
+    using L = Layout<P, NT>;
+    return 1024 + (size_t)L::kStages * L::kStageBytes + sizeof(SmemHead) +
+           sizeof(float) * (size_t)(C::kKS - 1) * C::kRT * C::kNTile * NT * 4 * 32;
+}
+
+template <int P, int NT>
+cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cudaStream_t st) {
+    static bool configured = false;
+    const size_t sm = smem_bytes<P, NT>();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_tma_kernel<P, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sm);
+        if (e != cudaSuccess) return e;
+        configured = true;
     }
-    for (int i = 0; i < 8; ++i)
-        if (!keys[i]) {
-            keys[i] = fn;
-            vals[i] = n;
-            break;
-        }
-    return n;
+    ffn_tma_kernel<P, NT><<<grid, kThreads, sm, st>>>(a, lo, hi, sel);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t ffn_decode_workspace(int T, int k, int H, int I) { return ws_layout(T, k, H, I).total; }
 
-cudaError_t launch_ffn_decode(FfnArgs a, void* workspace, int sm_count, cudaStream_t st) {
-    if (a.T == 0) return cudaSuccess;
+cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     const WsLayout w = ws_layout(a.T, a.k, a.H, a.I);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.x16 = reinterpret_cast<__half*>(ws + w.x16);
     a.xexp = reinterpret_cast<int32_t*>(ws + w.xexp);
     a.hamax = reinterpret_cast<unsigned*>(ws + w.hamax);
     a.h = reinterpret_cast<float*>(ws + w.h);
-    xprep_kernel<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp, a.hamax);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    a.h16 = reinterpret_cast<__half*>(ws + w.h16);
+    a.hexp = reinterpret_cast<int32_t*>(ws + w.hexp);
+    if (a.T == 0) return cudaSuccess;
+    xprep_kernel<<<a.T, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp, a.hamax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st) {
+    if (a.T == 0) return cudaSuccess;
     // token-count ranges per kernel; a bound on the largest bucket is T
-    const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
     struct Range {
         int nt, lo, hi;
     };
     const Range ranges[3] = {{1, 0, 8}, {2, 8, 16}, {4, 16, 1 << 30}};
-    for (int phase = 0; phase < 2; ++phase) {
-        for (const Range& r : ranges) {
-            if (a.T <= r.lo) break;
-            const long tasks = dmax * (phase == 0 ? a.I / 16 : a.H / 32);
-            const void* fn = nullptr;
-            if (phase == 0) fn = r.nt == 1 ? (const void*)ffn_decode_kernel<0, 1>
-                               : r.nt == 2 ? (const void*)ffn_decode_kernel<0, 2>
-                                           : (const void*)ffn_decode_kernel<0, 4>;
-            else fn = r.nt == 1 ? (const void*)ffn_decode_kernel<1, 1>
-                    : r.nt == 2 ? (const void*)ffn_decode_kernel<1, 2>
-                                : (const void*)ffn_decode_kernel<1, 4>;
-            const long cap = (long)sm_count * occupancy(fn);
-            const int grid = (int)(tasks < cap ? tasks : cap);
-            int lo = r.lo, hi = r.hi;
-            void* args[] = {&a, &lo, &hi};
-            err = cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, 0, st);
-            if (err != cudaSuccess) return err;
+    const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
+    const long tasks = dmax * ((phase == 0 ? a.I : a.H) / 32);
+    if (phase == 1) {
+        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.hamax, a.phys_ids, a.n_hot, a.n_phys, sel, a.I, a.h16,
+                                                a.hexp);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int grid = (int)(tasks < sm_count ? tasks : sm_count);
+    for (const Range& r : ranges) {
+        if (a.T <= r.lo) break;
+        cudaError_t err;
+        if (phase == 0) {
+            err = r.nt == 1 ? launch_phase<0, 1>(a, r.lo, r.hi, sel, grid, st)
+                : r.nt == 2 ? launch_phase<0, 2>(a, r.lo, r.hi, sel, grid, st)
+                            : launch_phase<0, 4>(a, r.lo, r.hi, sel, grid, st);
+        } else {
+            err = r.nt == 1 ? launch_phase<1, 1>(a, r.lo, r.hi, sel, grid, st)
+                : r.nt == 2 ? launch_phase<1, 2>(a, r.lo, r.hi, sel, grid, st)
+                            : launch_phase<1, 4>(a, r.lo, r.hi, sel, grid, st);
         }
+        if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }

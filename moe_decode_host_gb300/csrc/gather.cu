@@ -6,9 +6,10 @@
 // ones among them into their scratch slots.  Section 3 measured that copy at
 // 2.60 ms of a 10.49 ms step, so the copy is the host-link-bound part of the path.
 //
-// Every CTA rebuilds the (tiny) set of picked cold slots in shared memory, then
-// the grid streams the listed host blobs into their slots with 16-byte zero-copy
-// loads, several in flight per thread to cover the link latency.
+// A one-CTA remap kernel marks the picked cold slots in shared memory and lists
+// them in ascending order with warp ballots; a copy kernel then streams the listed
+// host blobs into their slots with 16-byte zero-copy loads, several in flight per
+// thread to cover the link latency.
 #include "internal.cuh"
 
 namespace moe {
@@ -26,28 +27,31 @@ __device__ __forceinline__ uint4 ld_host_v4(const uint4* p) {
     return v;
 }
 
-// Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA.
+// Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA,
+// kUnroll loads in flight per thread including the ragged last round.
 __device__ __forceinline__ void copy_range(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t c0,
                                            size_t c1) {
     const size_t stride = (size_t)kGatherThreads * kUnroll;
-    size_t base = c0 + threadIdx.x;
-    for (; base + (size_t)kGatherThreads * (kUnroll - 1) < c1; base += stride) {
+    for (size_t base = c0 + threadIdx.x; base < c1; base += stride) {
         uint4 v[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_host_v4(src + base + (size_t)u * kGatherThreads);
+        for (int u = 0; u < kUnroll; ++u) {
+            const size_t i = base + (size_t)u * kGatherThreads;
+            if (i < c1) v[u] = ld_host_v4(src + i);
+        }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) dst[base + (size_t)u * kGatherThreads] = v[u];
+        for (int u = 0; u < kUnroll; ++u) {
+            const size_t i = base + (size_t)u * kGatherThreads;
+            if (i < c1) dst[i] = v[u];
+        }
     }
-    for (; base < c1; base += kGatherThreads) dst[base] = ld_host_v4(src + base);
 }
 
-__global__ void __launch_bounds__(kGatherThreads) cold_gather_kernel(
+// Distinct picked cold slots (ascending) and the physical id of every pick.
+__global__ void __launch_bounds__(kGatherThreads) cold_remap_kernel(
     const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
-    const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes,
     int32_t* __restrict__ phys, int32_t* __restrict__ cold_list, int32_t* __restrict__ n_picked, int* status) {
     __shared__ unsigned char flag[kMaxColdSlots];
-    __shared__ int32_t list[kMaxColdSlots];
-    __shared__ int s_cnt;
     for (int c = threadIdx.x; c < n_cold; c += blockDim.x) flag[c] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n_picks; i += blockDim.x) {
@@ -56,10 +60,10 @@ __global__ void __launch_bounds__(kGatherThreads) cold_gather_kernel(
         if (id >= 0 && id < E) {
             p = __ldg(loc + id);
             if (p >= n_hot) flag[p - n_hot] = 1;
-        } else if (blockIdx.x == 0) {
+        } else {
             set_status(status, MOE_ERR_BAD_EXPERT);
         }
-        if (blockIdx.x == 0) phys[i] = p;
+        phys[i] = p;
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -69,25 +73,28 @@ __global__ void __launch_bounds__(kGatherThreads) cold_gather_kernel(
             int c = base + lane;
             bool f = (c < n_cold) && flag[c];
             unsigned m = __ballot_sync(0xffffffffu, f);
-            if (f) list[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+            if (f) cold_list[cnt + __popc(m & ((1u << lane) - 1u))] = c;
             cnt += __popc(m);
         }
-        if (lane == 0) s_cnt = cnt;
+        if (lane == 0) *n_picked = cnt;
     }
-    __syncthreads();
-    const int cnt = s_cnt;
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i < cnt; i += blockDim.x) cold_list[i] = list[i];
-        if (threadIdx.x == 0) *n_picked = cnt;
-    }
-    if (cnt == 0) return;
-    // work items: each picked slot is cut into `seg` contiguous pieces
+}
+
+// Streams every listed host blob into its scratch slot; each picked slot is cut
+// into `seg` contiguous pieces spread over the grid.
+__global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(const int32_t* __restrict__ cold_list,
+                                                                   const int32_t* __restrict__ n_picked,
+                                                                   const uint8_t* const* __restrict__ cold_src,
+                                                                   uint8_t* __restrict__ slot_base,
+                                                                   size_t blob_bytes) {
+    const int cnt = *n_picked;
+    if (cnt <= 0) return;
     const size_t chunks = blob_bytes / 16;
     int seg = (int)gridDim.x / cnt;
     if (seg < 1) seg = 1;
     const int items = cnt * seg;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
-        const int c = list[it / seg];
+        const int c = __ldg(cold_list + it / seg);
         const int s = it % seg;
         const size_t c0 = chunks * (size_t)s / (size_t)seg;
         const size_t c1 = chunks * (size_t)(s + 1) / (size_t)seg;
@@ -106,13 +113,17 @@ __global__ void __launch_bounds__(kGatherThreads) link_probe_kernel(const uint8_
 
 }  // namespace
 
-cudaError_t launch_cold_gather(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                               const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes,
-                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, int ctas,
-                               cudaStream_t st) {
+cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                              int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st) {
     if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
-    cold_gather_kernel<<<ctas, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, cold_src, slot_base,
-                                                        blob_bytes, phys, cold_list, n_picked, status);
+    cold_remap_kernel<<<1, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, phys, cold_list, n_picked,
+                                                    status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cold_copy(const int32_t* cold_list, const int32_t* n_picked, const uint8_t* const* cold_src,
+                             uint8_t* slot_base, size_t blob_bytes, int ctas, cudaStream_t st) {
+    cold_copy_kernel<<<ctas, kGatherThreads, 0, st>>>(cold_list, n_picked, cold_src, slot_base, blob_bytes);
     return cudaGetLastError();
 }
 

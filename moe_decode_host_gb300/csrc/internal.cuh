@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -41,15 +42,26 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          int32_t* counts, int32_t* offsets, int32_t* entries, int32_t* window, int* status,
                          cudaStream_t st);
 
-cudaError_t launch_cold_gather(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                               const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes,
-                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, int ctas,
-                               cudaStream_t st);
+// Remap (phys ids, picked cold slots) on the caller's stream.
+cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                              int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st);
+// Byte copy of the listed slots (reads cold_list / n_picked written by the remap).
+cudaError_t launch_cold_copy(const int32_t* cold_list, const int32_t* n_picked, const uint8_t* const* cold_src,
+                             uint8_t* slot_base, size_t blob_bytes, int ctas, cudaStream_t st);
 
 cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
 
+// 2D TMA descriptors of the two nibble planes of the blob at one physical id.
+struct TmapPair {
+    CUtensorMap w13n;  // [2I rows][H/2 bytes], box 128 B x 32 rows, 128-byte swizzle
+    CUtensorMap w2n;   // [H rows][I/2 bytes], same box
+};
+
 struct FfnArgs {
     const uint8_t* const* ptr;  // phys id -> blob base (device)
+    const TmapPair* tmaps;      // phys id -> descriptors (device)
+    const int32_t* loc;         // placement map, for the hot/cold split
+    int n_hot;
     int n_phys;
     const int32_t* phys_ids;  // [T*k]
     const int32_t* counts;    // [E]
@@ -61,13 +73,20 @@ struct FfnArgs {
     int32_t* xexp;           // workspace [T]
     unsigned* hamax;         // workspace [T*k]
     float* h;                // workspace [T*k][I]
+    __half* h16;             // workspace [T*k][I], prescaled copy of h
+    int32_t* hexp;           // workspace [T*k]
     float* y;                // [T*k][H]
     int* status;
+    int* diag;               // [16] where the first timed-out wait gave up
     size_t w13s, w2n, w2s;   // plane offsets in a blob
 };
 
 size_t ffn_decode_workspace(int T, int k, int H, int I);
-cudaError_t launch_ffn_decode(FfnArgs a, void* workspace, int sm_count, cudaStream_t st);
+// Points the workspace fields of `a` at `workspace` and launches the activation prep.
+cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st);
+// One phase (0: gate/up -> h, 1: down -> y) over the experts selected by sel
+// (0: all, 1: placed in HBM, 2: placed in cold slots).
+cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st);
 
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
                            cudaStream_t st);

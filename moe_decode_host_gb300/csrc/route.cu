@@ -13,6 +13,7 @@ namespace {
 
 constexpr int kMaxV = 32;  // logits per lane: E <= 1024
 
+
 // One warp routes one token.  Lane l holds experts l, l+32, ...
 template <int V>
 __device__ __forceinline__ void route_token(const float* __restrict__ lrow, int E, int k, int renorm,
@@ -132,9 +133,11 @@ __device__ __forceinline__ void bucket_expert(const int32_t* ids, int n, int e, 
     }
 }
 
-// Small batches: one CTA routes every token and buckets from shared memory.
+// Small batches: one CTA routes every token, then buckets from shared memory with
+// one thread per expert (count, block-wide exclusive scan, ordered placement).
 constexpr int kSmallThreads = 512;
 constexpr int kSmallMaxPicks = 2048;
+constexpr int kMaxE = 1024;
 
 __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const float* __restrict__ logits, int T, int E,
                                                                     int k, int renorm, int32_t* ids, float* w,
@@ -142,13 +145,53 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const float*
                                                                     int32_t* entries, int32_t* window,
                                                                     int* status) {
     __shared__ int32_t sids[kSmallMaxPicks];
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    __shared__ int32_t scnt[kMaxE];
+    __shared__ int32_t wsum[kSmallThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     for (int t = warp; t < T; t += nwarps)
         route_any(logits + (size_t)t * E, E, k, renorm, ids + (size_t)t * k, w + (size_t)t * k, sids + t * k,
                   status);
     __syncthreads();
-    for (int e = warp; e < E; e += nwarps) bucket_expert(sids, T * k, e, E, counts, offsets, entries, window);
-    if (T == 0 && threadIdx.x == 0) offsets[E] = 0;
+    const int n = T * k;
+    // counts: one thread per expert scans the pick list (a broadcast read per step)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+        for (int i = 0; i < n; ++i) c += (sids[i] == e);
+        scnt[e] = c;
+        counts[e] = c;
+        if (c > 0 && window) atomicAdd(window + e, c);
+    }
+    __syncthreads();
+    // exclusive scan of scnt over E (E <= 1024): each thread owns up to 2 entries
+    const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+    const int v0 = e0 < E ? scnt[e0] : 0, v1 = e1 < E ? scnt[e1] : 0;
+    int incl = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w2 = 0; w2 < warp; ++w2) base += wsum[w2];
+    const int ex0 = base + incl - v0 - v1;
+    __syncthreads();
+    if (e0 < E) scnt[e0] = ex0;
+    if (e1 < E) scnt[e1] = ex0 + v0;
+    if (threadIdx.x == 0) offsets[E] = n;
+    __syncthreads();
+    // placement: picks of expert e in ascending pick order
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int start = scnt[e];
+        offsets[e] = start;
+        const int end = (e + 1 < E) ? scnt[e + 1] : n;
+        if (end > start) {
+            int pos = start;
+            for (int i = 0; i < n && pos < end; ++i)
+                if (sids[i] == e) entries[pos++] = i;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,

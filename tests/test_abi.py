@@ -19,9 +19,9 @@ def _declared_functions():
 
 @pytest.fixture(scope="module")
 def mlib():
-    from moe_decode_host_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__.build()
     import moe_decode_host_gb300 as m
 
     return m

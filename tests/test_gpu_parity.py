@@ -23,9 +23,9 @@ OUT_TOL = 5e-3
 def _lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from moe_decode_host_gb300 import build as b
+    import __graft_entry__
 
-    b.build()
+    __graft_entry__.build()
     oracle.build()
 
 
@@ -144,6 +144,7 @@ def _gather_check(fx, logits, T):
     m.moe_route(fx.layer, torch.from_numpy(logits).cuda(), T, buf.topk_ids, buf.topk_w, buf.counts, buf.offsets,
                 buf.entries)
     m.cold_gather(fx.layer, buf.topk_ids, T, buf.phys_ids, buf.cold_list, buf.n_cold_picked)
+    m.moe_gather_join(fx.layer)
     torch.cuda.synchronize()
     ids = buf.topk_ids.cpu().numpy()[:T]
     phys, cold = oracle.remap(ids, loc, fx.n_hot, fx.n_cold)
@@ -175,6 +176,7 @@ def test_cold_gather_bad_expert_ids():
     ids = torch.tensor([[3, 13], [-1, 16]], dtype=torch.int32, device="cuda")
     buf = m.StepBuffers(fx.layer, 2)
     m.cold_gather(fx.layer, ids, 2, buf.phys_ids, buf.cold_list, buf.n_cold_picked)
+    m.moe_gather_join(fx.layer)
     torch.cuda.synchronize()
     assert buf.phys_ids.cpu().numpy()[:4].tolist() == [3, 13, -1, -1]
     assert int(buf.n_cold_picked.item()) == 1 and int(buf.cold_list[0].item()) == 1
@@ -191,7 +193,7 @@ def _run_layer(fx, logits, x, out_fp32):
     buf = m.StepBuffers(fx.layer, T, out_fp32=out_fp32)
     m.run_step(fx.layer, buf, torch.from_numpy(logits).cuda(), x.cuda(), residency=False)
     torch.cuda.synchronize()
-    assert fx.layer.status() == 0
+    assert fx.layer.status() == 0, fx.layer.diag().tolist()
     return buf
 
 
