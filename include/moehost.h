@@ -60,6 +60,7 @@ extern "C" {
 #define MOE_ERR_TIMEOUT (-5)
 #define MOE_ERR_NOMEM (-6)
 #define MOE_ERR_INJECTED (-7)
+#define MOE_ERR_SCRATCH_TOO_SMALL (-8)
 
 /* Layer parameters.
  *  E, k        experts and picks per token ("Milo and James Try Inference
@@ -172,6 +173,26 @@ int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes);
 int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
                     const int32_t* offsets, const int32_t* entries, float* y, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/* moe_grouped_ffn for callers that cannot allocate device memory (an engine that
+ * has given all free HBM to its own pools and forbids later allocations, code
+ * running during a global-mode stream capture, embedders with their own
+ * allocator).  No counterpart in the paper: same arguments and results as
+ * moe_grouped_ffn minus the workspace, which here is a fixed array of
+ * MOE_NOALLOC_SCRATCH_BYTES inside the library's device image (every GPU that
+ * loads the library holds one copy until the process exits).  The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls on
+ * a device share the array and it keeps the previous call's contents (the FFN
+ * clears what must start at zero itself), so calls that overlap on the GPU race:
+ * order them on one stream or otherwise serialise them.
+ * Errors: MOE_ERR_SCRATCH_TOO_SMALL when T needs more than the array holds
+ * (moe_ffn_workspace_bytes(L, T) > MOE_NOALLOC_SCRATCH_BYTES; about T = 70 at
+ * H=4096, I=3072, k=6), MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int moe_grouped_ffn_noalloc(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* entries, float* y, void* stream);
 
 /* Combine ("DeepSeek-V4.1-Flash on One GB300 ...", section 4: contributions are
  * summed; the order only moves the last decimal places).  out[t] = sum over

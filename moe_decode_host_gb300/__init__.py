@@ -12,13 +12,14 @@ import ctypes
 import numpy as np
 
 from ._lib import (LIB_PATH, MOE_ERR_BAD_EXPERT, MOE_ERR_CUDA, MOE_ERR_INJECTED, MOE_ERR_INVALID_ARG,
-                   MOE_ERR_NOMEM, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT, MOE_OK, MoeError, check, lib, moe_params,
-                   ptr, stream_handle)
+                   MOE_ERR_NOMEM, MOE_ERR_NONFINITE, MOE_ERR_SCRATCH_TOO_SMALL, MOE_ERR_TIMEOUT,
+                   MOE_NOALLOC_SCRATCH_BYTES, MOE_OK, MoeError, check, lib, moe_params, ptr, stream_handle)
 
 __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_bytes", "moe_route", "cold_gather",
            "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
-           "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED"]
+           "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED", "MOE_ERR_SCRATCH_TOO_SMALL",
+           "moe_grouped_ffn_noalloc"]
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -128,6 +129,13 @@ def moe_grouped_ffn(layer: Layer, x, T, phys_ids, counts, offsets, entries, y, w
         workspace_bytes = workspace.numel() * workspace.element_size()
     check(lib.moe_grouped_ffn(layer.handle, ptr(x), T, ptr(phys_ids), ptr(counts), ptr(offsets), ptr(entries),
                               ptr(y), ptr(workspace), workspace_bytes, stream_handle(stream)), "moe_grouped_ffn")
+
+
+def moe_grouped_ffn_noalloc(layer: Layer, x, T, phys_ids, counts, offsets, entries, y, stream=None):
+    """moe_grouped_ffn with the library's static workspace (no device allocation;
+    for callers that cannot allocate)."""
+    check(lib.moe_grouped_ffn_noalloc(layer.handle, ptr(x), T, ptr(phys_ids), ptr(counts), ptr(offsets),
+                                      ptr(entries), ptr(y), stream_handle(stream)), "moe_grouped_ffn_noalloc")
 
 
 def moe_combine(y, topk_w, T, k, H, out, out_fp32=False, stream=None):

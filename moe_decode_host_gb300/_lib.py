@@ -28,6 +28,8 @@ MOE_ERR_BAD_EXPERT = -4
 MOE_ERR_TIMEOUT = -5
 MOE_ERR_NOMEM = -6
 MOE_ERR_INJECTED = -7
+MOE_ERR_SCRATCH_TOO_SMALL = -8
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20  # size of moe_grouped_ffn_noalloc's static workspace (moehost.h)
 
 
 class moe_params(ctypes.Structure):
@@ -52,6 +54,7 @@ _SIGS = {
     "moe_ffn_workspace_bytes": (_I, [_P, _I, ctypes.POINTER(_Z)]),
     "moe_grouped_ffn": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _I, _I, _I, _P, _I, _P]),
+    "moe_grouped_ffn_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "residency_update": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_layer_get_loc": (_I, [_P, _P]),
     "moe_layer_get_counts": (_I, [_P, _P]),

@@ -459,6 +459,7 @@ const char* moe_strerror(int code) {
         case MOE_ERR_TIMEOUT: return "device wait timed out";
         case MOE_ERR_NOMEM: return "out of memory";
         case MOE_ERR_INJECTED: return "injected fault (test hook)";
+        case MOE_ERR_SCRATCH_TOO_SMALL: return "batch needs more workspace than the static no-allocation array holds";
         default: return "unknown status";
     }
 }

@@ -74,7 +74,7 @@ def test_host_side_argument_checks(mlib):
     dup = (ctypes.c_int32 * 16)(*([0] + list(range(1, 15)) + [0]))
     assert lib.moe_layer_create(ctypes.byref(p), None, None, None, dup, ctypes.byref(out)) == \
         mlib.MOE_ERR_INVALID_ARG
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, -99):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -99):
         assert lib.moe_strerror(code)
 
 
