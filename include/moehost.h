@@ -237,6 +237,18 @@ int moe_get_diag(moe_layer* L, int32_t* diag_host);
 /* Text for a status code. */
 const char* moe_strerror(int code);
 
+/* Number of CTAs the cold copy kernel runs on (0 = the default, a quarter of the
+ * SMs: enough to saturate the host link on GB300).
+ * The copy shares the GPU with the FFN over HBM-resident experts. */
+int moe_layer_set_copy_ctas(moe_layer* L, int ctas);
+
+/* Copy timing: after moe_layer_profile(L, n) the next n cold_gather calls record
+ * CUDA events around their byte copy on the layer's copy stream (n = 0 stops and
+ * frees them).  moe_layer_profile_read waits for them and writes up to `max`
+ * durations in ms to host float copy_ms[] and their number to *n_out. */
+int moe_layer_profile(moe_layer* L, int max_records);
+int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out);
+
 /* Test hook for host-side fault injection: what = 1 makes the next acting
  * residency_update fail with MOE_ERR_INJECTED before any copy or map change (as a
  * failed host copy would); what = 0 clears it.  Never set in normal use. */

@@ -105,6 +105,19 @@ class Layer:
     def clear_status(self):
         check(lib.moe_clear_status(self.handle), "moe_clear_status")
 
+    def set_copy_ctas(self, ctas: int):
+        check(lib.moe_layer_set_copy_ctas(self.handle, ctas), "moe_layer_set_copy_ctas")
+
+    def profile(self, max_records: int):
+        check(lib.moe_layer_profile(self.handle, max_records), "moe_layer_profile")
+
+    def profile_read(self, max_records: int) -> np.ndarray:
+        out = np.zeros(max(1, max_records), np.float32)
+        n = ctypes.c_int()
+        check(lib.moe_layer_profile_read(self.handle, out.ctypes.data, max_records, ctypes.byref(n)),
+              "moe_layer_profile_read")
+        return out[: n.value].copy()
+
     def inject_fault(self, what: int):
         check(lib.moe_layer_inject_fault(self.handle, what), "moe_layer_inject_fault")
 

@@ -63,6 +63,9 @@ _SIGS = {
     "moe_get_diag": (_I, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [_I]),
     "moe_layer_inject_fault": (_I, [_P, _I]),
+    "moe_layer_set_copy_ctas": (_I, [_P, _I]),
+    "moe_layer_profile": (_I, [_P, _I]),
+    "moe_layer_profile_read": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "moe_link_probe": (_I, [_P, _P, _Z, _I, _P]),
     "moe_debug_e2m1_pairs": (_I, [_P, _P]),
 }

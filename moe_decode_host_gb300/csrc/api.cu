@@ -45,6 +45,8 @@ struct moe_layer {
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     bool copy_pending = false;
     int copy_ctas = 0;
+    std::vector<cudaEvent_t> prof_ev;  // pairs of events around recorded cold copies
+    int prof_n = 0;
     long steps = 0;
     int fault = 0;
 };
@@ -121,9 +123,16 @@ cudaError_t join_copy(moe_layer* L, cudaStream_t st) {
     return cudaStreamWaitEvent(st, L->ev_join, 0);
 }
 
+void free_prof(moe_layer* L) {
+    for (cudaEvent_t e : L->prof_ev) cudaEventDestroy(e);
+    L->prof_ev.clear();
+    L->prof_n = 0;
+}
+
 void free_layer(moe_layer* L) {
     if (!L) return;
     if (L->copy_stream) cudaStreamSynchronize(L->copy_stream);
+    free_prof(L);
     if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
     if (L->ev_fork) cudaEventDestroy(L->ev_fork);
     if (L->ev_join) cudaEventDestroy(L->ev_join);
@@ -254,7 +263,7 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
         err = cudaMalloc(&L->d_tmaps, sizeof(TmapPair) * p.E);
         err = err ? err : cudaMemcpy(L->d_tmaps, maps.data(), sizeof(TmapPair) * p.E, cudaMemcpyHostToDevice);
     }
-    L->copy_ctas = L->sm_count / 2 > 0 ? L->sm_count / 2 : 1;
+    L->copy_ctas = L->sm_count / 4 > 0 ? L->sm_count / 4 : 1;
     if (err != cudaSuccess) {
         cudaGetLastError();
         free_layer(L);
@@ -285,18 +294,28 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
     if (T > 0 && (!topk_ids || !phys_ids)) return MOE_ERR_INVALID_ARG;
     if (L->p.n_cold > 0 && T > 0 && !cold_list) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
-    cudaError_t err = launch_cold_remap(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, phys_ids,
-                                        cold_list, n_cold_picked, L->d_status, st);
-    if (err != cudaSuccess || L->p.n_cold == 0 || T == 0) return cuda_status(err);
-    // the byte copy forks onto the layer's copy stream so that the FFN over the
-    // experts already in HBM can run while the link streams the cold ones
-    err = cudaEventRecord(L->ev_fork, st);
-    if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
+    cudaError_t err = cudaSuccess;
+    if (L->p.n_cold > 0 && T > 0) {
+        // the byte copy forks onto the layer's copy stream first, so that it starts
+        // while the remap kernel runs and the FFN over HBM-resident experts can run
+        // while the link streams the cold ones
+        err = cudaEventRecord(L->ev_fork, st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
+        const bool prof = L->prof_n < (int)L->prof_ev.size() / 2;
+        if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
+        if (err == cudaSuccess)
+            err = launch_cold_copy(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, L->d_cold_src,
+                                   L->scratch->base, L->lay.total, L->copy_ctas, L->copy_stream);
+        if (err == cudaSuccess && prof) {
+            err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
+            ++L->prof_n;
+        }
+        if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
+        if (err == cudaSuccess) L->copy_pending = true;
+    }
     if (err == cudaSuccess)
-        err = launch_cold_copy(cold_list, n_cold_picked, L->d_cold_src, L->scratch->base, L->lay.total, L->copy_ctas,
-                               L->copy_stream);
-    if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
-    if (err == cudaSuccess) L->copy_pending = true;
+        err = launch_cold_remap(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, phys_ids, cold_list,
+                                n_cold_picked, L->d_status, st);
     return cuda_status(err);
 }
 
@@ -462,6 +481,42 @@ const char* moe_strerror(int code) {
         case MOE_ERR_SCRATCH_TOO_SMALL: return "batch needs more workspace than the static no-allocation array holds";
         default: return "unknown status";
     }
+}
+
+int moe_layer_set_copy_ctas(moe_layer* L, int ctas) {
+    if (!L || ctas < 0 || ctas > 64 * 1024) return MOE_ERR_INVALID_ARG;
+    L->copy_ctas = ctas > 0 ? ctas : (L->sm_count / 4 > 0 ? L->sm_count / 4 : 1);
+    return MOE_OK;
+}
+
+int moe_layer_profile(moe_layer* L, int max_records) {
+    if (!L || max_records < 0) return MOE_ERR_INVALID_ARG;
+    if (L->copy_stream && cudaStreamSynchronize(L->copy_stream) != cudaSuccess) return MOE_ERR_CUDA;
+    free_prof(L);
+    for (int i = 0; i < 2 * max_records; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            cudaGetLastError();
+            free_prof(L);
+            return MOE_ERR_CUDA;
+        }
+        L->prof_ev.push_back(e);
+    }
+    return MOE_OK;
+}
+
+int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out) {
+    if (!L || !n_out || max < 0 || (max > 0 && !copy_ms)) return MOE_ERR_INVALID_ARG;
+    const int n = L->prof_n < max ? L->prof_n : max;
+    for (int i = 0; i < n; ++i) {
+        if (cudaEventSynchronize(L->prof_ev[2 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&copy_ms[i], L->prof_ev[2 * i], L->prof_ev[2 * i + 1]) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+    }
+    *n_out = n;
+    return MOE_OK;
 }
 
 int moe_layer_inject_fault(moe_layer* L, int what) {

@@ -7,9 +7,10 @@
 // 2.60 ms of a 10.49 ms step, so the copy is the host-link-bound part of the path.
 //
 // A one-CTA remap kernel marks the picked cold slots in shared memory and lists
-// them in ascending order with warp ballots; a copy kernel then streams the listed
-// host blobs into their slots with 16-byte zero-copy loads, several in flight per
-// thread to cover the link latency.
+// them in ascending order with warp ballots; a copy kernel, running concurrently,
+// derives the same list per CTA and streams the listed host blobs into their
+// slots with 16-byte zero-copy loads, several in flight per thread to cover the
+// link latency.
 #include "internal.cuh"
 
 namespace moe {
@@ -80,21 +81,48 @@ __global__ void __launch_bounds__(kGatherThreads) cold_remap_kernel(
     }
 }
 
-// Streams every listed host blob into its scratch slot; each picked slot is cut
+// Streams every picked cold expert's host blob into its scratch slot.  Each CTA
+// derives the ascending list of picked cold slots from the picks itself (the same
+// marking and ballot compaction as the remap kernel), so the copy needs nothing
+// from the remap kernel and the two run concurrently.  Each picked slot is cut
 // into `seg` contiguous pieces spread over the grid.
-__global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(const int32_t* __restrict__ cold_list,
-                                                                   const int32_t* __restrict__ n_picked,
-                                                                   const uint8_t* const* __restrict__ cold_src,
-                                                                   uint8_t* __restrict__ slot_base,
-                                                                   size_t blob_bytes) {
-    const int cnt = *n_picked;
+__global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(
+    const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
+    const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes) {
+    __shared__ unsigned char flag[kMaxColdSlots];
+    __shared__ int32_t list[kMaxColdSlots];
+    __shared__ int s_cnt;
+    for (int c = threadIdx.x; c < n_cold; c += blockDim.x) flag[c] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_picks; i += blockDim.x) {
+        const int id = __ldg(ids + i);
+        if (id >= 0 && id < E) {
+            const int p = __ldg(loc + id);
+            if (p >= n_hot) flag[p - n_hot] = 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int cnt = 0;
+        for (int base = 0; base < n_cold; base += 32) {
+            const int c = base + lane;
+            const bool f = (c < n_cold) && flag[c];
+            const unsigned m = __ballot_sync(0xffffffffu, f);
+            if (f) list[cnt + __popc(m & ((1u << lane) - 1u))] = c;
+            cnt += __popc(m);
+        }
+        if (lane == 0) s_cnt = cnt;
+    }
+    __syncthreads();
+    const int cnt = s_cnt;
     if (cnt <= 0) return;
     const size_t chunks = blob_bytes / 16;
     int seg = (int)gridDim.x / cnt;
     if (seg < 1) seg = 1;
     const int items = cnt * seg;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
-        const int c = __ldg(cold_list + it / seg);
+        const int c = list[it / seg];
         const int s = it % seg;
         const size_t c0 = chunks * (size_t)s / (size_t)seg;
         const size_t c1 = chunks * (size_t)(s + 1) / (size_t)seg;
@@ -121,9 +149,12 @@ cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* lo
     return cudaGetLastError();
 }
 
-cudaError_t launch_cold_copy(const int32_t* cold_list, const int32_t* n_picked, const uint8_t* const* cold_src,
-                             uint8_t* slot_base, size_t blob_bytes, int ctas, cudaStream_t st) {
-    cold_copy_kernel<<<ctas, kGatherThreads, 0, st>>>(cold_list, n_picked, cold_src, slot_base, blob_bytes);
+cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int ctas,
+                             cudaStream_t st) {
+    if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
+    cold_copy_kernel<<<ctas, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, cold_src, slot_base,
+                                                      blob_bytes);
     return cudaGetLastError();
 }
 

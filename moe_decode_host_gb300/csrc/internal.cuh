@@ -45,9 +45,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 // Remap (phys ids, picked cold slots) on the caller's stream.
 cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st);
-// Byte copy of the listed slots (reads cold_list / n_picked written by the remap).
-cudaError_t launch_cold_copy(const int32_t* cold_list, const int32_t* n_picked, const uint8_t* const* cold_src,
-                             uint8_t* slot_base, size_t blob_bytes, int ctas, cudaStream_t st);
+// Byte copy of the picked cold slots (derives the slot list from the picks itself).
+cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int ctas,
+                             cudaStream_t st);
 
 cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
 
