@@ -33,10 +33,9 @@
  *   dimension ("A 475 GB Model Across Two Workstations, With the Table on Disk",
  *   Abstract: routed experts ship in MXFP4).  w13 rows 0..I-1 are the gate
  *   projection, rows I..2I-1 the up projection (the fused w13/w2 planes of "Milo
- *   and James Try Inference Engineering", offload flag table).  Inside a row,
- *   elements sit in 64-byte groups of 128: element e (0..31) of block j (0..3) of
- *   a group is in byte 16*(e/8) + 4*j + (e%8)/2 of the group, low nibble when e is
- *   even.  Scale byte b of a row is the exponent of elements 32b..32b+31.
+ *   and James Try Inference Engineering", offload flag table).  Rows are K-major:
+ *   element k of a row is in byte k/2, low nibble when k is even.  Scale byte b
+ *   of a row is the exponent of elements 32b..32b+31.
  *
  * Placement: loc[e] in [0, n_hot) is an HBM slot; loc[e] = n_hot + c is cold slot
  * c, whose bytes live in host blob c and are copied to scratch slot c when routed.

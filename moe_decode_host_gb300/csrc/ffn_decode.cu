@@ -16,15 +16,14 @@
 //    f16 x f16 -> fp32 dot-product engine; each 32-element block's E8M0 scale is
 //    applied in fp32 to that block's partial sums.  Warps split the rows and the
 //    reduction dimension; partial sums meet in shared memory in a fixed order.
-// The blob layout puts, in every 64-byte group of a row, the 8 elements of each of
-// 4 blocks that one lane of a quad needs into that lane's 16 bytes, so every mma
-// step sees a single block.  Activations are staged as f16 with an exact
+// Each lane of a quad reads 8 elements of each 32-element block from the staged
+// K-major rows, so every mma step sees a single block.  Activations are staged as f16 with an exact
 // power-of-two prescale per row.  Every wait is bounded by a deadline; a wait
 // that runs out sets MOE_ERR_TIMEOUT in the status word and the CTA drains its
 // copies and returns.
 #include <cuda.h>
 
-#include "internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -33,7 +32,6 @@ constexpr int kConsumers = 8;
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kMaxE = 1024;
 constexpr int kSliceBytes = 128;  // bytes of one row per stage (256 elements)
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 template <int P>
 struct Cfg;
@@ -58,70 +56,6 @@ struct Layout {
     static constexpr int kStageBytes = ((kWBytes + kABytes) + 1023) & ~1023;
     static constexpr int kStages = (kStageBudget / kStageBytes) < 64 ? (kStageBudget / kStageBytes) : 64;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the barrier phase with the given parity; false when the deadline
-// passed (status set, abort raised, the place recorded in diag) or another warp
-// raised abort.  where: 1 = stage full (consumer), 2 = stage empty (producer).
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity, volatile int* abort, int* status, int* diag,
-                                       int where, int slot, int stage, int extra) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (unsigned it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *abort = 1;
-                if (diag && atomicCAS(diag, 0, 1) == 0) {
-                    diag[1] = blockIdx.x;
-                    diag[2] = (int)(threadIdx.x >> 5);
-                    diag[3] = where;
-                    diag[4] = slot;
-                    diag[5] = (int)parity;
-                    diag[6] = stage;
-                    diag[7] = extra;
-                    diag[8] = mbar_try_wait(bar, parity ^ 1u) ? 1 : 0;
-                    __threadfence();
-                }
-                set_status(status, MOE_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
 
 // Waits until the producer has stamped `slot` with global stage `g` (it stamps a
 // slot only after the slot's previous stage was released), so that the following
@@ -152,78 +86,6 @@ __device__ __noinline__ bool seq_wait(volatile int* seq, int g, volatile int* ab
     }
 }
 
-// Bounded wait used when draining copies in flight before exit (ignores abort).
-__device__ __noinline__ void mbar_drain(uint64_t* bar, unsigned parity) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kTimeoutNs) return;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
-
-__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
-    uint32_t v;
-    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// Four E8M0 exponent bytes (byte j = block j) -> 2^(e_j - 127) as fp32, exactly
-// (e = 0 gives the subnormal 2^-127, e = 255 gives NaN): two ue8m0x2 -> bf16x2
-// conversions, then the bf16 halves are widened to fp32.
-__device__ __forceinline__ void e8m0x4_to_f32(uint32_t w, float (&s)[4]) {
-    uint32_t lo, hi;
-    asm("{\n\t.reg .b16 h0, h1;\n\t"
-        "mov.b32 {h0, h1}, %2;\n\t"
-        "cvt.rn.bf16x2.ue8m0x2 %0, h0;\n\t"
-        "cvt.rn.bf16x2.ue8m0x2 %1, h1;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-    s[0] = __uint_as_float(lo << 16);
-    s[1] = __uint_as_float(lo & 0xffff0000u);
-    s[2] = __uint_as_float(hi << 16);
-    s[3] = __uint_as_float(hi & 0xffff0000u);
-}
-
-// 8 E2M1 nibbles (byte b holds elements 2b, 2b+1) -> 4 f16x2 (r[b] = {elem 2b, elem 2b+1}).
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-        : "r"(w));
-}
-
-// 2^p for p in [-126, 127].
-__device__ __forceinline__ float pow2i(int p) { return __uint_as_float((uint32_t)(p + 127) << 23); }
-
-// Power-of-two prescale exponent so that amax * 2^-p lies in [2^14, 2^15).
-__device__ __forceinline__ int prescale_exp(float amax) {
-    uint32_t b = __float_as_uint(amax) & 0x7fffffffu;
-    if (b == 0u) return 0;
-    int e = (int)(b >> 23);
-    if (e == 255) return 0;
-    int p = (e == 0 ? -126 : e - 127) - 14;
-    return p < -126 ? -126 : (p > 126 ? 126 : p);
-}
-
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
     asm(
@@ -231,10 +93,6 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
-    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
 // Fragment row g (0..7) of an m16 tile is weight row perm8(g) (and +8): with the
@@ -264,14 +122,20 @@ __device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow
 #pragma unroll
     for (int gl = 0; gl < 2; ++gl) {
         if (gl >= ng) break;
-        uint4 wv[NTILE][2];
+        // word j of this lane: elements 8q..8q+7 of block j of the group (16-byte
+        // chunk gl*4+j of the swizzled row); the 8 rows of a quarter-warp have
+        // distinct row%8, so the 32 lanes hit 32 distinct banks
+        uint32_t wv[NTILE][2][4];
 #pragma unroll
         for (int i = 0; i < NTILE; ++i)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int row = srow[i][r];
-                const int chunk = (gl * 4 + q) ^ (row & 7);
-                wv[i][r] = *reinterpret_cast<const uint4*>(stage + row * kSliceBytes + chunk * 16);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int chunk = (gl * 4 + j) ^ (row & 7);
+                    wv[i][r][j] = *reinterpret_cast<const uint32_t*>(stage + row * kSliceBytes + chunk * 16 + q * 4);
+                }
             }
         float scf[NTILE][2][4];
 #pragma unroll
@@ -284,7 +148,7 @@ __device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow
 #pragma unroll
             for (int i = 0; i < NTILE; ++i)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(word_of(wv[i][r], j), af[i][r]);
+                for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(wv[i][r][j], af[i][r]);
             uint4 bv[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) bv[nt] = bl.load(nt, gl * 256 + 64 * j + 16 * q);

@@ -1,0 +1,151 @@
+// PTX helpers shared by the FFN kernels (sm_103a): shared-memory addresses,
+// mbarriers with bounded waits, TMA and bulk copies, E2M1/E8M0 conversions and
+// power-of-two prescales.  Every wait ends by a deadline; a wait that runs out
+// sets MOE_ERR_TIMEOUT and records where it gave up.
+#pragma once
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the barrier phase with the given parity; false when the deadline
+// passed (status set, abort raised, the place recorded in diag) or another warp
+// raised abort.  where: 1 = stage full (consumer), 2 = stage empty (producer).
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity, volatile int* abort, int* status, int* diag,
+                                       int where, int slot, int stage, int extra) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (unsigned it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *abort = 1;
+                if (diag && atomicCAS(diag, 0, 1) == 0) {
+                    diag[1] = blockIdx.x;
+                    diag[2] = (int)(threadIdx.x >> 5);
+                    diag[3] = where;
+                    diag[4] = slot;
+                    diag[5] = (int)parity;
+                    diag[6] = stage;
+                    diag[7] = extra;
+                    diag[8] = mbar_try_wait(bar, parity ^ 1u) ? 1 : 0;
+                    __threadfence();
+                }
+                set_status(status, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used when draining copies in flight before exit (ignores abort).
+__device__ __noinline__ void mbar_drain(uint64_t* bar, unsigned parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
+    uint32_t v;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Four E8M0 exponent bytes (byte j = block j) -> 2^(e_j - 127) as fp32, exactly
+// (e = 0 gives the subnormal 2^-127, e = 255 gives NaN): two ue8m0x2 -> bf16x2
+// conversions, then the bf16 halves are widened to fp32.
+__device__ __forceinline__ void e8m0x4_to_f32(uint32_t w, float (&s)[4]) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "mov.b32 {h0, h1}, %2;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %0, h0;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %1, h1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+    s[0] = __uint_as_float(lo << 16);
+    s[1] = __uint_as_float(lo & 0xffff0000u);
+    s[2] = __uint_as_float(hi << 16);
+    s[3] = __uint_as_float(hi & 0xffff0000u);
+}
+
+// 8 E2M1 nibbles (byte b holds elements 2b, 2b+1) -> 4 f16x2 (r[b] = {elem 2b, elem 2b+1}).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(w));
+}
+
+// 2^p for p in [-126, 127].
+__device__ __forceinline__ float pow2i(int p) { return __uint_as_float((uint32_t)(p + 127) << 23); }
+
+// Power-of-two prescale exponent so that amax * 2^-p lies in [2^14, 2^15).
+__device__ __forceinline__ int prescale_exp(float amax) {
+    uint32_t b = __float_as_uint(amax) & 0x7fffffffu;
+    if (b == 0u) return 0;
+    int e = (int)(b >> 23);
+    if (e == 255) return 0;
+    int p = (e == 0 ? -126 : e - 127) - 14;
+    return p < -126 ? -126 : (p > 126 ? 126 : p);
+}
+
+}  // namespace
+}  // namespace moe

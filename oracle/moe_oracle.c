@@ -46,9 +46,8 @@
  *     w2  nibbles [H rows][I/2 bytes],  w2  scales [H rows][I/32 bytes].
  *   Rows 0..I-1 of w13 are the gate projection, rows I..2I-1 the up projection.
  *   Scale byte (r, b) is the E8M0 exponent of block b = elements 32b..32b+31 of
- *   row r.  Inside a row, elements are stored in 64-byte groups of 128 elements;
- *   in a group, element e (0..31) of block j (0..3) sits in byte
- *   16*(e/8) + 4*j + (e%8)/2, in the low nibble when e is even, else the high.
+ *   row r.  Inside a row, element k sits in byte k/2, in the low nibble when k is
+ *   even, else the high nibble (plain K-major MXFP4 packing).
  */
 #include <math.h>
 #include <stdint.h>
@@ -75,13 +74,10 @@ double or_e8m0(unsigned e) {
     return ldexp(1.0, (int)e - 127);
 }
 
-/* Nibble code of logical element k in one row of the documented layout. */
+/* Nibble code of element k in one row of the documented layout. */
 unsigned or_nibble_at(const uint8_t* row, int k) {
-    int group = k / 128, kk = k % 128;
-    int j = kk / 32, e = kk % 32;
-    size_t byte = (size_t)group * 64 + (size_t)(16 * (e / 8) + 4 * j + (e % 8) / 2);
-    uint8_t b = row[byte];
-    return (e % 2 == 0) ? (unsigned)(b & 0x0F) : (unsigned)(b >> 4);
+    uint8_t b = row[k / 2];
+    return (k % 2 == 0) ? (unsigned)(b & 0x0F) : (unsigned)(b >> 4);
 }
 
 /* Decode one row of K elements (K a multiple of 128) to doubles. */

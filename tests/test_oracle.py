@@ -249,13 +249,10 @@ def _pack_matrix(W_codes, W_scales):
     nib = np.zeros((R, K // 2), np.uint8)
     for r in range(R):
         for k in range(K):
-            g, kk = divmod(k, 128)
-            j, e = divmod(kk, 32)
-            byte = 64 * g + 16 * (e // 8) + 4 * j + (e % 8) // 2
-            if e % 2 == 0:
-                nib[r, byte] |= W_codes[r, k]
+            if k % 2 == 0:
+                nib[r, k // 2] |= W_codes[r, k]
             else:
-                nib[r, byte] |= W_codes[r, k] << 4
+                nib[r, k // 2] |= W_codes[r, k] << 4
     return nib, np.asarray(W_scales, np.uint8)
 
 
