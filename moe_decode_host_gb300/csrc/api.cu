@@ -40,7 +40,7 @@ struct moe_layer {
     int* d_diag = nullptr;            // [16] record of the first device-side wait that timed out
     int32_t* h_counts = nullptr;      // pinned [E]
     int32_t* h_loc = nullptr;         // pinned [E]
-    TmapPair* d_tmaps = nullptr;      // [E] TMA descriptors per physical id
+    ExpertMaps* d_tmaps = nullptr;      // [E] TMA descriptors per physical id
     cudaStream_t copy_stream = nullptr;  // cold slot copies run here, joined by moe_grouped_ffn
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     bool copy_pending = false;
@@ -103,17 +103,31 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2D u8 view [rows][row_bytes] at base; box = 128 bytes x 32 rows, 128-byte swizzle.
-bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
+}  // namespace
+
+bool moe::encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {128, 32};
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+// 2D u8 view [rows][row_bytes] at base: the decode kernel's box (128 bytes x 32
+// rows, 128-byte swizzle) and the prefill kernel's (32 bytes x 128 rows, plain).
+bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 128, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 32, 128,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Makes `st` wait for the layer's cold copy in flight, if any.
@@ -252,16 +266,18 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     err = err ? err : cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
     if (err == cudaSuccess) {
-        std::vector<TmapPair> maps(p.E);
+        std::vector<ExpertMaps> maps(p.E);
         for (int i = 0; i < p.E; ++i) {
             if (!encode_plane(&maps[i].w13n, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||
-                !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H)) {
+                !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H) ||
+                !encode_plane_raw(&maps[i].w13r, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||
+                !encode_plane_raw(&maps[i].w2r, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H)) {
                 free_layer(L);
                 return MOE_ERR_CUDA;
             }
         }
-        err = cudaMalloc(&L->d_tmaps, sizeof(TmapPair) * p.E);
-        err = err ? err : cudaMemcpy(L->d_tmaps, maps.data(), sizeof(TmapPair) * p.E, cudaMemcpyHostToDevice);
+        err = cudaMalloc(&L->d_tmaps, sizeof(ExpertMaps) * p.E);
+        err = err ? err : cudaMemcpy(L->d_tmaps, maps.data(), sizeof(ExpertMaps) * p.E, cudaMemcpyHostToDevice);
     }
     L->copy_ctas = L->sm_count / 4 > 0 ? L->sm_count / 4 : 1;
     if (err != cudaSuccess) {

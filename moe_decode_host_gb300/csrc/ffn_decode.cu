@@ -605,7 +605,7 @@ __global__ void debug_e2m1_kernel(uint32_t* out) {
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t x16, xexp, hamax, h, h16, hexp, total;
+    size_t x16, xexp, hamax, h, h16, hexp, g, total;
 };
 
 WsLayout ws_layout(int T, int k, int H, int I) {
@@ -623,6 +623,8 @@ WsLayout ws_layout(int T, int k, int H, int I) {
     o = align256(o + (size_t)T * k * I * sizeof(__half));
     w.hexp = o;
     o = align256(o + (size_t)T * k * sizeof(int32_t));
+    w.g = o;
+    if (T > kTcMinTokens) o = align256(o + (size_t)T * k * (H > I ? H : I) * sizeof(__half));
     w.total = o;
     return w;
 }
@@ -662,6 +664,7 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     a.h = reinterpret_cast<float*>(ws + w.h);
     a.h16 = reinterpret_cast<__half*>(ws + w.h16);
     a.hexp = reinterpret_cast<int32_t*>(ws + w.hexp);
+    a.g = a.T > kTcMinTokens ? reinterpret_cast<__half*>(ws + w.g) : nullptr;
     if (a.T == 0) return cudaSuccess;
     xprep_kernel<<<a.T, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp, a.hamax);
     return cudaGetLastError();
@@ -669,11 +672,12 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
 
 cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st) {
     if (a.T == 0) return cudaSuccess;
-    // token-count ranges per kernel; a bound on the largest bucket is T
+    // token-count ranges per kernel (a bound on the largest bucket is T); buckets
+    // above kTcMinTokens go to the tensor-core kernel
     struct Range {
         int nt, lo, hi;
     };
-    const Range ranges[3] = {{1, 0, 8}, {2, 8, 16}, {4, 16, 1 << 30}};
+    const Range ranges[3] = {{1, 0, 8}, {2, 8, 16}, {4, 16, kTcMinTokens}};
     const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / 32);
     if (phase == 1) {
@@ -697,6 +701,7 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
         }
         if (err != cudaSuccess) return err;
     }
+    if (a.T > kTcMinTokens) return launch_ffn_tc(a, phase, sel, kTcMinTokens, sm_count, st);
     return cudaSuccess;
 }
 

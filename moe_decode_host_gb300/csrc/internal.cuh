@@ -52,15 +52,25 @@ cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc
 
 cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
 
-// 2D TMA descriptors of the two nibble planes of the blob at one physical id.
-struct TmapPair {
+// 2D TMA descriptors of the two nibble planes of the blob at one physical id:
+// a swizzled view for the decode kernel and a plain one for the prefill kernel.
+struct ExpertMaps {
     CUtensorMap w13n;  // [2I rows][H/2 bytes], box 128 B x 32 rows, 128-byte swizzle
     CUtensorMap w2n;   // [H rows][I/2 bytes], same box
+    CUtensorMap w13r;  // [2I rows][H/2 bytes], box 32 B x 128 rows, no swizzle
+    CUtensorMap w2r;   // [H rows][I/2 bytes], same box
 };
+
+// Buckets with more than this many tokens run on the tensor-core prefill kernel.
+constexpr int kTcMinTokens = 64;
+
+// Encodes a 2D tiled TMA descriptor (inner dimension contiguous); false on failure.
+bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 struct FfnArgs {
     const uint8_t* const* ptr;  // phys id -> blob base (device)
-    const TmapPair* tmaps;      // phys id -> descriptors (device)
+    const ExpertMaps* tmaps;    // phys id -> descriptors (device)
     const int32_t* loc;         // placement map, for the hot/cold split
     int n_hot;
     int n_phys;
@@ -76,6 +86,8 @@ struct FfnArgs {
     float* h;                // workspace [T*k][I]
     __half* h16;             // workspace [T*k][I], prescaled copy of h
     int32_t* hexp;           // workspace [T*k]
+    __half* g;               // workspace [T*k][max(H, I)] activations gathered in bucket order
+                             // (prefill kernel only; null when T <= kTcMinTokens)
     float* y;                // [T*k][H]
     int* status;
     int* diag;               // [16] where the first timed-out wait gave up
@@ -88,6 +100,8 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st);
 // One phase (0: gate/up -> h, 1: down -> y) over the experts selected by sel
 // (0: all, 1: placed in HBM, 2: placed in cold slots).
 cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st);
+// The tensor-core kernel of one phase over the selected experts with more than lo tokens.
+cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_count, cudaStream_t st);
 
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
                            cudaStream_t st);

@@ -270,6 +270,78 @@ def test_layer_ragged_shapes(H, I, E, n_hot, k, T, dist):
         assert np.bincount(ids.ravel(), minlength=E).max() > 32
 
 
+# ------------------------------------------------------------------ prefill-sized buckets
+
+def _assigned_logits(counts, E, seed):
+    """k=1 logits giving expert e exactly counts[e] tokens (tokens in shuffled order)."""
+    rng = np.random.default_rng(seed)
+    owner = rng.permutation(np.repeat(np.arange(E), counts))
+    l = rng.standard_normal((owner.size, E)).astype(np.float32)
+    l[np.arange(owner.size), owner] += 12.0
+    return l
+
+
+@pytest.mark.parametrize("H,I,E,n_hot,k,T,dist", [
+    (256, 512, 16, 12, 2, 1024, "uniform"),  # ~128 tokens per expert, four of them cold
+    (256, 256, 4, 4, 2, 600, "uniform"),     # ~300 per expert: two column passes (192 + rest)
+    (384, 640, 40, 30, 5, 600, "zipf1.5"),   # buckets on both sides of 64, uneven K
+])
+def test_layer_prefill_buckets(H, I, E, n_hot, k, T, dist):
+    n_cold = E - n_hot
+    loc = np.random.default_rng(E + 1).permutation(E).astype(np.int32)
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=E + T, loc=loc)
+    if dist == "uniform":
+        logits = synth.gen_logits_uniform(T, E, seed=T)
+    else:
+        logits = synth.gen_logits_zipf(T, E, 1.5, synth.zipf_permutation(E, 2), seed=T)
+    x = synth.gen_x(T, H, seed=T + 1)
+    buf = _run_layer(fx, logits, x, True)
+    rc, ids, w, want = oracle.layer(logits, bf16_bits(x), k, 0, H, I, fx.all_blobs_now())
+    assert rc == 0
+    cnt = np.bincount(ids.ravel(), minlength=E)
+    assert cnt.max() > 64
+    assert rel_l2(buf.out.cpu().numpy(), want) <= OUT_TOL
+    _compare_layer(fx, buf, logits, x, list(range(0, T, 7)), True)
+    fx.layer.close()
+
+
+def test_layer_prefill_bucket_edges():
+    """Buckets of exactly 64 (decode kernel) and 65 (tensor cores), one token, a
+    column pass of 192 plus a padded tail, and an empty expert; cold ones included."""
+    counts = [65, 64, 193, 0, 1, 128, 129, 70]
+    E, H, I = 8, 256, 512
+    loc = np.array([6, 0, 7, 1, 2, 3, 4, 5], np.int32)  # experts 0 and 2 are cold
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=6, n_cold=2, k=1, seed=99, loc=loc)
+    logits = _assigned_logits(counts, E, seed=3)
+    T = logits.shape[0]
+    x = synth.gen_x(T, H, seed=4)
+    buf = _run_layer(fx, logits, x, True)
+    rc, ids, w, want = oracle.layer(logits, bf16_bits(x), 1, 0, H, I, fx.all_blobs_now())
+    assert rc == 0
+    assert np.array_equal(np.bincount(ids.ravel(), minlength=E), counts)
+    got = buf.out.cpu().numpy()
+    assert rel_l2(got, want) <= OUT_TOL
+    for e in range(E):  # every bucket on its own
+        rows = np.nonzero(ids[:, 0] == e)[0]
+        if rows.size:
+            assert rel_l2(got[rows], want[rows]) <= OUT_TOL, e
+    fx.layer.close()
+
+
+def test_layer_prefill_full_size_with_cold_experts():
+    """H=4096, I=3072 with 16 experts (4 cold) and 320 tokens of top-6: ~120 tokens
+    per expert, so the hot and the cold experts both run on the tensor cores."""
+    H, I, E, n_hot, k, T = 4096, 3072, 16, 12, 6, 320
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=E - n_hot, k=k, seed=123)
+    logits = synth.gen_logits_uniform(T, E, seed=5)
+    x = synth.gen_x(T, H, seed=6)
+    buf = _run_layer(fx, logits, x, False)
+    ids = buf.topk_ids.cpu().numpy()
+    assert np.bincount(ids.ravel(), minlength=E).min() > 64
+    _compare_layer(fx, buf, logits, x, [0, 1, 130, T - 1], False)
+    fx.layer.close()
+
+
 # ------------------------------------------------------------------ full sizes
 
 @pytest.fixture(scope="module")
