@@ -476,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
                             const float uv = acc[NTILE - 1][nt][c] * sx;
                             const float hv = gv / (1.0f + expf(-gv)) * uv;
                             a.h[(size_t)pick * I + orow] = hv;
-                            atomicMax(a.hamax + pick, __float_as_uint(fabsf(hv)));
                         } else {
                             a.y[(size_t)pick * H + orow] = acc[0][nt][c] * pow2i(__ldg(a.hexp + pick));
                         }
@@ -502,39 +501,62 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
 }
 
 // One CTA per pick of the selected class: per-pick power-of-two prescale of h
-// (from the amax the gate/up phase accumulated) and its f16 copy for the down
-// projection.
-__global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h, const unsigned* __restrict__ hamax,
-                                                    const int32_t* __restrict__ phys_ids, int n_hot, int n_phys,
-                                                    int sel, int I, __half* __restrict__ h16,
+// (from the row's amax) and its f16 copy for the down projection.
+__global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h, const int32_t* __restrict__ phys_ids,
+                                                    int n_hot, int n_phys, int sel, int I, __half* __restrict__ h16,
                                                     int32_t* __restrict__ hexp) {
+    __shared__ float wmax[8];
     const int p = blockIdx.x;
     const int ph = __ldg(phys_ids + p);
     const bool hot = ph >= 0 && ph < n_hot;
     const bool valid = ph >= 0 && ph < n_phys;
     if (sel == 1 && !hot) return;
     if (sel == 2 && (hot || !valid)) return;
-    const int e = prescale_exp(__uint_as_float(__ldcg(hamax + p)));
-    const float sc = pow2i(-e);
     const float4* src = reinterpret_cast<const float4*>(h + (size_t)p * I);
+    const int nch = I / 4;
+    constexpr int kPer = 4;  // up to 4 float4 per thread kept in registers (I <= 4096)
+    float4 v[kPer];
+    float amax = 0.f;
+    auto upd = [&](const float4& f) { amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)))); };
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int c = threadIdx.x + u * 256;
+        if (c < nch) {
+            v[u] = __ldcg(src + c);
+            upd(v[u]);
+        }
+    }
+    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) upd(__ldcg(src + c));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
+    const int e = prescale_exp(amax);
+    const float sc = pow2i(-e);
     uint2* dst = reinterpret_cast<uint2*>(h16 + (size_t)p * I);
-    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
-        float4 v = __ldcg(src + c);
-        __half2 lo = __floats2half2_rn(v.x * sc, v.y * sc);
-        __half2 hi = __floats2half2_rn(v.z * sc, v.w * sc);
+    auto conv = [&](const float4& f) {
+        __half2 lo = __floats2half2_rn(f.x * sc, f.y * sc);
+        __half2 hi = __floats2half2_rn(f.z * sc, f.w * sc);
         uint2 o;
         o.x = *reinterpret_cast<uint32_t*>(&lo);
         o.y = *reinterpret_cast<uint32_t*>(&hi);
-        dst[c] = o;
+        return o;
+    };
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int c = threadIdx.x + u * 256;
+        if (c < nch) dst[c] = conv(v[u]);
     }
+    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) dst[c] = conv(__ldcg(src + c));
     if (threadIdx.x == 0) hexp[p] = e;
 }
 
-// One CTA per token: per-token power-of-two prescale, f16 copy of x, and the
-// per-pick amax slots of h cleared.
+// One CTA per token: per-token power-of-two prescale and f16 copy of x.
 __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int k,
-                                                    __half* __restrict__ x16, int32_t* __restrict__ xexp,
-                                                    unsigned* __restrict__ hamax) {
+                                                    __half* __restrict__ x16, int32_t* __restrict__ xexp) {
     __shared__ float wmax[8];
     const int t = blockIdx.x;
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
@@ -592,7 +614,6 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
     }
     for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) out[c] = conv(__ldg(row + c));
     if (threadIdx.x == 0) xexp[t] = p;
-    if (threadIdx.x < k) hamax[(size_t)t * k + threadIdx.x] = 0u;
 }
 
 __global__ void debug_e2m1_kernel(uint32_t* out) {
@@ -605,7 +626,7 @@ __global__ void debug_e2m1_kernel(uint32_t* out) {
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t x16, xexp, hamax, h, h16, hexp, g, total;
+    size_t x16, xexp, h, h16, hexp, g, total;
 };
 
 WsLayout ws_layout(int T, int k, int H, int I) {
@@ -615,8 +636,6 @@ WsLayout ws_layout(int T, int k, int H, int I) {
     o = align256(o + (size_t)T * H * sizeof(__half));
     w.xexp = o;
     o = align256(o + (size_t)T * sizeof(int32_t));
-    w.hamax = o;
-    o = align256(o + (size_t)T * k * sizeof(unsigned));
     w.h = o;
     o = align256(o + (size_t)T * k * I * sizeof(float));
     w.h16 = o;
@@ -660,13 +679,12 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.x16 = reinterpret_cast<__half*>(ws + w.x16);
     a.xexp = reinterpret_cast<int32_t*>(ws + w.xexp);
-    a.hamax = reinterpret_cast<unsigned*>(ws + w.hamax);
     a.h = reinterpret_cast<float*>(ws + w.h);
     a.h16 = reinterpret_cast<__half*>(ws + w.h16);
     a.hexp = reinterpret_cast<int32_t*>(ws + w.hexp);
     a.g = a.T > kTcMinTokens ? reinterpret_cast<__half*>(ws + w.g) : nullptr;
     if (a.T == 0) return cudaSuccess;
-    xprep_kernel<<<a.T, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp, a.hamax);
+    xprep_kernel<<<a.T, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp);
     return cudaGetLastError();
 }
 
@@ -681,7 +699,7 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
     const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / 32);
     if (phase == 1) {
-        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.hamax, a.phys_ids, a.n_hot, a.n_phys, sel, a.I, a.h16,
+        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.phys_ids, a.n_hot, a.n_phys, sel, a.I, a.h16,
                                                 a.hexp);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

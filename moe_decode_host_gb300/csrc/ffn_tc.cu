@@ -7,21 +7,26 @@
 // GEMM: D[128 weight rows x N tokens] += W[128 x K] * X[N x K]^T with
 // tcgen05.mma (kind::f16, f16 operands, fp32 accumulators in tensor memory).
 //
-// Warp roles of one persistent CTA per SM:
-//   warp 0      TMA of the raw MXFP4 weight slices (128 rows x 64 elements) into a
-//               ring of raw stages;
-//   warp 1      owns tensor memory and issues the MMAs (one thread), committing
-//               each stage back to its producers and each tile to the epilogue;
-//   warp 2      TMA of the activation tiles (64 tokens x 64 elements, f16,
-//               128-byte swizzle), gathered per expert beforehand;
-//   warps 4-7   converters: one weight row per thread, E2M1 -> f16 with the row's
-//               E8M0 block scales rebased to 2^12 below the row's largest scale,
-//               so that every block whose scale is within 2^35 of the largest is
-//               exact in f16 (smaller blocks lose low bits), written in the
-//               128-byte-swizzled K-major layout the MMA reads;
-//   warps 8-11  epilogue: tensor memory -> registers -> h (gate/up phase, SiLU
-//               gate times up) or y (down phase), undoing the power-of-two
-//               rebasing of weights and activations.
+// Warp roles of one persistent CTA per SM (16 warps):
+//   warp 0       TMA of the raw MXFP4 weight slices (128 rows x 64 elements; gate
+//                and up rows together in the gate/up phase) into a ring of raw
+//                stages;
+//   warp 1       owns tensor memory and issues the MMAs (one thread): each stage
+//                is committed back to its two producers, each tile to the
+//                epilogue; two accumulator buffers let a tile's epilogue overlap
+//                the next tile's main loop;
+//   warp 2       TMA of the activation tiles (64 tokens x 64 elements, f16,
+//                128-byte swizzle), gathered in bucket order beforehand, into a
+//                ring of its own;
+//   warps 4-11   converters: E2M1 -> f16 for one weight row (gate/up phase) or one
+//                half of a row's stage (down phase) per thread, each E8M0 block
+//                scale rebased to 2^12 below the row's largest scale, so that every
+//                block whose scale is within 2^35 of the largest is exact in f16
+//                (smaller blocks lose low bits); written in the 128-byte-swizzled
+//                K-major layout the MMA reads;
+//   warps 12-15  epilogue: tensor memory -> registers -> h (gate/up phase, SiLU
+//                gate times up) or y (down phase), undoing the power-of-two
+//                rebasing of weights and activations.
 // Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT, and the CTA
 // drains its copies and MMAs before it frees tensor memory and returns.
 #include <cuda.h>
@@ -31,34 +36,47 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;        // weight rows per tile = tensor-memory lanes
-constexpr int kBK = 64;         // K elements per stage (128 bytes of f16 per row)
-constexpr int kNMax = 192;      // token columns per pass
-constexpr int kRawStages = 8;
-constexpr int kABStages = 2;
-constexpr int kThreadsTC = 384;
-constexpr int kRawBytes = 2 * kBM * 32;            // gate + up raw slices (phase 1 uses half)
-constexpr int kATile = kBM * 128;                  // f16 tile, 16 KB
-constexpr int kBTile = kNMax * 128;                // activation tile, 24 KB
-constexpr int kABBytes = 2 * kATile + kBTile;      // 56 KB
+constexpr int kBM = 128;    // weight rows per tile = tensor-memory lanes
+constexpr int kBK = 64;     // K elements per stage (128 bytes of f16 per row)
+constexpr int kNMax = 128;  // token columns per pass
+constexpr int kRawStages = 6;
+constexpr int kAStages = 3;
+constexpr int kBStages = 4;
+constexpr int kFirstConv = 4;   // first converter warp
+constexpr int kConvWarps = 8;
+constexpr int kFirstEpi = 12;   // first epilogue warp (warp % 4 = lane quarter)
+constexpr int kThreadsTC = 512;
+constexpr int kRawBytes = 2 * kBM * 32;      // gate + up raw slices (down phase uses half)
+constexpr int kATile = kBM * 128;            // one f16 weight tile, 16 KB
+constexpr int kAStageBytes = 2 * kATile;     // gate + up tiles
+constexpr int kBStageBytes = kNMax * 128;    // activation tile, 16 KB
+constexpr uint32_t kAccCols = 256;           // tensor-memory columns per accumulator buffer
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
 struct alignas(16) TcHead {
     uint64_t raw_full[kRawStages];
     uint64_t raw_empty[kRawStages];
-    uint64_t a_full[kABStages];
-    uint64_t b_full[kABStages];
-    uint64_t ab_empty[kABStages];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t a_full[kAStages];
+    uint64_t a_empty[kAStages];
+    uint64_t b_full[kBStages];
+    uint64_t b_empty[kBStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
     int D;
     int list[kMaxE];
+    int col_pick[4][kNMax];     // per epilogue warp: pick of each column of the pass
+    float col_scale[4][kNMax];  // and its activation prescale 2^p
 };
 
-constexpr size_t kTcSmem = 1024 + (size_t)kRawStages * kRawBytes + (size_t)kABStages * kABBytes + sizeof(TcHead);
+constexpr size_t kRawOff = 0;
+constexpr size_t kAOff = kRawOff + (size_t)kRawStages * kRawBytes;
+constexpr size_t kBOff = kAOff + (size_t)kAStages * kAStageBytes;
+constexpr size_t kHeadOff = kBOff + (size_t)kBStages * kBStageBytes;
+constexpr size_t kTcSmem = 1024 + kHeadOff + sizeof(TcHead);
+static_assert(kTcSmem <= 232448, "shared memory budget of one CTA");
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     // K-major operand, 128-byte swizzle: 8-row core groups 1024 bytes apart
@@ -84,16 +102,39 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
+// 16 consecutive fp32 columns of this thread's lane, waited for in the same asm.
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 16-column loads (gate and up accumulators) with one wait.
+__device__ __forceinline__ void tc_ld16x2(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+        "[%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
 }
 
 // Largest E8M0 exponent of a scale row (n bytes, n a multiple of 4).
@@ -117,6 +158,18 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     return d;
 }
 
+// 8 E2M1 values (one 32-bit word) times the f16x2 multiplier mm -> one 16-byte chunk.
+__device__ __forceinline__ uint4 convert_chunk(uint32_t word, uint32_t mm) {
+    uint32_t h4[4];
+    e2m1x8_to_f16x2(word, h4);
+    uint4 o;
+    o.x = hmul2(h4[0], mm);
+    o.y = hmul2(h4[1], mm);
+    o.z = hmul2(h4[2], mm);
+    o.w = hmul2(h4[3], mm);
+    return o;
+}
+
 struct TcTask {
     int e, rb, cnt, off, phys;
     bool valid;
@@ -133,20 +186,36 @@ __device__ __forceinline__ TcTask tc_task(const FfnArgs& a, const TcHead& hd, in
     return t;
 }
 
-__device__ __forceinline__ int ncols_pad(int nb) { return nb <= 64 ? 64 : (nb <= 128 ? 128 : 192); }
+// MMA width of a pass over nb tokens: a multiple of 16 (the M = 128 shape's step).
+__device__ __forceinline__ int ncols16(int nb) { return (nb + 15) & ~15; }
+
+// A wait taken by a whole warp: every lane polls, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, unsigned parity, const FfnArgs& a, volatile int* abort,
+                                          int where, int slot, int stage, int extra) {
+    const bool w = mbar_wait_fast(bar, parity, abort, a.status, a.diag, where, slot, stage, extra);
+    return __all_sync(0xffffffffu, w);
+}
+
+__device__ __forceinline__ void advance(int& slot, unsigned& phase, int n) {
+    if (++slot == n) {
+        slot = 0;
+        phase ^= 1u;
+    }
+}
 
 template <int P>
 __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
                                                                int lo, int sel) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* raw = base;                                  // [kRawStages][kRawBytes]
-    uint8_t* ab = base + (size_t)kRawStages * kRawBytes;  // [kABStages][kABBytes]
-    TcHead& hd = *reinterpret_cast<TcHead*>(ab + (size_t)kABStages * kABBytes);
+    uint8_t* raw = base + kRawOff;
+    uint8_t* sa = base + kAOff;
+    uint8_t* sb = base + kBOff;
+    TcHead& hd = *reinterpret_cast<TcHead*>(base + kHeadOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I;
     const int K = P == 0 ? H : I;
-    const int nks = K / kBK;
+    const int nks = K / kBK;  // even: K is a multiple of 128
     const int tiles = (P == 0 ? I : H) / kBM;
     volatile int* abort = &hd.abort;
 
@@ -171,15 +240,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             hd.abort = 0;
             for (int s = 0; s < kRawStages; ++s) {
                 mbar_init(&hd.raw_full[s], 1);
-                mbar_init(&hd.raw_empty[s], 4);
+                mbar_init(&hd.raw_empty[s], kConvWarps);
             }
-            for (int s = 0; s < kABStages; ++s) {
-                mbar_init(&hd.a_full[s], 4);
+            for (int s = 0; s < kAStages; ++s) {
+                mbar_init(&hd.a_full[s], kConvWarps);
+                mbar_init(&hd.a_empty[s], 1);
+            }
+            for (int s = 0; s < kBStages; ++s) {
                 mbar_init(&hd.b_full[s], 1);
-                mbar_init(&hd.ab_empty[s], 1);
+                mbar_init(&hd.b_empty[s], 1);
             }
-            mbar_init(&hd.acc_full, 1);
-            mbar_init(&hd.acc_empty, 4);
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&hd.acc_full[s], 1);
+                mbar_init(&hd.acc_empty[s], 4);
+            }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
@@ -195,8 +269,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const uint32_t tmem = hd.tmem_base;
     const int ntask = hd.D * tiles;
 
-    if (warp == 0 && lane == 0) {
-        // ---------------- raw weight producer ----------------
+    if (warp == 0) {
+        // ---------------- raw weight producer (lane 0 issues) ----------------
         int rs = 0;
         unsigned rph = 0;
         bool ok = true;
@@ -204,28 +278,29 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const TcTask t = tc_task(a, hd, task, tiles);
             if (!t.valid) continue;
             const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13r : &a.tmaps[t.phys].w2r;
-            asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+            if (lane == 0) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
             const int r0 = t.rb * kBM;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                 for (int s = 0; s < nks; ++s) {
-                    if (!mbar_wait(&hd.raw_empty[rs], rph ^ 1u, abort, a.status, a.diag, 12, rs, s, task)) {
+                    if (!warp_wait(&hd.raw_empty[rs], rph ^ 1u, a, abort, 12, rs, s, task)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* dst = raw + (size_t)rs * kRawBytes;
-                    mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * 32 : kBM * 32);
-                    tma_load_2d(dst, map, s * 32, r0, &hd.raw_full[rs]);
-                    if (P == 0) tma_load_2d(dst + kBM * 32, map, s * 32, I + r0, &hd.raw_full[rs]);
-                    if (++rs == kRawStages) {
-                        rs = 0;
-                        rph ^= 1u;
+                    if (lane == 0) {
+                        uint8_t* dst = raw + (size_t)rs * kRawBytes;
+                        mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * 32 : kBM * 32);
+                        tma_load_2d(dst, map, s * 32, r0, &hd.raw_full[rs]);
+                        if (P == 0) tma_load_2d(dst + kBM * 32, map, s * 32, I + r0, &hd.raw_full[rs]);
                     }
+                    __syncwarp();
+                    advance(rs, rph, kRawStages);
                 }
             }
         }
-        for (int s = 0; s < kRawStages; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
-    } else if (warp == 2 && lane == 0) {
-        // ---------------- activation producer ----------------
+        if (lane == 0)
+            for (int s = 0; s < kRawStages; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
+    } else if (warp == 2) {
+        // ---------------- activation producer (lane 0 issues) ----------------
         int bs = 0;
         unsigned bph = 0;
         bool ok = true;
@@ -233,78 +308,89 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const TcTask t = tc_task(a, hd, task, tiles);
             if (!t.valid) continue;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                const int N = ncols_pad(min(kNMax, t.cnt - tb));
+                const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + 63) / 64;
                 for (int s = 0; s < nks; ++s) {
-                    if (!mbar_wait(&hd.ab_empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, s, task)) {
+                    if (!warp_wait(&hd.b_empty[bs], bph ^ 1u, a, abort, 13, bs, s, task)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* dst = ab + (size_t)bs * kABBytes + 2 * kATile;
-                    mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)N * 128u);
-                    for (int c = 0; c < N / 64; ++c)
-                        tma_load_2d(dst + c * 64 * 128, &act_map, s * kBK, t.off + tb + 64 * c, &hd.b_full[bs]);
-                    if (++bs == kABStages) {
-                        bs = 0;
-                        bph ^= 1u;
+                    if (lane == 0) {
+                        uint8_t* dst = sb + (size_t)bs * kBStageBytes;
+                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)boxes * 64u * 128u);
+                        for (int c = 0; c < boxes; ++c)
+                            tma_load_2d(dst + c * 64 * 128, &act_map, s * kBK, t.off + tb + 64 * c, &hd.b_full[bs]);
                     }
+                    __syncwarp();
+                    advance(bs, bph, kBStages);
                 }
             }
         }
-        for (int s = 0; s < kABStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer ----------------
-        int bs = 0;
-        unsigned bph = 0;
-        unsigned aph = 0;  // acc_empty parity
+        if (lane == 0)
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (lane 0 issues) ----------------
+        int as = 0, bs = 0, buf = 0;
+        unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
         bool ok = true;
-        int issued = 0;    // commits to ab_empty / acc_full not yet known complete
         for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
             const TcTask t = tc_task(a, hd, task, tiles);
             if (!t.valid) continue;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                const int N = ncols_pad(min(kNMax, t.cnt - tb));
+                const int N = ncols16(min(kNMax, t.cnt - tb));
                 const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-                if (!mbar_wait(&hd.acc_empty, aph ^ 1u, abort, a.status, a.diag, 14, 0, 0, task)) {
+                if (!warp_wait(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, a, abort, 14, buf, 0, task)) {
                     ok = false;
                     break;
                 }
-                aph ^= 1u;
+                accph ^= 1u << buf;
                 tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)buf * kAccCols;
                 for (int s = 0; s < nks; ++s) {
-                    if (!mbar_wait(&hd.a_full[bs], bph, abort, a.status, a.diag, 15, bs, s, task) ||
-                        !mbar_wait(&hd.b_full[bs], bph, abort, a.status, a.diag, 16, bs, s, task)) {
+                    if (!warp_wait(&hd.a_full[as], aph, a, abort, 15, as, s, task) ||
+                        !warp_wait(&hd.b_full[bs], bph, a, abort, 16, bs, s, task)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(ab + (size_t)bs * kABBytes);
-                    const uint32_t sb = sa + 2 * kATile;
+                    // descriptors of k-step 0; a 16-element step advances the start address by 32 bytes
+                    const uint64_t ad = sw128_desc(smem_u32(sa + (size_t)as * kAStageBytes));
+                    const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
+                    if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bdesc = sw128_desc(sb + kk * 32);
-                        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                        tc_mma_f16(tmem, sw128_desc(sa + kk * 32), bdesc, idesc, acc);
-                        if (P == 0) tc_mma_f16(tmem + kNMax, sw128_desc(sa + kATile + kk * 32), bdesc, idesc, acc);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                            tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+                            if (P == 0) tc_mma_f16(d + kNMax, ad + (kATile >> 4) + 2 * kk, bd + 2 * kk, idesc, acc);
+                        }
+                        tc_commit(&hd.a_empty[as]);
+                        tc_commit(&hd.b_empty[bs]);
                     }
-                    tc_commit(&hd.ab_empty[bs]);
-                    ++issued;
-                    if (++bs == kABStages) {
-                        bs = 0;
-                        bph ^= 1u;
-                    }
+                    __syncwarp();
+                    advance(as, aph, kAStages);
+                    advance(bs, bph, kBStages);
                 }
                 if (!ok) break;
-                tc_commit(&hd.acc_full);
+                if (lane == 0) tc_commit(&hd.acc_full[buf]);
+                __syncwarp();
+                buf ^= 1;
             }
         }
-        // drain: wait for the last commit on each stage (bounded) so no MMA is in flight
-        for (int s = 0; s < kABStages; ++s) mbar_drain(&hd.ab_empty[s], (s < bs) ? bph : (bph ^ 1u));
-        (void)issued;
-    } else if (warp >= 4 && warp < 8) {
+        // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
+        // last commit of every stage
+        if (lane == 0) {
+            for (int s = 0; s < kAStages; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
+        }
+    } else if (warp >= kFirstConv && warp < kFirstConv + kConvWarps) {
         // ---------------- converters ----------------
-        const int t_row = (warp - 4) * 32 + lane;  // weight row within the tile
-        int rs = 0, bs = 0;
-        unsigned rph = 0, bph = 0;
+        // gate/up phase: thread = (matrix hi, row); down phase: thread = (half hi of the
+        // stage's 64 elements, row)
+        const int cidx = threadIdx.x - kFirstConv * 32;
+        const int row = cidx & (kBM - 1);
+        const int hi = cidx >> 7;
+        const uint32_t swz = (uint32_t)(row & 7);
+        int rs = 0, as = 0;
+        unsigned rph = 0, aph = 0;
         bool ok = true;
         for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
             const TcTask t = tc_task(a, hd, task, tiles);
@@ -312,77 +398,75 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const uint8_t* blob = a.ptr[t.phys];
             const int r0 = t.rb * kBM;
             const int srl = K / 32;  // scale bytes per row
-            const uint8_t* sc0 = blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + t_row) * srl;
-            const uint8_t* sc1 = P == 0 ? blob + a.w13s + (size_t)(I + r0 + t_row) * srl : sc0;
-            const int c0 = row_max_exp(sc0, srl) - 12;
-            const int c1 = P == 0 ? row_max_exp(sc1, srl) - 12 : c0;
+            const uint8_t* sc = P == 0 ? blob + a.w13s + (size_t)(hi * I + r0 + row) * srl
+                                       : blob + a.w2s + (size_t)(r0 + row) * srl;
+            const int cb = row_max_exp(sc, srl) - 12;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                for (int s = 0; s < nks; ++s) {
-                    // scale bytes of blocks 2s, 2s+1 (read before the waits)
-                    const uint32_t e0 = *reinterpret_cast<const uint16_t*>(sc0 + 2 * s);
-                    const uint32_t e1 = P == 0 ? *reinterpret_cast<const uint16_t*>(sc1 + 2 * s) : e0;
-                    bool w = mbar_wait(&hd.raw_full[rs], rph, abort, a.status, a.diag, 17, rs, s, task) &&
-                             mbar_wait(&hd.ab_empty[bs], bph ^ 1u, abort, a.status, a.diag, 18, bs, s, task);
-                    if (!__all_sync(0xffffffffu, w)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
-                    uint8_t* adst = ab + (size_t)bs * kABBytes;
+                // scale word of stages s, s+1 (blocks 2s..2s+3), fetched two stages ahead
+                uint32_t wcur = ld_u32(sc);
+                for (int s = 0; s < nks && ok; s += 2) {
+                    const uint32_t wnext = (s + 2 < nks) ? ld_u32(sc + 2 * (s + 2)) : 0u;
 #pragma unroll
-                    for (int ti = 0; ti < (P == 0 ? 2 : 1); ++ti) {
-                        const uint4* rp = reinterpret_cast<const uint4*>(rsrc + ti * kBM * 32 + t_row * 32);
-                        const uint4 w0 = rp[0], w1 = rp[1];
-                        const uint32_t ew = ti == 0 ? e0 : e1;
-                        const int cb = ti == 0 ? c0 : c1;
-                        const uint32_t m0 = f16_pow2((int)(ew & 0xffu) - cb);
-                        const uint32_t m1 = f16_pow2((int)(ew >> 8) - cb);
-                        const uint32_t mm0 = m0 | (m0 << 16), mm1 = m1 | (m1 << 16);
-                        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                        uint8_t* arow = adst + ti * kATile + t_row * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c = elements 8c..8c+7
-                            uint32_t h4[4];
-                            e2m1x8_to_f16x2(words[c], h4);
-                            const uint32_t mm = c < 4 ? mm0 : mm1;
-                            uint4 o;
-                            o.x = hmul2(h4[0], mm);
-                            o.y = hmul2(h4[1], mm);
-                            o.z = hmul2(h4[2], mm);
-                            o.w = hmul2(h4[3], mm);
-                            *reinterpret_cast<uint4*>(arow + ((c ^ (t_row & 7)) * 16)) = o;
+                    for (int u = 0; u < 2; ++u) {
+                        if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, s + u, task) ||
+                            !warp_wait(&hd.a_empty[as], aph ^ 1u, a, abort, 18, as, s + u, task)) {
+                            ok = false;
+                            break;
                         }
+                        const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
+                        uint8_t* arow = sa + (size_t)as * kAStageBytes + row * 128;
+                        if constexpr (P == 0) {
+                            const uint4* rp = reinterpret_cast<const uint4*>(rsrc + hi * kBM * 32 + row * 32);
+                            const uint4 w0 = rp[0], w1 = rp[1];
+                            const uint32_t e0 = (wcur >> (16 * u)) & 0xffu, e1 = (wcur >> (16 * u + 8)) & 0xffu;
+                            const uint32_t m0 = f16_pow2((int)e0 - cb), m1 = f16_pow2((int)e1 - cb);
+                            const uint32_t mm0 = m0 | (m0 << 16), mm1 = m1 | (m1 << 16);
+                            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                            arow += hi * kATile;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(arow + (((uint32_t)c ^ swz) * 16)) =
+                                    convert_chunk(words[c], c < 4 ? mm0 : mm1);
+                        } else {
+                            const uint4 w0 = *reinterpret_cast<const uint4*>(rsrc + row * 32 + hi * 16);
+                            const uint32_t e = (wcur >> (16 * u + 8 * hi)) & 0xffu;
+                            const uint32_t m = f16_pow2((int)e - cb);
+                            const uint32_t mm = m | (m << 16);
+                            const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                *reinterpret_cast<uint4*>(arow + (((uint32_t)(4 * hi + c) ^ swz) * 16)) =
+                                    convert_chunk(words[c], mm);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&hd.a_full[as]);
+                            mbar_arrive(&hd.raw_empty[rs]);
+                        }
+                        advance(rs, rph, kRawStages);
+                        advance(as, aph, kAStages);
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&hd.a_full[bs]);
-                        mbar_arrive(&hd.raw_empty[rs]);
-                    }
-                    if (++rs == kRawStages) {
-                        rs = 0;
-                        rph ^= 1u;
-                    }
-                    if (++bs == kABStages) {
-                        bs = 0;
-                        bph ^= 1u;
-                    }
+                    wcur = wnext;
                 }
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= kFirstEpi) {
         // ---------------- epilogue ----------------
-        const int q4 = warp - 8;                // tensor-memory lane quarter
+        const int q4 = warp - kFirstEpi;  // tensor-memory lane quarter (= warp % 4)
         const int t_row = q4 * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-        unsigned fph = 0;
+        int* cpick = hd.col_pick[q4];
+        float* cscale = hd.col_scale[q4];
+        int buf = 0;
+        unsigned accph = 0;
         bool ok = true;
         for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
             const TcTask t = tc_task(a, hd, task, tiles);
+            const int r0 = t.rb * kBM;
             if (!t.valid) {
                 // zero outputs for an expert whose physical id is out of range
-                if (t.rb == 0 && threadIdx.x == 8 * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
-                const int r0 = t.rb * kBM;
+                if (t.rb == 0 && threadIdx.x == kFirstEpi * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
                 for (int c = 0; c < t.cnt; ++c) {
                     const int pick = __ldg(a.entries + t.off + c);
                     if (P == 0) a.h[(size_t)pick * I + r0 + t_row] = 0.f;
@@ -391,7 +475,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 continue;
             }
             const uint8_t* blob = a.ptr[t.phys];
-            const int r0 = t.rb * kBM;
             const int srl = K / 32;
             const int c0 = row_max_exp(blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + t_row) * srl, srl) - 12;
             const int c1 = P == 0 ? row_max_exp(blob + a.w13s + (size_t)(I + r0 + t_row) * srl, srl) - 12 : c0;
@@ -399,38 +482,43 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const float s1 = pow2i(max(-126, min(127, c1 - 127)));
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                 const int nb = min(kNMax, t.cnt - tb);
-                const bool w = mbar_wait(&hd.acc_full, fph, abort, a.status, a.diag, 19, 0, tb, task);
-                if (!__all_sync(0xffffffffu, w)) {
+                // the pass's columns: pick and activation prescale, fetched before the wait
+                for (int n = lane; n < nb; n += 32) {
+                    const int pick = __ldg(a.entries + t.off + tb + n);
+                    cpick[n] = pick;
+                    cscale[n] = pow2i(P == 0 ? __ldg(a.xexp + pick / a.k) : __ldg(a.hexp + pick));
+                }
+                __syncwarp();
+                if (!warp_wait(&hd.acc_full[buf], (accph >> buf) & 1u, a, abort, 19, buf, tb, task)) {
                     ok = false;
                     break;
                 }
-                fph ^= 1u;
+                accph ^= 1u << buf;
                 tc_fence_after();
+                const uint32_t d = lane_addr + (uint32_t)buf * kAccCols;
                 for (int cb = 0; cb < nb; cb += 16) {
                     float v0[16], v1[16];
-                    tc_ld16(lane_addr + cb, v0);
-                    if (P == 0) tc_ld16(lane_addr + kNMax + cb, v1);
+                    if constexpr (P == 0) tc_ld16x2(d + cb, d + kNMax + cb, v0, v1);
+                    else tc_ld16(d + cb, v0);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int n = cb + i;
                         if (n >= nb) break;
-                        const int pick = __ldg(a.entries + t.off + tb + n);
+                        const int pick = cpick[n];
+                        const float sx = cscale[n];
                         if constexpr (P == 0) {
-                            const float sx = pow2i(__ldg(a.xexp + pick / a.k));
                             const float gv = v0[i] * s0 * sx;
                             const float uv = v1[i] * s1 * sx;
-                            const float hv = gv / (1.0f + expf(-gv)) * uv;
-                            a.h[(size_t)pick * I + r0 + t_row] = hv;
-                            const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-                            if (lane == 0) atomicMax(a.hamax + pick, m);
+                            a.h[(size_t)pick * I + r0 + t_row] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                         } else {
-                            a.y[(size_t)pick * H + r0 + t_row] = v0[i] * s0 * pow2i(__ldg(a.hexp + pick));
+                            a.y[(size_t)pick * H + r0 + t_row] = v0[i] * s0 * sx;
                         }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&hd.acc_empty);
+                if (lane == 0) mbar_arrive(&hd.acc_empty[buf]);
+                buf ^= 1;
             }
         }
     }

@@ -82,7 +82,6 @@ struct FfnArgs {
     const __nv_bfloat16* x;  // [T][H]
     __half* x16;             // workspace [T][H]
     int32_t* xexp;           // workspace [T]
-    unsigned* hamax;         // workspace [T*k]
     float* h;                // workspace [T*k][I]
     __half* h16;             // workspace [T*k][I], prescaled copy of h
     int32_t* hexp;           // workspace [T*k]

@@ -75,6 +75,13 @@ __device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity, volatile 
     }
 }
 
+// mbar_wait with its first poll inline: the call is made only when the phase is
+// not complete yet.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, unsigned parity, volatile int* abort, int* status,
+                                               int* diag, int where, int slot, int stage, int extra) {
+    return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort, status, diag, where, slot, stage, extra);
+}
+
 // Bounded wait used when draining copies in flight before exit (ignores abort).
 __device__ __noinline__ void mbar_drain(uint64_t* bar, unsigned parity) {
     const uint64_t t0 = globaltimer();
