@@ -241,12 +241,18 @@ const char* moe_strerror(int code);
  * The copy shares the GPU with the FFN over HBM-resident experts. */
 int moe_layer_set_copy_ctas(moe_layer* L, int ctas);
 
-/* Copy timing: after moe_layer_profile(L, n) the next n cold_gather calls record
- * CUDA events around their byte copy on the layer's copy stream (n = 0 stops and
- * frees them).  moe_layer_profile_read waits for them and writes up to `max`
- * durations in ms to host float copy_ms[] and their number to *n_out. */
+/* Timing: after moe_layer_profile(L, n) (which first waits for the device to go
+ * idle) the next n cold_gather calls record CUDA events around their byte copy on
+ * the layer's copy stream, and the next n moe_grouped_ffn calls record events
+ * around their kernels on the caller's stream; n = 0 stops and frees them.
+ * moe_layer_profile_read waits for the copy records and writes up to `max`
+ * durations in ms to host float copy_ms[] and their number to *n_out.
+ * moe_layer_profile_read_ffn does the same for the FFN calls: each duration is the
+ * call's kernel time without the wait for the cold copy (start to the join, plus
+ * the join to the end). */
 int moe_layer_profile(moe_layer* L, int max_records);
 int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out);
+int moe_layer_profile_read_ffn(moe_layer* L, float* ffn_ms, int max, int* n_out);
 
 /* Test hook for host-side fault injection: what = 1 makes the next acting
  * residency_update fail with MOE_ERR_INJECTED before any copy or map change (as a

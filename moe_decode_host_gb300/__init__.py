@@ -118,6 +118,13 @@ class Layer:
               "moe_layer_profile_read")
         return out[: n.value].copy()
 
+    def profile_read_ffn(self, max_records: int) -> np.ndarray:
+        out = np.zeros(max(1, max_records), np.float32)
+        n = ctypes.c_int()
+        check(lib.moe_layer_profile_read_ffn(self.handle, out.ctypes.data, max_records, ctypes.byref(n)),
+              "moe_layer_profile_read_ffn")
+        return out[: n.value].copy()
+
     def inject_fault(self, what: int):
         check(lib.moe_layer_inject_fault(self.handle, what), "moe_layer_inject_fault")
 

@@ -66,6 +66,7 @@ _SIGS = {
     "moe_layer_set_copy_ctas": (_I, [_P, _I]),
     "moe_layer_profile": (_I, [_P, _I]),
     "moe_layer_profile_read": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
+    "moe_layer_profile_read_ffn": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "moe_link_probe": (_I, [_P, _P, _Z, _I, _P]),
     "moe_debug_e2m1_pairs": (_I, [_P, _P]),
 }

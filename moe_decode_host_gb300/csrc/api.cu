@@ -47,6 +47,8 @@ struct moe_layer {
     int copy_ctas = 0;
     std::vector<cudaEvent_t> prof_ev;  // pairs of events around recorded cold copies
     int prof_n = 0;
+    std::vector<cudaEvent_t> fprof_ev;  // quadruples around recorded FFN calls (see moe_layer_profile_read_ffn)
+    int fprof_n = 0;
     long steps = 0;
     int fault = 0;
 };
@@ -119,10 +121,11 @@ bool moe::encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* bas
 
 namespace {
 
-// 2D u8 view [rows][row_bytes] at base: the decode kernel's box (128 bytes x 32
-// rows, 128-byte swizzle) and the prefill kernel's (32 bytes x 128 rows, plain).
-bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
-    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 128, 32,
+// 2D u8 view [rows][row_bytes] at base: the decode kernel's box (128 bytes x
+// box_rows rows, 128-byte swizzle) and the prefill kernel's (32 bytes x 128 rows,
+// plain).
+bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows, uint32_t box_rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 128, box_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
@@ -141,6 +144,9 @@ void free_prof(moe_layer* L) {
     for (cudaEvent_t e : L->prof_ev) cudaEventDestroy(e);
     L->prof_ev.clear();
     L->prof_n = 0;
+    for (cudaEvent_t e : L->fprof_ev) cudaEventDestroy(e);
+    L->fprof_ev.clear();
+    L->fprof_n = 0;
 }
 
 void free_layer(moe_layer* L) {
@@ -268,8 +274,8 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     if (err == cudaSuccess) {
         std::vector<ExpertMaps> maps(p.E);
         for (int i = 0; i < p.E; ++i) {
-            if (!encode_plane(&maps[i].w13n, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||
-                !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H) ||
+            if (!encode_plane(&maps[i].w13n, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I, 32) ||
+                !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H, 64) ||
                 !encode_plane_raw(&maps[i].w13r, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||
                 !encode_plane_raw(&maps[i].w2r, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H)) {
                 free_layer(L);
@@ -378,19 +384,28 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     a.w2n = L->lay.w2n;
     a.w2s = L->lay.w2s;
     cudaStream_t st = S(stream);
-    cudaError_t err = launch_ffn_prep(a, workspace, st);
+    // profiled calls record: start, end of the work before the join, after the
+    // join, end (the two middle events coincide when no copy is pending)
+    cudaEvent_t* pe = L->fprof_n < (int)L->fprof_ev.size() / 4 ? &L->fprof_ev[4 * L->fprof_n++] : nullptr;
+    cudaError_t err = pe ? cudaEventRecord(pe[0], st) : cudaSuccess;
+    if (err == cudaSuccess) err = launch_ffn_prep(a, workspace, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (L->copy_pending) {
         // experts in HBM first, while the cold copy is in flight; then the cold ones
         err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
         if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
         if (err == cudaSuccess) err = join_copy(L, st);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
         if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 2, L->sm_count, st);
         if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 2, L->sm_count, st);
     } else {
-        err = launch_ffn_phase(a, 0, 0, L->sm_count, st);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 0, L->sm_count, st);
         if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 0, L->sm_count, st);
     }
+    if (err == cudaSuccess && pe) err = cudaEventRecord(pe[3], st);
     return cuda_status(err);
 }
 
@@ -508,15 +523,16 @@ int moe_layer_set_copy_ctas(moe_layer* L, int ctas) {
 int moe_layer_profile(moe_layer* L, int max_records) {
     if (!L || max_records < 0) return MOE_ERR_INVALID_ARG;
     if (L->copy_stream && cudaStreamSynchronize(L->copy_stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
     free_prof(L);
-    for (int i = 0; i < 2 * max_records; ++i) {
+    for (int i = 0; i < 6 * max_records; ++i) {
         cudaEvent_t e;
         if (cudaEventCreate(&e) != cudaSuccess) {
             cudaGetLastError();
             free_prof(L);
             return MOE_ERR_CUDA;
         }
-        L->prof_ev.push_back(e);
+        (i < 2 * max_records ? L->prof_ev : L->fprof_ev).push_back(e);
     }
     return MOE_OK;
 }
@@ -530,6 +546,23 @@ int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
+    }
+    *n_out = n;
+    return MOE_OK;
+}
+
+int moe_layer_profile_read_ffn(moe_layer* L, float* ffn_ms, int max, int* n_out) {
+    if (!L || !n_out || max < 0 || (max > 0 && !ffn_ms)) return MOE_ERR_INVALID_ARG;
+    const int n = L->fprof_n < max ? L->fprof_n : max;
+    for (int i = 0; i < n; ++i) {
+        const cudaEvent_t* e = &L->fprof_ev[4 * i];
+        float before = 0.f, after = 0.f;
+        if (cudaEventSynchronize(e[3]) != cudaSuccess || cudaEventElapsedTime(&before, e[0], e[1]) != cudaSuccess ||
+            cudaEventElapsedTime(&after, e[2], e[3]) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        ffn_ms[i] = before + after;
     }
     *n_out = n;
     return MOE_OK;

@@ -8,9 +8,11 @@
 // the few tokens routed to it, so the kernel is bound by HBM bandwidth.
 //
 // Structure (one persistent CTA per SM):
-//  - a producer warp streams 128-byte-wide slices of the weight rows of each task
-//    (an expert and 32 output rows) into a ring of shared-memory stages with 2D
-//    TMA loads (128-byte swizzle), signalling mbarriers;
+//  - two producer threads (one per producer warp, taking alternate stages) stream
+//    128-byte-wide slices of the weight rows of each task (an expert and 32 or 64
+//    output rows) into a ring of shared-memory stages with 2D TMA loads (128-byte
+//    swizzle), and with them the stage's slice of the bucket-ordered activation
+//    rows of the expert's tokens (one 2D TMA load), signalling mbarriers;
 //  - eight consumer warps dequantise the E2M1 nibbles in registers (one
 //    e2m1x2 -> f16x2 conversion per byte) and feed mma.sync m16n8k16 as an exact
 //    f16 x f16 -> fp32 dot-product engine; each 32-element block's E8M0 scale is
@@ -18,7 +20,8 @@
 //    reduction dimension; partial sums meet in shared memory in a fixed order.
 // Each lane of a quad reads 8 elements of each 32-element block from the staged
 // K-major rows, so every mma step sees a single block.  Activations are staged as f16 with an exact
-// power-of-two prescale per row.  Every wait is bounded by a deadline; a wait
+// power-of-two prescale per row, in bucket order (row i belongs to entries[i]), so
+// that an expert's tokens are consecutive rows.  Every wait is bounded by a deadline; a wait
 // that runs out sets MOE_ERR_TIMEOUT in the status word and the CTA drains its
 // copies and returns.
 #include <cuda.h>
@@ -29,7 +32,8 @@ namespace moe {
 namespace {
 
 constexpr int kConsumers = 8;
-constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kProducers = 2;  // producer warps; producer p fills the stages g with g % 2 == p
+constexpr int kThreads = 32 * (kConsumers + kProducers);
 constexpr int kMaxE = 1024;
 constexpr int kSliceBytes = 128;  // bytes of one row per stage (256 elements)
 
@@ -41,20 +45,38 @@ template <>
 struct Cfg<0> {
     static constexpr int kRows = 64, kNTile = 2, kRT = 2, kKS = 4, kTaskRows = 32;
 };
-// phase 1: task = 32 rows of w2; one 16-row tile per warp; 2 row tiles x 4 K-splits
+// phase 1: task = 64 rows of w2 (one 8 KB stage, like phase 0); one 16-row tile per
+// warp; 4 row tiles x 2 K-splits
 template <>
 struct Cfg<1> {
-    static constexpr int kRows = 32, kNTile = 1, kRT = 2, kKS = 4, kTaskRows = 32;
+    static constexpr int kRows = 64, kNTile = 1, kRT = 4, kKS = 2, kTaskRows = 64;
 };
-constexpr int kActStride = 576;  // bytes per activation column slice in a stage (512 + 64 pad)
-constexpr int kStageBudget = 160 * 1024;
+constexpr int kActRow = 512;  // bytes of one activation row's slice in a stage (256 f16)
+
+struct alignas(16) SmemHead {
+    uint64_t full[64];
+    uint64_t empty[64];
+    int seq[64];  // global stage number last issued into each slot
+    int D;
+    int abort;
+    int pad[2];
+    int e[kMaxE];     // experts of this launch, ascending
+    int cnt[kMaxE];   // and for each: its picks,
+    int off[kMaxE];   // its first bucket entry,
+    int phys[kMaxE];  // its physical id
+};
 
 template <int P, int NT>
 struct Layout {
     static constexpr int kWBytes = Cfg<P>::kRows * 128;
-    static constexpr int kABytes = 8 * NT * kActStride;
+    static constexpr int kABytes = 8 * NT * kActRow;
     static constexpr int kStageBytes = ((kWBytes + kABytes) + 1023) & ~1023;
-    static constexpr int kStages = (kStageBudget / kStageBytes) < 64 ? (kStageBudget / kStageBytes) : 64;
+    static constexpr int kRedBytes =
+        (int)sizeof(float) * (Cfg<P>::kKS - 1) * Cfg<P>::kRT * Cfg<P>::kNTile * NT * 4 * 32;
+    static constexpr int kBudget = 232448 - 1024 - (int)sizeof(SmemHead) - kRedBytes;
+    // an even number of slots, so that each producer owns the slots of its parity
+    static constexpr int kStages = ((kBudget / kStageBytes) < 64 ? (kBudget / kStageBytes) : 64) & ~1;
+    static_assert(kStages >= 4, "ring too shallow");
 };
 
 // Waits until the producer has stamped `slot` with global stage `g` (it stamps a
@@ -99,9 +121,9 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 // 128-byte swizzle this keeps the two rows a quarter-warp reads in disjoint banks.
 __device__ __forceinline__ int perm8(int g) { return (g >> 1) | ((g & 1) << 2); }
 
-// B operand from the stage's activation slices: column n (token or pick) of the
-// stage lives at act + n * kActStride, 256 prescaled f16 values; missing columns read
-// as zero.
+// B operand from the stage's activation slices: column n (bucket row off + tb + n)
+// of the stage lives at act + n * kActRow, 256 prescaled f16 values; missing columns
+// read as zero.
 template <int NT>
 struct SmemB {
     const uint8_t* col[NT];  // this lane's column in each n-tile, or nullptr
@@ -178,34 +200,26 @@ __device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow
     }
 }
 
-struct alignas(16) SmemHead {
-    uint64_t full[64];
-    uint64_t empty[64];
-    int seq[64];  // global stage number last issued into each slot
-    int list[kMaxE];
-    int D;
-    int abort;
-};
-
-// Task t of this CTA: expert list[t / tiles], rows (t % tiles) * 64.
+// Task t of this CTA: listed expert t / tiles, row tile t % tiles.
 struct TaskInfo {
-    int e, rt, cnt, off, phys;
+    int rt, cnt, off, phys;
     bool valid;
 };
 
 __device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& hd, int task, int tiles) {
     TaskInfo ti;
-    ti.e = hd.list[task / tiles];
+    const int i = task / tiles;
     ti.rt = task % tiles;
-    ti.cnt = __ldg(a.counts + ti.e);
-    ti.off = __ldg(a.offsets + ti.e);
-    ti.phys = __ldg(a.phys_ids + __ldg(a.entries + ti.off));
+    ti.cnt = hd.cnt[i];
+    ti.off = hd.off[i];
+    ti.phys = hd.phys[i];
     ti.valid = ti.phys >= 0 && ti.phys < a.n_phys;
     return ti;
 }
 
 template <int P, int NT>
-__global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo, int hi, int sel) {
+__global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
+                                                                int lo, int hi, int sel) {
     using C = Cfg<P>;
     using L = Layout<P, NT>;
     constexpr int NTILE = C::kNTile;
@@ -219,8 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
     const int ngroups = K / 128;
     const int nst = (ngroups + 1) / 2;
     const int tiles = (P == 0 ? I : H) / C::kTaskRows;
-    const __half* act = P == 0 ? a.x16 : a.h16;  // prescaled f16 activations
-    const int act_len = K;
 
     // active experts in this launch's token-count range and placement class, ascending
     if (warp == 0) {
@@ -237,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
                 }
             }
             const unsigned m = __ballot_sync(0xffffffffu, act_e);
-            if (act_e) hd.list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
+            if (act_e) hd.e[cnt + __popc(m & ((1u << lane) - 1u))] = e;
             cnt += __popc(m);
         }
         if (lane == 0) {
@@ -252,74 +264,70 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
         }
     }
     __syncthreads();
+    // per listed expert: picks, first bucket entry, physical id (all threads)
+    for (int i = threadIdx.x; i < hd.D; i += kThreads) {
+        const int e = hd.e[i];
+        const int off = __ldg(a.offsets + e);
+        hd.cnt[i] = __ldg(a.counts + e);
+        hd.off[i] = off;
+        hd.phys[i] = __ldg(a.phys_ids + __ldg(a.entries + off));
+    }
+    __syncthreads();
     const int ntask = hd.D * tiles;
     volatile int* abort = &hd.abort;
 
-    if (warp == kConsumers) {
-        // ---------------- producer (whole warp) ----------------
-        int slot = 0;
-        unsigned phase = 0;
-        int gstage = 0;  // global stage number in this CTA's stream
-        bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
-            const TaskInfo ti = task_info(a, hd, task, tiles);
-            if (!ti.valid) continue;
-            const CUtensorMap* map = P == 0 ? &a.tmaps[ti.phys].w13n : &a.tmaps[ti.phys].w2n;
-            // descriptors live in global memory and a layer's table may reuse the address
-            // of a destroyed one: acquire the current contents for the async proxy
-            if (lane == 0) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
-            const int r0 = ti.rt * C::kTaskRows;
-            for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
-                const int ncols = min(8 * NT, ti.cnt - tb);
-                // this lane's activation row (one column of the tile), if any
-                const __half* arow = nullptr;
-                if (lane < ncols) {
-                    const int pick = __ldg(a.entries + ti.off + tb + lane);
-                    arow = act + (size_t)(P == 0 ? pick / a.k : pick) * act_len;
-                }
-                for (int s = 0; s < nst; ++s) {
-                    bool got = true;
-                    if (lane == 0)
-                        got = mbar_wait(&hd.empty[slot], phase ^ 1u, abort, a.status, a.diag, 2, slot, s,
-                                        (task << 8) | ncols);
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
-                        ok = false;
-                        break;
-                    }
-                    const int kelems = min(256, K - s * 256);  // 256, or 128 at an odd tail
-                    const unsigned abytes = (unsigned)kelems * 2u;
-                    uint8_t* dst = stages + slot * L::kStageBytes;
-                    if (lane == 0) {
-                        *reinterpret_cast<volatile int*>(&hd.seq[slot]) = gstage;
-                        mbar_arrive_expect_tx(&hd.full[slot], (unsigned)L::kWBytes + abytes * (unsigned)ncols);
-                        if (P == 0) {
-                            tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
-                            tma_load_2d(dst + C::kTaskRows * kSliceBytes, map, s * kSliceBytes, I + r0,
-                                        &hd.full[slot]);
-                        } else {
-                            tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+    if (warp >= kConsumers) {
+        // ---------------- producers (lane 0 of each producer warp) ----------------
+        if (lane == 0) {
+            const unsigned pp = (unsigned)(warp - kConsumers);
+            int slot = 0;
+            unsigned phase = 0;
+            int gstage = 0;  // global stage number in this CTA's stream
+            bool ok = true;
+            for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+                const TaskInfo ti = task_info(a, hd, task, tiles);
+                if (!ti.valid) continue;
+                const CUtensorMap* map = P == 0 ? &a.tmaps[ti.phys].w13n : &a.tmaps[ti.phys].w2n;
+                // descriptors live in global memory and a layer's table may reuse the
+                // address of a destroyed one: acquire the current contents for the async proxy
+                asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                const int r0 = ti.rt * C::kTaskRows;
+                for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
+                    for (int s = 0; s < nst; ++s) {
+                        if (((unsigned)gstage & 1u) == pp) {
+                            if (!mbar_wait_fast(&hd.empty[slot], phase ^ 1u, abort, a.status, a.diag, 2, slot, s,
+                                                (task << 8) | min(8 * NT, ti.cnt - tb))) {
+                                ok = false;
+                                break;
+                            }
+                            uint8_t* dst = stages + slot * L::kStageBytes;
+                            *reinterpret_cast<volatile int*>(&hd.seq[slot]) = gstage;
+                            // full boxes land even past the tensor's edge (zero filled)
+                            mbar_arrive_expect_tx(&hd.full[slot], (unsigned)(L::kWBytes + L::kABytes));
+                            if (P == 0) {
+                                tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+                                tma_load_2d(dst + C::kTaskRows * kSliceBytes, map, s * kSliceBytes, I + r0,
+                                            &hd.full[slot]);
+                            } else {
+                                tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+                            }
+                            tma_load_2d(dst + L::kWBytes, &act_map, s * 256, ti.off + tb, &hd.full[slot]);
                         }
-                    }
-                    __syncwarp();
-                    if (arow)
-                        bulk_load(dst + L::kWBytes + lane * kActStride, arow + (size_t)s * 256, abytes,
-                                  &hd.full[slot]);
-                    ++gstage;
-                    if (++slot == L::kStages) {
-                        slot = 0;
-                        phase ^= 1u;
+                        ++gstage;
+                        if (++slot == L::kStages) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
-        }
-        // drain: every issued copy has landed before the CTA may exit
-        if (lane == 0) {
-            for (int s = 0; s < L::kStages; ++s) {
-                // slot s was last filled in the current phase if it lies before the next
-                // slot to fill, else in the previous one (or never)
-                const unsigned par = (s < slot) ? phase : (phase ^ 1u);
-                mbar_drain(&hd.full[s], par);
+            // drain: every copy this producer issued has landed before the CTA may exit.
+            // Slot s (of this producer's parity) last held stage s + S * ((G - 1 - s) / S)
+            // of the G stages counted, if s < G.
+            for (int s = (int)pp; s < L::kStages; s += kProducers) {
+                if (s >= gstage) break;
+                const int g_last = s + L::kStages * ((gstage - 1 - s) / L::kStages);
+                mbar_drain(&hd.full[s], (unsigned)(g_last / L::kStages) & 1u);
             }
         }
         return;
@@ -331,8 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
     const int g = lane >> 2, q = lane & 3;
     const int pg = perm8(g);
     const size_t srs = (size_t)K / 32;  // scale bytes per row
-    int slot = 0;
-    unsigned phase = 0;
     int gstage = 0;
     bool done = false;
     for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
@@ -342,10 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
             // zero outputs for an expert whose physical id is out of range
             if (ti.rt == 0 && threadIdx.x == 0) set_status(a.status, MOE_ERR_BAD_EXPERT);
             for (int c = threadIdx.x; c < ti.cnt * C::kTaskRows; c += 32 * kConsumers) {
-                const int pick = __ldg(a.entries + ti.off + c / C::kTaskRows);
+                const int pos = ti.off + c / C::kTaskRows;
                 const int row = r0 + c % C::kTaskRows;
-                if (P == 0) a.h[(size_t)pick * I + row] = 0.f;
-                else a.y[(size_t)pick * H + row] = 0.f;
+                if (P == 0) a.h[(size_t)pos * I + row] = 0.f;
+                else a.y[(size_t)__ldg(a.entries + pos) * H + row] = 0.f;
             }
             continue;
         }
@@ -383,6 +389,20 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
         }
         for (int tb = 0; tb < ti.cnt; tb += 8 * NT) {
             const int ncols = min(8 * NT, ti.cnt - tb);
+            // this lane's output columns: prescale (and for the down phase the pick),
+            // fetched now so that their latency hides behind the stage loop
+            // (the exponents are converted where they are used, so nothing waits here)
+            int cexp[NT][2];
+            int cpick[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int col = nt * 8 + 2 * q + c2;
+                    const int pos = ti.off + tb + col;
+                    cexp[nt][c2] = col < ncols ? __ldg(a.gexp + pos) : 0;
+                    cpick[nt][c2] = (P == 1 && col < ncols) ? __ldg(a.entries + pos) : 0;
+                }
             float acc[NTILE][NT][4];
 #pragma unroll
             for (int i = 0; i < NTILE; ++i)
@@ -390,8 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
-            // scale words of this warp's first stage, then one own stage ahead
-            uint32_t sc[2][NTILE][2], scn[2][NTILE][2];
+            // this warp's stages are ks, ks + KS, ks + 2 KS, ...; their scale words sit in
+            // two register sets used alternately, each refilled right after use for the
+            // stage two own stages later (no register moves that would wait on a load)
+            uint32_t scA[2][NTILE][2], scB[2][NTILE][2];
             auto load_sc = [&](int s, uint32_t(&dst)[2][NTILE][2]) {
                 const int G0 = 2 * s;
                 const int ng = min(2, ngroups - G0);
@@ -404,39 +426,34 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
                             dst[gl][i][r] = (gl < ng) ? ld_u32(sb + (size_t)grow[i][r] * srs + (size_t)(G0 + gl) * 4)
                                                       : 0u;
             };
-            if (ks < nst) load_sc(ks, sc);
+            if (ks < nst) load_sc(ks, scA);
+            if (ks + C::kKS < nst) load_sc(ks + C::kKS, scB);
             bool ok = true;
-            for (int s = 0; s < nst; ++s) {
-                if ((s % C::kKS) == ks) {
-                    if (s + C::kKS < nst) load_sc(s + C::kKS, scn);
-                    if (!seq_wait(&hd.seq[slot], gstage, abort, a.status, a.diag, slot) ||
-                        !mbar_wait(&hd.full[slot], phase, abort, a.status, a.diag, 1, slot, s, (task << 8) | ncols)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* stage = stages + slot * L::kStageBytes;
-                    SmemB<NT> bl;
+            auto own_stage = [&](int s, uint32_t(&sc)[2][NTILE][2]) -> bool {
+                const int gs = gstage + s;
+                const int sl = gs % L::kStages;
+                const unsigned ph = (unsigned)(gs / L::kStages) & 1u;
+                if (!(hd.seq[sl] == gs || seq_wait(&hd.seq[sl], gs, abort, a.status, a.diag, sl)) ||
+                    !mbar_wait_fast(&hd.full[sl], ph, abort, a.status, a.diag, 1, sl, s, (task << 8) | ncols))
+                    return false;
+                const uint8_t* stage = stages + sl * L::kStageBytes;
+                SmemB<NT> bl;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int n = nt * 8 + g;
-                        bl.col[nt] = n < ncols ? stage + L::kWBytes + n * kActStride : nullptr;
-                    }
-                    stage_mma<NTILE, NT>(stage, srow, sc, min(2, ngroups - 2 * s), bl, acc);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&hd.empty[slot]);
-#pragma unroll
-                    for (int gl = 0; gl < 2; ++gl)
-#pragma unroll
-                        for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                            for (int r = 0; r < 2; ++r) sc[gl][i][r] = scn[gl][i][r];
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int n = nt * 8 + g;
+                    bl.col[nt] = n < ncols ? stage + L::kWBytes + n * kActRow : nullptr;
                 }
-                ++gstage;
-                if (++slot == L::kStages) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
+                stage_mma<NTILE, NT>(stage, srow, sc, min(2, ngroups - 2 * s), bl, acc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hd.empty[sl]);
+                if (s + 2 * C::kKS < nst) load_sc(s + 2 * C::kKS, sc);
+                return true;
+            };
+            for (int s = ks; s < nst && ok; s += 2 * C::kKS) {
+                ok = own_stage(s, scA);
+                if (ok && s + C::kKS < nst) ok = own_stage(s + C::kKS, scB);
             }
+            gstage += nst;
             // partial sums of the K-splits meet in shared memory (fixed order)
             constexpr int kFrag = NTILE * NT * 4 * 32;
             asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
@@ -468,16 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
                     for (int c = 0; c < 4; ++c) {
                         const int col = nt * 8 + 2 * q + (c & 1);
                         if (col >= ncols) continue;
-                        const int pick = __ldg(a.entries + ti.off + tb + col);
                         const int orow = r0 + 16 * rt + pg + ((c >> 1) << 3);  // output row
+                        const float sx = pow2i(cexp[nt][c & 1]);
                         if constexpr (P == 0) {
-                            const float sx = pow2i(__ldg(a.xexp + pick / a.k));
                             const float gv = acc[0][nt][c] * sx;
                             const float uv = acc[NTILE - 1][nt][c] * sx;
                             const float hv = gv / (1.0f + expf(-gv)) * uv;
-                            a.h[(size_t)pick * I + orow] = hv;
+                            a.h[(size_t)(ti.off + tb + col) * I + orow] = hv;
                         } else {
-                            a.y[(size_t)pick * H + orow] = acc[0][nt][c] * pow2i(__ldg(a.hexp + pick));
+                            a.y[(size_t)cpick[nt][c & 1] * H + orow] = acc[0][nt][c] * sx;
                         }
                     }
             }
@@ -500,92 +516,49 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, int lo,
     }
 }
 
-// One CTA per pick of the selected class: per-pick power-of-two prescale of h
-// (from the row's amax) and its f16 copy for the down projection.
-__global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h, const int32_t* __restrict__ phys_ids,
-                                                    int n_hot, int n_phys, int sel, int I, __half* __restrict__ h16,
-                                                    int32_t* __restrict__ hexp) {
+// Row of `rows` fp32 or bf16 values -> f16 with a power-of-two prescale that puts
+// the row's amax in [2^14, 2^15) (exact up to the f16 rounding of each value).  One
+// CTA of 256 threads; up to 4 chunks of 8 values per thread stay in registers.
+template <bool BF16>
+__device__ __forceinline__ void prescale_row(const void* src_row, int len, __half* dst_row, int32_t* exp_out) {
     __shared__ float wmax[8];
-    const int p = blockIdx.x;
-    const int ph = __ldg(phys_ids + p);
-    const bool hot = ph >= 0 && ph < n_hot;
-    const bool valid = ph >= 0 && ph < n_phys;
-    if (sel == 1 && !hot) return;
-    if (sel == 2 && (hot || !valid)) return;
-    const float4* src = reinterpret_cast<const float4*>(h + (size_t)p * I);
-    const int nch = I / 4;
-    constexpr int kPer = 4;  // up to 4 float4 per thread kept in registers (I <= 4096)
-    float4 v[kPer];
+    const int nch = len / 8;
+    constexpr int kPer = 4;
+    float v[kPer][8];
     float amax = 0.f;
-    auto upd = [&](const float4& f) { amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)))); };
+    auto load = [&](int c, float (&f)[8]) {
+        if constexpr (BF16) {
+            const uint4 w = __ldg(reinterpret_cast<const uint4*>(src_row) + c);
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int c = threadIdx.x + u * 256;
-        if (c < nch) {
-            v[u] = __ldcg(src + c);
-            upd(v[u]);
+            for (int i = 0; i < 4; ++i) {
+                const float2 t = __bfloat1622float2(p[i]);
+                f[2 * i] = t.x;
+                f[2 * i + 1] = t.y;
+            }
+        } else {
+            const float4 a0 = __ldcg(reinterpret_cast<const float4*>(src_row) + 2 * c);
+            const float4 a1 = __ldcg(reinterpret_cast<const float4*>(src_row) + 2 * c + 1);
+            f[0] = a0.x, f[1] = a0.y, f[2] = a0.z, f[3] = a0.w;
+            f[4] = a1.x, f[5] = a1.y, f[6] = a1.z, f[7] = a1.w;
         }
-    }
-    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) upd(__ldcg(src + c));
+    };
+    auto upd = [&](const float (&f)[8]) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
-    __syncthreads();
-    amax = wmax[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
-    const int e = prescale_exp(amax);
-    const float sc = pow2i(-e);
-    uint2* dst = reinterpret_cast<uint2*>(h16 + (size_t)p * I);
-    auto conv = [&](const float4& f) {
-        __half2 lo = __floats2half2_rn(f.x * sc, f.y * sc);
-        __half2 hi = __floats2half2_rn(f.z * sc, f.w * sc);
-        uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&lo);
-        o.y = *reinterpret_cast<uint32_t*>(&hi);
-        return o;
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
     };
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int c = threadIdx.x + u * 256;
-        if (c < nch) dst[c] = conv(v[u]);
-    }
-    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) dst[c] = conv(__ldcg(src + c));
-    if (threadIdx.x == 0) hexp[p] = e;
-}
-
-// One CTA per token: per-token power-of-two prescale and f16 copy of x.
-__global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int k,
-                                                    __half* __restrict__ x16, int32_t* __restrict__ xexp) {
-    __shared__ float wmax[8];
-    const int t = blockIdx.x;
-    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    uint4* out = reinterpret_cast<uint4*>(x16 + (size_t)t * H);
-    const int nch = H / 8;
-    constexpr int kPer = 4;  // up to 4 chunks of 8 per thread kept in registers (H <= 8192)
-    uint4 v[kPer];
-    float amax = 0.f;
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int c = threadIdx.x + u * 256;
         if (c < nch) {
-            v[u] = __ldg(row + c);
-            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float2 f = __bfloat1622float2(p[i]);
-                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-            }
+            load(c, v[u]);
+            upd(v[u]);
         }
     }
     for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) {
-        uint4 w = __ldg(row + c);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(p[i]);
-            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
+        float f[8];
+        load(c, f);
+        upd(f);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -595,25 +568,48 @@ __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restr
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
     const int p = prescale_exp(amax);
-    const float s = pow2i(-p);
-    auto conv = [&](const uint4& in) {
-        const __nv_bfloat162* pi = reinterpret_cast<const __nv_bfloat162*>(&in);
+    const float sc = pow2i(-p);
+    auto store = [&](int c, const float (&f)[8]) {
         uint4 o;
         __half2* po = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f = __bfloat1622float2(pi[i]);
-            po[i] = __floats2half2_rn(f.x * s, f.y * s);
-        }
-        return o;
+        for (int i = 0; i < 4; ++i) po[i] = __floats2half2_rn(f[2 * i] * sc, f[2 * i + 1] * sc);
+        reinterpret_cast<uint4*>(dst_row)[c] = o;
     };
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int c = threadIdx.x + u * 256;
-        if (c < nch) out[c] = conv(v[u]);
+        if (c < nch) store(c, v[u]);
     }
-    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) out[c] = conv(__ldg(row + c));
-    if (threadIdx.x == 0) xexp[t] = p;
+    for (int c = threadIdx.x + kPer * 256; c < nch; c += 256) {
+        float f[8];
+        load(c, f);
+        store(c, f);
+    }
+    if (threadIdx.x == 0) *exp_out = p;
+}
+
+// One CTA per bucket row i: x of token entries[i] / k, prescaled, into g row i.
+__global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k,
+                                                    const int32_t* __restrict__ entries, int gstride,
+                                                    __half* __restrict__ g, int32_t* __restrict__ gexp) {
+    const int i = blockIdx.x;
+    const int t = __ldg(entries + i) / k;
+    prescale_row<true>(x + (size_t)t * H, H, g + (size_t)i * gstride, gexp + i);
+}
+
+// One CTA per bucket row i of the selected class: h row i, prescaled, into g row i.
+__global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h, const int32_t* __restrict__ entries,
+                                                    const int32_t* __restrict__ phys_ids, int n_hot, int n_phys,
+                                                    int sel, int I, int gstride, __half* __restrict__ g,
+                                                    int32_t* __restrict__ gexp) {
+    const int i = blockIdx.x;
+    const int ph = __ldg(phys_ids + __ldg(entries + i));
+    const bool hot = ph >= 0 && ph < n_hot;
+    const bool valid = ph >= 0 && ph < n_phys;
+    if (sel == 1 && !hot) return;
+    if (sel == 2 && (hot || !valid)) return;
+    prescale_row<false>(h + (size_t)i * I, I, g + (size_t)i * gstride, gexp + i);
 }
 
 __global__ void debug_e2m1_kernel(uint32_t* out) {
@@ -626,34 +622,27 @@ __global__ void debug_e2m1_kernel(uint32_t* out) {
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t x16, xexp, h, h16, hexp, g, total;
+    size_t g, gexp, h, total;
 };
 
 WsLayout ws_layout(int T, int k, int H, int I) {
     WsLayout w;
+    const size_t n = (size_t)T * k;
     size_t o = 0;
-    w.x16 = o;
-    o = align256(o + (size_t)T * H * sizeof(__half));
-    w.xexp = o;
-    o = align256(o + (size_t)T * sizeof(int32_t));
-    w.h = o;
-    o = align256(o + (size_t)T * k * I * sizeof(float));
-    w.h16 = o;
-    o = align256(o + (size_t)T * k * I * sizeof(__half));
-    w.hexp = o;
-    o = align256(o + (size_t)T * k * sizeof(int32_t));
     w.g = o;
-    if (T > kTcMinTokens) o = align256(o + (size_t)T * k * (H > I ? H : I) * sizeof(__half));
+    o = align256(o + n * (H > I ? H : I) * sizeof(__half));
+    w.gexp = o;
+    o = align256(o + n * sizeof(int32_t));
+    w.h = o;
+    o = align256(o + n * I * sizeof(float));
     w.total = o;
     return w;
 }
 
 template <int P, int NT>
 size_t smem_bytes() {
-    using C = Cfg<P>;
     using L = Layout<P, NT>;
-    return 1024 + (size_t)L::kStages * L::kStageBytes + sizeof(SmemHead) +
-           sizeof(float) * (size_t)(C::kKS - 1) * C::kRT * C::kNTile * NT * 4 * 32;
+    return 1024 + (size_t)L::kStages * L::kStageBytes + sizeof(SmemHead) + (size_t)L::kRedBytes;
 }
 
 template <int P, int NT>
@@ -666,7 +655,10 @@ cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cu
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    ffn_tma_kernel<P, NT><<<grid, kThreads, sm, st>>>(a, lo, hi, sel);
+    // the stage's activation slice: 256 elements of 8 * NT consecutive bucket rows
+    CUtensorMap act_map;
+    if (!encode_act_map(&act_map, a, P, 256, 8 * NT, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    ffn_tma_kernel<P, NT><<<grid, kThreads, sm, st>>>(a, act_map, lo, hi, sel);
     return cudaGetLastError();
 }
 
@@ -674,17 +666,21 @@ cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cu
 
 size_t ffn_decode_workspace(int T, int k, int H, int I) { return ws_layout(T, k, H, I).total; }
 
+bool encode_act_map(CUtensorMap* m, const FfnArgs& a, int phase, uint32_t box_inner, uint32_t box_rows,
+                    CUtensorMapSwizzle sw) {
+    const uint64_t stride = (uint64_t)(a.H > a.I ? a.H : a.I) * sizeof(__half);
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.g, (uint64_t)(phase == 0 ? a.H : a.I),
+                          (uint64_t)a.T * a.k, stride, box_inner, box_rows, sw);
+}
+
 cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     const WsLayout w = ws_layout(a.T, a.k, a.H, a.I);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    a.x16 = reinterpret_cast<__half*>(ws + w.x16);
-    a.xexp = reinterpret_cast<int32_t*>(ws + w.xexp);
+    a.g = reinterpret_cast<__half*>(ws + w.g);
+    a.gexp = reinterpret_cast<int32_t*>(ws + w.gexp);
     a.h = reinterpret_cast<float*>(ws + w.h);
-    a.h16 = reinterpret_cast<__half*>(ws + w.h16);
-    a.hexp = reinterpret_cast<int32_t*>(ws + w.hexp);
-    a.g = a.T > kTcMinTokens ? reinterpret_cast<__half*>(ws + w.g) : nullptr;
     if (a.T == 0) return cudaSuccess;
-    xprep_kernel<<<a.T, 256, 0, st>>>(a.x, a.T, a.H, a.k, a.x16, a.xexp);
+    xprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.x, a.H, a.k, a.entries, a.H > a.I ? a.H : a.I, a.g, a.gexp);
     return cudaGetLastError();
 }
 
@@ -697,10 +693,10 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
     };
     const Range ranges[3] = {{1, 0, 8}, {2, 8, 16}, {4, 16, kTcMinTokens}};
     const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
-    const long tasks = dmax * ((phase == 0 ? a.I : a.H) / 32);
+    const long tasks = dmax * (phase == 0 ? a.I / Cfg<0>::kTaskRows : a.H / Cfg<1>::kTaskRows);
     if (phase == 1) {
-        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.phys_ids, a.n_hot, a.n_phys, sel, a.I, a.h16,
-                                                a.hexp);
+        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.entries, a.phys_ids, a.n_hot, a.n_phys, sel, a.I,
+                                                a.H > a.I ? a.H : a.I, a.g, a.gexp);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

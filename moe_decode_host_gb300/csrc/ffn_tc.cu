@@ -15,8 +15,9 @@
 //                is committed back to its two producers, each tile to the
 //                epilogue; two accumulator buffers let a tile's epilogue overlap
 //                the next tile's main loop;
-//   warp 2       TMA of the activation tiles (64 tokens x 64 elements, f16,
-//                128-byte swizzle), gathered in bucket order beforehand, into a
+//   warp 2       TMA of the activation tiles (64 bucket rows x 64 elements, f16,
+//                128-byte swizzle; the prescale kernels write the activations in
+//                bucket order, so an expert's tokens are consecutive rows), into a
 //                ring of its own;
 //   warps 4-11   converters: E2M1 -> f16 for one weight row (gate/up phase) or one
 //                half of a row's stage (down phase) per thread, each E8M0 block
@@ -67,7 +68,7 @@ struct alignas(16) TcHead {
     int abort;
     int D;
     int list[kMaxE];
-    int col_pick[4][kNMax];     // per epilogue warp: pick of each column of the pass
+    int col_pick[4][kNMax];     // per epilogue warp: output row of each column of the pass
     float col_scale[4][kNMax];  // and its activation prescale 2^p
 };
 
@@ -468,9 +469,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 // zero outputs for an expert whose physical id is out of range
                 if (t.rb == 0 && threadIdx.x == kFirstEpi * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
                 for (int c = 0; c < t.cnt; ++c) {
-                    const int pick = __ldg(a.entries + t.off + c);
-                    if (P == 0) a.h[(size_t)pick * I + r0 + t_row] = 0.f;
-                    else a.y[(size_t)pick * H + r0 + t_row] = 0.f;
+                    if (P == 0) a.h[(size_t)(t.off + c) * I + r0 + t_row] = 0.f;
+                    else a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + t_row] = 0.f;
                 }
                 continue;
             }
@@ -482,11 +482,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const float s1 = pow2i(max(-126, min(127, c1 - 127)));
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                 const int nb = min(kNMax, t.cnt - tb);
-                // the pass's columns: pick and activation prescale, fetched before the wait
+                // the pass's columns: activation prescale (and for the down phase the
+                // pick), fetched before the wait
                 for (int n = lane; n < nb; n += 32) {
-                    const int pick = __ldg(a.entries + t.off + tb + n);
-                    cpick[n] = pick;
-                    cscale[n] = pow2i(P == 0 ? __ldg(a.xexp + pick / a.k) : __ldg(a.hexp + pick));
+                    const int pos = t.off + tb + n;
+                    cpick[n] = P == 0 ? pos : __ldg(a.entries + pos);
+                    cscale[n] = pow2i(__ldg(a.gexp + pos));
                 }
                 __syncwarp();
                 if (!warp_wait(&hd.acc_full[buf], (accph >> buf) & 1u, a, abort, 19, buf, tb, task)) {
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         if constexpr (P == 0) {
                             const float gv = v0[i] * s0 * sx;
                             const float uv = v1[i] * s1 * sx;
-                            a.h[(size_t)pick * I + r0 + t_row] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            a.h[(size_t)pick * I + r0 + t_row] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // bucket row
                         } else {
                             a.y[(size_t)pick * H + r0 + t_row] = v0[i] * s0 * sx;
                         }
@@ -530,35 +531,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     }
 }
 
-// dst[i][:] = src[row(i)][:] for every bucketed pick i; row = token (mode 0) or pick (mode 1).
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restrict__ src, int len,
-                                                          const int32_t* __restrict__ entries, int n, int k, int mode,
-                                                          __half* __restrict__ dst) {
-    const int i = blockIdx.x;
-    if (i >= n) return;
-    const int pick = __ldg(entries + i);
-    const int row = mode == 0 ? pick / k : pick;
-    const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)row * len);
-    uint4* d = reinterpret_cast<uint4*>(dst + (size_t)i * len);
-    for (int c = threadIdx.x; c < len / 8; c += blockDim.x) d[c] = __ldg(s + c);
-}
-
 }  // namespace
 
 size_t ffn_tc_smem_bytes() { return kTcSmem; }
 
 cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_count, cudaStream_t st) {
-    const int K = phase == 0 ? a.H : a.I;
     const int n = a.T * a.k;
-    __half* g = a.g;
-    if (!g) return cudaErrorInvalidValue;
-    gather_rows_kernel<<<n, 256, 0, st>>>(phase == 0 ? a.x16 : a.h16, K, a.entries, n, a.k, phase, g);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
+    // activation tiles: 64 elements (128 bytes) x 64 bucket rows, 128-byte swizzle
     CUtensorMap map;
-    if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g, (uint64_t)K, (uint64_t)n, (uint64_t)K * 2, 64, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    if (!encode_act_map(&map, a, phase, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     const long dmax = (long)(a.E < n / (lo + 1) + 1 ? a.E : n / (lo + 1) + 1);
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kBM);
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);

@@ -56,7 +56,7 @@ cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, in
 // a swizzled view for the decode kernel and a plain one for the prefill kernel.
 struct ExpertMaps {
     CUtensorMap w13n;  // [2I rows][H/2 bytes], box 128 B x 32 rows, 128-byte swizzle
-    CUtensorMap w2n;   // [H rows][I/2 bytes], same box
+    CUtensorMap w2n;   // [H rows][I/2 bytes], box 128 B x 64 rows, 128-byte swizzle
     CUtensorMap w13r;  // [2I rows][H/2 bytes], box 32 B x 128 rows, no swizzle
     CUtensorMap w2r;   // [H rows][I/2 bytes], same box
 };
@@ -80,13 +80,11 @@ struct FfnArgs {
     const int32_t* entries;   // [T*k]
     int E, k, H, I, T;
     const __nv_bfloat16* x;  // [T][H]
-    __half* x16;             // workspace [T][H]
-    int32_t* xexp;           // workspace [T]
-    float* h;                // workspace [T*k][I]
-    __half* h16;             // workspace [T*k][I], prescaled copy of h
-    int32_t* hexp;           // workspace [T*k]
-    __half* g;               // workspace [T*k][max(H, I)] activations gathered in bucket order
-                             // (prefill kernel only; null when T <= kTcMinTokens)
+    // workspace, all in bucket order (row i = entries[i]):
+    __half* g;               // [T*k][max(H, I)] prescaled f16 activations: x rows for the
+                             // gate/up phase, then h rows for the down phase
+    int32_t* gexp;           // [T*k] their power-of-two prescale exponents
+    float* h;                // [T*k][I] SiLU(gate) * up
     float* y;                // [T*k][H]
     int* status;
     int* diag;               // [16] where the first timed-out wait gave up
@@ -94,7 +92,12 @@ struct FfnArgs {
 };
 
 size_t ffn_decode_workspace(int T, int k, int H, int I);
-// Points the workspace fields of `a` at `workspace` and launches the activation prep.
+// 2D TMA descriptor of the bucket-ordered activations a.g for a phase (0: H
+// columns, 1: I columns), rows T*k, with the given box and swizzle.
+bool encode_act_map(CUtensorMap* m, const FfnArgs& a, int phase, uint32_t box_inner, uint32_t box_rows,
+                    CUtensorMapSwizzle sw);
+// Points the workspace fields of `a` at `workspace` and launches the x prescale
+// into bucket order.
 cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st);
 // One phase (0: gate/up -> h, 1: down -> y) over the experts selected by sel
 // (0: all, 1: placed in HBM, 2: placed in cold slots).
