@@ -28,6 +28,30 @@ import numpy as np  # noqa: E402
 HBM_NOMINAL_GBS = 8000.0
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work,
+# from the ncu captures summarised under profiles/ (a smaller layer of the same
+# expert shape; traffic scales with the experts processed).  An entry is set to
+# None whenever its kernel changes after the capture.
+NCU_TRAFFIC = {
+    # per cold expert copied: the slot writes stay in L2 during the launch
+    "cold_copy": {"bytes_per_expert": (35584 + 7168) / 2,
+                  "source": "profiles/cold_copy_kernel_c1_small.md"},
+    # per distinct expert through the decode kernels (gate/up + down launches)
+    "ffn_decode": {"bytes_per_expert": (66947840 + 678912 + 33496320) / 5,
+                   "source": "profiles/ffn_decode_kernel_c1_small.md"},
+    # per expert through the tcgen05 kernels at about 128 tokens per expert
+    "ffn_tc": {"bytes_per_expert": (1116370000 + 93775872 + 478885000 + 116250368) / 64,
+               "source": "profiles/ffn_tc_kernel_c4_small.md"},
+}
+
+
+def _traffic(kind, experts_per_call):
+    t = NCU_TRAFFIC.get(kind)
+    if not t or t.get("bytes_per_expert") is None:
+        return None, None
+    return float(t["bytes_per_expert"] * experts_per_call), t["source"]
+
+
 def _tensor_peak():
     """Dense f16/bf16 tensor peak: the measured sustained cuBLAS bf16 rate (the
     kernel is timed inside a long step loop); kind::f16 with f16 operands runs at
@@ -463,22 +487,32 @@ def run_ours(args):
     # copy (on the copy stream) or the FFN call's kernels (wait for the copy excluded)
     tot = {n: float(np.sum(per[n])) for n in names}
     dom = "cold_gather" if copy_tot_ms > ffn_k_tot_ms else "moe_grouped_ffn"
+    mean_distinct = float(distinct.mean())
+    mean_cold = float(ncold_h.mean())
     if dom == "moe_grouped_ffn" and T > 64:
         tc_peak, tc_kind = _tensor_peak()
+        tr, src = _traffic("ffn_tc", mean_distinct)
         roof = {"kernel": "moe_grouped_ffn (tcgen05 kind::f16 grouped GEMM for buckets > 64 tokens)",
                 "bound": "tensor", "achieved": ffn_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": ffn_tflops / tc_peak, "traffic": None, "ms_mean": ffn_k_tot_ms / (K * NL),
-                "flops_per_call": ffn_flops / (K * NL), "peak_kind": tc_kind,
+                "frac": ffn_tflops / tc_peak, "traffic": tr, "traffic_source": src,
+                "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
+                "ms_mean": ffn_k_tot_ms / (K * NL), "flops_per_call": ffn_flops / (K * NL), "peak_kind": tc_kind,
                 "hbm_gbs_same_calls": ffn_gbs}
     elif dom == "moe_grouped_ffn":
+        tr, src = _traffic("ffn_decode", mean_distinct)
         roof = {"kernel": "moe_grouped_ffn (decode dequant-GEMV)", "bound": "hbm", "achieved": ffn_gbs,
-                "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak, "traffic": None,
+                "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak, "traffic": tr,
+                "traffic_source": src, "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
                 "ms_mean": ffn_k_tot_ms / (K * NL), "peak_kind": peak_kind}
     else:
+        tr, src = _traffic("cold_copy", mean_cold)
         roof = {"kernel": "cold_copy_kernel (cold_gather's zero-copy host reads)", "bound": "link",
                 "achieved": gather_gbs, "launches": n_copies, "ms_mean": copy_tot_ms / max(1, n_copies),
                 "peak": link_peak, "unit": "GB/s", "frac": gather_gbs / link_peak if link_peak else None,
-                "traffic": None,
+                "traffic": tr, "traffic_source": src,
+                "traffic_note": "DRAM bytes only: the copy reads host memory over the C2C link and its slot "
+                                "writes stay in L2 during the launch",
+                "algorithmic_bytes_per_launch": float(gather_bytes.sum() / max(1, n_copies)),
                 "peak_kind": "measured in this run (max of pinned cudaMemcpyAsync and zero-copy probe)"}
     line = {"metric": "MoE layer tokens/s (decode)", "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
