@@ -92,6 +92,10 @@ def parse():
     ap.add_argument("--hot", type=int, default=None, help="override n_hot (with --experts)")
     ap.add_argument("--no-link-probe", action="store_true")
     ap.add_argument("--copy-ctas", type=int, default=0, help="CTAs of the cold copy kernel (0 = library default)")
+    ap.add_argument("--mirror", dest="mirror", action="store_true", default=None,
+                    help="keep a pinned host copy of every expert (residency moves bytes one way only); "
+                         "default on for single-layer workloads")
+    ap.add_argument("--no-mirror", dest="mirror", action="store_false")
     return ap.parse_args()
 
 
@@ -110,6 +114,9 @@ def workload(args):
         c["n_hot"] = args.hot if args.hot is not None else min(c["n_hot"], args.experts)
         c["n_cold"] = c["E"] - c["n_hot"]
     c["name"] = args.config
+    # host copies of every expert: default for one layer (7.7 GB pinned); a 20-layer
+    # stack would need 154 GB of pinned host memory, so it keeps the in-place exchange
+    c["mirror"] = args.mirror if args.mirror is not None else (c.get("layers", 1) == 1 and c["n_cold"] > 0)
     return c
 
 
@@ -259,7 +266,8 @@ def _config_json(c, args):
                         f"{'Zipf s=%.2f' % c.get('s', 1.1) if c.get('routing') == 'zipf' else 'uniform'} routing"
                         + (f", {c['layers']} layers sharing one slot scratch" if c.get("layers", 1) > 1 else ""),
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
-            "residency": "off" if args.no_residency else "every 16 steps, hysteresis 3.0, <=8 swaps",
+            "residency": "off" if args.no_residency else ("every 16 steps, hysteresis 3.0, <=8 swaps, " + (
+                "host copy of every expert" if c.get("mirror") else "in-place HBM/host exchange")),
             "step_pool": args.pool, "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
@@ -290,11 +298,19 @@ def build_layers(c, dev, seed_tag="bench"):
             perm = None
             loc = synth.loc_identity(E, n_hot)
         hot = torch.empty((max(1, n_hot), eb), dtype=torch.uint8, device=dev)
-        cold = torch.empty((max(1, n_cold), eb), dtype=torch.uint8).pin_memory()
-        synth.fill_layer(hot, cold, loc, H, I, synth.sub_seed(seed_tag, c["name"], li), device=dev)
+        mirror = bool(c.get("mirror"))
+        if mirror:
+            # a pinned host copy of every expert (indexed by expert id)
+            cold = torch.empty((E, eb), dtype=torch.uint8, pin_memory=True)
+            synth.fill_layer(hot, None, loc, H, I, synth.sub_seed(seed_tag, c["name"], li), device=dev, mirror=cold)
+        else:
+            cold = torch.empty((max(1, n_cold), eb), dtype=torch.uint8, pin_memory=True)
+            synth.fill_layer(hot, cold, loc, H, I, synth.sub_seed(seed_tag, c["name"], li), device=dev)
+        n_host = E if mirror else n_cold
         layer = m.Layer(E=E, k=k, H=H, I=I, n_hot=n_hot, n_cold=n_cold, scratch=scratch,
-                        hot_ptrs=[hot[h] for h in range(n_hot)], cold_ptrs=[cold[i] for i in range(n_cold)],
-                        init_loc=loc, swap_every=0 if c.get("no_res") else 16, max_swaps=8, hysteresis=3.0)
+                        hot_ptrs=[hot[h] for h in range(n_hot)], cold_ptrs=[cold[i] for i in range(n_host)],
+                        init_loc=loc, swap_every=0 if c.get("no_res") else 16, max_swaps=8, hysteresis=3.0,
+                        host_mirror=mirror)
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
 

@@ -74,13 +74,21 @@ extern "C" {
  *  max_swaps   at most this many swaps per acting update (<= 64).
  *  hysteresis  a cold expert is promoted over a hot one only when its window
  *              count exceeds hysteresis times the hot one's (same page, section 3:
- *              3.0 is the published default). */
+ *              3.0 is the published default).
+ *  host_mirror 0: cold_blobs_host holds the n_cold cold slots' blobs and a swap
+ *              exchanges bytes between an HBM slot and a host blob.  1:
+ *              cold_blobs_host holds a pinned copy of every expert, indexed by
+ *              expert id (E blobs); a demotion moves no bytes and a promotion
+ *              copies the expert into its HBM slot from its scratch slot when that
+ *              slot still holds this layer's copy of it, else from its host copy.
+ *              The host copies must equal the HBM-resident experts' bytes. */
 typedef struct moe_params {
     int E, k, H, I, n_hot, n_cold;
     int renorm;
     int swap_every;
     int max_swaps;
     float hysteresis;
+    int host_mirror;
 } moe_params;
 
 typedef struct moe_scratch moe_scratch;
@@ -95,15 +103,18 @@ size_t moe_expert_bytes(int H, int I);
  * run one after another).  slot_dev: caller-owned device memory of
  * n_slots * expert_bytes bytes, 256-byte aligned; slot c starts at
  * slot_dev + c * expert_bytes.  All layers that share it must run their
- * cold_gather and moe_grouped_ffn calls in stream order.
- * Errors: MOE_ERR_INVALID_ARG (null, n_slots < 0, misaligned, not device memory). */
+ * cold_gather and moe_grouped_ffn calls in stream order.  The library keeps a
+ * small device table of which layer last copied into each slot.
+ * Errors: MOE_ERR_INVALID_ARG (null, n_slots < 0, misaligned, not device memory),
+ * MOE_ERR_CUDA, MOE_ERR_NOMEM. */
 int moe_scratch_create(int n_slots, size_t expert_bytes, void* slot_dev, moe_scratch** out);
 int moe_scratch_destroy(moe_scratch* s);
 
 /* One MoE layer.  hot_blobs_dev[h] (h < n_hot): device pointer of HBM slot h's
  * blob.  cold_blobs_host[c] (c < n_cold): host pointer of cold slot c's blob,
- * pinned and mapped.  init_loc: host array [E], a bijection onto [0, E).  The
- * scratch must have at least n_cold slots of moe_expert_bytes(H, I) bytes.
+ * pinned and mapped; with host_mirror = 1 instead cold_blobs_host[e] (e < E) is
+ * the host copy of expert e.  init_loc: host array [E], a bijection onto [0, E).
+ * The scratch must have at least n_cold slots of moe_expert_bytes(H, I) bytes.
  * Validates shapes, 16-byte alignment, memory kinds (cudaPointerGetAttributes)
  * and the map.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_NOMEM. */
 int moe_layer_create(const moe_params* p, moe_scratch* scratch, void* const* hot_blobs_dev,
@@ -207,9 +218,12 @@ int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* 
  * every swap_every-th call it synchronises `stream`, reads the window counters,
  * pairs cold experts picked at least once (count desc, id asc) with hot experts
  * (count asc, id asc), swaps pair i while count(cold) > hysteresis * count(hot)
- * (at most max_swaps, stopping at the first pair that fails), exchanges the two
- * experts' bytes in place between the HBM slot and the host blob, rewrites the
- * placement map and clears the counters.  Other calls only count the step.
+ * (at most max_swaps, stopping at the first pair that fails), moves the bytes
+ * (host_mirror 0: exchanges the two experts' bytes in place between the HBM slot
+ * and the host blob; host_mirror 1: copies the promoted expert into the HBM slot,
+ * see moe_params), rewrites the placement map and clears the counters.  Other
+ * calls only count the step.  Layers sharing a scratch must make this call before
+ * a later layer's cold_gather on the same stream order (it may read a slot).
  *  n_swaps_out host int32 [1] out (0 on non-acting calls).
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_INJECTED (test hook). */
 int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream);

@@ -52,14 +52,18 @@ class Layer:
     """One MoE layer handle (moe_layer_create)."""
 
     def __init__(self, *, E, k, H, I, n_hot, n_cold, scratch, hot_ptrs, cold_ptrs, init_loc, renorm=0,
-                 swap_every=16, max_swaps=8, hysteresis=3.0):
-        self.p = moe_params(E, k, H, I, n_hot, n_cold, renorm, swap_every, max_swaps, hysteresis)
+                 swap_every=16, max_swaps=8, hysteresis=3.0, host_mirror=False):
+        """cold_ptrs: the n_cold cold slots' host blobs, or with host_mirror the host
+        copies of all E experts indexed by expert id."""
+        self.p = moe_params(E, k, H, I, n_hot, n_cold, renorm, swap_every, max_swaps, hysteresis,
+                            1 if host_mirror else 0)
         hot = (ctypes.c_void_p * max(1, n_hot))(*[ptr(x) for x in hot_ptrs])
-        cold = (ctypes.c_void_p * max(1, n_cold))(*[ptr(x) for x in cold_ptrs])
+        n_host = E if host_mirror else n_cold
+        cold = (ctypes.c_void_p * max(1, n_host))(*[ptr(x) for x in cold_ptrs])
         loc = np.ascontiguousarray(init_loc, dtype=np.int32)
         h = ctypes.c_void_p()
         check(lib.moe_layer_create(ctypes.byref(self.p), scratch.handle if scratch else None,
-                                   hot if n_hot else None, cold if n_cold else None, loc.ctypes.data,
+                                   hot if n_hot else None, cold if n_host else None, loc.ctypes.data,
                                    ctypes.byref(h)), "moe_layer_create")
         self.handle = h
         self.scratch = scratch

@@ -9,6 +9,7 @@
 // reads them, builds the swap list, exchanges the bytes with one kernel and
 // rewrites the placement map.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -22,6 +23,8 @@ struct moe_scratch {
     int n_slots;
     size_t expert_bytes;
     uint8_t* base;
+    int32_t* d_tag = nullptr;  // [n_slots] id of the layer that last copied into the slot, or -1
+    int32_t* h_tag = nullptr;  // pinned [n_slots] staging for reads of d_tag
 };
 
 struct moe_layer {
@@ -30,7 +33,9 @@ struct moe_layer {
     BlobLayout lay;
     int sm_count;
     std::vector<uint8_t*> hot;        // device blobs of the HBM slots
-    std::vector<uint8_t*> cold_dev;   // device-mapped pointers of the host blobs
+    std::vector<uint8_t*> cold_dev;   // device-mapped pointers of the cold slots' host blobs
+    std::vector<uint8_t*> mirror_dev;  // host_mirror: device-mapped pointer of every expert's host copy
+    int uid = 0;                      // this layer's id in the scratch slot tags
     std::vector<int32_t> loc;         // host mirror of the placement map
     int32_t* d_loc = nullptr;         // [E]
     const uint8_t** d_ptr = nullptr;  // [n_hot + n_cold] phys id -> blob base
@@ -149,6 +154,8 @@ void free_prof(moe_layer* L) {
     L->fprof_n = 0;
 }
 
+std::atomic<int> g_next_uid{1};
+
 void free_layer(moe_layer* L) {
     if (!L) return;
     if (L->copy_stream) cudaStreamSynchronize(L->copy_stream);
@@ -185,11 +192,26 @@ int moe_scratch_create(int n_slots, size_t expert_bytes, void* slot_dev, moe_scr
     s->n_slots = n_slots;
     s->expert_bytes = expert_bytes;
     s->base = static_cast<uint8_t*>(slot_dev);
+    const size_t tb = sizeof(int32_t) * (n_slots > 0 ? n_slots : 1);
+    cudaError_t err = cudaMalloc(&s->d_tag, tb);
+    err = err ? err : cudaMemset(s->d_tag, 0xff, tb);
+    err = err ? err : cudaHostAlloc(&s->h_tag, tb, cudaHostAllocDefault);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(s->d_tag);
+        cudaFreeHost(s->h_tag);
+        delete s;
+        return err == cudaErrorMemoryAllocation ? MOE_ERR_NOMEM : MOE_ERR_CUDA;
+    }
     *out = s;
     return MOE_OK;
 }
 
 int moe_scratch_destroy(moe_scratch* s) {
+    if (s) {
+        cudaFree(s->d_tag);
+        cudaFreeHost(s->h_tag);
+    }
     delete s;
     return MOE_OK;
 }
@@ -204,11 +226,13 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     if (p.renorm != 0 && p.renorm != 1) return MOE_ERR_INVALID_ARG;
     if (p.swap_every < 0 || p.max_swaps < 0 || p.max_swaps > kMaxSwaps) return MOE_ERR_INVALID_ARG;
     if (!(p.hysteresis >= 0.0f) || p.hysteresis > 1e30f) return MOE_ERR_INVALID_ARG;
+    if (p.host_mirror != 0 && p.host_mirror != 1) return MOE_ERR_INVALID_ARG;
     const size_t eb = moe_expert_bytes(p.H, p.I);
     if (p.n_cold > 0 && (!scratch || scratch->expert_bytes != eb || scratch->n_slots < p.n_cold))
         return MOE_ERR_INVALID_ARG;
     if (p.n_hot > 0 && !hot_blobs_dev) return MOE_ERR_INVALID_ARG;
-    if (p.n_cold > 0 && !cold_blobs_host) return MOE_ERR_INVALID_ARG;
+    const int n_host = p.host_mirror ? p.E : p.n_cold;  // host blobs passed
+    if (n_host > 0 && !cold_blobs_host) return MOE_ERR_INVALID_ARG;
     // placement map: a bijection onto [0, E)
     std::vector<char> seen(p.E, 0);
     for (int e = 0; e < p.E; ++e) {
@@ -237,16 +261,25 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
         }
         L->hot[h] = static_cast<uint8_t*>(b);
     }
-    L->cold_dev.resize(p.n_cold);
-    for (int c = 0; c < p.n_cold; ++c) {
-        void* b = cold_blobs_host[c];
+    std::vector<uint8_t*> host_dev(n_host);
+    for (int i = 0; i < n_host; ++i) {
+        void* b = cold_blobs_host[i];
         void* d = b ? mapped_host_ptr(b) : nullptr;
         if (!d || !aligned(b, 16) || !aligned(d, 16)) {
             delete L;
             return MOE_ERR_INVALID_ARG;
         }
-        L->cold_dev[c] = static_cast<uint8_t*>(d);
+        host_dev[i] = static_cast<uint8_t*>(d);
     }
+    L->cold_dev.resize(p.n_cold);
+    if (p.host_mirror) {
+        L->mirror_dev = host_dev;
+        for (int e = 0; e < p.E; ++e)
+            if (init_loc[e] >= p.n_hot) L->cold_dev[init_loc[e] - p.n_hot] = host_dev[e];
+    } else {
+        for (int c = 0; c < p.n_cold; ++c) L->cold_dev[c] = host_dev[c];
+    }
+    L->uid = g_next_uid.fetch_add(1);
     L->loc.assign(init_loc, init_loc + p.E);
     std::vector<const uint8_t*> ptr(p.E);
     for (int h = 0; h < p.n_hot; ++h) ptr[h] = L->hot[h];
@@ -327,7 +360,8 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
         if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
         if (err == cudaSuccess)
             err = launch_cold_copy(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, L->d_cold_src,
-                                   L->scratch->base, L->lay.total, L->copy_ctas, L->copy_stream);
+                                   L->scratch->base, L->lay.total, L->scratch->d_tag, L->uid, L->copy_ctas,
+                                   L->copy_stream);
         if (err == cudaSuccess && prof) {
             err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
             ++L->prof_n;
@@ -391,9 +425,14 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     if (err == cudaSuccess) err = launch_ffn_prep(a, workspace, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (L->copy_pending) {
-        // experts in HBM first, while the cold copy is in flight; then the cold ones
-        err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        // experts in HBM first, while the cold copy is in flight; then the cold ones.
+        // An FFN CTA leaves no room on its SM for a copy CTA, so the hot phases run
+        // on the SMs the copy kernel does not hold (else the CTAs queued behind the
+        // copy would hold the hot phase until the copy ends)
+        const int copy_sms = L->copy_ctas < L->sm_count / 2 ? L->copy_ctas : L->sm_count / 2;
+        const int hot_sms = L->sm_count - copy_sms;
+        err = launch_ffn_phase(a, 0, 1, hot_sms, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
         if (err == cudaSuccess) err = join_copy(L, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
@@ -430,6 +469,9 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
     cudaError_t err = join_copy(L, st);
     if (err == cudaSuccess)
         err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess && p.host_mirror && p.n_cold > 0)
+        err = cudaMemcpyAsync(L->scratch->h_tag, L->scratch->d_tag, sizeof(int32_t) * p.n_cold,
+                              cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     const int32_t* cnt = L->h_counts;
@@ -448,19 +490,46 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
     SwapList sw;
     sw.n = 0;
     std::vector<int32_t> loc = L->loc;
+    std::vector<int> moved_slots;  // host_mirror: cold slots whose expert changes
     for (size_t i = 0; i < lim; ++i) {
         const int a = cold[i], b = hot[i];
         if (!((double)cnt[a] > (double)p.hysteresis * (double)cnt[b])) break;
         const int slot_h = loc[b];             // HBM slot of the demoted expert
         const int slot_c = loc[a] - p.n_hot;   // cold slot of the promoted expert
         sw.hot[sw.n] = L->hot[slot_h];
-        sw.host[sw.n] = L->cold_dev[slot_c];
+        if (p.host_mirror) {
+            // promote from the scratch slot if this layer's copy of the expert is still
+            // there, else from the expert's host copy; the demoted expert's bytes are
+            // already in its host copy
+            const bool in_scratch = L->scratch->h_tag[slot_c] == L->uid;
+            sw.host[sw.n] = in_scratch ? L->scratch->base + (size_t)slot_c * L->lay.total : L->mirror_dev[a];
+            moved_slots.push_back(slot_c);
+        } else {
+            sw.host[sw.n] = L->cold_dev[slot_c];
+        }
         ++sw.n;
         std::swap(loc[a], loc[b]);
     }
     if (sw.n > 0) {
-        err = launch_swap(sw, L->lay.total, L->sm_count, st);
+        err = p.host_mirror ? launch_copy_list(sw, L->lay.total, L->sm_count, st)
+                            : launch_swap(sw, L->lay.total, L->sm_count, st);
         if (err != cudaSuccess) return MOE_ERR_CUDA;
+        if (p.host_mirror) {
+            // each moved cold slot now belongs to the demoted expert: point the copy at
+            // its host copy and drop the slot's tag (the scratch holds the promoted one)
+            for (int c : moved_slots) {
+                int e = -1;
+                for (int x = 0; x < p.E; ++x)
+                    if (loc[x] == p.n_hot + c) e = x;
+                L->cold_dev[c] = L->mirror_dev[e];
+                err = cudaMemsetAsync(L->scratch->d_tag + c, 0xff, sizeof(int32_t), st);
+                if (err != cudaSuccess) return MOE_ERR_CUDA;
+            }
+            err = cudaMemcpyAsync(L->d_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold,
+                                  cudaMemcpyHostToDevice, st);
+            if (err == cudaSuccess) err = cudaStreamSynchronize(st);  // the host vector is the copy's source
+            if (err != cudaSuccess) return MOE_ERR_CUDA;
+        }
         std::memcpy(L->h_loc, loc.data(), sizeof(int32_t) * p.E);
         err = cudaMemcpyAsync(L->d_loc, L->h_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice, st);
         if (err != cudaSuccess) return MOE_ERR_CUDA;

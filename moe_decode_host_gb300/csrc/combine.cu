@@ -76,6 +76,33 @@ __global__ void __launch_bounds__(kSwapThreads) swap_kernel(SwapList s, size_t b
     }
 }
 
+// dst[i] <- src[i] (blob_bytes each) for every pair; s.hot holds dst, s.host src.
+__global__ void __launch_bounds__(kSwapThreads) copy_list_kernel(SwapList s, size_t blob_bytes, int seg) {
+    const size_t chunks = blob_bytes / 16;
+    const int items = s.n * seg;
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const int i = it / seg, part = it % seg;
+        uint4* a = reinterpret_cast<uint4*>(s.hot[i]);
+        const uint4* b = reinterpret_cast<const uint4*>(s.host[i]);
+        const size_t c0 = chunks * (size_t)part / (size_t)seg;
+        const size_t c1 = chunks * (size_t)(part + 1) / (size_t)seg;
+        const size_t stride = (size_t)kSwapThreads * kSwapUnroll;
+        for (size_t base = c0 + threadIdx.x; base < c1; base += stride) {
+            uint4 vb[kSwapUnroll];
+#pragma unroll
+            for (int u = 0; u < kSwapUnroll; ++u) {
+                const size_t ci = base + (size_t)u * kSwapThreads;
+                if (ci < c1) vb[u] = b[ci];
+            }
+#pragma unroll
+            for (int u = 0; u < kSwapUnroll; ++u) {
+                const size_t ci = base + (size_t)u * kSwapThreads;
+                if (ci < c1) a[ci] = vb[u];
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
@@ -93,6 +120,15 @@ cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cuda
     int seg = ctas / s.n;
     if (seg < 1) seg = 1;
     swap_kernel<<<ctas, kSwapThreads, 0, st>>>(s, blob_bytes, seg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st) {
+    if (s.n <= 0) return cudaSuccess;
+    int ctas = 2 * sm_count;
+    int seg = ctas / s.n;
+    if (seg < 1) seg = 1;
+    copy_list_kernel<<<ctas, kSwapThreads, 0, st>>>(s, blob_bytes, seg);
     return cudaGetLastError();
 }
 

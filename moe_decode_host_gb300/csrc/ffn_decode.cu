@@ -13,11 +13,13 @@
 //    output rows) into a ring of shared-memory stages with 2D TMA loads (128-byte
 //    swizzle), and with them the stage's slice of the bucket-ordered activation
 //    rows of the expert's tokens (one 2D TMA load), signalling mbarriers;
-//  - eight consumer warps dequantise the E2M1 nibbles in registers (one
+//  - sixteen consumer warps dequantise the E2M1 nibbles in registers (one
 //    e2m1x2 -> f16x2 conversion per byte) and feed mma.sync m16n8k16 as an exact
 //    f16 x f16 -> fp32 dot-product engine; each 32-element block's E8M0 scale is
-//    applied in fp32 to that block's partial sums.  Warps split the rows and the
-//    reduction dimension; partial sums meet in shared memory in a fixed order.
+//    applied in fp32 to that block's partial sums.  Eight warps share each stage
+//    (one 16-row tile and one 128-element half each) and the two groups of eight
+//    take alternate stages; at the end of a task the partial sums meet in shared
+//    memory and the first two or four warps add them in a fixed order.
 // Each lane of a quad reads 8 elements of each 32-element block from the staged
 // K-major rows, so every mma step sees a single block.  Activations are staged as f16 with an exact
 // power-of-two prescale per row, in bucket order (row i belongs to entries[i]), so
@@ -31,82 +33,52 @@
 namespace moe {
 namespace {
 
-constexpr int kConsumers = 8;
-constexpr int kProducers = 2;  // producer warps; producer p fills the stages g with g % 2 == p
+// Consumer warps: 16, in two groups of 8 that take the even and the odd stages.
+// Within a group each warp handles one 16-row tile of the stage's 64 weight rows and
+// one of its two 128-element groups, so every stage is worked on by 8 warps at once
+// and two stages are in flight.
+constexpr int kConsumers = 16;
+constexpr int kPerStage = 8;    // consumer warps that read each stage
+constexpr int kProducers = 2;   // producer warps; producer p fills the stages g with g % 2 == p
 constexpr int kThreads = 32 * (kConsumers + kProducers);
 constexpr int kMaxE = 1024;
 constexpr int kSliceBytes = 128;  // bytes of one row per stage (256 elements)
+constexpr int kStageRows = 64;    // weight rows per stage (both phases)
 
+// Output rows per task: gate/up phase 32 (32 gate + 32 up weight rows per stage),
+// down phase 64.
 template <int P>
-struct Cfg;
-// phase 0: task = 32 output rows -> 32 gate + 32 up weight rows per stage; each warp
-// holds a gate tile and the matching up tile (16 rows); 2 row tiles x 4 K-splits
-template <>
-struct Cfg<0> {
-    static constexpr int kRows = 64, kNTile = 2, kRT = 2, kKS = 4, kTaskRows = 32;
-};
-// phase 1: task = 64 rows of w2 (one 8 KB stage, like phase 0); one 16-row tile per
-// warp; 4 row tiles x 2 K-splits
-template <>
-struct Cfg<1> {
-    static constexpr int kRows = 64, kNTile = 1, kRT = 4, kKS = 2, kTaskRows = 64;
+struct Cfg {
+    static constexpr int kTaskRows = P == 0 ? 32 : 64;
 };
 constexpr int kActRow = 512;  // bytes of one activation row's slice in a stage (256 f16)
 
 struct alignas(16) SmemHead {
     uint64_t full[64];
     uint64_t empty[64];
-    int seq[64];  // global stage number last issued into each slot
     int D;
     int abort;
     int pad[2];
     int e[kMaxE];     // experts of this launch, ascending
     int cnt[kMaxE];   // and for each: its picks,
     int off[kMaxE];   // its first bucket entry,
-    int phys[kMaxE];  // its physical id
+    int phys[kMaxE];  // its physical id,
+    const uint8_t* blob[kMaxE];  // and the base of its blob (null when phys is invalid)
 };
 
 template <int P, int NT>
 struct Layout {
-    static constexpr int kWBytes = Cfg<P>::kRows * 128;
+    static constexpr int kWBytes = kStageRows * 128;
     static constexpr int kABytes = 8 * NT * kActRow;
     static constexpr int kStageBytes = ((kWBytes + kABytes) + 1023) & ~1023;
-    static constexpr int kRedBytes =
-        (int)sizeof(float) * (Cfg<P>::kKS - 1) * Cfg<P>::kRT * Cfg<P>::kNTile * NT * 4 * 32;
+    // one partial-sum fragment per consumer warp, reduced once per task
+    static constexpr int kFrag = NT * 4 * 32;
+    static constexpr int kRedBytes = (int)sizeof(float) * kConsumers * kFrag;
     static constexpr int kBudget = 232448 - 1024 - (int)sizeof(SmemHead) - kRedBytes;
     // an even number of slots, so that each producer owns the slots of its parity
     static constexpr int kStages = ((kBudget / kStageBytes) < 64 ? (kBudget / kStageBytes) : 64) & ~1;
     static_assert(kStages >= 4, "ring too shallow");
 };
-
-// Waits until the producer has stamped `slot` with global stage `g` (it stamps a
-// slot only after the slot's previous stage was released), so that the following
-// parity wait on the slot's full barrier cannot match an older phase.
-__device__ __noinline__ bool seq_wait(volatile int* seq, int g, volatile int* abort, int* status, int* diag,
-                                      int slot) {
-    if (*seq == g) return true;
-    const uint64_t t0 = globaltimer();
-    for (unsigned it = 1;; ++it) {
-        if (*seq == g) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *abort = 1;
-                if (diag && atomicCAS(diag, 0, 1) == 0) {
-                    diag[1] = blockIdx.x;
-                    diag[2] = (int)(threadIdx.x >> 5);
-                    diag[3] = 3;
-                    diag[4] = slot;
-                    diag[5] = *seq;
-                    diag[6] = g;
-                    __threadfence();
-                }
-                set_status(status, MOE_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
@@ -122,80 +94,56 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 __device__ __forceinline__ int perm8(int g) { return (g >> 1) | ((g & 1) << 2); }
 
 // B operand from the stage's activation slices: column n (bucket row off + tb + n)
-// of the stage lives at act + n * kActRow, 256 prescaled f16 values; missing columns
-// read as zero.
+// of the stage lives at act + n * kActRow, 256 prescaled f16 values.  Columns past
+// the expert's tokens hold other rows (or the zero fill past the tensor's end); an
+// mma output column depends only on its own B column, and those columns are never
+// stored, so every column is read unconditionally.
 template <int NT>
 struct SmemB {
-    const uint8_t* col[NT];  // this lane's column in each n-tile, or nullptr
+    const uint8_t* col[NT];  // this lane's column in each n-tile
     __device__ __forceinline__ uint4 load(int nt, int byte_off) const {
-        if (col[nt]) return *reinterpret_cast<const uint4*>(col[nt] + byte_off);
-        return make_uint4(0u, 0u, 0u, 0u);
+        return *reinterpret_cast<const uint4*>(col[nt] + byte_off);
     }
 };
 
-// One stage: acc[i][nt] += W_i[rows of this lane, groups G0..G0+ng) x B.
-// srow[i][r]: shared-memory row (within the stage) of tile i, fragment row r (g or g+8).
-// sc[gl][i][r]: the 4 scale bytes of group gl for that row (prefetched).
-template <int NTILE, int NT>
-__device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow)[NTILE][2],
-                                          const uint32_t (&sc)[2][NTILE][2], int ng, const SmemB<NT>& bl,
-                                          float (&acc)[NTILE][NT][4]) {
+// One warp's slice of a stage: acc[nt] += W[rows g, g+8 of the warp's 16-row tile,
+// 128-element group gl] x B.  srow[r]: the two shared-memory rows of this lane;
+// sc[r]: their 4 scale bytes for the group (byte j = 32-element block j).
+template <int NT>
+__device__ __forceinline__ void slice_mma(const uint8_t* stage, const int (&srow)[2], const uint32_t (&sc)[2],
+                                          int gl, const SmemB<NT>& bl, float (&acc)[NT][4]) {
     const int q = threadIdx.x & 3;
+    // word j of this lane: elements 8q..8q+7 of block j of the group (16-byte chunk
+    // gl*4+j of the swizzled row); the 8 rows of a quarter-warp have distinct row%8,
+    // so the 32 lanes hit 32 distinct banks
+    uint32_t wv[2][4];
 #pragma unroll
-    for (int gl = 0; gl < 2; ++gl) {
-        if (gl >= ng) break;
-        // word j of this lane: elements 8q..8q+7 of block j of the group (16-byte
-        // chunk gl*4+j of the swizzled row); the 8 rows of a quarter-warp have
-        // distinct row%8, so the 32 lanes hit 32 distinct banks
-        uint32_t wv[NTILE][2][4];
-#pragma unroll
-        for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int row = srow[i][r];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int chunk = (gl * 4 + j) ^ (row & 7);
-                    wv[i][r][j] = *reinterpret_cast<const uint32_t*>(stage + row * kSliceBytes + chunk * 16 + q * 4);
-                }
-            }
-        float scf[NTILE][2][4];
-#pragma unroll
-        for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) e8m0x4_to_f32(sc[gl][i][r], scf[i][r]);
+    for (int r = 0; r < 2; ++r) {
+        const int row = srow[r];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            uint32_t af[NTILE][2][4];
+            const int chunk = (gl * 4 + j) ^ (row & 7);
+            wv[r][j] = *reinterpret_cast<const uint32_t*>(stage + row * kSliceBytes + chunk * 16 + q * 4);
+        }
+    }
+    float scf[2][4];
 #pragma unroll
-            for (int i = 0; i < NTILE; ++i)
+    for (int r = 0; r < 2; ++r) e8m0x4_to_f32(sc[r], scf[r]);
 #pragma unroll
-                for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(wv[i][r][j], af[i][r]);
-            uint4 bv[NT];
+    for (int j = 0; j < 4; ++j) {
+        uint32_t af[2][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) bv[nt] = bl.load(nt, gl * 256 + 64 * j + 16 * q);
-            float d[NTILE][NT][4];
+        for (int r = 0; r < 2; ++r) e2m1x8_to_f16x2(wv[r][j], af[r]);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < NTILE; ++i) {
-                    mma_f16(d[i][nt], af[i][0][0], af[i][1][0], af[i][0][1], af[i][1][1], bv[nt].x, bv[nt].y, 0.f,
-                            0.f, 0.f, 0.f);
-                    mma_f16(d[i][nt], af[i][0][2], af[i][1][2], af[i][0][3], af[i][1][3], bv[nt].z, bv[nt].w,
-                            d[i][nt][0], d[i][nt][1], d[i][nt][2], d[i][nt][3]);
-                }
-#pragma unroll
-            for (int i = 0; i < NTILE; ++i) {
-                const float s0 = scf[i][0][j];
-                const float s1 = scf[i][1][j];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    acc[i][nt][0] = fmaf(s0, d[i][nt][0], acc[i][nt][0]);
-                    acc[i][nt][1] = fmaf(s0, d[i][nt][1], acc[i][nt][1]);
-                    acc[i][nt][2] = fmaf(s1, d[i][nt][2], acc[i][nt][2]);
-                    acc[i][nt][3] = fmaf(s1, d[i][nt][3], acc[i][nt][3]);
-                }
-            }
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4 bv = bl.load(nt, gl * 256 + 64 * j + 16 * q);
+            float d[4];
+            mma_f16(d, af[0][0], af[1][0], af[0][1], af[1][1], bv.x, bv.y, 0.f, 0.f, 0.f, 0.f);
+            mma_f16(d, af[0][2], af[1][2], af[0][3], af[1][3], bv.z, bv.w, d[0], d[1], d[2], d[3]);
+            acc[nt][0] = fmaf(scf[0][j], d[0], acc[nt][0]);
+            acc[nt][1] = fmaf(scf[0][j], d[1], acc[nt][1]);
+            acc[nt][2] = fmaf(scf[1][j], d[2], acc[nt][2]);
+            acc[nt][3] = fmaf(scf[1][j], d[3], acc[nt][3]);
         }
     }
 }
@@ -204,6 +152,7 @@ __device__ __forceinline__ void stage_mma(const uint8_t* stage, const int (&srow
 struct TaskInfo {
     int rt, cnt, off, phys;
     bool valid;
+    const uint8_t* blob;
 };
 
 __device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& hd, int task, int tiles) {
@@ -214,6 +163,7 @@ __device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& 
     ti.off = hd.off[i];
     ti.phys = hd.phys[i];
     ti.valid = ti.phys >= 0 && ti.phys < a.n_phys;
+    ti.blob = hd.blob[i];
     return ti;
 }
 
@@ -222,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                                                                 int lo, int hi, int sel) {
     using C = Cfg<P>;
     using L = Layout<P, NT>;
-    constexpr int NTILE = C::kNTile;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     SmemHead& hd = *reinterpret_cast<SmemHead*>(stages + L::kStages * L::kStageBytes);
@@ -257,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             hd.abort = 0;
             for (int s = 0; s < L::kStages; ++s) {
                 mbar_init(&hd.full[s], 1);
-                mbar_init(&hd.empty[s], C::kRT);
-                hd.seq[s] = -1;
+                mbar_init(&hd.empty[s], kPerStage);
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
@@ -270,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
         const int off = __ldg(a.offsets + e);
         hd.cnt[i] = __ldg(a.counts + e);
         hd.off[i] = off;
-        hd.phys[i] = __ldg(a.phys_ids + __ldg(a.entries + off));
+        const int ph = __ldg(a.phys_ids + __ldg(a.entries + off));
+        hd.phys[i] = ph;
+        hd.blob[i] = (ph >= 0 && ph < a.n_phys) ? a.ptr[ph] : nullptr;
     }
     __syncthreads();
     const int ntask = hd.D * tiles;
@@ -301,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                                 break;
                             }
                             uint8_t* dst = stages + slot * L::kStageBytes;
-                            *reinterpret_cast<volatile int*>(&hd.seq[slot]) = gstage;
                             // full boxes land even past the tensor's edge (zero filled)
                             mbar_arrive_expect_tx(&hd.full[slot], (unsigned)(L::kWBytes + L::kABytes));
                             if (P == 0) {
@@ -334,11 +283,20 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     }
 
     // ---------------- consumers ----------------
-    const int rt = warp % C::kRT;  // row tile
-    const int ks = warp / C::kRT;  // reduction split
+    // warp = sp * 8 + (tile << 2 | rt << 1 | gl) in the gate/up phase (tile 0 gate, 1 up;
+    // rt = 16-row tile of the 32 output rows), sp * 8 + (rt << 1 | gl) in the down
+    // phase (rt = 16-row tile of 64); sp = parity of the stages this warp reads, gl =
+    // its 128-element group of each stage
+    const int sp = warp >> 3;
+    const int gl = warp & 1;
+    const int tile = P == 0 ? ((warp >> 2) & 1) : 0;
+    const int rt = P == 0 ? ((warp >> 1) & 1) : ((warp >> 1) & 3);
     const int g = lane >> 2, q = lane & 3;
     const int pg = perm8(g);
     const size_t srs = (size_t)K / 32;  // scale bytes per row
+    // epilogue warps: the first 2 (gate/up phase) or 4 (down phase) consumer warps,
+    // one per 16 output rows
+    constexpr int kEpi = P == 0 ? 2 : 4;
     int gstage = 0;
     bool done = false;
     for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
@@ -355,148 +313,81 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             }
             continue;
         }
-        const uint8_t* blob = a.ptr[ti.phys];
-        const uint8_t* sb = blob + (P == 0 ? a.w13s : a.w2s);
-        // rows of this lane: shared-memory rows within a stage and global rows
-        int srow[NTILE][2];
-        int grow[NTILE][2];
+        const uint8_t* sb = ti.blob + (P == 0 ? a.w13s : a.w2s);
+        // this lane's two weight rows: within the stage and in the plane
+        int srow[2], grow[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const int lr = 16 * rt + pg + 8 * r;  // local output row
-            srow[0][r] = lr;
-            grow[0][r] = r0 + lr;
-            if (NTILE == 2) {
-                srow[NTILE - 1][r] = C::kTaskRows + lr;
-                grow[NTILE - 1][r] = I + r0 + lr;
-            }
+            const int lr = 16 * rt + pg + 8 * r;
+            srow[r] = (P == 0 ? tile * C::kTaskRows : 0) + lr;
+            grow[r] = (P == 0 && tile == 1 ? I : 0) + r0 + lr;
         }
         // warm L1 with the scale lines of this warp's rows in the next task
         {
             const int nxt = task + gridDim.x;
-            if (nxt < ntask && q == 0) {
+            if (nxt < ntask && q == 0 && gl == 0) {
                 const TaskInfo tn = task_info(a, hd, nxt, tiles);
                 if (tn.valid) {
-                    const uint8_t* nsb = a.ptr[tn.phys] + (P == 0 ? a.w13s : a.w2s);
+                    const uint8_t* nsb = tn.blob + (P == 0 ? a.w13s : a.w2s);
                     const int nr0 = tn.rt * C::kTaskRows;
 #pragma unroll
-                    for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r)
-                            for (size_t o = 0; o < srs; o += 128)
-                                prefetch_l1(nsb + (size_t)(grow[i][r] - r0 + nr0) * srs + o);
+                    for (int r = 0; r < 2; ++r)
+                        for (size_t o = 0; o < srs; o += 128)
+                            prefetch_l1(nsb + (size_t)(grow[r] - r0 + nr0) * srs + o);
                 }
             }
         }
         for (int tb = 0; tb < ti.cnt; tb += 8 * NT) {
             const int ncols = min(8 * NT, ti.cnt - tb);
-            // this lane's output columns: prescale (and for the down phase the pick),
-            // fetched now so that their latency hides behind the stage loop
-            // (the exponents are converted where they are used, so nothing waits here)
-            int cexp[NT][2];
-            int cpick[NT][2];
+            float acc[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int col = nt * 8 + 2 * q + c2;
-                    const int pos = ti.off + tb + col;
-                    cexp[nt][c2] = col < ncols ? __ldg(a.gexp + pos) : 0;
-                    cpick[nt][c2] = (P == 1 && col < ncols) ? __ldg(a.entries + pos) : 0;
-                }
-            float acc[NTILE][NT][4];
+                for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
+            // this warp reads stages sp, sp + 2, sp + 4, ...; the 4 scale bytes of its
+            // group for its two rows sit in two register pairs used alternately, each
+            // refilled right after use for the stage two own stages later
+            uint32_t scA[2], scB[2];
+            auto load_sc = [&](int s, uint32_t(&dst)[2]) {
+                const int grp = 2 * s + gl;
 #pragma unroll
-            for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
-            // this warp's stages are ks, ks + KS, ks + 2 KS, ...; their scale words sit in
-            // two register sets used alternately, each refilled right after use for the
-            // stage two own stages later (no register moves that would wait on a load)
-            uint32_t scA[2][NTILE][2], scB[2][NTILE][2];
-            auto load_sc = [&](int s, uint32_t(&dst)[2][NTILE][2]) {
-                const int G0 = 2 * s;
-                const int ng = min(2, ngroups - G0);
-#pragma unroll
-                for (int gl = 0; gl < 2; ++gl)
-#pragma unroll
-                    for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                        for (int r = 0; r < 2; ++r)
-                            dst[gl][i][r] = (gl < ng) ? ld_u32(sb + (size_t)grow[i][r] * srs + (size_t)(G0 + gl) * 4)
-                                                      : 0u;
+                for (int r = 0; r < 2; ++r)
+                    dst[r] = grp < ngroups ? ld_u32(sb + (size_t)grow[r] * srs + (size_t)grp * 4) : 0u;
             };
-            if (ks < nst) load_sc(ks, scA);
-            if (ks + C::kKS < nst) load_sc(ks + C::kKS, scB);
+            if (sp < nst) load_sc(sp, scA);
+            if (sp + 2 < nst) load_sc(sp + 2, scB);
             bool ok = true;
-            auto own_stage = [&](int s, uint32_t(&sc)[2][NTILE][2]) -> bool {
+            // The parity wait below cannot match a phase one lap old: slots have the parity
+            // of their stages (kStages is even), so this warp's group reads every stage
+            // ever put in slot sl, and it waited for the previous one (gs - kStages)
+            // before this; every warp of the group waits on every stage of its parity,
+            // even where its group is past the K tail.
+            auto own_stage = [&](int s, uint32_t(&sc)[2]) -> bool {
                 const int gs = gstage + s;
                 const int sl = gs % L::kStages;
                 const unsigned ph = (unsigned)(gs / L::kStages) & 1u;
-                if (!(hd.seq[sl] == gs || seq_wait(&hd.seq[sl], gs, abort, a.status, a.diag, sl)) ||
-                    !mbar_wait_fast(&hd.full[sl], ph, abort, a.status, a.diag, 1, sl, s, (task << 8) | ncols))
+                if (!mbar_wait_fast(&hd.full[sl], ph, abort, a.status, a.diag, 1, sl, s, (task << 8) | ncols))
                     return false;
-                const uint8_t* stage = stages + sl * L::kStageBytes;
-                SmemB<NT> bl;
+                if (2 * s + gl < ngroups) {  // (an odd K tail leaves group 1 of the last stage empty)
+                    const uint8_t* stage = stages + sl * L::kStageBytes;
+                    SmemB<NT> bl;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int n = nt * 8 + g;
-                    bl.col[nt] = n < ncols ? stage + L::kWBytes + n * kActRow : nullptr;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int n = nt * 8 + g;
+                        bl.col[nt] = stage + L::kWBytes + n * kActRow;
+                    }
+                    slice_mma<NT>(stage, srow, sc, gl, bl, acc);
                 }
-                stage_mma<NTILE, NT>(stage, srow, sc, min(2, ngroups - 2 * s), bl, acc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&hd.empty[sl]);
-                if (s + 2 * C::kKS < nst) load_sc(s + 2 * C::kKS, sc);
+                if (s + 4 < nst) load_sc(s + 4, sc);
                 return true;
             };
-            for (int s = ks; s < nst && ok; s += 2 * C::kKS) {
+            for (int s = sp; s < nst && ok; s += 4) {
                 ok = own_stage(s, scA);
-                if (ok && s + C::kKS < nst) ok = own_stage(s + C::kKS, scB);
+                if (ok && s + 2 < nst) ok = own_stage(s + 2, scB);
             }
             gstage += nst;
-            // partial sums of the K-splits meet in shared memory (fixed order)
-            constexpr int kFrag = NTILE * NT * 4 * 32;
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
-            if (ks > 0) {
-                float* dst = red + (size_t)((ks - 1) * C::kRT + rt) * kFrag;
-#pragma unroll
-                for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) dst[((i * NT + nt) * 4 + c) * 32 + lane] = acc[i][nt][c];
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
-            if (ks == 0 && ok) {
-#pragma unroll
-                for (int i = 0; i < NTILE; ++i)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-#pragma unroll
-                            for (int k2 = 1; k2 < C::kKS; ++k2)
-                                acc[i][nt][c] += red[(size_t)((k2 - 1) * C::kRT + rt) * kFrag +
-                                                     ((i * NT + nt) * 4 + c) * 32 + lane];
-                // epilogue
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int col = nt * 8 + 2 * q + (c & 1);
-                        if (col >= ncols) continue;
-                        const int orow = r0 + 16 * rt + pg + ((c >> 1) << 3);  // output row
-                        const float sx = pow2i(cexp[nt][c & 1]);
-                        if constexpr (P == 0) {
-                            const float gv = acc[0][nt][c] * sx;
-                            const float uv = acc[NTILE - 1][nt][c] * sx;
-                            const float hv = gv / (1.0f + expf(-gv)) * uv;
-                            a.h[(size_t)(ti.off + tb + col) * I + orow] = hv;
-                        } else {
-                            a.y[(size_t)cpick[nt][c & 1] * H + orow] = acc[0][nt][c] * sx;
-                        }
-                    }
-            }
             // all consumer warps take the same decision to stop (a timed-out wait anywhere)
             unsigned stop;
             asm volatile(
@@ -511,6 +402,69 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 done = true;
                 break;
             }
+            // partial sums meet in shared memory; the epilogue warps add them in a fixed
+            // order (stage parity, then group)
+            float* mine = red + (size_t)warp * L::kFrag;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mine[(nt * 4 + c) * 32 + lane] = acc[nt][c];
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumers));
+            if (warp < kEpi) {
+                const int ert = warp;  // output row tile of this epilogue warp
+                // this lane's output columns: prescale exponent (and for the down phase
+                // the pick), loaded first so that the partial-sum reads hide their latency
+                int cexp[NT][2], cpick[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int col = nt * 8 + 2 * q + c2;
+                        const int pos = ti.off + tb + col;
+                        cexp[nt][c2] = col < ncols ? __ldg(a.gexp + pos) : 0;
+                        cpick[nt][c2] = (P == 1 && col < ncols) ? __ldg(a.entries + pos) : 0;
+                    }
+                float v0[NT][4], v1[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) v0[nt][c] = v1[nt][c] = 0.f;
+#pragma unroll
+                for (int sp2 = 0; sp2 < 2; ++sp2)
+#pragma unroll
+                    for (int gl2 = 0; gl2 < 2; ++gl2) {
+                        const int w0 = sp2 * 8 + (ert << 1) + gl2;             // gate (or w2) rows
+                        const int w1 = sp2 * 8 + (1 << 2) + (ert << 1) + gl2;  // up rows
+                        const float* p0 = red + (size_t)w0 * L::kFrag;
+                        const float* p1 = red + (size_t)w1 * L::kFrag;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                v0[nt][c] += p0[(nt * 4 + c) * 32 + lane];
+                                if (P == 0) v1[nt][c] += p1[(nt * 4 + c) * 32 + lane];
+                            }
+                    }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = nt * 8 + 2 * q + (c & 1);
+                        if (col >= ncols) continue;
+                        const int pos = ti.off + tb + col;
+                        const float sx = pow2i(cexp[nt][c & 1]);
+                        const int orow = r0 + 16 * ert + pg + ((c >> 1) << 3);  // output row
+                        if constexpr (P == 0) {
+                            const float gv = v0[nt][c] * sx;
+                            const float uv = v1[nt][c] * sx;
+                            a.h[(size_t)pos * I + orow] = gv / (1.0f + expf(-gv)) * uv;
+                        } else {
+                            a.y[(size_t)cpick[nt][c & 1] * H + orow] = v0[nt][c] * sx;
+                        }
+                    }
+            }
+            // (the next writes to the partial sums come after the next task's first
+            // barrier, which the epilogue warps reach only when done)
         }
         if (done) break;
     }

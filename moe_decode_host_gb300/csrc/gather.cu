@@ -85,10 +85,13 @@ __global__ void __launch_bounds__(kGatherThreads) cold_remap_kernel(
 // derives the ascending list of picked cold slots from the picks itself (the same
 // marking and ballot compaction as the remap kernel), so the copy needs nothing
 // from the remap kernel and the two run concurrently.  Each picked slot is cut
-// into `seg` contiguous pieces spread over the grid.
+// into `seg` contiguous pieces spread over the grid.  CTA 0 also marks every
+// picked slot with the copying layer's id (slot_tag), which tells the residency
+// manager which slots hold this layer's copy of their expert.
 __global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(
     const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
-    const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes) {
+    const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes,
+    int32_t* __restrict__ slot_tag, int uid) {
     __shared__ unsigned char flag[kMaxColdSlots];
     __shared__ int32_t list[kMaxColdSlots];
     __shared__ int s_cnt;
@@ -117,6 +120,8 @@ __global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(
     __syncthreads();
     const int cnt = s_cnt;
     if (cnt <= 0) return;
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < cnt; i += blockDim.x) slot_tag[list[i]] = uid;
     const size_t chunks = blob_bytes / 16;
     int seg = (int)gridDim.x / cnt;
     if (seg < 1) seg = 1;
@@ -150,11 +155,11 @@ cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* lo
 }
 
 cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int ctas,
-                             cudaStream_t st) {
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int32_t* slot_tag,
+                             int uid, int ctas, cudaStream_t st) {
     if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
     cold_copy_kernel<<<ctas, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, cold_src, slot_base,
-                                                      blob_bytes);
+                                                      blob_bytes, slot_tag, uid);
     return cudaGetLastError();
 }
 

@@ -45,10 +45,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 // Remap (phys ids, picked cold slots) on the caller's stream.
 cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st);
-// Byte copy of the picked cold slots (derives the slot list from the picks itself).
+// Byte copy of the picked cold slots (derives the slot list from the picks itself);
+// marks each copied slot's tag with uid.
 cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int ctas,
-                             cudaStream_t st);
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int32_t* slot_tag,
+                             int uid, int ctas, cudaStream_t st);
 
 cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
 
@@ -113,7 +114,10 @@ struct SwapList {
     uint8_t* hot[kMaxSwaps];   // device blob of the HBM slot
     uint8_t* host[kMaxSwaps];  // device-mapped pointer of the host blob
 };
+// Exchanges hot[i] and host[i] in place for every pair.
 cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st);
+// Copies src[i] -> dst[i] (blob_bytes each) for every pair.
+cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st);
 
 cudaError_t launch_debug_e2m1(uint32_t* out, cudaStream_t st);
 

@@ -133,11 +133,13 @@ def gen_blobs(n: int, H: int, I: int, seed: int, device="cpu", out: torch.Tensor
 
 
 def fill_layer(hot: torch.Tensor, cold: torch.Tensor, loc: np.ndarray, H: int, I: int, seed: int,
-               device="cpu") -> None:
+               device="cpu", mirror: torch.Tensor | None = None) -> None:
     """Draws every expert's blob (expert ids in ascending order, one generator) and
     writes it where the placement map puts it: hot[loc[e]] when loc[e] < n_hot,
-    else cold[loc[e] - n_hot].  hot/cold may live on any device (cold is usually
-    pinned host memory)."""
+    else cold[loc[e] - n_hot] (cold may be None when a mirror is given).  With
+    `mirror` ([E, blob_bytes]) every expert's blob is also written to mirror[e].
+    hot/cold/mirror may live on any device (cold and mirror are usually pinned host
+    memory)."""
     n_hot = hot.shape[0]
     sec = blob_sections(H, I)
     gen = torch.Generator(device=device)
@@ -153,8 +155,10 @@ def fill_layer(hot: torch.Tensor, cold: torch.Tensor, loc: np.ndarray, H: int, I
         p = int(loc[e])
         if p < n_hot:
             hot[p].copy_(tmp)
-        else:
+        elif cold is not None:
             cold[p - n_hot].copy_(tmp)
+        if mirror is not None:
+            mirror[e].copy_(tmp)
 
 
 def gen_x(T: int, H: int, seed: int, device="cpu") -> torch.Tensor:

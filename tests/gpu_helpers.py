@@ -11,7 +11,7 @@ import synth
 
 class LayerFixture:
     def __init__(self, *, H, I, E, n_hot, n_cold, k, seed, loc=None, swap_every=0, max_swaps=8,
-                 hysteresis=3.0, renorm=0, scratch=None, slots=None, gen_device="cuda"):
+                 hysteresis=3.0, renorm=0, scratch=None, slots=None, gen_device="cuda", host_mirror=False):
         import moe_decode_host_gb300 as m
 
         self.m = m
@@ -19,9 +19,16 @@ class LayerFixture:
         self.eb = m.expert_bytes(H, I)
         dev = torch.device("cuda")
         self.loc0 = np.arange(E, dtype=np.int32) if loc is None else np.asarray(loc, np.int32)
+        self.host_mirror = host_mirror
         self.hot = torch.empty((max(1, n_hot), self.eb), dtype=torch.uint8, device=dev)
-        self.cold = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8).pin_memory()
-        synth.fill_layer(self.hot, self.cold, self.loc0, H, I, seed, device=gen_device)
+        if host_mirror:
+            # a host copy of every expert, indexed by expert id
+            self.cold = torch.empty((E, self.eb), dtype=torch.uint8).pin_memory()
+            synth.fill_layer(self.hot, None, self.loc0, H, I, seed, device=gen_device, mirror=self.cold)
+        else:
+            self.cold = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8).pin_memory()
+            synth.fill_layer(self.hot, self.cold, self.loc0, H, I, seed, device=gen_device)
+        n_host = E if host_mirror else n_cold
         if scratch is None:
             self.slots = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8, device=dev)
             self.scratch = m.Scratch(n_cold, self.eb, self.slots) if n_cold > 0 else None
@@ -29,8 +36,9 @@ class LayerFixture:
             self.slots, self.scratch = slots, scratch
         self.layer = m.Layer(E=E, k=k, H=H, I=I, n_hot=n_hot, n_cold=n_cold, scratch=self.scratch,
                              hot_ptrs=[self.hot[h] for h in range(n_hot)],
-                             cold_ptrs=[self.cold[c] for c in range(n_cold)], init_loc=self.loc0,
-                             renorm=renorm, swap_every=swap_every, max_swaps=max_swaps, hysteresis=hysteresis)
+                             cold_ptrs=[self.cold[c] for c in range(n_host)], init_loc=self.loc0,
+                             renorm=renorm, swap_every=swap_every, max_swaps=max_swaps, hysteresis=hysteresis,
+                             host_mirror=host_mirror)
 
     def expert_bytes_now(self, e: int, loc=None) -> np.ndarray:
         """Current bytes of expert e (from its HBM slot or its host blob)."""
@@ -38,6 +46,8 @@ class LayerFixture:
         p = int(loc[e])
         if p < self.n_hot:
             return self.hot[p].cpu().numpy()
+        if self.host_mirror:
+            return self.cold[e].numpy().copy()
         return self.cold[p - self.n_hot].numpy().copy()
 
     def all_blobs_now(self) -> list:

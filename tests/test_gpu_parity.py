@@ -409,14 +409,17 @@ def _skewed_logits(T, E, step, hot_first):
     return l
 
 
-def test_residency_matches_oracle_and_keeps_bytes():
+@pytest.mark.parametrize("host_mirror", [False, True])
+def test_residency_matches_oracle_and_keeps_bytes(host_mirror):
     import moe_decode_host_gb300 as m
 
     H, I, E, n_hot, n_cold, k, T = 256, 512, 16, 12, 4, 2, 4
     seed = synth.sub_seed("residency")
-    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=3, max_swaps=2)
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=3, max_swaps=2,
+                      host_mirror=host_mirror)
     frozen = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=0)
     fp0 = [oracle.fnv1a64(b) for b in fx.all_blobs_now()]
+    host0 = [oracle.fnv1a64(fx.cold[i].numpy()) for i in range(fx.cold.shape[0])]
     loc_o = fx.loc0.copy()
     window = np.zeros(E, np.int64)
     total_swaps = 0
@@ -450,6 +453,9 @@ def test_residency_matches_oracle_and_keeps_bytes():
         assert rel_l2(buf.out.cpu().numpy(), want) <= OUT_TOL
     assert total_swaps > 0
     assert sorted(fx.layer.get_loc().tolist()) == list(range(E))
+    if host_mirror:
+        # with host copies nothing is ever written to host memory
+        assert [oracle.fnv1a64(fx.cold[i].numpy()) for i in range(E)] == host0
 
 
 def test_residency_injected_fault_leaves_map():
@@ -469,9 +475,12 @@ def test_residency_injected_fault_leaves_map():
     assert m.residency_update(fx.layer) > 0
 
 
-def test_shared_scratch_across_layers():
+@pytest.mark.parametrize("host_mirror", [False, True])
+def test_shared_scratch_across_layers(host_mirror):
     """Several layers share one slot scratch and run one after another (the c3
-    structure at c0 size): each layer's output still matches the oracle."""
+    structure at c0 size), swapping every other step: each layer's output still
+    matches the oracle and every expert keeps its bytes (with host copies a
+    promotion may read a scratch slot only while it holds that layer's copy)."""
     import moe_decode_host_gb300 as m
 
     H, I, E, n_hot, n_cold, k, T = 256, 512, 16, 12, 4, 2, 4
@@ -482,24 +491,29 @@ def test_shared_scratch_across_layers():
     for L in range(3):
         loc = synth.loc_from_hot_set(E, n_hot, np.random.default_rng(L).permutation(E)[:n_hot])
         layers.append(LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=100 + L, loc=loc,
-                                   scratch=scratch, slots=slots, swap_every=2))
+                                   scratch=scratch, slots=slots, swap_every=2, max_swaps=2, hysteresis=0.5,
+                                   host_mirror=host_mirror))
+    fp0 = [[oracle.fnv1a64(b) for b in fx.all_blobs_now()] for fx in layers]
     x = synth.gen_x(T, H, seed=5).cuda()
-    for step in range(4):
+    swaps = 0
+    for step in range(6):
         bufs = []
         for L, fx in enumerate(layers):
             logits = synth.gen_logits_uniform(T, E, seed=step * 10 + L)
             buf = m.StepBuffers(fx.layer, T, out_fp32=True)
-            m.run_step(fx.layer, buf, torch.from_numpy(logits).cuda(), x, residency=True)
+            swaps += m.run_step(fx.layer, buf, torch.from_numpy(logits).cuda(), x, residency=True)
             bufs.append((fx, logits, buf))
         torch.cuda.synchronize()
-        for fx, logits, buf in bufs:
-            pass
         # compare each layer's output with the oracle on the bytes it used (the maps only
         # change at the end of a step, after every layer ran)
         for fx, logits, buf in bufs:
             blobs = fx.all_blobs_now()
             rc, ids, w, want = oracle.layer(logits, bf16_bits(x), k, 0, H, I, blobs)
             assert rel_l2(buf.out.cpu().numpy(), want) <= OUT_TOL
+    assert swaps > 0
+    for fx, f0 in zip(layers, fp0):
+        assert [oracle.fnv1a64(b) for b in fx.all_blobs_now()] == f0
+        assert fx.layer.status() == 0
 
 
 def test_invalid_arguments_launch_nothing():
