@@ -344,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
-            // this warp reads stages sp, sp + 2, sp + 4, ...; the 4 scale bytes of its
-            // group for its two rows sit in two register pairs used alternately, each
-            // refilled right after use for the stage two own stages later
+            // this warp reads every other stage; the 4 scale bytes of its group for its
+            // two rows sit in two register pairs used alternately, each refilled right
+            // after use for the stage two own stages later
             uint32_t scA[2], scB[2];
             auto load_sc = [&](int s, uint32_t(&dst)[2]) {
                 const int grp = 2 * s + gl;
@@ -354,8 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 for (int r = 0; r < 2; ++r)
                     dst[r] = grp < ngroups ? ld_u32(sb + (size_t)grow[r] * srs + (size_t)grp * 4) : 0u;
             };
-            if (sp < nst) load_sc(sp, scA);
-            if (sp + 2 < nst) load_sc(sp + 2, scB);
+            // own stages: those whose global number gstage + s has parity sp (a pass can
+            // have an odd number of stages, so the first one depends on gstage)
+            const int sf = (sp ^ gstage) & 1;
+            if (sf < nst) load_sc(sf, scA);
+            if (sf + 2 < nst) load_sc(sf + 2, scB);
             bool ok = true;
             // The parity wait below cannot match a phase one lap old: slots have the parity
             // of their stages (kStages is even), so this warp's group reads every stage
@@ -383,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 if (s + 4 < nst) load_sc(s + 4, sc);
                 return true;
             };
-            for (int s = sp; s < nst && ok; s += 4) {
+            for (int s = sf; s < nst && ok; s += 4) {
                 ok = own_stage(s, scA);
                 if (ok && s + 2 < nst) ok = own_stage(s + 2, scB);
             }
