@@ -183,20 +183,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     const int nst = (ngroups + 1) / 2;
     const int tiles = (P == 0 ? I : H) / C::kTaskRows;
 
-    // active experts in this launch's token-count range and placement class, ascending
+    // active experts in this launch's token-count range and placement class: every
+    // thread flags some experts (one round of independent loads), then warp 0
+    // compacts the flags into an ascending list
+    for (int e = threadIdx.x; e < a.E; e += kThreads) {
+        const int c = __ldg(a.counts + e);
+        bool act_e = c > lo && c <= hi;
+        if (act_e && sel != 0) {
+            const bool hot = __ldg(a.loc + e) < a.n_hot;
+            act_e = (sel == 1) ? hot : !hot;
+        }
+        hd.off[e] = act_e;  // scratch use of off[] until the list is built
+    }
+    __syncthreads();
     if (warp == 0) {
         int cnt = 0;
         for (int base = 0; base < a.E; base += 32) {
             const int e = base + lane;
-            bool act_e = false;
-            if (e < a.E) {
-                const int c = __ldg(a.counts + e);
-                act_e = c > lo && c <= hi;
-                if (act_e && sel != 0) {
-                    const bool hot = __ldg(a.loc + e) < a.n_hot;
-                    act_e = (sel == 1) ? hot : !hot;
-                }
-            }
+            const bool act_e = e < a.E && hd.off[e] != 0;
             const unsigned m = __ballot_sync(0xffffffffu, act_e);
             if (act_e) hd.e[cnt + __popc(m & ((1u << lane) - 1u))] = e;
             cnt += __popc(m);

@@ -220,19 +220,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const int tiles = (P == 0 ? I : H) / kBM;
     volatile int* abort = &hd.abort;
 
+    // active experts (more than lo tokens, in the selected placement class): every
+    // thread flags some experts (one round of independent loads), then warp 0
+    // compacts the flags into an ascending list
+    for (int e = threadIdx.x; e < a.E; e += kThreadsTC) {
+        bool act = __ldg(a.counts + e) > lo;
+        if (act && sel != 0) {
+            const bool hot = __ldg(a.loc + e) < a.n_hot;
+            act = (sel == 1) ? hot : !hot;
+        }
+        hd.list[e] = act;  // flags first, compacted in place below
+    }
+    __syncthreads();
     if (warp == 0) {
         int cnt = 0;
         for (int base_e = 0; base_e < a.E; base_e += 32) {
             const int e = base_e + lane;
-            bool act = false;
-            if (e < a.E) {
-                act = __ldg(a.counts + e) > lo;
-                if (act && sel != 0) {
-                    const bool hot = __ldg(a.loc + e) < a.n_hot;
-                    act = (sel == 1) ? hot : !hot;
-                }
-            }
+            const bool act = e < a.E && hd.list[e] != 0;
             const unsigned m = __ballot_sync(0xffffffffu, act);
+            __syncwarp();  // every lane has read its flag before the chunk is overwritten
             if (act) hd.list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
             cnt += __popc(m);
         }
