@@ -17,6 +17,8 @@ namespace {
 template <bool F32>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const float* __restrict__ w, int T,
                                                       int k, int H, void* __restrict__ out) {
+    // launched behind the FFN (programmatic dependent launch): y is complete after this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.y;
     const int c4 = blockIdx.x * blockDim.x + threadIdx.x;  // index of 4 consecutive columns
     if (c4 * 4 >= H) return;
@@ -109,9 +111,8 @@ cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, 
                            cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     dim3 grid((H / 4 + 255) / 256, T);
-    if (out_fp32) combine_kernel<true><<<grid, 256, 0, st>>>(y, w, T, k, H, out);
-    else combine_kernel<false><<<grid, 256, 0, st>>>(y, w, T, k, H, out);
-    return cudaGetLastError();
+    if (out_fp32) return launch_pdl(combine_kernel<true>, grid, dim3(256), 0, st, y, w, T, k, H, out);
+    return launch_pdl(combine_kernel<false>, grid, dim3(256), 0, st, y, w, T, k, H, out);
 }
 
 cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st) {

@@ -227,6 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
         hd.blob[i] = (ph >= 0 && ph < a.n_phys) ? a.ptr[ph] : nullptr;
     }
     __syncthreads();
+    // the activations, their prescales and the outputs belong to the previous kernel
+    // until it completes; the work above only read routing results
+    grid_dep_wait();
     const int ntask = hd.D * tiles;
     volatile int* abort = &hd.abort;
 
@@ -564,6 +567,7 @@ __global__ void __launch_bounds__(256) hprep_kernel(const float* __restrict__ h,
                                                     const int32_t* __restrict__ phys_ids, int n_hot, int n_phys,
                                                     int sel, int I, int gstride, __half* __restrict__ g,
                                                     int32_t* __restrict__ gexp) {
+    grid_dep_wait();
     const int i = blockIdx.x;
     const int ph = __ldg(phys_ids + __ldg(entries + i));
     const bool hot = ph >= 0 && ph < n_hot;
@@ -619,8 +623,7 @@ cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cu
     // the stage's activation slice: 256 elements of 8 * NT consecutive bucket rows
     CUtensorMap act_map;
     if (!encode_act_map(&act_map, a, P, 256, 8 * NT, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
-    ffn_tma_kernel<P, NT><<<grid, kThreads, sm, st>>>(a, act_map, lo, hi, sel);
-    return cudaGetLastError();
+    return launch_pdl(ffn_tma_kernel<P, NT>, dim3(grid), dim3(kThreads), sm, st, a, act_map, lo, hi, sel);
 }
 
 }  // namespace
@@ -656,9 +659,9 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
     const long dmax = (long)(a.E < a.T * a.k ? a.E : a.T * a.k);
     const long tasks = dmax * (phase == 0 ? a.I / Cfg<0>::kTaskRows : a.H / Cfg<1>::kTaskRows);
     if (phase == 1) {
-        hprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.h, a.entries, a.phys_ids, a.n_hot, a.n_phys, sel, a.I,
-                                                a.H > a.I ? a.H : a.I, a.g, a.gexp);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(hprep_kernel, dim3(a.T * a.k), dim3(256), 0, st, (const float*)a.h,
+                                   (const int32_t*)a.entries, (const int32_t*)a.phys_ids, a.n_hot, a.n_phys, sel, a.I,
+                                   a.H > a.I ? a.H : a.I, a.g, a.gexp);
         if (e != cudaSuccess) return e;
     }
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);

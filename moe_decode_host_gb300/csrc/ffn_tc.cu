@@ -273,6 +273,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // activations, prescales and outputs belong to the previous kernel until it completes
+    grid_dep_wait();
     const uint32_t tmem = hd.tmem_base;
     const int ntask = hd.D * tiles;
 
@@ -560,9 +562,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
         if (err != cudaSuccess) return err;
         configured[phase] = true;
     }
-    if (phase == 0) ffn_tc_kernel<0><<<grid, kThreadsTC, kTcSmem, st>>>(a, map, lo, sel);
-    else ffn_tc_kernel<1><<<grid, kThreadsTC, kTcSmem, st>>>(a, map, lo, sel);
-    return cudaGetLastError();
+    if (phase == 0) return launch_pdl(ffn_tc_kernel<0>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel);
+    return launch_pdl(ffn_tc_kernel<1>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel);
 }
 
 }  // namespace moe

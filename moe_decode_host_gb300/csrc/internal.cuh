@@ -13,6 +13,25 @@ namespace moe {
 
 constexpr int kMaxSwaps = 64;
 
+// Launches `kernel` so that it may start while the previous kernel on the stream
+// finishes (programmatic dependent launch); the kernel waits with grid_dep_wait
+// before it touches that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Blob plane offsets for (H, I); see the blob format in moehost.h.
 struct BlobLayout {
     size_t w13n, w13s, w2n, w2s, total;

@@ -13,6 +13,13 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Waits until the grid this one was launched behind (programmatic dependent
+// launch) has completed and its writes are visible; returns at once otherwise.
+// Every kernel launched with launch_pdl calls it before it reads the previous
+// kernel's outputs and before any of its CTAs can exit, so that a kernel's
+// completion implies its predecessors'.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
