@@ -84,7 +84,10 @@ def parse():
     ap.add_argument("--skew", type=float, default=None, help="Zipf exponent for skewed routing")
     ap.add_argument("--layers", type=int, default=None, help="layers for c3")
     ap.add_argument("--pool", type=int, default=64)
-    ap.add_argument("--no-residency", action="store_true")
+    ap.add_argument("--residency", dest="no_residency", action="store_false", default=None,
+                    help="run the residency manager (default: only where the workload specifies it, the "
+                         "20-layer stack)")
+    ap.add_argument("--no-residency", dest="no_residency", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -103,6 +106,9 @@ def workload(args):
     import synth
 
     c = dict(synth.CONFIGS[args.config])
+    if args.no_residency is None:
+        # residency only where the workload asks for it (the stacked-layer config)
+        args.no_residency = "swap_every" not in c
     if args.batch is not None:
         c["T"] = args.batch
     if args.skew is not None:
@@ -116,7 +122,8 @@ def workload(args):
     c["name"] = args.config
     # host copies of every expert: default for one layer (7.7 GB pinned); a 20-layer
     # stack would need 154 GB of pinned host memory, so it keeps the in-place exchange
-    c["mirror"] = args.mirror if args.mirror is not None else (c.get("layers", 1) == 1 and c["n_cold"] > 0)
+    c["mirror"] = args.mirror if args.mirror is not None else (
+        c.get("layers", 1) == 1 and c["n_cold"] > 0 and not args.no_residency)
     return c
 
 
@@ -268,7 +275,9 @@ def _config_json(c, args):
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
             "residency": "off" if args.no_residency else ("every 16 steps, hysteresis 3.0, <=8 swaps, " + (
                 "host copy of every expert" if c.get("mirror") else "in-place HBM/host exchange")),
-            "step_pool": args.pool, "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
+            "step_pool": (min(max(args.pool, args.steps + args.warmup), 2048)
+                          if (not args.no_residency and c["n_cold"] > 0) else args.pool),
+            "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -315,14 +324,20 @@ def build_layers(c, dev, seed_tag="bench"):
     return layers, scratch, slots
 
 
-def gen_pool(c, layers, P, dev):
+def gen_pool(c, layers, P, PL, dev):
+    """Inputs of PL distinct steps: entry i holds, per layer, the logits of step i and
+    the activations of step i % P.  Routing never repeats within PL steps, so with
+    PL large the residency manager sees the workload's picking frequencies rather
+    than a short loop it could learn."""
     import torch
 
     import synth
 
     T, E, H = c["T"], c["E"], c["H"]
+    xs = [[synth.gen_x(T, H, seed=synth.sub_seed(c["name"], "x", li, p)).to(dev) for li in range(len(layers))]
+          for p in range(min(P, PL))]
     pool = []
-    for p in range(P):
+    for p in range(PL):
         per_layer = []
         for li, L in enumerate(layers):
             if c.get("routing") == "zipf":
@@ -330,8 +345,7 @@ def gen_pool(c, layers, P, dev):
                                            seed=synth.sub_seed(c["name"], "logits", li, p))
             else:
                 lg = synth.gen_logits_uniform(T, E, seed=synth.sub_seed(c["name"], "logits", li, p))
-            x = synth.gen_x(T, H, seed=synth.sub_seed(c["name"], "x", li, p))
-            per_layer.append((torch.from_numpy(lg).to(dev), x.to(dev), lg))
+            per_layer.append((torch.from_numpy(lg).to(dev), xs[p % len(xs)][li], lg))
         pool.append(per_layer)
     return pool
 
@@ -390,8 +404,10 @@ def run_ours(args):
     else:
         link_peak, link_detail = measure_link_peak(dev)
     layers, scratch, slots = build_layers(c, dev)
-    P = args.pool
-    pool = gen_pool(c, layers, P, dev)
+    # with residency on, routing comes from up to 2048 distinct steps (no short loop)
+    resid = not args.no_residency and c["n_cold"] > 0
+    P = min(max(args.pool, args.steps + args.warmup), 2048) if resid else args.pool
+    pool = gen_pool(c, layers, args.pool, P, dev)
     T, k, H, E = c["T"], c["k"], c["H"], c["E"]
     eb = m.expert_bytes(H, c["I"])
     NL = len(layers)

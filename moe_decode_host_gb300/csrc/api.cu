@@ -426,13 +426,11 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (L->copy_pending) {
         // experts in HBM first, while the cold copy is in flight; then the cold ones.
-        // An FFN CTA leaves no room on its SM for a copy CTA, so the hot phases run
-        // on the SMs the copy kernel does not hold (else the CTAs queued behind the
-        // copy would hold the hot phase until the copy ends)
-        const int copy_sms = L->copy_ctas < L->sm_count / 2 ? L->copy_ctas : L->sm_count / 2;
-        const int hot_sms = L->sm_count - copy_sms;
-        err = launch_ffn_phase(a, 0, 1, hot_sms, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
+        // An FFN CTA leaves no room on its SM for a copy CTA; the decode kernel's CTAs
+        // take tasks from a shared counter, so those that start only when the copy
+        // frees their SM simply take fewer
+        err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
         if (err == cudaSuccess) err = join_copy(L, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);

@@ -52,10 +52,16 @@ struct Cfg {
     static constexpr int kTaskRows = P == 0 ? 32 : 64;
 };
 constexpr int kActRow = 512;  // bytes of one activation row's slice in a stage (256 f16)
+constexpr int kTaskQ = 4;     // depth of the CTA's task queue
 
 struct alignas(16) SmemHead {
     uint64_t full[64];
     uint64_t empty[64];
+    // tasks come from a launch-wide counter: producer 0 takes the next index and
+    // publishes it in slot k % kTaskQ for the other producer and the consumer warps
+    uint64_t tq_full[kTaskQ];
+    uint64_t tq_empty[kTaskQ];
+    int tq[kTaskQ];
     int D;
     int abort;
     int pad[2];
@@ -169,7 +175,7 @@ __device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& 
 
 template <int P, int NT>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
-                                                                int lo, int hi, int sel) {
+                                                                int lo, int hi, int sel, int ctr) {
     using C = Cfg<P>;
     using L = Layout<P, NT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -212,6 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 mbar_init(&hd.full[s], 1);
                 mbar_init(&hd.empty[s], kPerStage);
             }
+            for (int j = 0; j < kTaskQ; ++j) {
+                mbar_init(&hd.tq_full[j], 1);
+                mbar_init(&hd.tq_empty[j], 1 + kConsumers);
+            }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
@@ -241,7 +251,22 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             unsigned phase = 0;
             int gstage = 0;  // global stage number in this CTA's stream
             bool ok = true;
-            for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const int j = k % kTaskQ;
+                const unsigned qpar = (unsigned)(k / kTaskQ) & 1u;
+                int task;
+                if (pp == 0) {
+                    if (!mbar_wait_fast(&hd.tq_empty[j], qpar ^ 1u, abort, a.status, a.diag, 4, j, k, 0)) break;
+                    task = atomicAdd(a.task_ctr + ctr, 1);
+                    if (task >= ntask) task = -1;
+                    *reinterpret_cast<volatile int*>(&hd.tq[j]) = task;
+                    mbar_arrive(&hd.tq_full[j]);
+                } else {
+                    if (!mbar_wait_fast(&hd.tq_full[j], qpar, abort, a.status, a.diag, 5, j, k, 0)) break;
+                    task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+                    mbar_arrive(&hd.tq_empty[j]);
+                }
+                if (task < 0) break;
                 const TaskInfo ti = task_info(a, hd, task, tiles);
                 if (!ti.valid) continue;
                 const CUtensorMap* map = P == 0 ? &a.tmaps[ti.phys].w13n : &a.tmaps[ti.phys].w2n;
@@ -306,7 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     constexpr int kEpi = P == 0 ? 2 : 4;
     int gstage = 0;
     bool done = false;
-    for (int task = blockIdx.x; task < ntask; task += gridDim.x) {
+    for (int k = 0;; ++k) {
+        const int j = k % kTaskQ;
+        const unsigned qpar = (unsigned)(k / kTaskQ) & 1u;
+        const bool got = __all_sync(0xffffffffu, mbar_wait_fast(&hd.tq_full[j], qpar, abort, a.status, a.diag, 5, j,
+                                                                k, 1));
+        // all consumer warps must take the same task or stop together (they meet at
+        // named barriers inside a task)
+        unsigned qstop;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.eq.u32 p, %1, 0;\n\t"
+            "bar.red.or.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(qstop)
+            : "r"((unsigned)got), "n"(32 * kConsumers)
+            : "memory");
+        const int task = qstop ? -1 : *reinterpret_cast<volatile int*>(&hd.tq[j]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd.tq_empty[j]);
+        if (task < 0) break;
         const TaskInfo ti = task_info(a, hd, task, tiles);
         const int r0 = ti.rt * C::kTaskRows;
         if (!ti.valid) {
@@ -328,21 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             const int lr = 16 * rt + pg + 8 * r;
             srow[r] = (P == 0 ? tile * C::kTaskRows : 0) + lr;
             grow[r] = (P == 0 && tile == 1 ? I : 0) + r0 + lr;
-        }
-        // warm L1 with the scale lines of this warp's rows in the next task
-        {
-            const int nxt = task + gridDim.x;
-            if (nxt < ntask && q == 0 && gl == 0) {
-                const TaskInfo tn = task_info(a, hd, nxt, tiles);
-                if (tn.valid) {
-                    const uint8_t* nsb = tn.blob + (P == 0 ? a.w13s : a.w2s);
-                    const int nr0 = tn.rt * C::kTaskRows;
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        for (size_t o = 0; o < srs; o += 128)
-                            prefetch_l1(nsb + (size_t)(grow[r] - r0 + nr0) * srs + o);
-                }
-            }
         }
         for (int tb = 0; tb < ti.cnt; tb += 8 * NT) {
             const int ncols = min(8 * NT, ti.cnt - tb);
@@ -556,8 +585,10 @@ __device__ __forceinline__ void prescale_row(const void* src_row, int len, __hal
 // One CTA per bucket row i: x of token entries[i] / k, prescaled, into g row i.
 __global__ void __launch_bounds__(256) xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k,
                                                     const int32_t* __restrict__ entries, int gstride,
-                                                    __half* __restrict__ g, int32_t* __restrict__ gexp) {
+                                                    __half* __restrict__ g, int32_t* __restrict__ gexp,
+                                                    int32_t* __restrict__ task_ctr) {
     const int i = blockIdx.x;
+    if (i == 0 && threadIdx.x < kTaskCounters) task_ctr[threadIdx.x] = 0;
     const int t = __ldg(entries + i) / k;
     prescale_row<true>(x + (size_t)t * H, H, g + (size_t)i * gstride, gexp + i);
 }
@@ -587,13 +618,15 @@ __global__ void debug_e2m1_kernel(uint32_t* out) {
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t g, gexp, h, total;
+    size_t ctr, g, gexp, h, total;
 };
 
 WsLayout ws_layout(int T, int k, int H, int I) {
     WsLayout w;
     const size_t n = (size_t)T * k;
     size_t o = 0;
+    w.ctr = o;
+    o = align256(o + kTaskCounters * sizeof(int32_t));
     w.g = o;
     o = align256(o + n * (H > I ? H : I) * sizeof(__half));
     w.gexp = o;
@@ -611,7 +644,7 @@ size_t smem_bytes() {
 }
 
 template <int P, int NT>
-cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cudaStream_t st) {
+cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int ctr, int grid, cudaStream_t st) {
     static bool configured = false;
     const size_t sm = smem_bytes<P, NT>();
     if (!configured) {
@@ -623,7 +656,7 @@ cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int grid, cu
     // the stage's activation slice: 256 elements of 8 * NT consecutive bucket rows
     CUtensorMap act_map;
     if (!encode_act_map(&act_map, a, P, 256, 8 * NT, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
-    return launch_pdl(ffn_tma_kernel<P, NT>, dim3(grid), dim3(kThreads), sm, st, a, act_map, lo, hi, sel);
+    return launch_pdl(ffn_tma_kernel<P, NT>, dim3(grid), dim3(kThreads), sm, st, a, act_map, lo, hi, sel, ctr);
 }
 
 }  // namespace
@@ -640,11 +673,13 @@ bool encode_act_map(CUtensorMap* m, const FfnArgs& a, int phase, uint32_t box_in
 cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     const WsLayout w = ws_layout(a.T, a.k, a.H, a.I);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.task_ctr = reinterpret_cast<int32_t*>(ws + w.ctr);
     a.g = reinterpret_cast<__half*>(ws + w.g);
     a.gexp = reinterpret_cast<int32_t*>(ws + w.gexp);
     a.h = reinterpret_cast<float*>(ws + w.h);
     if (a.T == 0) return cudaSuccess;
-    xprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.x, a.H, a.k, a.entries, a.H > a.I ? a.H : a.I, a.g, a.gexp);
+    xprep_kernel<<<a.T * a.k, 256, 0, st>>>(a.x, a.H, a.k, a.entries, a.H > a.I ? a.H : a.I, a.g, a.gexp,
+                                            a.task_ctr);
     return cudaGetLastError();
 }
 
@@ -665,17 +700,20 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
         if (e != cudaSuccess) return e;
     }
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);
-    for (const Range& r : ranges) {
+    for (int ri = 0; ri < 3; ++ri) {
+        const Range& r = ranges[ri];
         if (a.T <= r.lo) break;
+        // each launch of the call takes tasks from its own counter (zeroed by xprep)
+        const int ctr = ((sel == 2 ? 2 : 0) + phase) * 3 + ri;
         cudaError_t err;
         if (phase == 0) {
-            err = r.nt == 1 ? launch_phase<0, 1>(a, r.lo, r.hi, sel, grid, st)
-                : r.nt == 2 ? launch_phase<0, 2>(a, r.lo, r.hi, sel, grid, st)
-                            : launch_phase<0, 4>(a, r.lo, r.hi, sel, grid, st);
+            err = r.nt == 1 ? launch_phase<0, 1>(a, r.lo, r.hi, sel, ctr, grid, st)
+                : r.nt == 2 ? launch_phase<0, 2>(a, r.lo, r.hi, sel, ctr, grid, st)
+                            : launch_phase<0, 4>(a, r.lo, r.hi, sel, ctr, grid, st);
         } else {
-            err = r.nt == 1 ? launch_phase<1, 1>(a, r.lo, r.hi, sel, grid, st)
-                : r.nt == 2 ? launch_phase<1, 2>(a, r.lo, r.hi, sel, grid, st)
-                            : launch_phase<1, 4>(a, r.lo, r.hi, sel, grid, st);
+            err = r.nt == 1 ? launch_phase<1, 1>(a, r.lo, r.hi, sel, ctr, grid, st)
+                : r.nt == 2 ? launch_phase<1, 2>(a, r.lo, r.hi, sel, ctr, grid, st)
+                            : launch_phase<1, 4>(a, r.lo, r.hi, sel, ctr, grid, st);
         }
         if (err != cudaSuccess) return err;
     }

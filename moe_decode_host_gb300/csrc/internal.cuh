@@ -83,6 +83,9 @@ struct ExpertMaps {
 
 // Buckets with more than this many tokens run on the tensor-core prefill kernel.
 constexpr int kTcMinTokens = 64;
+// Task counters in the FFN workspace: one per decode kernel launch of a call
+// (2 placement classes x 2 phases x 3 token-count ranges).
+constexpr int kTaskCounters = 16;
 
 // Encodes a 2D tiled TMA descriptor (inner dimension contiguous); false on failure.
 bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -106,6 +109,7 @@ struct FfnArgs {
     int32_t* gexp;           // [T*k] their power-of-two prescale exponents
     float* h;                // [T*k][I] SiLU(gate) * up
     float* y;                // [T*k][H]
+    int32_t* task_ctr;       // workspace [kTaskCounters] per-launch task counters (zeroed by xprep)
     int* status;
     int* diag;               // [16] where the first timed-out wait gave up
     size_t w13s, w2n, w2s;   // plane offsets in a blob
