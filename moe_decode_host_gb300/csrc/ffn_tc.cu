@@ -12,9 +12,9 @@
 //                and up rows together in the gate/up phase) into a ring of raw
 //                stages;
 //   warp 1       owns tensor memory and issues the MMAs (one thread): each stage
-//                is committed back to its two producers, each tile to the
-//                epilogue; two accumulator buffers let a tile's epilogue overlap
-//                the next tile's main loop;
+//                is committed back to its producers, each tile to the epilogue;
+//                the down phase has two accumulator buffers so that a tile's
+//                epilogue overlaps the next tile's main loop;
 //   warp 2       TMA of the activation tiles (64 bucket rows x 64 elements, f16,
 //                128-byte swizzle; the prescale kernels write the activations in
 //                bucket order, so an expert's tokens are consecutive rows), into a
@@ -23,8 +23,10 @@
 //                half of a row's stage (down phase) per thread, each E8M0 block
 //                scale rebased to 2^12 below the row's largest scale, so that every
 //                block whose scale is within 2^35 of the largest is exact in f16
-//                (smaller blocks lose low bits); written in the 128-byte-swizzled
-//                K-major layout the MMA reads;
+//                (smaller blocks lose low bits); the f16 tiles go to tensor memory
+//                (tcgen05.st: one weight row per lane, consecutive K elements
+//                packed two per column), where the MMA reads its A operand, so
+//                shared memory carries only raw weights and activations;
 //   warps 12-15  epilogue: tensor memory -> registers -> h (gate/up phase, SiLU
 //                gate times up) or y (down phase), undoing the power-of-two
 //                rebasing of weights and activations.
@@ -40,18 +42,22 @@ namespace {
 constexpr int kBM = 128;    // weight rows per tile = tensor-memory lanes
 constexpr int kBK = 64;     // K elements per stage (128 bytes of f16 per row)
 constexpr int kNMax = 128;  // token columns per pass
-constexpr int kRawStages = 6;
-constexpr int kAStages = 3;
-constexpr int kBStages = 4;
+constexpr int kRawStages = 8;
+constexpr int kAStages = 4;   // f16 weight stages in tensor memory
+constexpr int kBStages = 8;
 constexpr int kFirstConv = 4;   // first converter warp
 constexpr int kConvWarps = 8;
 constexpr int kFirstEpi = 12;   // first epilogue warp (warp % 4 = lane quarter)
 constexpr int kThreadsTC = 512;
 constexpr int kRawBytes = 2 * kBM * 32;      // gate + up raw slices (down phase uses half)
-constexpr int kATile = kBM * 128;            // one f16 weight tile, 16 KB
-constexpr int kAStageBytes = 2 * kATile;     // gate + up tiles
 constexpr int kBStageBytes = kNMax * 128;    // activation tile, 16 KB
-constexpr uint32_t kAccCols = 256;           // tensor-memory columns per accumulator buffer
+// Tensor memory (512 columns): accumulators in [0, 256) -- gate and up (128 each)
+// in the gate/up phase, two 128-column buffers in the down phase -- and the f16
+// weight stages in [256, 512): 64 columns each (gate 32, up 32; the down phase
+// uses 32).
+constexpr uint32_t kAccCols = 128;           // columns per accumulator (one matrix, N <= 128)
+constexpr uint32_t kACol0 = 256;             // first column of the weight stages
+constexpr uint32_t kAStageCols = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
@@ -73,8 +79,7 @@ struct alignas(16) TcHead {
 };
 
 constexpr size_t kRawOff = 0;
-constexpr size_t kAOff = kRawOff + (size_t)kRawStages * kRawBytes;
-constexpr size_t kBOff = kAOff + (size_t)kAStages * kAStageBytes;
+constexpr size_t kBOff = kRawOff + (size_t)kRawStages * kRawBytes;
 constexpr size_t kHeadOff = kBOff + (size_t)kBStages * kBStageBytes;
 constexpr size_t kTcSmem = 1024 + kHeadOff + sizeof(TcHead);
 static_assert(kTcSmem <= 232448, "shared memory budget of one CTA");
@@ -85,15 +90,28 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]: A is 128 lanes x 16 f16 (8 columns) at a_tmem.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// This thread's lane of tensor memory, 16 or 32 consecutive columns from taddr.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -210,7 +228,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* raw = base + kRawOff;
-    uint8_t* sa = base + kAOff;
     uint8_t* sb = base + kBOff;
     TcHead& hd = *reinterpret_cast<TcHead*>(base + kHeadOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -361,15 +378,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         break;
                     }
                     tc_fence_after();
-                    // descriptors of k-step 0; a 16-element step advances the start address by 32 bytes
-                    const uint64_t ad = sw128_desc(smem_u32(sa + (size_t)as * kAStageBytes));
+                    // A: the stage's f16 weights in tensor memory (gate at +0, up at +32
+                    // columns; 8 columns per 16-element k-step); B: descriptor of k-step 0,
+                    // a 16-element step advances its start address by 32 bytes
+                    const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
                     const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
                             const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                            tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, acc);
-                            if (P == 0) tc_mma_f16(d + kNMax, ad + (kATile >> 4) + 2 * kk, bd + 2 * kk, idesc, acc);
+                            tc_mma_f16_ta(d, at + 8 * kk, bd + 2 * kk, idesc, acc);
+                            if (P == 0) tc_mma_f16_ta(d + kAccCols, at + 32 + 8 * kk, bd + 2 * kk, idesc, acc);
                         }
                         tc_commit(&hd.a_empty[as]);
                         tc_commit(&hd.b_empty[bs]);
@@ -381,7 +400,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 if (!ok) break;
                 if (lane == 0) tc_commit(&hd.acc_full[buf]);
                 __syncwarp();
-                buf ^= 1;
+                if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 256)
             }
         }
         // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
@@ -395,9 +414,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         // gate/up phase: thread = (matrix hi, row); down phase: thread = (half hi of the
         // stage's 64 elements, row)
         const int cidx = threadIdx.x - kFirstConv * 32;
-        const int row = cidx & (kBM - 1);
+        const int row = cidx & (kBM - 1);  // = (warp % 4) * 32 + lane: this thread's tensor-memory lane
         const int hi = cidx >> 7;
-        const uint32_t swz = (uint32_t)(row & 7);
+        const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) * 32u << 16);
         int rs = 0, as = 0;
         unsigned rph = 0, aph = 0;
         bool ok = true;
@@ -422,8 +441,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                             ok = false;
                             break;
                         }
+                        tc_fence_after();
                         const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
-                        uint8_t* arow = sa + (size_t)as * kAStageBytes + row * 128;
+                        const uint32_t acol = lane_base + kACol0 + (uint32_t)as * kAStageCols;
                         if constexpr (P == 0) {
                             const uint4* rp = reinterpret_cast<const uint4*>(rsrc + hi * kBM * 32 + row * 32);
                             const uint4 w0 = rp[0], w1 = rp[1];
@@ -431,23 +451,36 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                             const uint32_t m0 = f16_pow2((int)e0 - cb), m1 = f16_pow2((int)e1 - cb);
                             const uint32_t mm0 = m0 | (m0 << 16), mm1 = m1 | (m1 << 16);
                             const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                            arow += hi * kATile;
+                            uint32_t v[2][16];  // the row's 64 elements as f16 pairs, in K order
 #pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                *reinterpret_cast<uint4*>(arow + (((uint32_t)c ^ swz) * 16)) =
-                                    convert_chunk(words[c], c < 4 ? mm0 : mm1);
+                            for (int c = 0; c < 8; ++c) {
+                                const uint4 o = convert_chunk(words[c], c < 4 ? mm0 : mm1);
+                                v[c >> 2][(c & 3) * 4 + 0] = o.x;
+                                v[c >> 2][(c & 3) * 4 + 1] = o.y;
+                                v[c >> 2][(c & 3) * 4 + 2] = o.z;
+                                v[c >> 2][(c & 3) * 4 + 3] = o.w;
+                            }
+                            tc_st16(acol + 32u * hi, v[0]);
+                            tc_st16(acol + 32u * hi + 16u, v[1]);
                         } else {
                             const uint4 w0 = *reinterpret_cast<const uint4*>(rsrc + row * 32 + hi * 16);
                             const uint32_t e = (wcur >> (16 * u + 8 * hi)) & 0xffu;
                             const uint32_t m = f16_pow2((int)e - cb);
                             const uint32_t mm = m | (m << 16);
                             const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
+                            uint32_t v[16];  // this half of the row's stage, in K order
 #pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<uint4*>(arow + (((uint32_t)(4 * hi + c) ^ swz) * 16)) =
-                                    convert_chunk(words[c], mm);
+                            for (int c = 0; c < 4; ++c) {
+                                const uint4 o = convert_chunk(words[c], mm);
+                                v[c * 4 + 0] = o.x;
+                                v[c * 4 + 1] = o.y;
+                                v[c * 4 + 2] = o.z;
+                                v[c * 4 + 3] = o.w;
+                            }
+                            tc_st16(acol + 16u * hi, v);
                         }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        tc_wait_st();
+                        tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
                             mbar_arrive(&hd.a_full[as]);
@@ -507,7 +540,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 const uint32_t d = lane_addr + (uint32_t)buf * kAccCols;
                 for (int cb = 0; cb < nb; cb += 16) {
                     float v0[16], v1[16];
-                    if constexpr (P == 0) tc_ld16x2(d + cb, d + kNMax + cb, v0, v1);
+                    if constexpr (P == 0) tc_ld16x2(d + cb, d + kAccCols + cb, v0, v1);
                     else tc_ld16(d + cb, v0);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -527,7 +560,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&hd.acc_empty[buf]);
-                buf ^= 1;
+                if (P == 1) buf ^= 1;
             }
         }
     }
