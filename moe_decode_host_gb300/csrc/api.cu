@@ -127,14 +127,14 @@ bool moe::encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* bas
 namespace {
 
 // 2D u8 view [rows][row_bytes] at base: the decode kernel's box (128 bytes x
-// box_rows rows, 128-byte swizzle) and the prefill kernel's (32 bytes x 128 rows,
+// box_rows rows, 128-byte swizzle) and the prefill kernel's (64 bytes x 128 rows,
 // plain).
 bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows, uint32_t box_rows) {
     return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 128, box_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
-    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 32, 128,
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 64, 128,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 

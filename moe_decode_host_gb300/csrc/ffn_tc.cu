@@ -8,17 +8,17 @@
 // tcgen05.mma (kind::f16, f16 operands, fp32 accumulators in tensor memory).
 //
 // Warp roles of one persistent CTA per SM (16 warps):
-//   warp 0       TMA of the raw MXFP4 weight slices (128 rows x 64 elements; gate
+//   warp 0       TMA of the raw MXFP4 weight slices (128 rows x 128 elements; gate
 //                and up rows together in the gate/up phase) into a ring of raw
 //                stages;
 //   warp 1       owns tensor memory and issues the MMAs (one thread): each stage
 //                is committed back to its producers, each tile to the epilogue;
 //                the down phase has two accumulator buffers so that a tile's
 //                epilogue overlaps the next tile's main loop;
-//   warp 2       TMA of the activation tiles (64 bucket rows x 64 elements, f16,
-//                128-byte swizzle; the prescale kernels write the activations in
-//                bucket order, so an expert's tokens are consecutive rows), into a
-//                ring of its own;
+//   warp 2       TMA of the activation tiles (up to 128 bucket rows x 128
+//                elements, f16, as two 64-element atoms with 128-byte swizzle; the
+//                prescale kernels write the activations in bucket order, so an
+//                expert's tokens are consecutive rows), into a ring of its own;
 //   warps 4-11   converters: E2M1 -> f16 for one weight row (gate/up phase) or one
 //                half of a row's stage (down phase) per thread, each E8M0 block
 //                scale rebased to 2^12 below the row's largest scale, so that every
@@ -40,24 +40,27 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;    // weight rows per tile = tensor-memory lanes
-constexpr int kBK = 64;     // K elements per stage (128 bytes of f16 per row)
+constexpr int kBK = 128;    // K elements per stage (two 128-byte swizzle atoms of f16 per row)
 constexpr int kNMax = 128;  // token columns per pass
-constexpr int kRawStages = 8;
-constexpr int kAStages = 4;   // f16 weight stages in tensor memory
-constexpr int kBStages = 8;
+constexpr int kRawStages = 4;
+constexpr int kAStages = 2;   // f16 weight stages in tensor memory
+constexpr int kBStages = 4;
 constexpr int kFirstConv = 4;   // first converter warp
 constexpr int kConvWarps = 8;
 constexpr int kFirstEpi = 12;   // first epilogue warp (warp % 4 = lane quarter)
 constexpr int kThreadsTC = 512;
-constexpr int kRawBytes = 2 * kBM * 32;      // gate + up raw slices (down phase uses half)
-constexpr int kBStageBytes = kNMax * 128;    // activation tile, 16 KB
+constexpr int kRawRow = kBK / 2;             // E2M1 bytes of one row per stage
+constexpr int kRawBytes = 2 * kBM * kRawRow;  // gate + up raw slices (down phase uses half)
+constexpr int kBAtom = kNMax * 128;          // 64 elements of K of the activation tile, 16 KB
+constexpr int kBStageBytes = 2 * kBAtom;     // activation tile, 32 KB
 // Tensor memory (512 columns): accumulators in [0, 256) -- gate and up (128 each)
 // in the gate/up phase, two 128-column buffers in the down phase -- and the f16
-// weight stages in [256, 512): 64 columns each (gate 32, up 32; the down phase
-// uses 32).
+// weight stages in [256, 512): 128 columns each (gate 64, up 64; the down phase
+// uses 64).
 constexpr uint32_t kAccCols = 128;           // columns per accumulator (one matrix, N <= 128)
 constexpr uint32_t kACol0 = 256;             // first column of the weight stages
-constexpr uint32_t kAStageCols = 64;
+constexpr uint32_t kAStageCols = 128;
+constexpr uint32_t kAMatCols = kBK / 2;      // columns of one matrix's stage (2 f16 per column)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I;
     const int K = P == 0 ? H : I;
-    const int nks = K / kBK;  // even: K is a multiple of 128
+    const int nks = K / kBK;  // K is a multiple of 128
     const int tiles = (P == 0 ? I : H) / kBM;
     volatile int* abort = &hd.abort;
 
@@ -314,9 +317,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     }
                     if (lane == 0) {
                         uint8_t* dst = raw + (size_t)rs * kRawBytes;
-                        mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * 32 : kBM * 32);
-                        tma_load_2d(dst, map, s * 32, r0, &hd.raw_full[rs]);
-                        if (P == 0) tma_load_2d(dst + kBM * 32, map, s * 32, I + r0, &hd.raw_full[rs]);
+                        mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * kRawRow : kBM * kRawRow);
+                        tma_load_2d(dst, map, s * kRawRow, r0, &hd.raw_full[rs]);
+                        if (P == 0) tma_load_2d(dst + kBM * kRawRow, map, s * kRawRow, I + r0, &hd.raw_full[rs]);
                     }
                     __syncwarp();
                     advance(rs, rph, kRawStages);
@@ -342,9 +345,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     }
                     if (lane == 0) {
                         uint8_t* dst = sb + (size_t)bs * kBStageBytes;
-                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)boxes * 64u * 128u);
-                        for (int c = 0; c < boxes; ++c)
-                            tma_load_2d(dst + c * 64 * 128, &act_map, s * kBK, t.off + tb + 64 * c, &hd.b_full[bs]);
+                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)boxes * 2u * 64u * 128u);
+                        for (int at = 0; at < 2; ++at)  // the stage's two 64-element atoms of K
+                            for (int c = 0; c < boxes; ++c)
+                                tma_load_2d(dst + at * kBAtom + c * 64 * 128, &act_map, s * kBK + 64 * at,
+                                            t.off + tb + 64 * c, &hd.b_full[bs]);
                     }
                     __syncwarp();
                     advance(bs, bph, kBStages);
@@ -378,7 +383,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         break;
                     }
                     tc_fence_after();
-                    // A: the stage's f16 weights in tensor memory (gate at +0, up at +32
+                    // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
                     // columns; 8 columns per 16-element k-step); B: descriptor of k-step 0,
                     // a 16-element step advances its start address by 32 bytes
                     const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
@@ -387,8 +392,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
                             const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                            tc_mma_f16_ta(d, at + 8 * kk, bd + 2 * kk, idesc, acc);
-                            if (P == 0) tc_mma_f16_ta(d + kAccCols, at + 32 + 8 * kk, bd + 2 * kk, idesc, acc);
+                            // k-steps 0-3 in the first activation atom, 4-7 in the second
+                            const uint64_t b = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
+                            tc_mma_f16_ta(d, at + 8 * kk, b, idesc, acc);
+                            if (P == 0) tc_mma_f16_ta(d + kAccCols, at + kAMatCols + 8 * kk, b, idesc, acc);
                         }
                         tc_commit(&hd.a_empty[as]);
                         tc_commit(&hd.b_empty[bs]);
@@ -430,65 +437,51 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                                        : blob + a.w2s + (size_t)(r0 + row) * srl;
             const int cb = row_max_exp(sc, srl) - 12;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                // scale word of stages s, s+1 (blocks 2s..2s+3), fetched two stages ahead
+                // scale word of stage s (blocks 4s..4s+3), fetched a stage ahead
                 uint32_t wcur = ld_u32(sc);
-                for (int s = 0; s < nks && ok; s += 2) {
-                    const uint32_t wnext = (s + 2 < nks) ? ld_u32(sc + 2 * (s + 2)) : 0u;
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, s + u, task) ||
-                            !warp_wait(&hd.a_empty[as], aph ^ 1u, a, abort, 18, as, s + u, task)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
-                        const uint32_t acol = lane_base + kACol0 + (uint32_t)as * kAStageCols;
-                        if constexpr (P == 0) {
-                            const uint4* rp = reinterpret_cast<const uint4*>(rsrc + hi * kBM * 32 + row * 32);
-                            const uint4 w0 = rp[0], w1 = rp[1];
-                            const uint32_t e0 = (wcur >> (16 * u)) & 0xffu, e1 = (wcur >> (16 * u + 8)) & 0xffu;
-                            const uint32_t m0 = f16_pow2((int)e0 - cb), m1 = f16_pow2((int)e1 - cb);
-                            const uint32_t mm0 = m0 | (m0 << 16), mm1 = m1 | (m1 << 16);
-                            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                            uint32_t v[2][16];  // the row's 64 elements as f16 pairs, in K order
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const uint4 o = convert_chunk(words[c], c < 4 ? mm0 : mm1);
-                                v[c >> 2][(c & 3) * 4 + 0] = o.x;
-                                v[c >> 2][(c & 3) * 4 + 1] = o.y;
-                                v[c >> 2][(c & 3) * 4 + 2] = o.z;
-                                v[c >> 2][(c & 3) * 4 + 3] = o.w;
-                            }
-                            tc_st16(acol + 32u * hi, v[0]);
-                            tc_st16(acol + 32u * hi + 16u, v[1]);
-                        } else {
-                            const uint4 w0 = *reinterpret_cast<const uint4*>(rsrc + row * 32 + hi * 16);
-                            const uint32_t e = (wcur >> (16 * u + 8 * hi)) & 0xffu;
-                            const uint32_t m = f16_pow2((int)e - cb);
-                            const uint32_t mm = m | (m << 16);
-                            const uint32_t words[4] = {w0.x, w0.y, w0.z, w0.w};
-                            uint32_t v[16];  // this half of the row's stage, in K order
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const uint4 o = convert_chunk(words[c], mm);
-                                v[c * 4 + 0] = o.x;
-                                v[c * 4 + 1] = o.y;
-                                v[c * 4 + 2] = o.z;
-                                v[c * 4 + 3] = o.w;
-                            }
-                            tc_st16(acol + 16u * hi, v);
-                        }
-                        tc_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            mbar_arrive(&hd.a_full[as]);
-                            mbar_arrive(&hd.raw_empty[rs]);
-                        }
-                        advance(rs, rph, kRawStages);
-                        advance(as, aph, kAStages);
+                for (int s = 0; s < nks && ok; ++s) {
+                    const uint32_t wnext = (s + 1 < nks) ? ld_u32(sc + 4 * (s + 1)) : 0u;
+                    if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, s, task) ||
+                        !warp_wait(&hd.a_empty[as], aph ^ 1u, a, abort, 18, as, s, task)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
+                    const uint32_t acol = lane_base + kACol0 + (uint32_t)as * kAStageCols;
+                    // gate/up phase: the row's 128 elements (16 words of 8) into its matrix's
+                    // 64 columns; down phase: one half of the row (8 words) into 32 columns
+                    constexpr int kWords = P == 0 ? 16 : 8;
+                    const uint4* rp = reinterpret_cast<const uint4*>(
+                        rsrc + (P == 0 ? hi * kBM * kRawRow + row * kRawRow : row * kRawRow + hi * (kRawRow / 2)));
+                    const uint32_t col0 = acol + (P == 0 ? kAMatCols * hi : (kAMatCols / 2) * hi);
+#pragma unroll
+                    for (int g = 0; g < kWords / 4; ++g) {  // 4 words = 32 elements = one scale block
+                        const uint4 w = rp[g];
+                        const int blk = P == 0 ? g : 2 * hi + g;
+                        const uint32_t m = f16_pow2((int)((wcur >> (8 * blk)) & 0xffu) - cb);
+                        const uint32_t mm = m | (m << 16);
+                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t v[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 o = convert_chunk(words[c], mm);
+                            v[4 * c + 0] = o.x;
+                            v[4 * c + 1] = o.y;
+                            v[4 * c + 2] = o.z;
+                            v[4 * c + 3] = o.w;
+                        }
+                        tc_st16(col0 + 16u * g, v);
+                    }
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&hd.a_full[as]);
+                        mbar_arrive(&hd.raw_empty[rs]);
+                    }
+                    advance(rs, rph, kRawStages);
+                    advance(as, aph, kAStages);
                     wcur = wnext;
                 }
             }
