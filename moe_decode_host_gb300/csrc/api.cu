@@ -128,14 +128,14 @@ namespace {
 
 // 2D u8 view [rows][row_bytes] at base: the decode kernel's box (128 bytes x
 // box_rows rows, 128-byte swizzle) and the prefill kernel's (64 bytes x 128 rows,
-// plain).
+// 64-byte swizzle).
 bool encode_plane(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows, uint32_t box_rows) {
     return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 128, box_rows,
                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
     return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 64, 128,
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
+                          CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Makes `st` wait for the layer's cold copy in flight, if any.

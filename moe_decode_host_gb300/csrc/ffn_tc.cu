@@ -77,8 +77,8 @@ struct alignas(16) TcHead {
     int abort;
     int D;
     int list[kMaxE];
-    int col_pick[4][kNMax];     // per epilogue warp: output row of each column of the pass
-    float col_scale[4][kNMax];  // and its activation prescale 2^p
+    alignas(16) int col_pick[4][kNMax];     // per epilogue warp: output row of each column of the pass
+    alignas(16) float col_scale[4][kNMax];  // and its activation prescale 2^p
 };
 
 constexpr size_t kRawOff = 0;
@@ -359,36 +359,39 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         if (lane == 0)
             for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
     } else if (warp == 1) {
-        // ---------------- MMA issuer (lane 0 issues) ----------------
-        int as = 0, bs = 0, buf = 0;
-        unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
-        bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
-            const TcTask t = tc_task(a, hd, task, tiles);
-            if (!t.valid) continue;
-            for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                const int N = ncols16(min(kNMax, t.cnt - tb));
-                const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-                if (!warp_wait(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, a, abort, 14, buf, 0, task)) {
-                    ok = false;
-                    break;
-                }
-                accph ^= 1u << buf;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)buf * kAccCols;
-                for (int s = 0; s < nks; ++s) {
-                    if (!warp_wait(&hd.a_full[as], aph, a, abort, 15, as, s, task) ||
-                        !warp_wait(&hd.b_full[bs], bph, a, abort, 16, bs, s, task)) {
+        // ---------------- MMA issuer (lane 0 alone) ----------------
+        // one thread runs this loop: its waits and issue overhead between stages are
+        // the time the tensor pipe idles, so it takes no warp-wide votes
+        if (lane == 0) {
+            int as = 0, bs = 0, buf = 0;
+            unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
+            bool ok = true;
+            for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+                const TcTask t = tc_task(a, hd, task, tiles);
+                if (!t.valid) continue;
+                for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
+                    const int N = ncols16(min(kNMax, t.cnt - tb));
+                    const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+                    if (!mbar_wait_fast(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, abort, a.status, a.diag, 14,
+                                        buf, 0, task)) {
                         ok = false;
                         break;
                     }
+                    accph ^= 1u << buf;
                     tc_fence_after();
-                    // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
-                    // columns; 8 columns per 16-element k-step); B: descriptor of k-step 0,
-                    // a 16-element step advances its start address by 32 bytes
-                    const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
-                    const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
-                    if (lane == 0) {
+                    const uint32_t d = tmem + (uint32_t)buf * kAccCols;
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.a_full[as], aph, abort, a.status, a.diag, 15, as, s, task) ||
+                            !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 16, bs, s, task)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
+                        // columns; 8 columns per 16-element k-step); B: descriptor of k-step
+                        // 0, a 16-element step advances its start address by 32 bytes
+                        const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
+                        const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
                             const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
@@ -399,23 +402,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         }
                         tc_commit(&hd.a_empty[as]);
                         tc_commit(&hd.b_empty[bs]);
+                        advance(as, aph, kAStages);
+                        advance(bs, bph, kBStages);
                     }
-                    __syncwarp();
-                    advance(as, aph, kAStages);
-                    advance(bs, bph, kBStages);
+                    if (!ok) break;
+                    tc_commit(&hd.acc_full[buf]);
+                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 256)
                 }
-                if (!ok) break;
-                if (lane == 0) tc_commit(&hd.acc_full[buf]);
-                __syncwarp();
-                if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 256)
             }
-        }
-        // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
-        // last commit of every stage
-        if (lane == 0) {
+            // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
+            // last commit of every stage
             for (int s = 0; s < kAStages; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
             for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
         }
+        __syncwarp();
     } else if (warp >= kFirstConv && warp < kFirstConv + kConvWarps) {
         // ---------------- converters ----------------
         // gate/up phase: thread = (matrix hi, row); down phase: thread = (half hi of the
@@ -452,12 +452,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     // gate/up phase: the row's 128 elements (16 words of 8) into its matrix's
                     // 64 columns; down phase: one half of the row (8 words) into 32 columns
                     constexpr int kWords = P == 0 ? 16 : 8;
-                    const uint4* rp = reinterpret_cast<const uint4*>(
-                        rsrc + (P == 0 ? hi * kBM * kRawRow + row * kRawRow : row * kRawRow + hi * (kRawRow / 2)));
+                    // the raw stage holds 64-byte rows with the 64-byte swizzle: 16-byte
+                    // chunk c of row r sits at chunk c ^ ((r >> 1) & 3), so the 8 rows a
+                    // quarter-warp reads fall in distinct banks
+                    const uint8_t* rrow = rsrc + (P == 0 ? hi * kBM * kRawRow : 0) + row * kRawRow;
+                    const int c0 = P == 0 ? 0 : 2 * hi;  // first chunk of this thread
+                    const int sw = (row >> 1) & 3;
                     const uint32_t col0 = acol + (P == 0 ? kAMatCols * hi : (kAMatCols / 2) * hi);
 #pragma unroll
                     for (int g = 0; g < kWords / 4; ++g) {  // 4 words = 32 elements = one scale block
-                        const uint4 w = rp[g];
+                        const uint4 w = *reinterpret_cast<const uint4*>(rrow + (((c0 + g) ^ sw) << 4));
                         const int blk = P == 0 ? g : 2 * hi + g;
                         const uint32_t m = f16_pow2((int)((wcur >> (8 * blk)) & 0xffu) - cb);
                         const uint32_t mm = m | (m << 16);
@@ -535,18 +539,36 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     float v0[16], v1[16];
                     if constexpr (P == 0) tc_ld16x2(d + cb, d + kAccCols + cb, v0, v1);
                     else tc_ld16(d + cb, v0);
+                    // the chunk's picks and prescales are read from shared memory before
+                    // any store (a store through a generic pointer could alias them and
+                    // would order every later read behind it); all 16 columns are
+                    // computed (columns past nb hold padding and are not stored)
+                    int pk[16];
+                    float sxv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        const int4 p4 = *reinterpret_cast<const int4*>(cpick + cb + i);
+                        const float4 s4 = *reinterpret_cast<const float4*>(cscale + cb + i);
+                        pk[i] = p4.x, pk[i + 1] = p4.y, pk[i + 2] = p4.z, pk[i + 3] = p4.w;
+                        sxv[i] = s4.x, sxv[i + 1] = s4.y, sxv[i + 2] = s4.z, sxv[i + 3] = s4.w;
+                    }
+                    float o[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int n = cb + i;
-                        if (n >= nb) break;
-                        const int pick = cpick[n];
-                        const float sx = cscale[n];
+                        const float sx = sxv[i];
                         if constexpr (P == 0) {
                             const float gv = v0[i] * s0 * sx;
                             const float uv = v1[i] * s1 * sx;
-                            a.h[(size_t)pick * I + r0 + t_row] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;  // bucket row
+                            o[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                         } else {
-                            a.y[(size_t)pick * H + r0 + t_row] = v0[i] * s0 * sx;
+                            o[i] = v0[i] * s0 * sx;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (cb + i < nb) {
+                            if constexpr (P == 0) a.h[(size_t)pk[i] * I + r0 + t_row] = o[i];  // bucket row
+                            else a.y[(size_t)pk[i] * H + r0 + t_row] = o[i];
                         }
                     }
                 }

@@ -77,7 +77,7 @@ cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, in
 struct ExpertMaps {
     CUtensorMap w13n;  // [2I rows][H/2 bytes], box 128 B x 32 rows, 128-byte swizzle
     CUtensorMap w2n;   // [H rows][I/2 bytes], box 128 B x 64 rows, 128-byte swizzle
-    CUtensorMap w13r;  // [2I rows][H/2 bytes], box 64 B x 128 rows, no swizzle
+    CUtensorMap w13r;  // [2I rows][H/2 bytes], box 64 B x 128 rows, 64-byte swizzle
     CUtensorMap w2r;   // [H rows][I/2 bytes], same box
 };
 
