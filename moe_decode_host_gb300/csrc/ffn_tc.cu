@@ -63,6 +63,10 @@ constexpr uint32_t kAStageCols = 128;
 constexpr uint32_t kAMatCols = kBK / 2;      // columns of one matrix's stage (2 f16 per column)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
+constexpr int kTaskQ = 4;  // depth of the CTA's task queue
+// roles that take each task from the queue: activation producer, MMA issuer,
+// converter warps, epilogue warps (the raw weight producer fetches them)
+constexpr int kTaskTakers = 2 + kConvWarps + 4;
 
 struct alignas(16) TcHead {
     uint64_t raw_full[kRawStages];
@@ -73,10 +77,16 @@ struct alignas(16) TcHead {
     uint64_t b_empty[kBStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    // tasks are taken from a global counter by the raw weight producer, which
+    // publishes task k in slot k % kTaskQ for the other roles (-1: no more)
+    uint64_t tq_full[kTaskQ];
+    uint64_t tq_empty[kTaskQ];
+    int tq[kTaskQ];
     uint32_t tmem_base;
     int abort;
     int D;
-    int list[kMaxE];
+    alignas(16) int key[kMaxE];  // tokens of each active expert, -1 when inactive
+    int list[kMaxE];             // active experts, most tokens first
     alignas(16) int col_pick[4][kNMax];     // per epilogue warp: output row of each column of the pass
     alignas(16) float col_scale[4][kNMax];  // and its activation prescale 2^p
 };
@@ -225,9 +235,30 @@ __device__ __forceinline__ void advance(int& slot, unsigned& phase, int n) {
     }
 }
 
+// Task k of this CTA from the queue (-1: no more tasks, or a wait ran out), taken
+// by one thread.
+__device__ __forceinline__ int take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who) {
+    const int j = k % kTaskQ;
+    if (!mbar_wait_fast(&hd.tq_full[j], (unsigned)(k / kTaskQ) & 1u, abort, a.status, a.diag, 20, j, k, who))
+        return -1;
+    const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    mbar_arrive(&hd.tq_empty[j]);
+    return task;
+}
+
+// The same, taken by a whole warp (every lane returns the same task).
+__device__ __forceinline__ int warp_take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who) {
+    const int j = k % kTaskQ;
+    if (!warp_wait(&hd.tq_full[j], (unsigned)(k / kTaskQ) & 1u, a, abort, 20, j, k, who)) return -1;
+    const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&hd.tq_empty[j]);
+    return task;
+}
+
 template <int P>
 __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
-                                                               int lo, int sel) {
+                                                               int lo, int sel, int ctr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* raw = base + kRawOff;
@@ -240,27 +271,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const int tiles = (P == 0 ? I : H) / kBM;
     volatile int* abort = &hd.abort;
 
-    // active experts (more than lo tokens, in the selected placement class): every
-    // thread flags some experts (one round of independent loads), then warp 0
-    // compacts the flags into an ascending list
+    // active experts (more than lo tokens, in the selected placement class), listed
+    // with the most tokens first (ties by id) so that the largest tasks start first
+    // and the CTAs' last tasks are short: every thread keys some experts (one round
+    // of independent loads), then ranks its experts against all keys
     for (int e = threadIdx.x; e < a.E; e += kThreadsTC) {
-        bool act = __ldg(a.counts + e) > lo;
+        const int c = __ldg(a.counts + e);
+        bool act = c > lo;
         if (act && sel != 0) {
             const bool hot = __ldg(a.loc + e) < a.n_hot;
             act = (sel == 1) ? hot : !hot;
         }
-        hd.list[e] = act;  // flags first, compacted in place below
+        hd.key[e] = act ? c : -1;
     }
+    for (int e = a.E + threadIdx.x; e < ((a.E + 3) & ~3); e += kThreadsTC) hd.key[e] = -1;  // pad to 4
     __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += kThreadsTC) {
+        const int ke = hd.key[e];
+        if (ke < 0) continue;
+        int r = 0;
+        for (int f = 0; f < a.E; f += 4) {
+            const int4 k4 = *reinterpret_cast<const int4*>(&hd.key[f]);
+            r += (k4.x > ke || (k4.x == ke && f < e)) + (k4.y > ke || (k4.y == ke && f + 1 < e)) +
+                 (k4.z > ke || (k4.z == ke && f + 2 < e)) + (k4.w > ke || (k4.w == ke && f + 3 < e));
+        }
+        hd.list[r] = e;
+    }
     if (warp == 0) {
         int cnt = 0;
         for (int base_e = 0; base_e < a.E; base_e += 32) {
             const int e = base_e + lane;
-            const bool act = e < a.E && hd.list[e] != 0;
-            const unsigned m = __ballot_sync(0xffffffffu, act);
-            __syncwarp();  // every lane has read its flag before the chunk is overwritten
-            if (act) hd.list[cnt + __popc(m & ((1u << lane) - 1u))] = e;
-            cnt += __popc(m);
+            cnt += __popc(__ballot_sync(0xffffffffu, e < a.E && hd.key[e] >= 0));
         }
         if (lane == 0) {
             hd.D = cnt;
@@ -281,6 +322,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 mbar_init(&hd.acc_full[s], 1);
                 mbar_init(&hd.acc_empty[s], 4);
             }
+            for (int j = 0; j < kTaskQ; ++j) {
+                mbar_init(&hd.tq_full[j], 1);
+                mbar_init(&hd.tq_empty[j], kTaskTakers);
+            }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
@@ -299,65 +344,74 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const int ntask = hd.D * tiles;
 
     if (warp == 0) {
-        // ---------------- raw weight producer (lane 0 issues) ----------------
-        int rs = 0;
-        unsigned rph = 0;
-        bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
-            const TcTask t = tc_task(a, hd, task, tiles);
-            if (!t.valid) continue;
-            const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13r : &a.tmaps[t.phys].w2r;
-            if (lane == 0) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
-            const int r0 = t.rb * kBM;
-            for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                for (int s = 0; s < nks; ++s) {
-                    if (!warp_wait(&hd.raw_empty[rs], rph ^ 1u, a, abort, 12, rs, s, task)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
+        // ---------------- raw weight producer, task fetcher (lane 0) ----------------
+        if (lane == 0) {
+            int rs = 0;
+            unsigned rph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int j = k % kTaskQ;
+                if (!mbar_wait_fast(&hd.tq_empty[j], ((unsigned)(k / kTaskQ) & 1u) ^ 1u, abort, a.status, a.diag, 21,
+                                    j, k, 0))
+                    break;
+                int task = atomicAdd(a.task_ctr + ctr, 1);
+                if (task >= ntask) task = -1;
+                *reinterpret_cast<volatile int*>(&hd.tq[j]) = task;
+                mbar_arrive(&hd.tq_full[j]);
+                if (task < 0) break;
+                const TcTask t = tc_task(a, hd, task, tiles);
+                if (!t.valid) continue;
+                const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13r : &a.tmaps[t.phys].w2r;
+                asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                const int r0 = t.rb * kBM;
+                for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.raw_empty[rs], rph ^ 1u, abort, a.status, a.diag, 12, rs, s, task)) {
+                            ok = false;
+                            break;
+                        }
                         uint8_t* dst = raw + (size_t)rs * kRawBytes;
                         mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * kRawRow : kBM * kRawRow);
                         tma_load_2d(dst, map, s * kRawRow, r0, &hd.raw_full[rs]);
                         if (P == 0) tma_load_2d(dst + kBM * kRawRow, map, s * kRawRow, I + r0, &hd.raw_full[rs]);
+                        advance(rs, rph, kRawStages);
                     }
-                    __syncwarp();
-                    advance(rs, rph, kRawStages);
                 }
             }
-        }
-        if (lane == 0)
             for (int s = 0; s < kRawStages; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
+        }
+        __syncwarp();
     } else if (warp == 2) {
-        // ---------------- activation producer (lane 0 issues) ----------------
-        int bs = 0;
-        unsigned bph = 0;
-        bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
-            const TcTask t = tc_task(a, hd, task, tiles);
-            if (!t.valid) continue;
-            for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + 63) / 64;
-                for (int s = 0; s < nks; ++s) {
-                    if (!warp_wait(&hd.b_empty[bs], bph ^ 1u, a, abort, 13, bs, s, task)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
+        // ---------------- activation producer (lane 0) ----------------
+        if (lane == 0) {
+            int bs = 0;
+            unsigned bph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int task = take_task(hd, k, a, abort, 1);
+                if (task < 0) break;
+                const TcTask t = tc_task(a, hd, task, tiles);
+                if (!t.valid) continue;
+                for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
+                    const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + 63) / 64;
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, s, task)) {
+                            ok = false;
+                            break;
+                        }
                         uint8_t* dst = sb + (size_t)bs * kBStageBytes;
                         mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)boxes * 2u * 64u * 128u);
                         for (int at = 0; at < 2; ++at)  // the stage's two 64-element atoms of K
                             for (int c = 0; c < boxes; ++c)
                                 tma_load_2d(dst + at * kBAtom + c * 64 * 128, &act_map, s * kBK + 64 * at,
                                             t.off + tb + 64 * c, &hd.b_full[bs]);
+                        advance(bs, bph, kBStages);
                     }
-                    __syncwarp();
-                    advance(bs, bph, kBStages);
                 }
             }
-        }
-        if (lane == 0)
             for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ---------------- MMA issuer (lane 0 alone) ----------------
         // one thread runs this loop: its waits and issue overhead between stages are
@@ -366,7 +420,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             int as = 0, bs = 0, buf = 0;
             unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
             bool ok = true;
-            for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const int task = take_task(hd, k, a, abort, 2);
+                if (task < 0) break;
                 const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
@@ -427,7 +483,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         int rs = 0, as = 0;
         unsigned rph = 0, aph = 0;
         bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int task = warp_take_task(hd, k, a, abort, 3);
+            if (task < 0) break;
             const TcTask t = tc_task(a, hd, task, tiles);
             if (!t.valid) continue;
             const uint8_t* blob = a.ptr[t.phys];
@@ -500,7 +558,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         int buf = 0;
         unsigned accph = 0;
         bool ok = true;
-        for (int task = blockIdx.x; task < ntask && ok; task += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int task = warp_take_task(hd, k, a, abort, 4);
+            if (task < 0) break;
             const TcTask t = tc_task(a, hd, task, tiles);
             const int r0 = t.rb * kBM;
             if (!t.valid) {
@@ -610,8 +670,12 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
         if (err != cudaSuccess) return err;
         configured[phase] = true;
     }
-    if (phase == 0) return launch_pdl(ffn_tc_kernel<0>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel);
-    return launch_pdl(ffn_tc_kernel<1>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel);
+    // task counters 12-15 of the call's workspace (zeroed by the gate/up prescale
+    // kernel): one per phase and placement class
+    const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;
+    if (phase == 0)
+        return launch_pdl(ffn_tc_kernel<0>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel, ctr);
+    return launch_pdl(ffn_tc_kernel<1>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel, ctr);
 }
 
 }  // namespace moe
