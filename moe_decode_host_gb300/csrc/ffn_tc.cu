@@ -64,9 +64,15 @@ constexpr uint32_t kAMatCols = kBK / 2;      // columns of one matrix's stage (2
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
 constexpr int kTaskQ = 4;  // depth of the CTA's task queue
-// roles that take each task from the queue: activation producer, MMA issuer,
+// MMA-issuing threads: the gate/up phase has one per matrix (a thread issues
+// about one MMA per 45 cycles, an M=128 N=128 K=16 MMA runs 64, so one thread
+// would leave the tensor pipe idle between stages); the down phase has one
+template <int P>
+__host__ __device__ constexpr int issuers() { return P == 0 ? 2 : 1; }
+// roles that take each task from the queue: activation producer, MMA issuers,
 // converter warps, epilogue warps (the raw weight producer fetches them)
-constexpr int kTaskTakers = 2 + kConvWarps + 4;
+template <int P>
+__host__ __device__ constexpr int task_takers() { return 1 + issuers<P>() + kConvWarps + 4; }
 
 struct alignas(16) TcHead {
     uint64_t raw_full[kRawStages];
@@ -91,9 +97,13 @@ struct alignas(16) TcHead {
     alignas(16) float col_scale[4][kNMax];  // and its activation prescale 2^p
 };
 
+constexpr int kEpiChunk = 16;  // token columns per epilogue chunk
+constexpr size_t kEpiBufBytes = (size_t)kEpiChunk * 32 * sizeof(float);  // one warp's [16 tokens][32 rows] of h
+
 constexpr size_t kRawOff = 0;
 constexpr size_t kBOff = kRawOff + (size_t)kRawStages * kRawBytes;
-constexpr size_t kHeadOff = kBOff + (size_t)kBStages * kBStageBytes;
+constexpr size_t kEpiOff = kBOff + (size_t)kBStages * kBStageBytes;  // 2 staging buffers per epilogue warp
+constexpr size_t kHeadOff = kEpiOff + 4 * 2 * kEpiBufBytes;
 constexpr size_t kTcSmem = 1024 + kHeadOff + sizeof(TcHead);
 static_assert(kTcSmem <= 232448, "shared memory budget of one CTA");
 
@@ -132,6 +142,30 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Bulk tensor store of a [box rows][box inner] tile from shared memory, and the
+// bulk async-group bookkeeping of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the bulk stores of all but the newest group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every bulk store of this thread is complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes become visible to the async proxy (bulk copies)
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// SiLU(x) = x * sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2: one
+// special-function operation per element (hardware tanh, relative error about
+// 2^-11, absolute error of sigmoid about 2^-12).
+__device__ __forceinline__ float silu_tanh(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return x * fmaf(0.5f, t, 0.5f);
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's lane, waited for in the same asm.
@@ -258,7 +292,8 @@ __device__ __forceinline__ int warp_take_task(TcHead& hd, int k, const FfnArgs& 
 
 template <int P>
 __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
-                                                               int lo, int sel, int ctr) {
+                                                               const __grid_constant__ CUtensorMap h_map, int lo,
+                                                               int sel, int ctr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* raw = base + kRawOff;
@@ -312,19 +347,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             }
             for (int s = 0; s < kAStages; ++s) {
                 mbar_init(&hd.a_full[s], kConvWarps);
-                mbar_init(&hd.a_empty[s], 1);
+                mbar_init(&hd.a_empty[s], issuers<P>());
             }
             for (int s = 0; s < kBStages; ++s) {
                 mbar_init(&hd.b_full[s], 1);
-                mbar_init(&hd.b_empty[s], 1);
+                mbar_init(&hd.b_empty[s], issuers<P>());
             }
             for (int s = 0; s < 2; ++s) {
-                mbar_init(&hd.acc_full[s], 1);
+                mbar_init(&hd.acc_full[s], issuers<P>());
                 mbar_init(&hd.acc_empty[s], 4);
             }
             for (int j = 0; j < kTaskQ; ++j) {
                 mbar_init(&hd.tq_full[j], 1);
-                mbar_init(&hd.tq_empty[j], kTaskTakers);
+                mbar_init(&hd.tq_empty[j], task_takers<P>());
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
@@ -412,16 +447,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ---------------- MMA issuer (lane 0 alone) ----------------
-        // one thread runs this loop: its waits and issue overhead between stages are
-        // the time the tensor pipe idles, so it takes no warp-wide votes
+    } else if (warp == 1 || (P == 0 && warp == 3)) {
+        // ---------------- MMA issuers (lane 0 alone) ----------------
+        // one thread per issuer runs this loop: its waits and issue overhead between
+        // stages are the time the tensor pipe idles, so it takes no warp-wide votes.
+        // Gate/up phase: warp 1 issues the gate MMAs, warp 3 the up MMAs.
+        const int mi = warp == 1 ? 0 : 1;
         if (lane == 0) {
             int as = 0, bs = 0, buf = 0;
             unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int task = take_task(hd, k, a, abort, 2);
+                const int task = take_task(hd, k, a, abort, 2 + mi);
                 if (task < 0) break;
                 const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
@@ -435,7 +472,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     }
                     accph ^= 1u << buf;
                     tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)buf * kAccCols;
+                    // gate/up phase: this issuer's matrix's accumulator; down phase: buffer buf
+                    const uint32_t d = tmem + (uint32_t)(P == 0 ? mi : buf) * kAccCols;
                     for (int s = 0; s < nks; ++s) {
                         if (!mbar_wait_fast(&hd.a_full[as], aph, abort, a.status, a.diag, 15, as, s, task) ||
                             !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 16, bs, s, task)) {
@@ -446,7 +484,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
                         // columns; 8 columns per 16-element k-step); B: descriptor of k-step
                         // 0, a 16-element step advances its start address by 32 bytes
-                        const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
+                        const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols + (uint32_t)mi * kAMatCols;
                         const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -454,7 +492,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                             // k-steps 0-3 in the first activation atom, 4-7 in the second
                             const uint64_t b = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
                             tc_mma_f16_ta(d, at + 8 * kk, b, idesc, acc);
-                            if (P == 0) tc_mma_f16_ta(d + kAccCols, at + kAMatCols + 8 * kk, b, idesc, acc);
                         }
                         tc_commit(&hd.a_empty[as]);
                         tc_commit(&hd.b_empty[bs]);
@@ -555,6 +592,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
         int* cpick = hd.col_pick[q4];
         float* cscale = hd.col_scale[q4];
+        // gate/up phase: full 16-token chunks of h leave through two staging buffers
+        // of this warp and a bulk tensor store each (lane 0 issues and tracks them)
+        float* stage_buf = reinterpret_cast<float*>(base + kEpiOff + (size_t)q4 * 2 * kEpiBufBytes);
+        int sbuf = 0;
         int buf = 0;
         unsigned accph = 0;
         bool ok = true;
@@ -619,16 +660,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         if constexpr (P == 0) {
                             const float gv = v0[i] * s0 * sx;
                             const float uv = v1[i] * s1 * sx;
-                            o[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            o[i] = silu_tanh(gv) * uv;
                         } else {
                             o[i] = v0[i] * s0 * sx;
                         }
                     }
+                    if (P == 0 && cb + kEpiChunk <= nb) {
+                        // h rows t.off + tb + cb .. +15 (bucket order), this warp's 32
+                        // columns r0 + 32 q4 ..: stage [token][row] and store as one box
+                        float* stg = stage_buf + (size_t)sbuf * (kEpiChunk * 32);
+                        if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it
+                        __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (cb + i < nb) {
-                            if constexpr (P == 0) a.h[(size_t)pk[i] * I + r0 + t_row] = o[i];  // bucket row
-                            else a.y[(size_t)pk[i] * H + r0 + t_row] = o[i];
+                        for (int i = 0; i < 16; ++i) stg[i * 32 + lane] = o[i];
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&h_map, r0 + q4 * 32, t.off + tb + cb, stg);
+                            bulk_commit();
+                        }
+                        sbuf ^= 1;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (cb + i < nb) {
+                                if constexpr (P == 0) a.h[(size_t)pk[i] * I + r0 + t_row] = o[i];  // bucket row
+                                else a.y[(size_t)pk[i] * H + r0 + t_row] = o[i];
+                            }
                         }
                     }
                 }
@@ -638,6 +696,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 if (P == 1) buf ^= 1;
             }
         }
+        // the stores must be complete (and done reading shared memory) before the CTA exits
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -655,8 +716,12 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
     const int n = a.T * a.k;
     cudaError_t err = cudaSuccess;
     // activation tiles: 64 elements (128 bytes) x 64 bucket rows, 128-byte swizzle
-    CUtensorMap map;
+    CUtensorMap map, hmap;
     if (!encode_act_map(&map, a, phase, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    // h [T·k][I] fp32 in bucket order, boxes of 32 columns x 16 rows (gate/up phase output)
+    if (!encode_tmap_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.h, (uint64_t)a.I, (uint64_t)n,
+                        (uint64_t)a.I * sizeof(float), 32, kEpiChunk, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     const long dmax = (long)(a.E < n / (lo + 1) + 1 ? a.E : n / (lo + 1) + 1);
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kBM);
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);
@@ -674,8 +739,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
     // kernel): one per phase and placement class
     const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;
     if (phase == 0)
-        return launch_pdl(ffn_tc_kernel<0>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel, ctr);
-    return launch_pdl(ffn_tc_kernel<1>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, lo, sel, ctr);
+        return launch_pdl(ffn_tc_kernel<0>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, hmap, lo, sel, ctr);
+    return launch_pdl(ffn_tc_kernel<1>, dim3(grid), dim3(kThreadsTC), kTcSmem, st, a, map, hmap, lo, sel, ctr);
 }
 
 }  // namespace moe
