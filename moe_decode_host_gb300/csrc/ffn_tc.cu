@@ -42,15 +42,26 @@ namespace {
 constexpr int kBM = 128;    // weight rows per tile = tensor-memory lanes
 constexpr int kBK = 128;    // K elements per stage (two 128-byte swizzle atoms of f16 per row)
 constexpr int kNMax = 128;  // token columns per pass
-constexpr int kRawStages = 4;
-constexpr int kAStages = 2;   // f16 weight stages in tensor memory
+// Stage rings per phase: the raw ring is 64 KB in both (gate/up stages hold two
+// matrices' slices, down-phase stages one, so the down phase has twice as many);
+// tensor memory [256, 512) holds 2 gate/up weight stages (128 columns each) or 4
+// down-phase ones (64 columns each).
+template <int P>
+struct Rings {
+    static constexpr int kRaw = P == 0 ? 4 : 8;
+    static constexpr int kA = P == 0 ? 2 : 4;
+};
+constexpr int kRawStagesMax = 8;
 constexpr int kBStages = 4;
+static_assert(kBStages % Rings<0>::kA == 0 && kBStages % Rings<1>::kA == 0, "weight slots follow the stage ring");
 constexpr int kFirstConv = 4;   // first converter warp
 constexpr int kConvWarps = 8;
 constexpr int kFirstEpi = 12;   // first epilogue warp (warp % 4 = lane quarter)
 constexpr int kThreadsTC = 512;
 constexpr int kRawRow = kBK / 2;             // E2M1 bytes of one row per stage
-constexpr int kRawBytes = 2 * kBM * kRawRow;  // gate + up raw slices (down phase uses half)
+constexpr int kRawRing = 2 * 4 * kBM * kRawRow;  // 64 KB of raw stages
+template <int P>
+__host__ __device__ constexpr int raw_bytes() { return (P == 0 ? 2 : 1) * kBM * kRawRow; }  // per stage
 constexpr int kBAtom = kNMax * 128;          // 64 elements of K of the activation tile, 16 KB
 constexpr int kBStageBytes = 2 * kBAtom;     // activation tile, 32 KB
 // Tensor memory (512 columns): accumulators in [0, 256) -- gate and up (128 each)
@@ -59,7 +70,8 @@ constexpr int kBStageBytes = 2 * kBAtom;     // activation tile, 32 KB
 // uses 64).
 constexpr uint32_t kAccCols = 128;           // columns per accumulator (one matrix, N <= 128)
 constexpr uint32_t kACol0 = 256;             // first column of the weight stages
-constexpr uint32_t kAStageCols = 128;
+template <int P>
+__host__ __device__ constexpr uint32_t a_stage_cols() { return P == 0 ? 128u : 64u; }
 constexpr uint32_t kAMatCols = kBK / 2;      // columns of one matrix's stage (2 f16 per column)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
@@ -75,12 +87,14 @@ template <int P>
 __host__ __device__ constexpr int task_takers() { return 1 + issuers<P>() + kConvWarps + 4; }
 
 struct alignas(16) TcHead {
-    uint64_t raw_full[kRawStages];
-    uint64_t raw_empty[kRawStages];
-    uint64_t a_full[kAStages];
-    uint64_t a_empty[kAStages];
-    uint64_t b_full[kBStages];
-    uint64_t b_empty[kBStages];
+    uint64_t raw_full[kRawStagesMax];
+    uint64_t raw_empty[kRawStagesMax];
+    // stage g of the CTA's stream uses activation slot g % kBStages and weight slot
+    // g % Rings<P>::kA (which divides kBStages); full[g % kBStages] completes when
+    // the activation tile has landed and the converters have written the weights,
+    // empty[g % kBStages] when the MMAs that read both are done
+    uint64_t full[kBStages];
+    uint64_t empty[kBStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     // tasks are taken from a global counter by the raw weight producer, which
@@ -101,7 +115,7 @@ constexpr int kEpiChunk = 16;  // token columns per epilogue chunk
 constexpr size_t kEpiBufBytes = (size_t)kEpiChunk * 32 * sizeof(float);  // one warp's [16 tokens][32 rows] of h
 
 constexpr size_t kRawOff = 0;
-constexpr size_t kBOff = kRawOff + (size_t)kRawStages * kRawBytes;
+constexpr size_t kBOff = kRawOff + (size_t)kRawRing;
 constexpr size_t kEpiOff = kBOff + (size_t)kBStages * kBStageBytes;  // 2 staging buffers per epilogue warp
 constexpr size_t kHeadOff = kEpiOff + 4 * 2 * kEpiBufBytes;
 constexpr size_t kTcSmem = 1024 + kHeadOff + sizeof(TcHead);
@@ -341,17 +355,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         if (lane == 0) {
             hd.D = cnt;
             hd.abort = 0;
-            for (int s = 0; s < kRawStages; ++s) {
+            for (int s = 0; s < Rings<P>::kRaw; ++s) {
                 mbar_init(&hd.raw_full[s], 1);
                 mbar_init(&hd.raw_empty[s], kConvWarps);
             }
-            for (int s = 0; s < kAStages; ++s) {
-                mbar_init(&hd.a_full[s], kConvWarps);
-                mbar_init(&hd.a_empty[s], issuers<P>());
-            }
             for (int s = 0; s < kBStages; ++s) {
-                mbar_init(&hd.b_full[s], 1);
-                mbar_init(&hd.b_empty[s], issuers<P>());
+                mbar_init(&hd.full[s], 1 + kConvWarps);
+                mbar_init(&hd.empty[s], issuers<P>());
             }
             for (int s = 0; s < 2; ++s) {
                 mbar_init(&hd.acc_full[s], issuers<P>());
@@ -405,15 +415,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                             ok = false;
                             break;
                         }
-                        uint8_t* dst = raw + (size_t)rs * kRawBytes;
+                        uint8_t* dst = raw + (size_t)rs * raw_bytes<P>();
                         mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * kRawRow : kBM * kRawRow);
                         tma_load_2d(dst, map, s * kRawRow, r0, &hd.raw_full[rs]);
                         if (P == 0) tma_load_2d(dst + kBM * kRawRow, map, s * kRawRow, I + r0, &hd.raw_full[rs]);
-                        advance(rs, rph, kRawStages);
+                        advance(rs, rph, Rings<P>::kRaw);
                     }
                 }
             }
-            for (int s = 0; s < kRawStages; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
+            for (int s = 0; s < Rings<P>::kRaw; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -430,21 +440,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                     const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + 63) / 64;
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, s, task)) {
+                        if (!mbar_wait_fast(&hd.empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, s, task)) {
                             ok = false;
                             break;
                         }
                         uint8_t* dst = sb + (size_t)bs * kBStageBytes;
-                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)boxes * 2u * 64u * 128u);
+                        mbar_arrive_expect_tx(&hd.full[bs], (unsigned)boxes * 2u * 64u * 128u);
                         for (int at = 0; at < 2; ++at)  // the stage's two 64-element atoms of K
                             for (int c = 0; c < boxes; ++c)
                                 tma_load_2d(dst + at * kBAtom + c * 64 * 128, &act_map, s * kBK + 64 * at,
-                                            t.off + tb + 64 * c, &hd.b_full[bs]);
+                                            t.off + tb + 64 * c, &hd.full[bs]);
                         advance(bs, bph, kBStages);
                     }
                 }
             }
-            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 1 || (P == 0 && warp == 3)) {
@@ -475,8 +485,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     // gate/up phase: this issuer's matrix's accumulator; down phase: buffer buf
                     const uint32_t d = tmem + (uint32_t)(P == 0 ? mi : buf) * kAccCols;
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.a_full[as], aph, abort, a.status, a.diag, 15, as, s, task) ||
-                            !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 16, bs, s, task)) {
+                        if (!mbar_wait_fast(&hd.full[bs], bph, abort, a.status, a.diag, 15, bs, s, task)) {
                             ok = false;
                             break;
                         }
@@ -484,7 +493,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
                         // columns; 8 columns per 16-element k-step); B: descriptor of k-step
                         // 0, a 16-element step advances its start address by 32 bytes
-                        const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols + (uint32_t)mi * kAMatCols;
+                        const uint32_t at = tmem + kACol0 + (uint32_t)as * a_stage_cols<P>() + (uint32_t)mi * kAMatCols;
                         const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -493,9 +502,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                             const uint64_t b = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
                             tc_mma_f16_ta(d, at + 8 * kk, b, idesc, acc);
                         }
-                        tc_commit(&hd.a_empty[as]);
-                        tc_commit(&hd.b_empty[bs]);
-                        advance(as, aph, kAStages);
+                        tc_commit(&hd.empty[bs]);
+                        advance(as, aph, Rings<P>::kA);
                         advance(bs, bph, kBStages);
                     }
                     if (!ok) break;
@@ -505,8 +513,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             }
             // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
             // last commit of every stage
-            for (int s = 0; s < kAStages; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
-            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.empty[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp >= kFirstConv && warp < kFirstConv + kConvWarps) {
@@ -517,8 +524,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         const int row = cidx & (kBM - 1);  // = (warp % 4) * 32 + lane: this thread's tensor-memory lane
         const int hi = cidx >> 7;
         const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) * 32u << 16);
-        int rs = 0, as = 0;
-        unsigned rph = 0, aph = 0;
+        int rs = 0;
+        unsigned rph = 0;
+        int gs = 0;  // stage number in the CTA's stream
         bool ok = true;
         for (int k = 0; ok; ++k) {
             const int task = warp_take_task(hd, k, a, abort, 3);
@@ -536,14 +544,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 uint32_t wcur = ld_u32(sc);
                 for (int s = 0; s < nks && ok; ++s) {
                     const uint32_t wnext = (s + 1 < nks) ? ld_u32(sc + 4 * (s + 1)) : 0u;
+                    // the weight slot of stage gs was last read by the MMAs of stage
+                    // gs - kA (use (gs - kA) / kBStages of its empty barrier)
+                    const int gp = gs - Rings<P>::kA;
                     if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, s, task) ||
-                        !warp_wait(&hd.a_empty[as], aph ^ 1u, a, abort, 18, as, s, task)) {
+                        (gp >= 0 && !warp_wait(&hd.empty[gp % kBStages], (unsigned)(gp / kBStages) & 1u, a, abort,
+                                               18, gp % kBStages, s, task))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t* rsrc = raw + (size_t)rs * kRawBytes;
-                    const uint32_t acol = lane_base + kACol0 + (uint32_t)as * kAStageCols;
+                    const uint8_t* rsrc = raw + (size_t)rs * raw_bytes<P>();
+                    const uint32_t acol = lane_base + kACol0 + (uint32_t)(gs % Rings<P>::kA) * a_stage_cols<P>();
                     // gate/up phase: the row's 128 elements (16 words of 8) into its matrix's
                     // 64 columns; down phase: one half of the row (8 words) into 32 columns
                     constexpr int kWords = P == 0 ? 16 : 8;
@@ -576,11 +588,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&hd.a_full[as]);
+                        mbar_arrive(&hd.full[gs % kBStages]);
                         mbar_arrive(&hd.raw_empty[rs]);
                     }
-                    advance(rs, rph, kRawStages);
-                    advance(as, aph, kAStages);
+                    advance(rs, rph, Rings<P>::kRaw);
+                    ++gs;
                     wcur = wnext;
                 }
             }
