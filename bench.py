@@ -34,13 +34,13 @@ HBM_NOMINAL_GBS = 8000.0
 # None whenever its kernel changes after the capture.
 NCU_TRAFFIC = {
     # per cold expert copied: the slot writes stay in L2 during the launch
-    "cold_copy": {"bytes_per_expert": (35584 + 7168) / 2,
+    "cold_copy": {"bytes_per_expert": (11520 + 15616) / 2,
                   "source": "profiles/cold_copy_kernel_c1_small.md"},
     # per distinct expert through the decode kernels (gate/up + down launches)
-    "ffn_decode": {"bytes_per_expert": (66947840 + 678912 + 33496320) / 5,
+    "ffn_decode": {"bytes_per_expert": (66932224 + 777984 + 33490688) / 5,
                    "source": "profiles/ffn_decode_kernel_c1_small.md"},
     # per expert through the tcgen05 kernels at about 128 tokens per expert
-    "ffn_tc": {"bytes_per_expert": (1116370000 + 93775872 + 478885000 + 116250368) / 64,
+    "ffn_tc": {"bytes_per_expert": (1135740000 + 92264448 + 488412000 + 113392896) / 64,
                "source": "profiles/ffn_tc_kernel_c4_small.md"},
 }
 
