@@ -190,23 +190,42 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     const int tiles = (P == 0 ? I : H) / C::kTaskRows;
 
     // active experts in this launch's token-count range and placement class: every
-    // thread flags some experts (one round of independent loads), then warp 0
-    // compacts the flags into an ascending list
+    // thread takes some experts and, for the active ones, follows the chain to the
+    // blob at once (picks, first entry and placement are independent loads, then the
+    // entry's physical id and the blob pointer), keeping per-expert values in the
+    // stage ring (unused until the producers start); then warp 0 compacts the flags
+    // into an ascending list and every thread copies the listed experts' values
+    struct PerExpert {
+        const uint8_t* blob;
+        int cnt, off, phys, act;
+    };
+    PerExpert* pe = reinterpret_cast<PerExpert*>(stages);
+    static_assert(sizeof(PerExpert) * kMaxE <= 2 * L::kStageBytes, "per-expert scratch fits two stages");
+#pragma unroll 1
     for (int e = threadIdx.x; e < a.E; e += kThreads) {
         const int c = __ldg(a.counts + e);
+        const int off = __ldg(a.offsets + e);
+        const int le = sel != 0 ? __ldg(a.loc + e) : 0;
         bool act_e = c > lo && c <= hi;
-        if (act_e && sel != 0) {
-            const bool hot = __ldg(a.loc + e) < a.n_hot;
-            act_e = (sel == 1) ? hot : !hot;
+        if (act_e && sel != 0) act_e = (sel == 1) ? (le < a.n_hot) : (le >= a.n_hot);
+        PerExpert v;
+        v.act = act_e;
+        v.cnt = c;
+        v.off = off;
+        v.phys = -1;
+        v.blob = nullptr;
+        if (act_e) {
+            v.phys = __ldg(a.phys_ids + __ldg(a.entries + off));
+            v.blob = (v.phys >= 0 && v.phys < a.n_phys) ? a.ptr[v.phys] : nullptr;
         }
-        hd.off[e] = act_e;  // scratch use of off[] until the list is built
+        pe[e] = v;
     }
     __syncthreads();
     if (warp == 0) {
         int cnt = 0;
         for (int base = 0; base < a.E; base += 32) {
             const int e = base + lane;
-            const bool act_e = e < a.E && hd.off[e] != 0;
+            const bool act_e = e < a.E && pe[e].act != 0;
             const unsigned m = __ballot_sync(0xffffffffu, act_e);
             if (act_e) hd.e[cnt + __popc(m & ((1u << lane) - 1u))] = e;
             cnt += __popc(m);
@@ -226,16 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
         }
     }
     __syncthreads();
-    // per listed expert: picks, first bucket entry, physical id (all threads)
     for (int i = threadIdx.x; i < hd.D; i += kThreads) {
-        const int e = hd.e[i];
-        const int off = __ldg(a.offsets + e);
-        hd.cnt[i] = __ldg(a.counts + e);
-        hd.off[i] = off;
-        const int ph = __ldg(a.phys_ids + __ldg(a.entries + off));
-        hd.phys[i] = ph;
-        hd.blob[i] = (ph >= 0 && ph < a.n_phys) ? a.ptr[ph] : nullptr;
+        const PerExpert v = pe[hd.e[i]];
+        hd.cnt[i] = v.cnt;
+        hd.off[i] = v.off;
+        hd.phys[i] = v.phys;
+        hd.blob[i] = v.blob;
     }
+    // the ring is rewritten by the async proxy (TMA) from here on
+    fence_proxy_async_shared();
     __syncthreads();
     // the activations, their prescales and the outputs belong to the previous kernel
     // until it completes; the work above only read routing results

@@ -169,8 +169,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // every bulk store of this thread is complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// generic-proxy shared-memory writes become visible to the async proxy (bulk copies)
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // SiLU(x) = x * sigmoid(x) with sigmoid(x) = (1 + tanh(x / 2)) / 2: one
 // special-function operation per element (hardware tanh, relative error about
@@ -685,7 +683,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                         __syncwarp();
 #pragma unroll
                         for (int i = 0; i < 16; ++i) stg[i * 32 + lane] = o[i];
-                        fence_proxy_async_smem();
+                        fence_proxy_async_shared();
                         __syncwarp();
                         if (lane == 0) {
                             tma_store_2d(&h_map, r0 + q4 * 32, t.off + tb + cb, stg);

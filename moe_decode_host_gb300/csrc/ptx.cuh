@@ -111,6 +111,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
                  : "memory");
 }
 
+// Generic-proxy writes to shared memory by this thread are ordered before later
+// async-proxy accesses (TMA, bulk copies) to the same bytes once a barrier follows.
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
