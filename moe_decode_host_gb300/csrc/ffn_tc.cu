@@ -7,28 +7,39 @@
 // GEMM: D[128 weight rows x N tokens] += W[128 x K] * X[N x K]^T with
 // tcgen05.mma (kind::f16, f16 operands, fp32 accumulators in tensor memory).
 //
+// A column pass covers up to 160 of an expert's tokens, so at about 128 tokens per
+// expert every expert's weights are expanded once. Its K dimension runs in chunks
+// of 128 elements; in the gate/up phase each chunk is two stages, one for the tile's
+// 128 gate rows and one for its 128 up rows, in the down phase one stage.
+//
 // Warp roles of one persistent CTA per SM (16 warps):
-//   warp 0       TMA of the raw MXFP4 weight slices (128 rows x 128 elements; gate
-//                and up rows together in the gate/up phase) into a ring of raw
-//                stages;
-//   warp 1       owns tensor memory and issues the MMAs (one thread): each stage
-//                is committed back to its producers, each tile to the epilogue;
-//                the down phase has two accumulator buffers so that a tile's
-//                epilogue overlaps the next tile's main loop;
-//   warp 2       TMA of the activation tiles (up to 128 bucket rows x 128
+//   warp 0       takes tasks (an expert and a 128-row tile) from a launch-wide
+//                counter, experts with the most tokens first, and publishes them in
+//                a small shared-memory queue; TMA of the raw MXFP4 slice of each
+//                stage (one matrix's 128 rows x 128 elements, 64-byte swizzle)
+//                into a ring of raw stages;
+//   warps 1, 3   own tensor memory (warp 1) and issue the MMAs, one thread each:
+//                in the gate/up phase warp 1 the gate stages into the gate
+//                accumulator and warp 3 the up stages into the up accumulator (a
+//                thread issues a tcgen05 MMA about every 45 cycles, so each issuer
+//                has the other matrix's MMA time as slack); the down phase has one
+//                issuer and two accumulator buffers, so a tile's epilogue overlaps
+//                the next tile's main loop;
+//   warp 2       TMA of the activation chunks (up to 160 bucket rows x 128
 //                elements, f16, as two 64-element atoms with 128-byte swizzle; the
 //                prescale kernels write the activations in bucket order, so an
 //                expert's tokens are consecutive rows), into a ring of its own;
-//   warps 4-11   converters: E2M1 -> f16 for one weight row (gate/up phase) or one
-//                half of a row's stage (down phase) per thread, each E8M0 block
-//                scale rebased to 2^12 below the row's largest scale, so that every
-//                block whose scale is within 2^35 of the largest is exact in f16
-//                (smaller blocks lose low bits); the f16 tiles go to tensor memory
-//                (tcgen05.st: one weight row per lane, consecutive K elements
-//                packed two per column), where the MMA reads its A operand, so
-//                shared memory carries only raw weights and activations;
+//   warps 4-11   converters: E2M1 -> f16 for one half of a weight row's stage per
+//                thread, each E8M0 block scale rebased to 2^12 below the row's
+//                largest scale, so that every block whose scale is within 2^35 of
+//                the largest is exact in f16 (smaller blocks lose low bits); the f16
+//                tiles go to tensor memory (tcgen05.st: one weight row per lane,
+//                consecutive K elements packed two per column) in a ring of three
+//                64-column slots, where the MMA reads its A operand, so shared
+//                memory carries only raw weights and activations;
 //   warps 12-15  epilogue: tensor memory -> registers -> h (gate/up phase, SiLU
-//                gate times up) or y (down phase), undoing the power-of-two
+//                gate times up, full 16-token chunks through shared memory and bulk
+//                tensor stores) or y (down phase), undoing the power-of-two
 //                rebasing of weights and activations.
 // Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT, and the CTA
 // drains its copies and MMAs before it frees tensor memory and returns.
@@ -41,60 +52,56 @@ namespace {
 
 constexpr int kBM = 128;    // weight rows per tile = tensor-memory lanes
 constexpr int kBK = 128;    // K elements per stage (two 128-byte swizzle atoms of f16 per row)
-constexpr int kNMax = 128;  // token columns per pass
-// Stage rings per phase: the raw ring is 64 KB in both (gate/up stages hold two
-// matrices' slices, down-phase stages one, so the down phase has twice as many);
-// tensor memory [256, 512) holds 2 gate/up weight stages (128 columns each) or 4
-// down-phase ones (64 columns each).
-template <int P>
-struct Rings {
-    static constexpr int kRaw = P == 0 ? 4 : 8;
-    static constexpr int kA = P == 0 ? 2 : 4;
-};
-constexpr int kRawStagesMax = 8;
-constexpr int kBStages = 4;
-static_assert(kBStages % Rings<0>::kA == 0 && kBStages % Rings<1>::kA == 0, "weight slots follow the stage ring");
+constexpr int kNMax = 160;  // token columns per pass (a multiple of 32)
+constexpr int kRawStages = 8;  // raw E2M1 slices of one matrix: 128 rows x 128 elements, 8 KB each
+constexpr int kAStages = 3;    // f16 weight stages in tensor memory, 64 columns each
+constexpr int kBStages = 3;    // activation tiles, one per 128-element chunk of K
 constexpr int kFirstConv = 4;   // first converter warp
 constexpr int kConvWarps = 8;
 constexpr int kFirstEpi = 12;   // first epilogue warp (warp % 4 = lane quarter)
 constexpr int kThreadsTC = 512;
 constexpr int kRawRow = kBK / 2;             // E2M1 bytes of one row per stage
-constexpr int kRawRing = 2 * 4 * kBM * kRawRow;  // 64 KB of raw stages
-template <int P>
-__host__ __device__ constexpr int raw_bytes() { return (P == 0 ? 2 : 1) * kBM * kRawRow; }  // per stage
-constexpr int kBAtom = kNMax * 128;          // 64 elements of K of the activation tile, 16 KB
-constexpr int kBStageBytes = 2 * kBAtom;     // activation tile, 32 KB
-// Tensor memory (512 columns): accumulators in [0, 256) -- gate and up (128 each)
-// in the gate/up phase, two 128-column buffers in the down phase -- and the f16
-// weight stages in [256, 512): 128 columns each (gate 64, up 64; the down phase
-// uses 64).
-constexpr uint32_t kAccCols = 128;           // columns per accumulator (one matrix, N <= 128)
-constexpr uint32_t kACol0 = 256;             // first column of the weight stages
-template <int P>
-__host__ __device__ constexpr uint32_t a_stage_cols() { return P == 0 ? 128u : 64u; }
-constexpr uint32_t kAMatCols = kBK / 2;      // columns of one matrix's stage (2 f16 per column)
+constexpr int kRawBytes = kBM * kRawRow;     // 8 KB
+constexpr int kActBoxRows = 32;              // activation rows per TMA box
+constexpr int kBAtom = kNMax * 128;          // 64 elements of K of the activation tile, 20 KB
+constexpr int kBStageBytes = 2 * kBAtom;     // activation tile, 40 KB
+// Tensor memory (512 columns): accumulators in [0, 320) -- gate and up (160 columns
+// each) in the gate/up phase, two 160-column buffers in the down phase -- and the
+// f16 weight stages in [320, 512), 64 columns each (one matrix, 128 elements of K,
+// two f16 per column).
+constexpr uint32_t kAccCols = 160;           // columns per accumulator (N <= 160)
+constexpr uint32_t kACol0 = 320;             // first column of the weight stages
+constexpr uint32_t kAStageCols = 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxE = 1024;
 constexpr int kTaskQ = 4;  // depth of the CTA's task queue
-// MMA-issuing threads: the gate/up phase has one per matrix (a thread issues
-// about one MMA per 45 cycles, an M=128 N=128 K=16 MMA runs 64, so one thread
-// would leave the tensor pipe idle between stages); the down phase has one
+// Gate/up phase: a pass runs its K chunks as stages that alternate between the gate
+// rows and the up rows of the tile (stage 2c: gate rows of chunk c, 2c+1: up rows),
+// so one weight stage holds one matrix and the pass needs no second column pass up
+// to 160 tokens. Warp 1 issues the gate MMAs into the gate accumulator and warp 3
+// the up MMAs (a thread issues a tcgen05 MMA about every 45 cycles, so each issuer
+// gets a stage's worth of slack while the other matrix's MMAs run). Down phase:
+// one stage per chunk, one issuer.
 template <int P>
 __host__ __device__ constexpr int issuers() { return P == 0 ? 2 : 1; }
+template <int P>
+__host__ __device__ constexpr int mats() { return P == 0 ? 2 : 1; }  // weight matrices per chunk
 // roles that take each task from the queue: activation producer, MMA issuers,
 // converter warps, epilogue warps (the raw weight producer fetches them)
 template <int P>
 __host__ __device__ constexpr int task_takers() { return 1 + issuers<P>() + kConvWarps + 4; }
 
 struct alignas(16) TcHead {
-    uint64_t raw_full[kRawStagesMax];
-    uint64_t raw_empty[kRawStagesMax];
-    // stage g of the CTA's stream uses activation slot g % kBStages and weight slot
-    // g % Rings<P>::kA (which divides kBStages); full[g % kBStages] completes when
-    // the activation tile has landed and the converters have written the weights,
-    // empty[g % kBStages] when the MMAs that read both are done
-    uint64_t full[kBStages];
-    uint64_t empty[kBStages];
+    uint64_t raw_full[kRawStages];
+    uint64_t raw_empty[kRawStages];
+    // weight stage g of the CTA's stream lives in tensor-memory slot g % kAStages:
+    // a_full when the converters have written it, a_empty when its MMAs are done
+    uint64_t a_full[kAStages];
+    uint64_t a_empty[kAStages];
+    // activation chunk c of the stream in slot c % kBStages: b_full when it has
+    // landed, b_empty when every issuer's MMAs on it are done
+    uint64_t b_full[kBStages];
+    uint64_t b_empty[kBStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     // tasks are taken from a global counter by the raw weight producer, which
@@ -115,7 +122,7 @@ constexpr int kEpiChunk = 16;  // token columns per epilogue chunk
 constexpr size_t kEpiBufBytes = (size_t)kEpiChunk * 32 * sizeof(float);  // one warp's [16 tokens][32 rows] of h
 
 constexpr size_t kRawOff = 0;
-constexpr size_t kBOff = kRawOff + (size_t)kRawRing;
+constexpr size_t kBOff = kRawOff + (size_t)kRawStages * kRawBytes;
 constexpr size_t kEpiOff = kBOff + (size_t)kBStages * kBStageBytes;  // 2 staging buffers per epilogue warp
 constexpr size_t kHeadOff = kEpiOff + 4 * 2 * kEpiBufBytes;
 constexpr size_t kTcSmem = 1024 + kHeadOff + sizeof(TcHead);
@@ -353,13 +360,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         if (lane == 0) {
             hd.D = cnt;
             hd.abort = 0;
-            for (int s = 0; s < Rings<P>::kRaw; ++s) {
+            for (int s = 0; s < kRawStages; ++s) {
                 mbar_init(&hd.raw_full[s], 1);
                 mbar_init(&hd.raw_empty[s], kConvWarps);
             }
+            for (int s = 0; s < kAStages; ++s) {
+                mbar_init(&hd.a_full[s], kConvWarps);
+                mbar_init(&hd.a_empty[s], 1);
+            }
             for (int s = 0; s < kBStages; ++s) {
-                mbar_init(&hd.full[s], 1 + kConvWarps);
-                mbar_init(&hd.empty[s], issuers<P>());
+                mbar_init(&hd.b_full[s], 1);
+                mbar_init(&hd.b_empty[s], issuers<P>());
             }
             for (int s = 0; s < 2; ++s) {
                 mbar_init(&hd.acc_full[s], issuers<P>());
@@ -386,6 +397,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
     const uint32_t tmem = hd.tmem_base;
     const int ntask = hd.D * tiles;
 
+    // stages per column pass: the K chunks, times the matrices of each chunk
+    const int nst = nks * mats<P>();
     if (warp == 0) {
         // ---------------- raw weight producer, task fetcher (lane 0) ----------------
         if (lane == 0) {
@@ -408,20 +421,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
                 const int r0 = t.rb * kBM;
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                    for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.raw_empty[rs], rph ^ 1u, abort, a.status, a.diag, 12, rs, s, task)) {
+                    for (int st = 0; st < nst; ++st) {
+                        if (!mbar_wait_fast(&hd.raw_empty[rs], rph ^ 1u, abort, a.status, a.diag, 12, rs, st, task)) {
                             ok = false;
                             break;
                         }
-                        uint8_t* dst = raw + (size_t)rs * raw_bytes<P>();
-                        mbar_arrive_expect_tx(&hd.raw_full[rs], P == 0 ? 2 * kBM * kRawRow : kBM * kRawRow);
-                        tma_load_2d(dst, map, s * kRawRow, r0, &hd.raw_full[rs]);
-                        if (P == 0) tma_load_2d(dst + kBM * kRawRow, map, s * kRawRow, I + r0, &hd.raw_full[rs]);
-                        advance(rs, rph, Rings<P>::kRaw);
+                        // stage st: chunk st / mats, matrix st % mats (gate/up phase: rows
+                        // r0.. of the gate half, then of the up half)
+                        const int c = st / mats<P>(), m = st % mats<P>();
+                        mbar_arrive_expect_tx(&hd.raw_full[rs], kRawBytes);
+                        tma_load_2d(raw + (size_t)rs * kRawBytes, map, c * kRawRow, m * I + r0, &hd.raw_full[rs]);
+                        advance(rs, rph, kRawStages);
                     }
                 }
             }
-            for (int s = 0; s < Rings<P>::kRaw; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
+            for (int s = 0; s < kRawStages; ++s) mbar_drain(&hd.raw_full[s], (s < rs) ? rph : (rph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -436,34 +450,35 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                    const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + 63) / 64;
-                    for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, s, task)) {
+                    const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + kActBoxRows - 1) / kActBoxRows;
+                    for (int c = 0; c < nks; ++c) {
+                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 13, bs, c, task)) {
                             ok = false;
                             break;
                         }
                         uint8_t* dst = sb + (size_t)bs * kBStageBytes;
-                        mbar_arrive_expect_tx(&hd.full[bs], (unsigned)boxes * 2u * 64u * 128u);
-                        for (int at = 0; at < 2; ++at)  // the stage's two 64-element atoms of K
-                            for (int c = 0; c < boxes; ++c)
-                                tma_load_2d(dst + at * kBAtom + c * 64 * 128, &act_map, s * kBK + 64 * at,
-                                            t.off + tb + 64 * c, &hd.full[bs]);
+                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * 2 * kActBoxRows * 128));
+                        for (int at = 0; at < 2; ++at)  // the chunk's two 64-element atoms of K
+                            for (int bx = 0; bx < boxes; ++bx)
+                                tma_load_2d(dst + at * kBAtom + bx * kActBoxRows * 128, &act_map, c * kBK + 64 * at,
+                                            t.off + tb + kActBoxRows * bx, &hd.b_full[bs]);
                         advance(bs, bph, kBStages);
                     }
                 }
             }
-            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.full[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 1 || (P == 0 && warp == 3)) {
         // ---------------- MMA issuers (lane 0 alone) ----------------
-        // one thread per issuer runs this loop: its waits and issue overhead between
-        // stages are the time the tensor pipe idles, so it takes no warp-wide votes.
-        // Gate/up phase: warp 1 issues the gate MMAs, warp 3 the up MMAs.
+        // one thread per issuer runs this loop and takes no warp-wide votes; in the
+        // gate/up phase warp 1 issues the gate stages into the gate accumulator and
+        // warp 3 the up stages into the up accumulator
         const int mi = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            int as = 0, bs = 0, buf = 0;
-            unsigned aph = 0, bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
+            int bs = 0, buf = 0;
+            unsigned bph = 0, accph = 0;  // accph: bit b = phase of accumulator buffer b
+            int g0 = 0;                   // stream number of the pass's first stage
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int task = take_task(hd, k, a, abort, 2 + mi);
@@ -482,42 +497,51 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     tc_fence_after();
                     // gate/up phase: this issuer's matrix's accumulator; down phase: buffer buf
                     const uint32_t d = tmem + (uint32_t)(P == 0 ? mi : buf) * kAccCols;
-                    for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.full[bs], bph, abort, a.status, a.diag, 15, bs, s, task)) {
+                    for (int c = 0; c < nks; ++c) {
+                        const int g = g0 + c * mats<P>() + (P == 0 ? mi : 0);  // this issuer's stage
+                        const int as = g % kAStages;
+                        if (!mbar_wait_fast(&hd.a_full[as], (unsigned)(g / kAStages) & 1u, abort, a.status, a.diag, 15,
+                                            as, c, task) ||
+                            !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 16, bs, c, task)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        // A: the stage's f16 weights in tensor memory (gate at +0, up at +64
-                        // columns; 8 columns per 16-element k-step); B: descriptor of k-step
-                        // 0, a 16-element step advances its start address by 32 bytes
-                        const uint32_t at = tmem + kACol0 + (uint32_t)as * a_stage_cols<P>() + (uint32_t)mi * kAMatCols;
+                        // A: the stage's f16 weights in tensor memory (8 columns per 16-element
+                        // k-step); B: descriptor of k-step 0, a 16-element step advances its
+                        // start address by 32 bytes
+                        const uint32_t at = tmem + kACol0 + (uint32_t)as * kAStageCols;
                         const uint64_t bd = sw128_desc(smem_u32(sb + (size_t)bs * kBStageBytes));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                            const uint32_t acc = (c > 0 || kk > 0) ? 1u : 0u;
                             // k-steps 0-3 in the first activation atom, 4-7 in the second
                             const uint64_t b = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
                             tc_mma_f16_ta(d, at + 8 * kk, b, idesc, acc);
                         }
-                        tc_commit(&hd.empty[bs]);
-                        advance(as, aph, Rings<P>::kA);
+                        tc_commit(&hd.a_empty[as]);
+                        tc_commit(&hd.b_empty[bs]);
                         advance(bs, bph, kBStages);
                     }
                     if (!ok) break;
                     tc_commit(&hd.acc_full[buf]);
-                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 256)
+                    g0 += nst;
+                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 320)
                 }
             }
             // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
-            // last commit of every stage
-            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.empty[s], (s < bs) ? bph : (bph ^ 1u));
+            // last commit of every weight and activation slot
+            for (int s = 0; s < kAStages && s < g0; ++s) {
+                const int gl = s + kAStages * ((g0 - 1 - s) / kAStages);  // last stage in slot s
+                mbar_drain(&hd.a_empty[s], (unsigned)(gl / kAStages) & 1u);
+            }
+            for (int s = 0; s < kBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp >= kFirstConv && warp < kFirstConv + kConvWarps) {
         // ---------------- converters ----------------
-        // gate/up phase: thread = (matrix hi, row); down phase: thread = (half hi of the
-        // stage's 64 elements, row)
+        // every stage is one matrix's 128 rows x 128 elements: thread = (half hi of the
+        // stage's elements, row); the gate/up phase alternates gate and up stages
         const int cidx = threadIdx.x - kFirstConv * 32;
         const int row = cidx & (kBM - 1);  // = (warp % 4) * 32 + lane: this thread's tensor-memory lane
         const int hi = cidx >> 7;
@@ -534,51 +558,51 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             const uint8_t* blob = a.ptr[t.phys];
             const int r0 = t.rb * kBM;
             const int srl = K / 32;  // scale bytes per row
-            const uint8_t* sc = P == 0 ? blob + a.w13s + (size_t)(hi * I + r0 + row) * srl
-                                       : blob + a.w2s + (size_t)(r0 + row) * srl;
-            const int cb = row_max_exp(sc, srl) - 12;
+            // this thread's row of each matrix (gate/up phase: gate, up): its scale row
+            // and the exponent its block scales are rebased to
+            const uint8_t* sc0 = P == 0 ? blob + a.w13s + (size_t)(r0 + row) * srl : blob + a.w2s + (size_t)(r0 + row) * srl;
+            const uint8_t* sc1 = P == 0 ? blob + a.w13s + (size_t)(I + r0 + row) * srl : sc0;
+            const int cb0 = row_max_exp(sc0, srl) - 12;
+            const int cb1 = P == 0 ? row_max_exp(sc1, srl) - 12 : cb0;
             for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
-                // scale word of stage s (blocks 4s..4s+3), fetched a stage ahead
-                uint32_t wcur = ld_u32(sc);
-                for (int s = 0; s < nks && ok; ++s) {
-                    const uint32_t wnext = (s + 1 < nks) ? ld_u32(sc + 4 * (s + 1)) : 0u;
-                    // the weight slot of stage gs was last read by the MMAs of stage
-                    // gs - kA (use (gs - kA) / kBStages of its empty barrier)
-                    const int gp = gs - Rings<P>::kA;
-                    if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, s, task) ||
-                        (gp >= 0 && !warp_wait(&hd.empty[gp % kBStages], (unsigned)(gp / kBStages) & 1u, a, abort,
-                                               18, gp % kBStages, s, task))) {
+                // scale word of each stage (the 4 blocks of its chunk), fetched a stage ahead
+                uint32_t wcur = ld_u32(sc0);
+                for (int st = 0; st < nst && ok; ++st) {
+                    const int m = st % mats<P>();  // matrix of this stage (chunk st / mats)
+                    const int sn = st + 1, cn = sn / mats<P>(), mn = sn % mats<P>();
+                    const uint32_t wnext = sn < nst ? ld_u32((mn ? sc1 : sc0) + 4 * cn) : 0u;
+                    // the weight slot of stage gs was last read by the MMAs of stage gs - kAStages
+                    const int as = gs % kAStages;
+                    if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, st, task) ||
+                        !warp_wait(&hd.a_empty[as], ((unsigned)(gs / kAStages) & 1u) ^ 1u, a, abort, 18, as, st,
+                                   task)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint8_t* rsrc = raw + (size_t)rs * raw_bytes<P>();
-                    const uint32_t acol = lane_base + kACol0 + (uint32_t)(gs % Rings<P>::kA) * a_stage_cols<P>();
-                    // gate/up phase: the row's 128 elements (16 words of 8) into its matrix's
-                    // 64 columns; down phase: one half of the row (8 words) into 32 columns
-                    constexpr int kWords = P == 0 ? 16 : 8;
+                    // this thread's half of the row (64 elements, 8 words of 8) into 32 columns;
                     // the raw stage holds 64-byte rows with the 64-byte swizzle: 16-byte
-                    // chunk c of row r sits at chunk c ^ ((r >> 1) & 3), so the 8 rows a
+                    // chunk q of row r sits at chunk q ^ ((r >> 1) & 3), so the 8 rows a
                     // quarter-warp reads fall in distinct banks
-                    const uint8_t* rrow = rsrc + (P == 0 ? hi * kBM * kRawRow : 0) + row * kRawRow;
-                    const int c0 = P == 0 ? 0 : 2 * hi;  // first chunk of this thread
+                    const uint8_t* rrow = raw + (size_t)rs * kRawBytes + row * kRawRow;
                     const int sw = (row >> 1) & 3;
-                    const uint32_t col0 = acol + (P == 0 ? kAMatCols * hi : (kAMatCols / 2) * hi);
+                    const uint32_t col0 = lane_base + kACol0 + (uint32_t)as * kAStageCols + 32u * (uint32_t)hi;
+                    const int cbm = m == 0 ? cb0 : cb1;
 #pragma unroll
-                    for (int g = 0; g < kWords / 4; ++g) {  // 4 words = 32 elements = one scale block
-                        const uint4 w = *reinterpret_cast<const uint4*>(rrow + (((c0 + g) ^ sw) << 4));
-                        const int blk = P == 0 ? g : 2 * hi + g;
-                        const uint32_t m = f16_pow2((int)((wcur >> (8 * blk)) & 0xffu) - cb);
-                        const uint32_t mm = m | (m << 16);
+                    for (int g = 0; g < 2; ++g) {  // 4 words = 32 elements = one scale block
+                        const uint4 w = *reinterpret_cast<const uint4*>(rrow + (((2 * hi + g) ^ sw) << 4));
+                        const int blk = 2 * hi + g;
+                        const uint32_t mf = f16_pow2((int)((wcur >> (8 * blk)) & 0xffu) - cbm);
+                        const uint32_t mm = mf | (mf << 16);
                         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
                         uint32_t v[16];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint4 o = convert_chunk(words[c], mm);
-                            v[4 * c + 0] = o.x;
-                            v[4 * c + 1] = o.y;
-                            v[4 * c + 2] = o.z;
-                            v[4 * c + 3] = o.w;
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 o = convert_chunk(words[q], mm);
+                            v[4 * q + 0] = o.x;
+                            v[4 * q + 1] = o.y;
+                            v[4 * q + 2] = o.z;
+                            v[4 * q + 3] = o.w;
                         }
                         tc_st16(col0 + 16u * g, v);
                     }
@@ -586,10 +610,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&hd.full[gs % kBStages]);
+                        mbar_arrive(&hd.a_full[as]);
                         mbar_arrive(&hd.raw_empty[rs]);
                     }
-                    advance(rs, rph, Rings<P>::kRaw);
+                    advance(rs, rph, kRawStages);
                     ++gs;
                     wcur = wnext;
                 }
@@ -725,9 +749,9 @@ size_t ffn_tc_smem_bytes() { return kTcSmem; }
 cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_count, cudaStream_t st) {
     const int n = a.T * a.k;
     cudaError_t err = cudaSuccess;
-    // activation tiles: 64 elements (128 bytes) x 64 bucket rows, 128-byte swizzle
+    // activation tiles: 64 elements (128 bytes) x 32 bucket rows per box, 128-byte swizzle
     CUtensorMap map, hmap;
-    if (!encode_act_map(&map, a, phase, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!encode_act_map(&map, a, phase, 64, kActBoxRows, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     // h [T·k][I] fp32 in bucket order, boxes of 32 columns x 16 rows (gate/up phase output)
     if (!encode_tmap_2d(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.h, (uint64_t)a.I, (uint64_t)n,
                         (uint64_t)a.I * sizeof(float), 32, kEpiChunk, CU_TENSOR_MAP_SWIZZLE_NONE))

@@ -305,10 +305,11 @@ def test_layer_prefill_buckets(H, I, E, n_hot, k, T, dist):
     fx.layer.close()
 
 
-def test_layer_prefill_bucket_edges():
-    """Buckets of exactly 64 (decode kernel) and 65 (tensor cores), one token, a
-    column pass of 192 plus a padded tail, and an empty expert; cold ones included."""
-    counts = [65, 64, 193, 0, 1, 128, 129, 70]
+@pytest.mark.parametrize("counts", [[65, 64, 193, 0, 1, 128, 129, 70], [160, 161, 320, 0, 2, 337, 96, 112]])
+def test_layer_prefill_bucket_edges(counts):
+    """Buckets of exactly 64 (decode kernel) and 65 (tensor cores), one token, full
+    column passes of 160 tokens with and without a padded tail, two and three
+    passes, and an empty expert; cold ones included."""
     E, H, I = 8, 256, 512
     loc = np.array([6, 0, 7, 1, 2, 3, 4, 5], np.int32)  # experts 0 and 2 are cold
     fx = LayerFixture(H=H, I=I, E=E, n_hot=6, n_cold=2, k=1, seed=99, loc=loc)
