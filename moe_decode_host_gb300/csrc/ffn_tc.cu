@@ -91,6 +91,14 @@ __host__ __device__ constexpr int mats() { return P == 0 ? 2 : 1; }  // weight m
 template <int P>
 __host__ __device__ constexpr int task_takers() { return 1 + issuers<P>() + kConvWarps + 4; }
 
+// One task: a listed expert (picks, first bucket entry, physical id, blob) and a
+// 128-row tile.
+struct TcTask {
+    const uint8_t* blob;
+    int e, rb, cnt, off, phys;
+    bool valid;
+};
+
 struct alignas(16) TcHead {
     uint64_t raw_full[kRawStages];
     uint64_t raw_empty[kRawStages];
@@ -105,10 +113,12 @@ struct alignas(16) TcHead {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     // tasks are taken from a global counter by the raw weight producer, which
-    // publishes task k in slot k % kTaskQ for the other roles (-1: no more)
+    // publishes task k in slot k % kTaskQ for the other roles (-1: no more) with
+    // its expert's routing values
     uint64_t tq_full[kTaskQ];
     uint64_t tq_empty[kTaskQ];
     int tq[kTaskQ];
+    TcTask tqt[kTaskQ];
     uint32_t tmem_base;
     int abort;
     int D;
@@ -255,11 +265,6 @@ __device__ __forceinline__ uint4 convert_chunk(uint32_t word, uint32_t mm) {
     return o;
 }
 
-struct TcTask {
-    int e, rb, cnt, off, phys;
-    bool valid;
-};
-
 __device__ __forceinline__ TcTask tc_task(const FfnArgs& a, const TcHead& hd, int task, int tiles) {
     TcTask t;
     t.e = hd.list[task / tiles];
@@ -268,6 +273,7 @@ __device__ __forceinline__ TcTask tc_task(const FfnArgs& a, const TcHead& hd, in
     t.off = __ldg(a.offsets + t.e);
     t.phys = __ldg(a.phys_ids + __ldg(a.entries + t.off));
     t.valid = t.phys >= 0 && t.phys < a.n_phys;
+    t.blob = t.valid ? a.ptr[t.phys] : nullptr;
     return t;
 }
 
@@ -290,20 +296,24 @@ __device__ __forceinline__ void advance(int& slot, unsigned& phase, int n) {
 
 // Task k of this CTA from the queue (-1: no more tasks, or a wait ran out), taken
 // by one thread.
-__device__ __forceinline__ int take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who) {
+__device__ __forceinline__ int take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who,
+                                         TcTask& t) {
     const int j = k % kTaskQ;
     if (!mbar_wait_fast(&hd.tq_full[j], (unsigned)(k / kTaskQ) & 1u, abort, a.status, a.diag, 20, j, k, who))
         return -1;
     const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    t = hd.tqt[j];
     mbar_arrive(&hd.tq_empty[j]);
     return task;
 }
 
 // The same, taken by a whole warp (every lane returns the same task).
-__device__ __forceinline__ int warp_take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who) {
+__device__ __forceinline__ int warp_take_task(TcHead& hd, int k, const FfnArgs& a, volatile int* abort, int who,
+                                              TcTask& t) {
     const int j = k % kTaskQ;
     if (!warp_wait(&hd.tq_full[j], (unsigned)(k / kTaskQ) & 1u, a, abort, 20, j, k, who)) return -1;
     const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    t = hd.tqt[j];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&hd.tq_empty[j]);
     return task;
@@ -412,10 +422,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                     break;
                 int task = atomicAdd(a.task_ctr + ctr, 1);
                 if (task >= ntask) task = -1;
+                TcTask t{};
+                if (task >= 0) t = tc_task(a, hd, task, tiles);
                 *reinterpret_cast<volatile int*>(&hd.tq[j]) = task;
+                hd.tqt[j] = t;
                 mbar_arrive(&hd.tq_full[j]);
                 if (task < 0) break;
-                const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
                 const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13r : &a.tmaps[t.phys].w2r;
                 asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
@@ -445,9 +457,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             unsigned bph = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int task = take_task(hd, k, a, abort, 1);
+                TcTask t;
+                const int task = take_task(hd, k, a, abort, 1, t);
                 if (task < 0) break;
-                const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                     const int boxes = (ncols16(min(kNMax, t.cnt - tb)) + kActBoxRows - 1) / kActBoxRows;
@@ -481,9 +493,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
             int g0 = 0;                   // stream number of the pass's first stage
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int task = take_task(hd, k, a, abort, 2 + mi);
+                TcTask t;
+                const int task = take_task(hd, k, a, abort, 2 + mi, t);
                 if (task < 0) break;
-                const TcTask t = tc_task(a, hd, task, tiles);
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += kNMax) {
                     const int N = ncols16(min(kNMax, t.cnt - tb));
@@ -551,11 +563,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         int gs = 0;  // stage number in the CTA's stream
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int task = warp_take_task(hd, k, a, abort, 3);
+            TcTask t;
+            const int task = warp_take_task(hd, k, a, abort, 3, t);
             if (task < 0) break;
-            const TcTask t = tc_task(a, hd, task, tiles);
             if (!t.valid) continue;
-            const uint8_t* blob = a.ptr[t.phys];
+            const uint8_t* blob = t.blob;
             const int r0 = t.rb * kBM;
             const int srl = K / 32;  // scale bytes per row
             // this thread's row of each matrix (gate/up phase: gate, up): its scale row
@@ -634,9 +646,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
         unsigned accph = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int task = warp_take_task(hd, k, a, abort, 4);
+            TcTask t;
+            const int task = warp_take_task(hd, k, a, abort, 4, t);
             if (task < 0) break;
-            const TcTask t = tc_task(a, hd, task, tiles);
             const int r0 = t.rb * kBM;
             if (!t.valid) {
                 // zero outputs for an expert whose physical id is out of range
@@ -647,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 }
                 continue;
             }
-            const uint8_t* blob = a.ptr[t.phys];
+            const uint8_t* blob = t.blob;
             const int srl = K / 32;
             const int c0 = row_max_exp(blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + t_row) * srl, srl) - 12;
             const int c1 = P == 0 ? row_max_exp(blob + a.w13s + (size_t)(I + r0 + t_row) * srl, srl) - 12 : c0;
