@@ -48,23 +48,34 @@ __device__ __forceinline__ void copy_range(const uint4* __restrict__ src, uint4*
     }
 }
 
-// Distinct picked cold slots (ascending) and the physical id of every pick.
-__global__ void __launch_bounds__(kGatherThreads) cold_remap_kernel(
+// Distinct picked cold slots (ascending) and the physical id of every pick.  One
+// CTA of 1024 threads; each thread takes four picks at a time so that their id and
+// placement loads overlap.
+constexpr int kRemapThreads = 1024;
+__global__ void __launch_bounds__(kRemapThreads) cold_remap_kernel(
     const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
     int32_t* __restrict__ phys, int32_t* __restrict__ cold_list, int32_t* __restrict__ n_picked, int* status) {
     __shared__ unsigned char flag[kMaxColdSlots];
     for (int c = threadIdx.x; c < n_cold; c += blockDim.x) flag[c] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n_picks; i += blockDim.x) {
-        int id = __ldg(ids + i);
-        int p = -1;
-        if (id >= 0 && id < E) {
-            p = __ldg(loc + id);
-            if (p >= n_hot) flag[p - n_hot] = 1;
-        } else {
-            set_status(status, MOE_ERR_BAD_EXPERT);
+    for (int base = 0; base < n_picks; base += 4 * kRemapThreads) {
+        int id[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * kRemapThreads + threadIdx.x;
+            id[u] = i < n_picks ? __ldg(ids + i) : 0;
         }
-        phys[i] = p;
+        int p[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p[u] = (id[u] >= 0 && id[u] < E) ? __ldg(loc + id[u]) : -1;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * kRemapThreads + threadIdx.x;
+            if (i >= n_picks) continue;
+            if (p[u] < 0) set_status(status, MOE_ERR_BAD_EXPERT);
+            else if (p[u] >= n_hot) flag[p[u] - n_hot] = 1;
+            phys[i] = p[u];
+        }
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -149,7 +160,7 @@ __global__ void __launch_bounds__(kGatherThreads) link_probe_kernel(const uint8_
 cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st) {
     if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
-    cold_remap_kernel<<<1, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, phys, cold_list, n_picked,
+    cold_remap_kernel<<<1, kRemapThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, phys, cold_list, n_picked,
                                                     status);
     return cudaGetLastError();
 }

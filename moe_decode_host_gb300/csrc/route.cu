@@ -209,6 +209,56 @@ __global__ void __launch_bounds__(256) route_bucket_kernel(const int32_t* __rest
     bucket_expert(ids, n, e, E, counts, offsets, entries, window);
 }
 
+// Large batches: one CTA per expert, its 8 warps each scanning one eighth of the
+// picks (counts first, then placement from each warp's exclusive start), so every
+// SM shares the scans; the entries keep ascending pick order.
+constexpr int kSplitWarps = 8;
+__global__ void __launch_bounds__(32 * kSplitWarps) route_bucket_split_kernel(const int32_t* __restrict__ ids, int n,
+                                                                              int E, int32_t* counts, int32_t* offsets,
+                                                                              int32_t* entries, int32_t* window) {
+    __shared__ int s_lt[kSplitWarps], s_eq[kSplitWarps];
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per = ((n + kSplitWarps - 1) / kSplitWarps + 31) & ~31;  // picks per warp, a multiple of 32
+    const int beg = min(n, warp * per), end = min(n, beg + per);
+    int c_lt = 0, c_eq = 0;
+    for (int base = beg; base < end; base += 32) {
+        const int i = base + lane;
+        const int id = (i < end) ? __ldg(ids + i) : 0x7fffffff;
+        c_lt += __popc(__ballot_sync(0xffffffffu, id < e));
+        c_eq += __popc(__ballot_sync(0xffffffffu, id == e));
+    }
+    if (lane == 0) {
+        s_lt[warp] = c_lt;
+        s_eq[warp] = c_eq;
+    }
+    __syncthreads();
+    int lt = 0, eq = 0, pos = 0;
+#pragma unroll
+    for (int w = 0; w < kSplitWarps; ++w) {
+        lt += s_lt[w];
+        eq += s_eq[w];
+        if (w < warp) pos += s_eq[w];
+    }
+    pos += lt;  // this warp's first entry
+    if (c_eq > 0) {
+        const unsigned lt_mask = (1u << lane) - 1u;
+        for (int base = beg; base < end; base += 32) {
+            const int i = base + lane;
+            const int id = (i < end) ? __ldg(ids + i) : 0x7fffffff;
+            const unsigned m = __ballot_sync(0xffffffffu, id == e);
+            if (id == e) entries[pos + __popc(m & lt_mask)] = i;
+            pos += __popc(m);
+        }
+    }
+    if (threadIdx.x == 0) {
+        counts[e] = eq;
+        offsets[e] = lt;
+        if (e == E - 1) offsets[E] = lt + eq;
+        if (eq > 0 && window) atomicAdd(window + e, eq);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids, float* w,
@@ -222,7 +272,10 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
     route_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(logits, T, E, k, renorm, ids, w, status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_bucket_kernel<<<(E + 7) / 8, 256, 0, st>>>(ids, T * k, E, counts, offsets, entries, window);
+    if (T * k >= 4096)
+        route_bucket_split_kernel<<<E, 32 * kSplitWarps, 0, st>>>(ids, T * k, E, counts, offsets, entries, window);
+    else
+        route_bucket_kernel<<<(E + 7) / 8, 256, 0, st>>>(ids, T * k, E, counts, offsets, entries, window);
     return cudaGetLastError();
 }
 

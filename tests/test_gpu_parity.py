@@ -74,7 +74,9 @@ def test_e2m1_pair_conversion_lane_layout():
     (384, 6, 32, 0, "zipf1.5"),    # c2, page-faithful skew
     (384, 6, 64, 1, "uniform"),    # largest single-CTA batch, renorm
     (384, 6, 65, 0, "uniform"),    # first two-kernel batch
-    (384, 6, 1000, 1, "zipf1.1"),  # ragged multi-CTA
+    (384, 6, 1000, 1, "zipf1.1"),  # ragged multi-CTA, split bucketing (6000 picks)
+    (96, 7, 700, 0, "zipf1.5"),    # split bucketing, 4900 picks (ragged per warp)
+    (1024, 32, 200, 0, "uniform"), # split bucketing at maximum E and k
     (40, 5, 13, 1, "ties"),
     (1024, 32, 7, 0, "uniform"),   # maximum E and k
     (8, 8, 3, 0, "uniform"),       # k == E
@@ -167,6 +169,15 @@ def test_cold_gather_c0():
         fx = LayerFixture(H=c["H"], I=c["I"], E=16, n_hot=12, n_cold=4, k=2, seed=2, loc=loc)
         for T in (1, 4, 9):
             _gather_check(fx, synth.gen_logits_uniform(T, 16, seed=T), T)
+
+
+def test_cold_gather_many_picks():
+    """12,000 picks over 64 experts (16 cold, permuted placement): the remap takes
+    several rounds of four picks per thread."""
+    loc = np.random.default_rng(11).permutation(64).astype(np.int32)
+    fx = LayerFixture(H=128, I=128, E=64, n_hot=48, n_cold=16, k=6, seed=6, loc=loc)
+    T = 2000
+    _gather_check(fx, synth.gen_logits_uniform(T, 64, seed=17), T)
 
 
 def test_cold_gather_bad_expert_ids():
