@@ -40,7 +40,7 @@ NCU_TRAFFIC = {
     "ffn_decode": {"bytes_per_expert": (66932224 + 777984 + 33490688) / 5,
                    "source": "profiles/ffn_decode_kernel_c1_small.md"},
     # per expert through the tcgen05 kernels at about 128 tokens per expert
-    "ffn_tc": {"bytes_per_expert": (1135740000 + 92264448 + 488412000 + 113392896) / 64,
+    "ffn_tc": {"bytes_per_expert": (935596288 + 92993792 + 483277568 + 112975360) / 64,
                "source": "profiles/ffn_tc_kernel_c4_small.md"},
 }
 
