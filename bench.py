@@ -99,6 +99,8 @@ def parse():
                     help="keep a pinned host copy of every expert (residency moves bytes one way only); "
                          "default on for single-layer workloads")
     ap.add_argument("--no-mirror", dest="mirror", action="store_false")
+    ap.add_argument("--zero-copy", action="store_true",
+                    help="the FFN reads picked cold experts in place from host memory (no slot copy)")
     return ap.parse_args()
 
 
@@ -124,6 +126,7 @@ def workload(args):
     # stack would need 154 GB of pinned host memory, so it keeps the in-place exchange
     c["mirror"] = args.mirror if args.mirror is not None else (
         c.get("layers", 1) == 1 and c["n_cold"] > 0 and not args.no_residency)
+    c["zero_copy"] = bool(args.zero_copy)
     return c
 
 
@@ -278,6 +281,8 @@ def _config_json(c, args):
             "step_pool": (min(max(args.pool, args.steps + args.warmup), 2048)
                           if (not args.no_residency and c["n_cold"] > 0) else args.pool),
             "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
+            "cold_experts": ("read in place from pinned host memory by the FFN (zero copy)"
+                             if c.get("zero_copy") and c["T"] <= 64 else "copied into the HBM slot scratch"),
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -319,7 +324,7 @@ def build_layers(c, dev, seed_tag="bench"):
         layer = m.Layer(E=E, k=k, H=H, I=I, n_hot=n_hot, n_cold=n_cold, scratch=scratch,
                         hot_ptrs=[hot[h] for h in range(n_hot)], cold_ptrs=[cold[i] for i in range(n_host)],
                         init_loc=loc, swap_every=0 if c.get("no_res") else 16, max_swaps=8, hysteresis=3.0,
-                        host_mirror=mirror)
+                        host_mirror=mirror, zero_copy=bool(c.get("zero_copy")))
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
 

@@ -81,7 +81,16 @@ extern "C" {
  *              expert id (E blobs); a demotion moves no bytes and a promotion
  *              copies the expert into its HBM slot from its scratch slot when that
  *              slot still holds this layer's copy of it, else from its host copy.
- *              The host copies must equal the HBM-resident experts' bytes. */
+ *              The host copies must equal the HBM-resident experts' bytes.
+ *  zero_copy   0: cold_gather copies the picked cold experts into their scratch
+ *              slots and moe_grouped_ffn reads them there.  1 (calls of at most 64
+ *              tokens): cold_gather only remaps, and moe_grouped_ffn reads the
+ *              picked cold experts' weights in place from their pinned host blobs,
+ *              on the layer's copy stream alongside the experts in HBM ("Milo and
+ *              James Try Inference Engineering": reading expert rows from pinned
+ *              host memory over the link; "Running High-Quality DeepSeek V4 Flash
+ *              on One 96 GB GPU": mapped host planes read in place).  Larger calls
+ *              copy as with 0. */
 typedef struct moe_params {
     int E, k, H, I, n_hot, n_cold;
     int renorm;
@@ -89,6 +98,7 @@ typedef struct moe_params {
     int max_swaps;
     float hysteresis;
     int host_mirror;
+    int zero_copy;
 } moe_params;
 
 typedef struct moe_scratch moe_scratch;

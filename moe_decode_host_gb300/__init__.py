@@ -52,11 +52,12 @@ class Layer:
     """One MoE layer handle (moe_layer_create)."""
 
     def __init__(self, *, E, k, H, I, n_hot, n_cold, scratch, hot_ptrs, cold_ptrs, init_loc, renorm=0,
-                 swap_every=16, max_swaps=8, hysteresis=3.0, host_mirror=False):
+                 swap_every=16, max_swaps=8, hysteresis=3.0, host_mirror=False, zero_copy=False):
         """cold_ptrs: the n_cold cold slots' host blobs, or with host_mirror the host
-        copies of all E experts indexed by expert id."""
+        copies of all E experts indexed by expert id. zero_copy: the FFN reads picked
+        cold experts in place from host memory (calls of at most 64 tokens)."""
         self.p = moe_params(E, k, H, I, n_hot, n_cold, renorm, swap_every, max_swaps, hysteresis,
-                            1 if host_mirror else 0)
+                            1 if host_mirror else 0, 1 if zero_copy else 0)
         hot = (ctypes.c_void_p * max(1, n_hot))(*[ptr(x) for x in hot_ptrs])
         n_host = E if host_mirror else n_cold
         cold = (ctypes.c_void_p * max(1, n_host))(*[ptr(x) for x in cold_ptrs])

@@ -36,7 +36,7 @@ class moe_params(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int), ("k", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
                 ("n_hot", ctypes.c_int), ("n_cold", ctypes.c_int), ("renorm", ctypes.c_int),
                 ("swap_every", ctypes.c_int), ("max_swaps", ctypes.c_int), ("hysteresis", ctypes.c_float),
-                ("host_mirror", ctypes.c_int)]
+                ("host_mirror", ctypes.c_int), ("zero_copy", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

@@ -227,6 +227,7 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     if (p.swap_every < 0 || p.max_swaps < 0 || p.max_swaps > kMaxSwaps) return MOE_ERR_INVALID_ARG;
     if (!(p.hysteresis >= 0.0f) || p.hysteresis > 1e30f) return MOE_ERR_INVALID_ARG;
     if (p.host_mirror != 0 && p.host_mirror != 1) return MOE_ERR_INVALID_ARG;
+    if (p.zero_copy != 0 && p.zero_copy != 1) return MOE_ERR_INVALID_ARG;
     const size_t eb = moe_expert_bytes(p.H, p.I);
     if (p.n_cold > 0 && (!scratch || scratch->expert_bytes != eb || scratch->n_slots < p.n_cold))
         return MOE_ERR_INVALID_ARG;
@@ -350,7 +351,9 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
     if (L->p.n_cold > 0 && T > 0 && !cold_list) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
     cudaError_t err = cudaSuccess;
-    if (L->p.n_cold > 0 && T > 0) {
+    // zero copy (decode-sized calls): the FFN reads the cold experts in place, no copy
+    const bool zc = L->p.zero_copy && T <= kTcMinTokens;
+    if (L->p.n_cold > 0 && T > 0 && !zc) {
         // the byte copy forks onto the layer's copy stream first, so that it starts
         // while the remap kernel runs and the FFN over HBM-resident experts can run
         // while the link streams the cold ones
@@ -424,7 +427,29 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     cudaError_t err = pe ? cudaEventRecord(pe[0], st) : cudaSuccess;
     if (err == cudaSuccess) err = launch_ffn_prep(a, workspace, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    if (L->copy_pending) {
+    if (L->p.zero_copy && L->p.n_cold > 0 && T <= kTcMinTokens) {
+        // zero copy: the cold experts' chain (gate/up, prescale, down) reads their
+        // weights in place over the host link on the layer's copy stream, with as
+        // many CTAs as the cold copy would use, while the experts in HBM run here;
+        // profiled calls record the cold chain as the layer's copy
+        a.cold_host = L->d_cold_src;
+        err = cudaEventRecord(L->ev_fork, st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
+        const bool prof = L->prof_n < (int)L->prof_ev.size() / 2;
+        if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 2, L->copy_ctas, L->copy_stream, true);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 2, L->copy_ctas, L->copy_stream, true);
+        if (err == cudaSuccess && prof) {
+            err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
+            ++L->prof_n;
+        }
+        if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(st, L->ev_join, 0);
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
+    } else if (L->copy_pending) {
         // experts in HBM first, while the cold copy is in flight; then the cold ones.
         // An FFN CTA leaves no room on its SM for a copy CTA; the decode kernel's CTAs
         // take tasks from a shared counter, so those that start only when the copy

@@ -173,7 +173,11 @@ __device__ __forceinline__ TaskInfo task_info(const FfnArgs& a, const SmemHead& 
     return ti;
 }
 
-template <int P, int NT>
+// ZC (zero copy): the listed experts are cold and their weights are read in place
+// from pinned host memory: the producer warps load each stage's 64 rows x 128 bytes
+// with 16-byte loads over the host link and store them in the layout the TMA gives
+// (128-byte swizzle); the activation slice still comes by TMA.
+template <int P, int NT, bool ZC>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
                                                                 int lo, int hi, int sel, int ctr) {
     using C = Cfg<P>;
@@ -216,7 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
         v.blob = nullptr;
         if (act_e) {
             v.phys = __ldg(a.phys_ids + __ldg(a.entries + off));
-            v.blob = (v.phys >= 0 && v.phys < a.n_phys) ? a.ptr[v.phys] : nullptr;
+            v.blob = (v.phys >= 0 && v.phys < a.n_phys)
+                         ? ((ZC && v.phys >= a.n_hot) ? a.cold_host[v.phys - a.n_hot] : a.ptr[v.phys])
+                         : nullptr;
         }
         pe[e] = v;
     }
@@ -234,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             hd.D = cnt;
             hd.abort = 0;
             for (int s = 0; s < L::kStages; ++s) {
-                mbar_init(&hd.full[s], 1);
+                // zero copy: the activation TMA's arrival and the producer warp's, after its stores
+                mbar_init(&hd.full[s], ZC ? 2 : 1);
                 mbar_init(&hd.empty[s], kPerStage);
             }
             for (int j = 0; j < kTaskQ; ++j) {
@@ -262,6 +269,101 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     volatile int* abort = &hd.abort;
 
     if (warp >= kConsumers) {
+        if constexpr (ZC) {
+            // ---------------- producers, zero copy (whole producer warp) ----------------
+            const unsigned pp = (unsigned)(warp - kConsumers);
+            const int rowb = K / 2;  // bytes of one weight row
+            const uint8_t* plane_off = nullptr;
+            int slot = 0;
+            unsigned phase = 0;
+            int gstage = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int j = k % kTaskQ;
+                const unsigned qpar = (unsigned)(k / kTaskQ) & 1u;
+                int task = -1;
+                bool got = true;
+                if (lane == 0) {
+                    if (pp == 0) {
+                        got = mbar_wait_fast(&hd.tq_empty[j], qpar ^ 1u, abort, a.status, a.diag, 4, j, k, 0);
+                        if (got) {
+                            task = atomicAdd(a.task_ctr + ctr, 1);
+                            if (task >= ntask) task = -1;
+                            *reinterpret_cast<volatile int*>(&hd.tq[j]) = task;
+                            mbar_arrive(&hd.tq_full[j]);
+                        }
+                    } else {
+                        got = mbar_wait_fast(&hd.tq_full[j], qpar, abort, a.status, a.diag, 5, j, k, 0);
+                        if (got) {
+                            task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+                            mbar_arrive(&hd.tq_empty[j]);
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, got, 0)) break;
+                task = __shfl_sync(0xffffffffu, task, 0);
+                if (task < 0) break;
+                const TaskInfo ti = task_info(a, hd, task, tiles);
+                if (!ti.valid) continue;
+                const uint8_t* wbase = ti.blob + (P == 0 ? 0 : a.w2n);
+                (void)plane_off;
+                const int r0 = ti.rt * C::kTaskRows;
+                for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
+                    for (int s = 0; s < nst && ok; ++s) {
+                        if (((unsigned)gstage & 1u) == pp) {
+                            // this lane's 16 of the stage's 512 16-byte chunks (64 rows x 128
+                            // bytes; the gate/up phase: 32 gate rows, then 32 up rows), loaded
+                            // before the slot is free so the host latency overlaps the wait;
+                            // chunks past the row's end (an odd K tail) read as zero
+                            uint4 v[16];
+#pragma unroll
+                            for (int i2 = 0; i2 < 16; ++i2) {
+                                const int idx = lane + 32 * i2;
+                                const int lr = idx >> 3, ch = idx & 7;
+                                const int grow = P == 0 ? (lr < 32 ? r0 + lr : I + r0 + lr - 32) : r0 + lr;
+                                const int col = s * kSliceBytes + ch * 16;
+                                v[i2] = col < rowb ? ld_host_v4(wbase + (size_t)grow * rowb + col)
+                                                   : make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            bool w = true;
+                            if (lane == 0)
+                                w = mbar_wait_fast(&hd.empty[slot], phase ^ 1u, abort, a.status, a.diag, 2, slot, s,
+                                                   (task << 8) | min(8 * NT, ti.cnt - tb));
+                            if (!__shfl_sync(0xffffffffu, w, 0)) {
+                                ok = false;
+                                break;
+                            }
+                            uint8_t* dst = stages + slot * L::kStageBytes;
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(&hd.full[slot], (unsigned)L::kABytes);
+                                tma_load_2d(dst + L::kWBytes, &act_map, s * 256, ti.off + tb, &hd.full[slot]);
+                            }
+#pragma unroll
+                            for (int i2 = 0; i2 < 16; ++i2) {
+                                const int idx = lane + 32 * i2;
+                                const int lr = idx >> 3, ch = idx & 7;
+                                *reinterpret_cast<uint4*>(dst + lr * kSliceBytes + ((ch ^ (lr & 7)) << 4)) = v[i2];
+                            }
+                            __syncwarp();  // the lanes' stores come before lane 0's arrival
+                            if (lane == 0) mbar_arrive(&hd.full[slot]);
+                        }
+                        ++gstage;
+                        if (++slot == L::kStages) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            // drain: every activation copy this producer issued has landed
+            if (lane == 0)
+                for (int s = (int)pp; s < L::kStages; s += kProducers) {
+                    if (s >= gstage) break;
+                    const int g_last = s + L::kStages * ((gstage - 1 - s) / L::kStages);
+                    mbar_drain(&hd.full[s], (unsigned)(g_last / L::kStages) & 1u);
+                }
+            return;
+        }
         // ---------------- producers (lane 0 of each producer warp) ----------------
         if (lane == 0) {
             const unsigned pp = (unsigned)(warp - kConsumers);
@@ -661,12 +763,12 @@ size_t smem_bytes() {
     return 1024 + (size_t)L::kStages * L::kStageBytes + sizeof(SmemHead) + (size_t)L::kRedBytes;
 }
 
-template <int P, int NT>
+template <int P, int NT, bool ZC>
 cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int ctr, int grid, cudaStream_t st) {
     static bool configured = false;
     const size_t sm = smem_bytes<P, NT>();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_tma_kernel<P, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ffn_tma_kernel<P, NT, ZC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sm);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -674,7 +776,7 @@ cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int ctr, int
     // the stage's activation slice: 256 elements of 8 * NT consecutive bucket rows
     CUtensorMap act_map;
     if (!encode_act_map(&act_map, a, P, 256, 8 * NT, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
-    return launch_pdl(ffn_tma_kernel<P, NT>, dim3(grid), dim3(kThreads), sm, st, a, act_map, lo, hi, sel, ctr);
+    return launch_pdl(ffn_tma_kernel<P, NT, ZC>, dim3(grid), dim3(kThreads), sm, st, a, act_map, lo, hi, sel, ctr);
 }
 
 }  // namespace
@@ -701,7 +803,7 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st) {
+cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st, bool zc) {
     if (a.T == 0) return cudaSuccess;
     // token-count ranges per kernel (a bound on the largest bucket is T); buckets
     // above kTcMinTokens go to the tensor-core kernel
@@ -724,18 +826,31 @@ cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count,
         // each launch of the call takes tasks from its own counter (zeroed by xprep)
         const int ctr = ((sel == 2 ? 2 : 0) + phase) * 3 + ri;
         cudaError_t err;
-        if (phase == 0) {
-            err = r.nt == 1 ? launch_phase<0, 1>(a, r.lo, r.hi, sel, ctr, grid, st)
-                : r.nt == 2 ? launch_phase<0, 2>(a, r.lo, r.hi, sel, ctr, grid, st)
-                            : launch_phase<0, 4>(a, r.lo, r.hi, sel, ctr, grid, st);
+        if (zc) {
+            if (phase == 0) {
+                err = r.nt == 1 ? launch_phase<0, 1, true>(a, r.lo, r.hi, sel, ctr, grid, st)
+                    : r.nt == 2 ? launch_phase<0, 2, true>(a, r.lo, r.hi, sel, ctr, grid, st)
+                                : launch_phase<0, 4, true>(a, r.lo, r.hi, sel, ctr, grid, st);
+            } else {
+                err = r.nt == 1 ? launch_phase<1, 1, true>(a, r.lo, r.hi, sel, ctr, grid, st)
+                    : r.nt == 2 ? launch_phase<1, 2, true>(a, r.lo, r.hi, sel, ctr, grid, st)
+                                : launch_phase<1, 4, true>(a, r.lo, r.hi, sel, ctr, grid, st);
+            }
+        } else if (phase == 0) {
+            err = r.nt == 1 ? launch_phase<0, 1, false>(a, r.lo, r.hi, sel, ctr, grid, st)
+                : r.nt == 2 ? launch_phase<0, 2, false>(a, r.lo, r.hi, sel, ctr, grid, st)
+                            : launch_phase<0, 4, false>(a, r.lo, r.hi, sel, ctr, grid, st);
         } else {
-            err = r.nt == 1 ? launch_phase<1, 1>(a, r.lo, r.hi, sel, ctr, grid, st)
-                : r.nt == 2 ? launch_phase<1, 2>(a, r.lo, r.hi, sel, ctr, grid, st)
-                            : launch_phase<1, 4>(a, r.lo, r.hi, sel, ctr, grid, st);
+            err = r.nt == 1 ? launch_phase<1, 1, false>(a, r.lo, r.hi, sel, ctr, grid, st)
+                : r.nt == 2 ? launch_phase<1, 2, false>(a, r.lo, r.hi, sel, ctr, grid, st)
+                            : launch_phase<1, 4, false>(a, r.lo, r.hi, sel, ctr, grid, st);
         }
         if (err != cudaSuccess) return err;
     }
-    if (a.T > kTcMinTokens) return launch_ffn_tc(a, phase, sel, kTcMinTokens, sm_count, st);
+    if (a.T > kTcMinTokens) {
+        if (zc) return cudaErrorInvalidValue;  // the tensor-core kernel reads the scratch copies
+        return launch_ffn_tc(a, phase, sel, kTcMinTokens, sm_count, st);
+    }
     return cudaSuccess;
 }
 

@@ -12,6 +12,7 @@
 // slots with 16-byte zero-copy loads, several in flight per thread to cover the
 // link latency.
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -20,13 +21,6 @@ constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 8;          // 16-byte loads in flight per thread
 constexpr int kMaxColdSlots = 4096;  // n_cold bound checked at layer creation
 
-__device__ __forceinline__ uint4 ld_host_v4(const uint4* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA,
 // kUnroll loads in flight per thread including the ragged last round.

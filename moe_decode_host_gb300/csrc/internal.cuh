@@ -113,6 +113,9 @@ struct FfnArgs {
     int* status;
     int* diag;               // [16] where the first timed-out wait gave up
     size_t w13s, w2n, w2s;   // plane offsets in a blob
+    // zero-copy launches: cold slot c's blob read in place from pinned host memory
+    // (device-mapped pointers), no scratch copy
+    const uint8_t* const* cold_host;
 };
 
 size_t ffn_decode_workspace(int T, int k, int H, int I);
@@ -125,7 +128,9 @@ bool encode_act_map(CUtensorMap* m, const FfnArgs& a, int phase, uint32_t box_in
 cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st);
 // One phase (0: gate/up -> h, 1: down -> y) over the experts selected by sel
 // (0: all, 1: placed in HBM, 2: placed in cold slots).
-cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st);
+// zc: the launch reads the weights of cold experts (sel == 2) in place from host
+// memory (decode-sized calls only: T <= kTcMinTokens).
+cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st, bool zc = false);
 // The tensor-core kernel of one phase over the selected experts with more than lo tokens.
 cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_count, cudaStream_t st);
 

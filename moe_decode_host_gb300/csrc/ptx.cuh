@@ -115,6 +115,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
 // async-proxy accesses (TMA, bulk copies) to the same bytes once a barrier follows.
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 16-byte read of pinned, device-mapped host memory (or any global memory),
+// bypassing L1.
+__device__ __forceinline__ uint4 ld_host_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {

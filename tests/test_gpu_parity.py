@@ -243,6 +243,49 @@ def _compare_layer(fx, buf, logits, x, tokens, out_fp32):
     return worst_y
 
 
+@pytest.mark.parametrize("T,dist", [(1, "uniform"), (8, "zipf1.1"), (33, "zipf1.5"), (64, "uniform")])
+def test_layer_zero_copy_matches_copy_path(T, dist):
+    """Zero copy: the cold experts' weights are read in place from host memory and
+    their slots stay untouched; the outputs match the copy path's to rounding (the
+    same arithmetic in the same order; the two kernel variants are compiled
+    separately, so the compiler's fused multiply-adds may differ in the last bit)
+    and the oracle within the bar."""
+    H, I, E, n_hot, k = 1024, 768, 32, 24, 6
+    loc = np.random.default_rng(T).permutation(E).astype(np.int32)
+    if dist == "uniform":
+        logits = synth.gen_logits_uniform(T, E, seed=40 + T)
+    else:
+        logits = synth.gen_logits_zipf(T, E, float(dist[4:]), synth.zipf_permutation(E, 3), seed=40 + T)
+    x = synth.gen_x(T, H, seed=41 + T)
+    outs = []
+    for zc in (False, True):
+        fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=E - n_hot, k=k, seed=77, loc=loc, zero_copy=zc)
+        fx.slots.fill_(0xAB)
+        buf = _run_layer(fx, logits, x, True)
+        outs.append((buf.y.cpu().clone(), buf.out.cpu().clone()))
+        if zc:
+            assert bool((fx.slots == 0xAB).all()), "zero copy wrote a scratch slot"
+            _compare_layer(fx, buf, logits, x, list(range(0, T, max(1, T // 8))), True)
+            assert int(buf.n_cold_picked.item()) > 0
+        fx.layer.close()
+    assert rel_l2(outs[1][0].numpy(), outs[0][0].numpy()) <= 1e-6
+    assert rel_l2(outs[1][1].numpy(), outs[0][1].numpy()) <= 1e-6
+
+
+def test_layer_zero_copy_large_call_copies():
+    """Zero copy applies to calls of at most 64 tokens; a 200-token call copies its
+    cold experts (the tensor-core kernel reads the scratch) and matches the oracle."""
+    H, I, E, n_hot, k, T = 256, 512, 8, 6, 2, 200
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=E - n_hot, k=k, seed=5, zero_copy=True)
+    logits = synth.gen_logits_uniform(T, E, seed=8)
+    x = synth.gen_x(T, H, seed=9)
+    buf = _run_layer(fx, logits, x, True)
+    rc, ids, w, want = oracle.layer(logits, bf16_bits(x), k, 0, H, I, fx.all_blobs_now())
+    assert rc == 0
+    assert rel_l2(buf.out.cpu().numpy(), want) <= OUT_TOL
+    fx.layer.close()
+
+
 @pytest.mark.parametrize("out_fp32", [False, True])
 def test_layer_c0(out_fp32):
     c = synth.CONFIGS["c0"]
