@@ -79,7 +79,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=8000)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c1", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--config", default="c1", choices=["c1", "c2", "c3", "c4", "v1"])
     ap.add_argument("--batch", type=int, default=None, help="tokens per step (c2/c3: 8 or 32)")
     ap.add_argument("--skew", type=float, default=None, help="Zipf exponent for skewed routing")
     ap.add_argument("--layers", type=int, default=None, help="layers for c3")
@@ -207,6 +207,8 @@ def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
         if c.get("routing") == "zipf":
             perm = synth.zipf_permutation(E, synth.sub_seed(c["name"], "perm"))
             logits = synth.gen_logits_zipf(T, E, c.get("s", 1.1), perm, seed=synth.sub_seed(seed_tag, step))
+        elif c.get("routing") == "verify":
+            logits = synth.gen_logits_verify(T, E, seed=synth.sub_seed(seed_tag, step))
         else:
             logits = synth.gen_logits_uniform(T, E, seed=synth.sub_seed(seed_tag, step))
         x = synth.gen_x(T, H, seed=synth.sub_seed(seed_tag, "x", step))
@@ -273,7 +275,7 @@ def run_reference(args, budget_s: float = 150.0):
 def _config_json(c, args):
     return {"workload": f"{c['name']}: MoE layer H={c['H']} I={c['I']} E={c['E']} ({c['n_hot']} HBM / "
                         f"{c['n_cold']} pinned host) top-{c['k']}, {c['T']} token(s)/step, "
-                        f"{'Zipf s=%.2f' % c.get('s', 1.1) if c.get('routing') == 'zipf' else 'uniform'} routing"
+                        f"{'Zipf s=%.2f' % c.get('s', 1.1) if c.get('routing') == 'zipf' else ('verify-window (6 tokens of one sequence, correlated)' if c.get('routing') == 'verify' else 'uniform')} routing"
                         + (f", {c['layers']} layers sharing one slot scratch" if c.get("layers", 1) > 1 else ""),
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
             "residency": "off" if args.no_residency else ("every 16 steps, hysteresis 3.0, <=8 swaps, " + (
@@ -348,6 +350,8 @@ def gen_pool(c, layers, P, PL, dev):
             if c.get("routing") == "zipf":
                 lg = synth.gen_logits_zipf(T, E, c.get("s", 1.1), L["perm"],
                                            seed=synth.sub_seed(c["name"], "logits", li, p))
+            elif c.get("routing") == "verify":
+                lg = synth.gen_logits_verify(T, E, seed=synth.sub_seed(c["name"], "logits", li, p))
             else:
                 lg = synth.gen_logits_uniform(T, E, seed=synth.sub_seed(c["name"], "logits", li, p))
             per_layer.append((torch.from_numpy(lg).to(dev), xs[p % len(xs)][li], lg))

@@ -38,7 +38,17 @@ CONFIGS = {
     "c3": dict(H=4096, I=3072, E=384, n_hot=255, n_cold=129, k=6, T=1, routing="zipf", s=1.1, layers=20,
                swap_every=16),
     "c4": dict(H=4096, I=3072, E=384, n_hot=384, n_cold=0, k=6, T=8192, routing="uniform", layers=1),
+    # verify window: the k + 1 = 6 tokens a speculative step checks, from one
+    # sequence, with routing correlated so that the window picks about 3.7 times the
+    # distinct experts of one token
+    "v1": dict(H=4096, I=3072, E=384, n_hot=255, n_cold=129, k=6, T=6, routing="verify", layers=1),
 }
+
+VERIFY_WINDOW = 6
+# Strength of the shared per-sequence logit component: with E = 384 and k = 6 a
+# window of 6 tokens then picks 3.7x the distinct experts of one token (Monte Carlo;
+# 0 gives 5.8x, independent tokens).
+VERIFY_BETA = 1.42
 
 
 def sub_seed(*parts) -> int:
@@ -193,6 +203,18 @@ def gen_logits_zipf(T: int, E: int, s: float, perm: np.ndarray, seed: int) -> np
     u = np.clip(u, 1e-300, 1.0 - 1e-16)
     g = -np.log(-np.log(u))
     return (logp[None, :] + g).astype(np.float32)
+
+
+def gen_logits_verify(T: int, E: int, seed: int, window: int = VERIFY_WINDOW,
+                      beta: float = VERIFY_BETA) -> np.ndarray:
+    """Logits of verify windows: tokens t of window w = t // window get
+    N(0,1) + beta * b_w, with b_w ~ N(0,1) per expert shared by the window, so the
+    tokens of one sequence tend to pick the same experts."""
+    rng = np.random.default_rng(seed)
+    n_win = (T + window - 1) // window
+    b = rng.standard_normal((n_win, E))
+    z = rng.standard_normal((T, E))
+    return (z + beta * b[np.arange(T) // window]).astype(np.float32)
 
 
 def loc_identity(E: int, n_hot: int) -> np.ndarray:

@@ -419,6 +419,19 @@ def test_layer_c1_batch1(c1_layer):
         _gather_check(fx, logits, 1)
 
 
+@pytest.mark.parametrize("T", [6, 12])
+def test_layer_verify_window(c1_layer, T):
+    """Verify windows (6 tokens of one sequence with correlated routing) on the c1
+    layer: one and two windows, cold experts included."""
+    c = synth.CONFIGS["v1"]
+    fx = c1_layer
+    logits = synth.gen_logits_verify(T, c["E"], seed=synth.sub_seed("v1", "logits", T))
+    x = synth.gen_x(T, c["H"], seed=synth.sub_seed("v1", "x", T))
+    buf = _run_layer(fx, logits, x, False)
+    _compare_layer(fx, buf, logits, x, list(range(0, T, 3)), False)
+    _gather_check(fx, logits, T)
+
+
 @pytest.fixture(scope="module")
 def c2_layer():
     c = synth.CONFIGS["c2"]
