@@ -99,6 +99,10 @@ def parse():
                     help="keep a pinned host copy of every expert (residency moves bytes one way only); "
                          "default on for single-layer workloads")
     ap.add_argument("--no-mirror", dest="mirror", action="store_false")
+    ap.add_argument("--hysteresis", type=float, default=3.0, help="residency threshold ratio")
+    ap.add_argument("--swap-every", type=int, default=16, help="residency update interval in steps")
+    ap.add_argument("--max-swaps", type=int, default=8, help="swaps per residency update")
+    ap.add_argument("--n-hot", type=int, default=None, help="HBM-resident experts per layer (rest cold)")
     ap.add_argument("--zero-copy", action="store_true",
                     help="the FFN reads picked cold experts in place from host memory (no slot copy)")
     return ap.parse_args()
@@ -127,6 +131,10 @@ def workload(args):
     c["mirror"] = args.mirror if args.mirror is not None else (
         c.get("layers", 1) == 1 and c["n_cold"] > 0 and not args.no_residency)
     c["zero_copy"] = bool(args.zero_copy)
+    if args.n_hot is not None and args.experts is None:
+        c["n_hot"] = min(args.n_hot, c["E"])
+        c["n_cold"] = c["E"] - c["n_hot"]
+    c["hysteresis"], c["swap_every_steps"], c["max_swaps"] = args.hysteresis, args.swap_every, args.max_swaps
     return c
 
 
@@ -278,7 +286,8 @@ def _config_json(c, args):
                         f"{'Zipf s=%.2f' % c.get('s', 1.1) if c.get('routing') == 'zipf' else ('verify-window (6 tokens of one sequence, correlated)' if c.get('routing') == 'verify' else 'uniform')} routing"
                         + (f", {c['layers']} layers sharing one slot scratch" if c.get("layers", 1) > 1 else ""),
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
-            "residency": "off" if args.no_residency else ("every 16 steps, hysteresis 3.0, <=8 swaps, " + (
+            "residency": "off" if args.no_residency else (
+                "every %d steps, hysteresis %g, <=%d swaps, " % (c["swap_every_steps"], c["hysteresis"], c["max_swaps"]) + (
                 "host copy of every expert" if c.get("mirror") else "in-place HBM/host exchange")),
             "step_pool": (min(max(args.pool, args.steps + args.warmup), 2048)
                           if (not args.no_residency and c["n_cold"] > 0) else args.pool),
@@ -325,7 +334,8 @@ def build_layers(c, dev, seed_tag="bench"):
         n_host = E if mirror else n_cold
         layer = m.Layer(E=E, k=k, H=H, I=I, n_hot=n_hot, n_cold=n_cold, scratch=scratch,
                         hot_ptrs=[hot[h] for h in range(n_hot)], cold_ptrs=[cold[i] for i in range(n_host)],
-                        init_loc=loc, swap_every=0 if c.get("no_res") else 16, max_swaps=8, hysteresis=3.0,
+                        init_loc=loc, swap_every=0 if c.get("no_res") else c["swap_every_steps"],
+                        max_swaps=c["max_swaps"], hysteresis=c["hysteresis"],
                         host_mirror=mirror, zero_copy=bool(c.get("zero_copy")))
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
