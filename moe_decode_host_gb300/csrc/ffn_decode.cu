@@ -273,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             // ---------------- producers, zero copy (whole producer warp) ----------------
             const unsigned pp = (unsigned)(warp - kConsumers);
             const int rowb = K / 2;  // bytes of one weight row
-            const uint8_t* plane_off = nullptr;
             int slot = 0;
             unsigned phase = 0;
             int gstage = 0;
@@ -306,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 const TaskInfo ti = task_info(a, hd, task, tiles);
                 if (!ti.valid) continue;
                 const uint8_t* wbase = ti.blob + (P == 0 ? 0 : a.w2n);
-                (void)plane_off;
                 const int r0 = ti.rt * C::kTaskRows;
                 for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
                     for (int s = 0; s < nst && ok; ++s) {
