@@ -37,7 +37,7 @@ NCU_TRAFFIC = {
     "cold_copy": {"bytes_per_expert": (11520 + 15616) / 2,
                   "source": "profiles/cold_copy_kernel_c1_small.md"},
     # per distinct expert through the decode kernels (gate/up + down launches)
-    "ffn_decode": {"bytes_per_expert": (66932224 + 777984 + 33490688) / 5,
+    "ffn_decode": {"bytes_per_expert": (66931968 + 642560 + 33490432) / 5,
                    "source": "profiles/ffn_decode_kernel_c1_small.md"},
     # per expert through the tcgen05 kernels at about 128 tokens per expert
     "ffn_tc": {"bytes_per_expert": (935596288 + 92993792 + 483277568 + 112975360) / 64,
