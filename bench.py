@@ -143,6 +143,24 @@ def _rank_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(dist, value: float, device) -> float:
+    """The largest of every rank's value (the slowest replica's elapsed time); the
+    value itself on a single process."""
+    if not dist:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, steps: int, tokens_per_step: int, elapsed_ms: float) -> float:
+    """Whole-job tokens/s: every replica processes its own steps, timed by the
+    slowest replica."""
+    return world * steps * tokens_per_step / (elapsed_ms * 1e-3)
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -495,11 +513,8 @@ def run_ours(args):
     t_end.record(st)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
     if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
         dist.barrier()
     copy_ms = [L["layer"].profile_read(K) for L in layers]
     ffn_kern_ms = np.array([L["layer"].profile_read_ffn(K) for L in layers]).T  # [K, NL]
@@ -537,7 +552,7 @@ def run_ours(args):
     tstar_nom = np.maximum(hot_bytes / (HBM_NOMINAL_GBS * 1e9), gather_bytes / (lp * 1e9))
     tstar_meas = np.maximum(hot_bytes / (hbm_peak * 1e9), gather_bytes / (lp * 1e9))
     step_ms = elapsed_ms / K
-    value = world * K * T / (elapsed_ms * 1e-3)
+    value = job_rate(world, K, T, elapsed_ms)
     # dominant kernel: the one with the most GPU time over the timed region, the cold
     # copy (on the copy stream) or the FFN call's kernels (wait for the copy excluded)
     tot = {n: float(np.sum(per[n])) for n in names}
@@ -645,12 +660,8 @@ def run_e2e(args, c, layers, pool, bufs, dev, dist, world):
         step(i)
     e1.record(st)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": world * K * T / (ms * 1e-3), "unit": "tokens/s",
+    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    return {"value": job_rate(world, K, T, ms), "unit": "tokens/s",
             "h2d_bytes_per_step": NL * (T * E * 4 + T * H * 2), "d2h_bytes_per_step": NL * T * H * 2}
 
 
