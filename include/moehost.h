@@ -160,7 +160,9 @@ int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float
  *                ascending.
  *  n_cold_picked device int32 [1] out.
  * Every listed slot of the scratch is overwritten with the bytes of its host blob,
- * read zero-copy with 16-byte loads; unlisted slots are left as they were.
+ * read zero-copy with 16-byte loads; unlisted slots are left as they were.  With
+ * moe_params.zero_copy set and T <= 64 nothing is copied (moe_grouped_ffn reads the
+ * cold experts in place) and only the outputs above are produced.
  * phys_ids, cold_list and n_cold_picked are ready in `stream` order.  The byte
  * copy itself runs on the layer's own copy stream, forked from `stream` at this
  * call, so that moe_grouped_ffn can work on the experts in HBM while the link
@@ -188,7 +190,10 @@ int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes);
  *  y        device fp32 [T*k][H] out, row i = pick i.
  *  workspace device memory of at least moe_ffn_workspace_bytes(L, T) bytes,
  *           256-byte aligned; its contents are overwritten.
- * Each distinct expert's weights are streamed once per call.  Errors:
+ * Each distinct expert's weights are streamed once per call (with
+ * moe_params.zero_copy set and T <= 64, the picked cold experts' straight from their
+ * pinned host blobs, on the layer's copy stream, joined into `stream` before the
+ * call returns).  Errors:
  * MOE_ERR_INVALID_ARG (null, T < 0, workspace too small), MOE_ERR_CUDA. */
 int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
                     const int32_t* offsets, const int32_t* entries, float* y, void* workspace,
