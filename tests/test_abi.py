@@ -67,6 +67,11 @@ def test_host_side_argument_checks(mlib):
     bad = mlib.moe_params(16, 2, 256, 512, 12, 5, 0, 16, 8, 3.0)
     assert lib.moe_layer_create(ctypes.byref(bad), None, None, None, loc, ctypes.byref(out)) == \
         mlib.MOE_ERR_INVALID_ARG
+    for field, value in (("host_mirror", 2), ("zero_copy", 2), ("zero_copy", -1), ("renorm", 3)):
+        bad = mlib.moe_params(16, 2, 256, 512, 12, 4, 0, 16, 8, 3.0)
+        setattr(bad, field, value)
+        assert lib.moe_layer_create(ctypes.byref(bad), None, None, None, loc, ctypes.byref(out)) == \
+            mlib.MOE_ERR_INVALID_ARG, field
     # cold experts but no scratch
     assert lib.moe_layer_create(ctypes.byref(p), None, None, None, loc, ctypes.byref(out)) == \
         mlib.MOE_ERR_INVALID_ARG
