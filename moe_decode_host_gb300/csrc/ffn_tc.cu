@@ -232,10 +232,24 @@ __device__ __forceinline__ void tc_ld16x2(uint32_t ta, uint32_t tb, float (&va)[
     }
 }
 
-// Largest E8M0 exponent of a scale row (n bytes, n a multiple of 4).
+// Largest E8M0 exponent of a scale row (n bytes, n a multiple of 4). A 16-byte
+// aligned row is read eight 16-byte words at a time, all in flight together.
 __device__ __forceinline__ int row_max_exp(const uint8_t* srow, int n) {
     uint32_t m = 0;
-    for (int i = 0; i < n; i += 4) m = __vmaxu4(m, ld_u32(srow + i));
+    if (((n | (int)reinterpret_cast<uintptr_t>(srow)) & 15) == 0) {
+        for (int i = 0; i < n; i += 128) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int o = min(i + 16 * j, n - 16);  // past the row: reread its last word
+                v[j] = __ldg(reinterpret_cast<const uint4*>(srow + o));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = __vmaxu4(m, __vmaxu4(__vmaxu4(v[j].x, v[j].y), __vmaxu4(v[j].z, v[j].w)));
+        }
+    } else {
+        for (int i = 0; i < n; i += 4) m = __vmaxu4(m, ld_u32(srow + i));
+    }
     const uint32_t a = max(m & 0xffu, (m >> 8) & 0xffu), b = max((m >> 16) & 0xffu, m >> 24);
     return (int)max(a, b);
 }
@@ -582,7 +596,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) ffn_tc_kernel(FfnArgs a, const 
                 for (int st = 0; st < nst && ok; ++st) {
                     const int m = st % mats<P>();  // matrix of this stage (chunk st / mats)
                     const int sn = st + 1, cn = sn / mats<P>(), mn = sn % mats<P>();
-                    const uint32_t wnext = sn < nst ? ld_u32((mn ? sc1 : sc0) + 4 * cn) : 0u;
+                    // unconditional (the last stage rereads its own word): the value is
+                    // not needed before the next stage
+                    const uint32_t wnext = ld_u32((mn ? sc1 : sc0) + 4 * min(cn, nks - 1));
                     // the weight slot of stage gs was last read by the MMAs of stage gs - kAStages
                     const int as = gs % kAStages;
                     if (!warp_wait(&hd.raw_full[rs], rph, a, abort, 17, rs, st, task) ||
