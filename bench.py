@@ -213,17 +213,25 @@ class Clocks:
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
+ORACLE_TOKENS_PER_CALL = 8  # one oracle token of the 384-expert layer takes about two seconds
+
+
 def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
     """Times the CPU oracle on a bounded sample of the workload: whole tokens of
     the layer (route + every pick's expert FFN + combine), expert bytes drawn by the
-    seeded generator on the CPU.  Returns (tokens/s, tokens, seconds, sample text)."""
+    seeded generator on the CPU.  The oracle runs every pick on its own token, so
+    its time per token does not depend on the batch: each call takes the first
+    ORACLE_TOKENS_PER_CALL tokens of a seeded step of the workload (routing is per
+    token, so they route as they do in the whole step).  Returns (tokens/s, tokens,
+    seconds, sample text)."""
     import torch
 
     import oracle
     import synth
 
     H, I, E, k = c["H"], c["I"], c["E"], c["k"]
-    T = max(1, c["T"])
+    T_step = max(1, c["T"])
+    T = min(T_step, ORACLE_TOKENS_PER_CALL)
     oracle.build()
     tok = 0
     t_total = 0.0
@@ -232,13 +240,14 @@ def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
     while t_total < seconds or tok == 0:
         if c.get("routing") == "zipf":
             perm = synth.zipf_permutation(E, synth.sub_seed(c["name"], "perm"))
-            logits = synth.gen_logits_zipf(T, E, c.get("s", 1.1), perm, seed=synth.sub_seed(seed_tag, step))
+            logits = synth.gen_logits_zipf(T_step, E, c.get("s", 1.1), perm, seed=synth.sub_seed(seed_tag, step))
         elif c.get("routing") == "verify":
-            logits = synth.gen_logits_verify(T, E, seed=synth.sub_seed(seed_tag, step))
+            logits = synth.gen_logits_verify(T_step, E, seed=synth.sub_seed(seed_tag, step))
         else:
-            logits = synth.gen_logits_uniform(T, E, seed=synth.sub_seed(seed_tag, step))
-        x = synth.gen_x(T, H, seed=synth.sub_seed(seed_tag, "x", step))
-        bits = x.view(torch.int16).numpy().view(np.uint16)
+            logits = synth.gen_logits_uniform(T_step, E, seed=synth.sub_seed(seed_tag, step))
+        x = synth.gen_x(T_step, H, seed=synth.sub_seed(seed_tag, "x", step))
+        logits = np.ascontiguousarray(logits[:T])
+        bits = np.ascontiguousarray(x[:T].view(torch.int16).numpy().view(np.uint16))
         # expert bytes are generated outside the timed region (they are inputs)
         _, ids, _, _, _, _ = oracle.route(logits, k)
         blobs = []
@@ -258,8 +267,8 @@ def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
         step += 1
         if len(blob_cache) > 64:
             blob_cache.clear()
-    sample = (f"{tok} token(s) of the {c['name']} layer (T={T} per step, {step} step(s)): route, {k} expert "
-              f"FFNs per token, combine; single-threaded C oracle, fp64")
+    sample = (f"{tok} token(s) of the {c['name']} layer (the first {T} of a {T_step}-token step, {step} "
+              f"step(s)): route, {k} expert FFNs per token, combine; single-threaded C oracle, fp64")
     return tok / t_total, tok, t_total, sample
 
 
@@ -285,7 +294,8 @@ def run_reference(args, budget_s: float = 150.0):
     total = sum(t_steps)
     value = tok_total / total
     n = len(t_steps)
-    sample = (f"{n} step(s) of {c['T']} token(s) of the {c['name']} layer (of {args.steps} requested; capped "
+    sample = (f"{n} step(s) of {min(max(1, c['T']), ORACLE_TOKENS_PER_CALL)} token(s) (the first of each "
+              f"{c['T']}-token step) of the {c['name']} layer (of {args.steps} requested; capped "
               f"at {budget_s:.0f} s of oracle time): route, {c['k']} expert FFNs per token, combine; "
               f"single-threaded C oracle, fp64")
     line = {"impl": "reference", "metric": "MoE layer tokens/s (decode)", "value": value, "unit": "tokens/s",

@@ -339,6 +339,7 @@ def _assigned_logits(counts, E, seed):
     (256, 512, 16, 12, 2, 1024, "uniform"),  # ~128 tokens per expert, four of them cold
     (256, 256, 4, 4, 2, 600, "uniform"),     # ~300 per expert: two column passes (192 + rest)
     (384, 640, 40, 30, 5, 600, "zipf1.5"),   # buckets on both sides of 64, uneven K
+    (512, 1536, 16, 12, 2, 1024, "uniform"),  # 16-byte scale rows: one group of 4 chunks, then three
 ])
 def test_layer_prefill_buckets(H, I, E, n_hot, k, T, dist):
     n_cold = E - n_hot
