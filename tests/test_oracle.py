@@ -347,6 +347,41 @@ def test_combine_identical_experts():
         np.testing.assert_allclose(out[t], w[t].sum() * y[t], rtol=1e-12, atol=1e-12 * np.abs(y).max())
 
 
+@pytest.mark.parametrize("renorm", [0, 1])
+def test_layer_distinct_experts_tagged_by_powers_of_two(renorm):
+    """Expert e is one base expert with every down-projection scale byte raised by
+    e, so its output is exactly 2^e times the base output: the layer's result then
+    names which experts each token used and with which weights. Picks come from a
+    descending stable sort of the logits, weights from the softmax closed form."""
+    H, I, E, k, T = 128, 256, 8, 3, 5
+    sec = oracle.blob_offsets(H, I)
+    base = synth.gen_blobs(1, H, I, seed=31)[0].numpy()
+    blobs = []
+    for e in range(E):
+        b = base.copy()
+        b[sec["w2s"]:] += e
+        blobs.append(b)
+    rng = np.random.default_rng(15)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    x = synth.gen_x(T, H, seed=6)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    y = oracle.expert_ffn(base, H, I, oracle.bf16_bits_to_f64(bits))
+    rc, ids, w, out = oracle.layer(logits, bits, k, renorm, H, I, blobs)
+    assert rc == 0
+    want_ids = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
+    assert np.array_equal(ids, want_ids)
+    l64 = logits.astype(np.float64)
+    p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    want_w = np.take_along_axis(p, want_ids, axis=1)
+    if renorm:
+        want_w /= want_w.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(w, want_w, rtol=1e-13)
+    tag = np.exp2(want_ids.astype(np.float64))
+    want = (want_w * tag).sum(axis=1, keepdims=True) * y
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
 # ---------------------------------------------------------------- residency
 
 def test_residency_hand_derived():
