@@ -202,7 +202,7 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
 /* moe_grouped_ffn for callers that cannot allocate device memory (an engine that
  * has given all free HBM to its own pools and forbids later allocations, code
  * running during a global-mode stream capture, embedders with their own
- * allocator).  No counterpart in the paper: same arguments and results as
+ * allocator).  No counterpart in the published method: same arguments and results as
  * moe_grouped_ffn minus the workspace, which here is a fixed array of
  * MOE_NOALLOC_SCRATCH_BYTES inside the library's device image (every GPU that
  * loads the library holds one copy until the process exits).  The call

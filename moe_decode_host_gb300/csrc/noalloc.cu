@@ -7,7 +7,7 @@
 // allocation calls are not permitted; or embedders whose allocator is not CUDA's.
 // moe_grouped_ffn_noalloc gives them the same FFN with its workspace in a
 // fixed-size array that lives in the library's own device image, so the call
-// allocates nothing.  The paper has no counterpart of this entry point.
+// allocates nothing.  The method as published has no counterpart of this entry point.
 #include <mutex>
 
 #include "internal.cuh"

@@ -262,7 +262,7 @@ def _blob(H, I, w13_codes, w13_sc, w2_codes, w2_sc):
     return np.concatenate([n13.ravel(), s13.ravel(), n2.ravel(), s2.ravel()])
 
 
-def test_blob_size_matches_survey_bytes():
+def test_blob_size_matches_hand_computed_bytes():
     # 3*H*I nibbles plus one scale byte per 32 elements
     assert oracle.blob_offsets(256, 512)["total"] == 208896
     assert oracle.blob_offsets(4096, 3072)["total"] == 20054016
