@@ -243,6 +243,22 @@ int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* 
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_INJECTED (test hook). */
 int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream);
 
+/* The plan one acting residency_update applies, computed on the host with no
+ * device work (callable without a GPU): the same ranking, pairing and stopping
+ * rule, from a window's pick counts and a placement.
+ *  counts    host int32 [E], each >= 0.
+ *  loc       host int32 [E]: a placement (a permutation of 0..E-1; values below
+ *            n_hot are HBM slots).
+ *  loc_out   host int32 [E] out: the placement after the swaps (may equal loc).
+ *  promoted, demoted  host int32 [max_swaps] out (may be NULL when max_swaps is
+ *            0): pair i moved promoted[i] into demoted[i]'s HBM slot and
+ *            demoted[i] into promoted[i]'s cold slot.
+ *  1 <= E <= 1024, 0 <= n_hot <= E, 0 <= max_swaps <= 64, hysteresis finite >= 0.
+ * Returns the number of swaps (>= 0), or MOE_ERR_INVALID_ARG (bad sizes, a
+ * negative count, or loc not a permutation). */
+int moe_residency_plan(const int32_t* counts, const int32_t* loc, int E, int n_hot, int max_swaps, float hysteresis,
+                       int32_t* loc_out, int32_t* promoted, int32_t* demoted);
+
 /* Copies the placement map to host int32 [E] (synchronous). */
 int moe_layer_get_loc(moe_layer* L, int32_t* loc_host);
 

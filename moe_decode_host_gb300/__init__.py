@@ -19,7 +19,7 @@ __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_by
            "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
            "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED", "MOE_ERR_SCRATCH_TOO_SMALL",
-           "moe_grouped_ffn_noalloc"]
+           "moe_grouped_ffn_noalloc", "residency_plan"]
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -172,6 +172,22 @@ def residency_update(layer: Layer, stream=None) -> int:
     n = ctypes.c_int32()
     check(lib.residency_update(layer.handle, ctypes.byref(n), stream_handle(stream)), "residency_update")
     return int(n.value)
+
+
+def residency_plan(counts, loc, n_hot: int, max_swaps: int, hysteresis: float):
+    """The swaps one acting residency_update would make (host only, no GPU):
+    returns (loc after the swaps, promoted experts, demoted experts)."""
+    counts = np.ascontiguousarray(counts, dtype=np.int32)
+    loc = np.ascontiguousarray(loc, dtype=np.int32)
+    E = int(counts.size)
+    out = np.empty(E, np.int32)
+    pro = np.empty(max(1, max_swaps), np.int32)
+    dem = np.empty(max(1, max_swaps), np.int32)
+    n = lib.moe_residency_plan(ptr(counts), ptr(loc), E, n_hot, max_swaps, float(hysteresis), ptr(out), ptr(pro),
+                               ptr(dem))
+    if n < 0:
+        check(n, "moe_residency_plan")
+    return out, pro[:n].copy(), dem[:n].copy()
 
 
 def link_probe(src_host, dst_dev, nbytes, ctas=0, stream=None):

@@ -478,6 +478,53 @@ int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* 
     return cuda_status(launch_combine(y, topk_w, T, k, H, out, out_fp32, S(stream)));
 }
 
+// The ranking and pairing of one acting residency update, on the host: cold
+// experts picked at least once (count desc, id asc) against hot experts (count
+// asc, id asc); pair i swaps while count(cold) > hysteresis * count(hot), at most
+// max_swaps pairs, stopping at the first pair that fails. loc_out is the placement
+// after the swaps; promoted[i] takes demoted[i]'s HBM slot and demoted[i] takes
+// promoted[i]'s cold slot. Returns the number of swaps.
+static int plan_residency(const int32_t* cnt, const int32_t* loc, int E, int n_hot, int max_swaps, float hysteresis,
+                          int32_t* loc_out, int32_t* promoted, int32_t* demoted) {
+    std::vector<int> cold, hot;
+    for (int e = 0; e < E; ++e) {
+        if (loc[e] >= n_hot) {
+            if (cnt[e] >= 1) cold.push_back(e);
+        } else {
+            hot.push_back(e);
+        }
+    }
+    std::sort(cold.begin(), cold.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] > cnt[b] : a < b; });
+    std::sort(hot.begin(), hot.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] < cnt[b] : a < b; });
+    const size_t lim = std::min({(size_t)max_swaps, cold.size(), hot.size()});
+    std::vector<int32_t> next(loc, loc + E);
+    int n = 0;
+    for (size_t i = 0; i < lim; ++i) {
+        const int a = cold[i], b = hot[i];
+        if (!((double)cnt[a] > (double)hysteresis * (double)cnt[b])) break;
+        promoted[n] = a;
+        demoted[n] = b;
+        ++n;
+        std::swap(next[a], next[b]);
+    }
+    std::memcpy(loc_out, next.data(), sizeof(int32_t) * (size_t)E);
+    return n;
+}
+
+int moe_residency_plan(const int32_t* counts, const int32_t* loc, int E, int n_hot, int max_swaps, float hysteresis,
+                       int32_t* loc_out, int32_t* promoted, int32_t* demoted) {
+    if (!counts || !loc || !loc_out || E < 1 || E > 1024 || n_hot < 0 || n_hot > E || max_swaps < 0 ||
+        max_swaps > kMaxSwaps || !(hysteresis >= 0.0f) || hysteresis > 1e30f)
+        return MOE_ERR_INVALID_ARG;
+    if (max_swaps > 0 && (!promoted || !demoted)) return MOE_ERR_INVALID_ARG;
+    std::vector<char> seen(E, 0);
+    for (int e = 0; e < E; ++e) {
+        if (counts[e] < 0 || loc[e] < 0 || loc[e] >= E || seen[loc[e]]) return MOE_ERR_INVALID_ARG;
+        seen[loc[e]] = 1;
+    }
+    return plan_residency(counts, loc, E, n_hot, max_swaps, hysteresis, loc_out, promoted, demoted);
+}
+
 int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
     if (!L || !n_swaps_out) return MOE_ERR_INVALID_ARG;
     *n_swaps_out = 0;
@@ -497,28 +544,18 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
                               cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    const int32_t* cnt = L->h_counts;
-    // candidates: picked cold experts (count desc, id asc), hot experts (count asc, id asc)
-    std::vector<int> cold, hot;
-    for (int e = 0; e < p.E; ++e) {
-        if (L->loc[e] >= p.n_hot) {
-            if (cnt[e] >= 1) cold.push_back(e);
-        } else {
-            hot.push_back(e);
-        }
-    }
-    std::sort(cold.begin(), cold.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] > cnt[b] : a < b; });
-    std::sort(hot.begin(), hot.end(), [&](int a, int b) { return cnt[a] != cnt[b] ? cnt[a] < cnt[b] : a < b; });
-    const size_t lim = std::min({(size_t)p.max_swaps, cold.size(), hot.size()});
+    int32_t promoted[kMaxSwaps], demoted[kMaxSwaps];
+    std::vector<int32_t> loc(p.E);
+    const int n_plan = plan_residency(L->h_counts, L->loc.data(), p.E, p.n_hot, p.max_swaps, p.hysteresis, loc.data(),
+                                      promoted, demoted);
     SwapList sw;
     sw.n = 0;
-    std::vector<int32_t> loc = L->loc;
     std::vector<int> moved_slots;  // host_mirror: cold slots whose expert changes
-    for (size_t i = 0; i < lim; ++i) {
-        const int a = cold[i], b = hot[i];
-        if (!((double)cnt[a] > (double)p.hysteresis * (double)cnt[b])) break;
-        const int slot_h = loc[b];             // HBM slot of the demoted expert
-        const int slot_c = loc[a] - p.n_hot;   // cold slot of the promoted expert
+    for (int i = 0; i < n_plan; ++i) {
+        // every expert is in at most one pair, so the old map gives both slots
+        const int a = promoted[i], b = demoted[i];
+        const int slot_h = L->loc[b];            // HBM slot of the demoted expert
+        const int slot_c = L->loc[a] - p.n_hot;  // cold slot of the promoted expert
         sw.hot[sw.n] = L->hot[slot_h];
         if (p.host_mirror) {
             // promote from the scratch slot if this layer's copy of the expert is still
@@ -531,7 +568,6 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
             sw.host[sw.n] = L->cold_dev[slot_c];
         }
         ++sw.n;
-        std::swap(loc[a], loc[b]);
     }
     if (sw.n > 0) {
         err = p.host_mirror ? launch_copy_list(sw, L->lay.total, L->sm_count, st)

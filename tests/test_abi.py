@@ -91,3 +91,63 @@ def test_package_has_no_oracle_dependency():
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "moe_oracle" not in src, f
+
+
+def _random_window(rng, E, n_hot):
+    loc = rng.permutation(E).astype("int32")
+    kind = rng.integers(0, 3)
+    if kind == 0:    # sparse window: most experts unpicked, small counts (many ties)
+        counts = rng.binomial(3, 0.15, E)
+    elif kind == 1:  # skewed window
+        counts = rng.zipf(1.5, E).clip(max=200) - 1
+    else:            # counts on the hysteresis boundary: cold = 3 x hot exactly
+        counts = rng.integers(0, 4, E) * rng.choice([1, 3], E)
+    return counts.astype("int32"), loc
+
+
+def test_residency_plan_matches_the_oracle_on_random_windows(mlib):
+    """The library's host planner (the one residency_update applies) against the
+    oracle's residency rule: identical placements and swap lists, bit for bit."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(2024)
+    cases = 0
+    for _ in range(400):
+        E = int(rng.choice([8, 16, 64, 384]))
+        n_hot = int(rng.integers(0, E + 1))
+        max_swaps = int(rng.choice([0, 1, 2, 8, 64]))
+        hyst = float(rng.choice([0.0, 1.5, 3.0, 6.0]))
+        counts, loc = _random_window(rng, E, n_hot)
+        got_loc, got_pro, got_dem = mlib.residency_plan(counts, loc, n_hot, max_swaps, hyst)
+        want_loc, want_pro, want_dem = oracle.residency(counts, loc, n_hot, max_swaps, hyst)
+        assert np.array_equal(got_loc, want_loc)
+        assert np.array_equal(got_pro, want_pro) and np.array_equal(got_dem, want_dem)
+        cases += int(got_pro.size > 0)
+    assert cases > 100  # most windows make at least one swap
+
+
+def test_residency_plan_rejects_bad_input(mlib):
+    import numpy as np
+
+    lib = mlib.lib
+    ok_counts = np.zeros(8, np.int32)
+    out = np.empty(8, np.int32)
+    pro = np.empty(8, np.int32)
+    dem = np.empty(8, np.int32)
+    P = mlib._lib.ptr
+
+    def plan(counts, loc, n_hot=4, max_swaps=8, hyst=3.0):
+        return lib.moe_residency_plan(P(counts), P(loc), counts.size, n_hot, max_swaps, hyst, P(out), P(pro), P(dem))
+
+    assert plan(ok_counts, np.arange(8, dtype=np.int32)) == 0
+    assert plan(ok_counts, np.array([0, 1, 2, 3, 4, 5, 6, 6], np.int32)) == mlib.MOE_ERR_INVALID_ARG  # not a permutation
+    assert plan(ok_counts, np.array([0, 1, 2, 3, 4, 5, 6, 8], np.int32)) == mlib.MOE_ERR_INVALID_ARG  # out of range
+    bad = ok_counts.copy()
+    bad[3] = -1
+    assert plan(bad, np.arange(8, dtype=np.int32)) == mlib.MOE_ERR_INVALID_ARG
+    assert plan(ok_counts, np.arange(8, dtype=np.int32), n_hot=9) == mlib.MOE_ERR_INVALID_ARG
+    assert plan(ok_counts, np.arange(8, dtype=np.int32), max_swaps=65) == mlib.MOE_ERR_INVALID_ARG
+    assert plan(ok_counts, np.arange(8, dtype=np.int32), hyst=float("nan")) == mlib.MOE_ERR_INVALID_ARG
+    assert plan(ok_counts, np.arange(8, dtype=np.int32), hyst=-1.0) == mlib.MOE_ERR_INVALID_ARG
