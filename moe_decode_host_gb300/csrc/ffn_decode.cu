@@ -763,14 +763,10 @@ size_t smem_bytes() {
 
 template <int P, int NT, bool ZC>
 cudaError_t launch_phase(const FfnArgs& a, int lo, int hi, int sel, int ctr, int grid, cudaStream_t st) {
-    static bool configured = false;
+    static std::atomic<uint64_t> configured{0};
     const size_t sm = smem_bytes<P, NT>();
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_tma_kernel<P, NT, ZC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sm);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = ensure_smem_limit((const void*)ffn_tma_kernel<P, NT, ZC>, (int)sm, configured);
+    if (e != cudaSuccess) return e;
     // the stage's activation slice: 256 elements of 8 * NT consecutive bucket rows
     CUtensorMap act_map;
     if (!encode_act_map(&act_map, a, P, 256, 8 * NT, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;

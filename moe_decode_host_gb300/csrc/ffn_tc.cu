@@ -788,15 +788,10 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kBM);
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);
     if (grid <= 0) return cudaSuccess;
-    static bool configured[2] = {false, false};
-    if (!configured[phase]) {
-        err = phase == 0 ? cudaFuncSetAttribute(ffn_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kTcSmem)
-                         : cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)kTcSmem);
-        if (err != cudaSuccess) return err;
-        configured[phase] = true;
-    }
+    static std::atomic<uint64_t> configured[2];
+    err = ensure_smem_limit(phase == 0 ? (const void*)ffn_tc_kernel<0> : (const void*)ffn_tc_kernel<1>, (int)kTcSmem,
+                            configured[phase]);
+    if (err != cudaSuccess) return err;
     // task counters 12-15 of the call's workspace (zeroed by the gate/up prescale
     // kernel): one per phase and placement class
     const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;

@@ -7,11 +7,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moehost.h"
 
 namespace moe {
 
 constexpr int kMaxSwaps = 64;
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device (the
+// attribute belongs to the device the calling thread has current): `done` holds
+// one bit per device ordinal below 64; higher ordinals set it on every call.
+// Setting it twice is harmless, so racing first calls need no lock.
+inline cudaError_t ensure_smem_limit(const void* kernel, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Launches `kernel` so that it may start while the previous kernel on the stream
 // finishes (programmatic dependent launch); the kernel waits with grid_dep_wait
