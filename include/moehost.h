@@ -294,7 +294,7 @@ int moe_layer_set_copy_ctas(moe_layer* L, int ctas);
  * durations in ms to host float copy_ms[] and their number to *n_out.
  * moe_layer_profile_read_ffn does the same for the FFN calls: each duration is the
  * call's kernel time without the wait for the cold copy (start to the join, plus
- * the join to the end). */
+ * the join to the end).  0 <= n <= 2^20, else MOE_ERR_INVALID_ARG. */
 int moe_layer_profile(moe_layer* L, int max_records);
 int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out);
 int moe_layer_profile_read_ffn(moe_layer* L, float* ffn_ms, int max, int* n_out);

@@ -649,7 +649,7 @@ int moe_layer_set_copy_ctas(moe_layer* L, int ctas) {
 }
 
 int moe_layer_profile(moe_layer* L, int max_records) {
-    if (!L || max_records < 0) return MOE_ERR_INVALID_ARG;
+    if (!L || max_records < 0 || max_records > (1 << 20)) return MOE_ERR_INVALID_ARG;
     if (L->copy_stream && cudaStreamSynchronize(L->copy_stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
     free_prof(L);
