@@ -59,10 +59,16 @@ def _load():
             lib.or_remap.argtypes = [P, I, P, I, I, P, P]
             lib.or_expert_ffn.restype = None
             lib.or_expert_ffn.argtypes = [P, I, I, P, I, P]
+            lib.or_expert_ffn_act4.restype = None
+            lib.or_expert_ffn_act4.argtypes = [P, I, I, P, I, P]
+            lib.or_quant_mxfp4.restype = None
+            lib.or_quant_mxfp4.argtypes = [P, I, P, P]
             lib.or_combine.restype = None
             lib.or_combine.argtypes = [P, P, I, I, I, P]
             lib.or_layer.restype = I
             lib.or_layer.argtypes = [P, P, I, I, I, I, I, I, P, P, P, P]
+            lib.or_layer_act4.restype = I
+            lib.or_layer_act4.argtypes = [P, P, I, I, I, I, I, I, P, P, P, P]
             lib.or_residency.restype = I
             lib.or_residency.argtypes = [P, P, I, I, I, D, P, P]
             lib.or_fnv1a64.restype = ctypes.c_uint64
@@ -142,14 +148,29 @@ def remap(ids: np.ndarray, loc: np.ndarray, n_hot: int, n_cold: int):
     return phys, cold[:n].copy()
 
 
-def expert_ffn(blob: np.ndarray, H: int, I: int, x: np.ndarray) -> np.ndarray:
-    """x: [n_tok, H] (any float dtype; converted to double).  Returns y [n_tok, H] double."""
+def expert_ffn(blob: np.ndarray, H: int, I: int, x: np.ndarray, act4: bool = False) -> np.ndarray:
+    """x: [n_tok, H] (any float dtype; converted to double).  Returns y [n_tok, H] double.
+    act4: the all-FP4 mode (x and h quantised to MXFP4 per token, 32-element blocks)."""
     blob = _c(blob, np.uint8)
     x = _c(np.atleast_2d(x), np.float64)
     n = x.shape[0]
     y = np.zeros((n, H), dtype=np.float64)
-    _load().or_expert_ffn(_p(blob), H, I, _p(x), n, _p(y))
+    fn = _load().or_expert_ffn_act4 if act4 else _load().or_expert_ffn
+    fn(_p(blob), H, I, _p(x), n, _p(y))
     return y
+
+
+def quant_mxfp4(v: np.ndarray):
+    """MXFP4 quantisation of a row of K values (K a multiple of 32) by the OCP rule:
+    returns (nibble bytes [K/2] in the documented row layout, scale bytes [K/32])."""
+    v = _c(np.ravel(v), np.float64)
+    K = v.size
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nib = np.zeros(K // 2, dtype=np.uint8)
+    sc = np.zeros(K // 32, dtype=np.uint8)
+    _load().or_quant_mxfp4(_p(v), K, _p(nib), _p(sc))
+    return nib, sc
 
 
 def combine(y: np.ndarray, w: np.ndarray, k: int) -> np.ndarray:
@@ -162,8 +183,10 @@ def combine(y: np.ndarray, w: np.ndarray, k: int) -> np.ndarray:
     return out
 
 
-def layer(logits: np.ndarray, x_bf16_bits: np.ndarray, k: int, renorm: int, H: int, I: int, blobs: list):
-    """Whole layer. blobs[e] = expert e's bytes (numpy uint8).  Returns (rc, ids, w, out)."""
+def layer(logits: np.ndarray, x_bf16_bits: np.ndarray, k: int, renorm: int, H: int, I: int, blobs: list,
+          act4: bool = False):
+    """Whole layer. blobs[e] = expert e's bytes (numpy uint8).  Returns (rc, ids, w, out).
+    act4: the all-FP4 mode for every pick (see expert_ffn)."""
     logits = _c(logits, np.float32)
     x = _c(x_bf16_bits, np.uint16)
     T, E = logits.shape
@@ -172,7 +195,8 @@ def layer(logits: np.ndarray, x_bf16_bits: np.ndarray, k: int, renorm: int, H: i
     ids = np.zeros((T, k), dtype=np.int32)
     w = np.zeros((T, k), dtype=np.float64)
     out = np.zeros((T, H), dtype=np.float64)
-    rc = _load().or_layer(_p(logits), _p(x), T, E, k, renorm, H, I, ptrs, _p(ids), _p(w), _p(out))
+    fn = _load().or_layer_act4 if act4 else _load().or_layer
+    rc = fn(_p(logits), _p(x), T, E, k, renorm, H, I, ptrs, _p(ids), _p(w), _p(out))
     return rc, ids, w, out
 
 

@@ -39,6 +39,11 @@
  *                               published default).
  *   byte audit fingerprint   -- same page, section 4 (fingerprint every expert at
  *                               boot, re-check wherever it now lives); FNV-1a 64.
+ *   MXFP4 activations        -- the all-FP4 prefill mode (FP4 x FP4 tensor-core
+ *                               products need both operands in MXFP4): x and h are
+ *                               quantised per 32-element block by the OCP
+ *                               Microscaling conversion rule and used at their
+ *                               decoded values.
  *
  * Weight format (the library's documented format, restated here on its own):
  *   An expert blob is four planes, back to back:
@@ -84,6 +89,65 @@ unsigned or_nibble_at(const uint8_t* row, int k) {
 void or_decode_row(const uint8_t* nib_row, const uint8_t* scale_row, int K, double* out) {
     for (int k = 0; k < K; ++k)
         out[k] = or_e2m1(or_nibble_at(nib_row, k)) * or_e8m0(scale_row[k / 32]);
+}
+
+/* ---- MXFP4 quantisation (all-FP4 mode) ---------------------------------------
+ *
+ * One block of 32 values v: with amax = max |v|, the shared exponent is
+ * floor(log2(amax)) - 2 (2 = the exponent of E2M1's largest value, 6 = 1.5 * 2^2),
+ * clamped to the E8M0 range [-127, 127]; the scale byte is that exponent + 127.
+ * Element i is |v_i| / 2^exp rounded to the nearest E2M1 magnitude
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}, a tie going to the even code (mantissa bit 0),
+ * anything above 6 saturating to 6; the sign bit is v_i's (so -0 and negative
+ * values that round to zero give code 8).  An all-zero block gets exponent -127.
+ */
+static const double or_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* E2M1 code (sign bit clear) of magnitude r >= 0 by the rule above. */
+static unsigned or_e2m1_round(double r) {
+    if (r >= 6.0) return 7u;
+    unsigned best = 0u;
+    for (unsigned c = 1u; c < 8u; ++c) {
+        const double dc = fabs(or_e2m1_mag[c] - r), db = fabs(or_e2m1_mag[best] - r);
+        if (dc < db || (dc == db && (c & 1u) == 0u)) best = c;
+    }
+    return best;
+}
+
+/* Quantise K values (K a multiple of 32) into the documented row layout: K/2
+ * nibble bytes (element k in byte k/2, low nibble when k is even) and K/32
+ * scale bytes. */
+void or_quant_mxfp4(const double* v, int K, uint8_t* nib, uint8_t* scale) {
+    memset(nib, 0, (size_t)K / 2);
+    for (int b = 0; b < K / 32; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(v[32 * b + i]));
+        int ex = -127;
+        if (amax > 0.0) {
+            int fe;
+            frexp(amax, &fe); /* amax = f * 2^fe, f in [0.5, 1): floor(log2 amax) = fe - 1 */
+            ex = fe - 1 - 2;
+            if (ex < -127) ex = -127;
+            if (ex > 127) ex = 127;
+        }
+        scale[b] = (uint8_t)(ex + 127);
+        for (int i = 0; i < 32; ++i) {
+            const int k = 32 * b + i;
+            unsigned code = or_e2m1_round(ldexp(fabs(v[k]), -ex));
+            if (signbit(v[k])) code |= 8u;
+            nib[k / 2] |= (uint8_t)((k % 2 == 0) ? code : (code << 4));
+        }
+    }
+}
+
+/* v <- its MXFP4 quantisation, decoded (K a multiple of 32). */
+static void or_quant_dequant(double* v, int K) {
+    uint8_t* nib = (uint8_t*)malloc((size_t)K / 2);
+    uint8_t* sc = (uint8_t*)malloc((size_t)K / 32);
+    or_quant_mxfp4(v, K, nib, sc);
+    or_decode_row(nib, sc, K, v);
+    free(nib);
+    free(sc);
 }
 
 /* Plane offsets of an expert blob, in bytes. */
@@ -197,12 +261,20 @@ void or_gather(uint8_t* const* slots, const uint8_t* const* host, const int32_t*
  *   y = W2 h                       (w2 is [H rows][I columns])
  * Dot products run in index order.
  */
-void or_expert_ffn(const uint8_t* blob, int H, int I, const double* x, int n_tok, double* y) {
+/* act4 = 1: the all-FP4 mode -- each token's x row is quantised to MXFP4 (blocks
+ * along H) and each token's h row (blocks along I) before it meets W2. */
+static void or_expert_ffn_mode(const uint8_t* blob, int H, int I, const double* x_in, int n_tok, double* y,
+                               int act4) {
     size_t o13n, o13s, o2n, o2s, tot;
     or_blob_offsets(H, I, &o13n, &o13s, &o2n, &o2s, &tot);
     double* row = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
     double* row2 = (double*)malloc(sizeof(double) * (size_t)H);
     double* h = (double*)malloc(sizeof(double) * (size_t)n_tok * I);
+    double* xq = (double*)malloc(sizeof(double) * (size_t)n_tok * H);
+    memcpy(xq, x_in, sizeof(double) * (size_t)n_tok * H);
+    if (act4)
+        for (int t = 0; t < n_tok; ++t) or_quant_dequant(xq + (size_t)t * H, H);
+    const double* x = xq;
     for (int r = 0; r < I; ++r) {
         or_decode_row(blob + o13n + (size_t)r * (H / 2), blob + o13s + (size_t)r * (H / 32), H, row);
         or_decode_row(blob + o13n + (size_t)(I + r) * (H / 2), blob + o13s + (size_t)(I + r) * (H / 32), H, row2);
@@ -215,6 +287,8 @@ void or_expert_ffn(const uint8_t* blob, int H, int I, const double* x, int n_tok
             h[(size_t)t * I + r] = g / (1.0 + exp(-g)) * u;
         }
     }
+    if (act4)
+        for (int t = 0; t < n_tok; ++t) or_quant_dequant(h + (size_t)t * I, I);
     for (int r = 0; r < H; ++r) {
         or_decode_row(blob + o2n + (size_t)r * (I / 2), blob + o2s + (size_t)r * (I / 32), I, row);
         for (int t = 0; t < n_tok; ++t) {
@@ -226,6 +300,15 @@ void or_expert_ffn(const uint8_t* blob, int H, int I, const double* x, int n_tok
     free(row);
     free(row2);
     free(h);
+    free(xq);
+}
+
+void or_expert_ffn(const uint8_t* blob, int H, int I, const double* x, int n_tok, double* y) {
+    or_expert_ffn_mode(blob, H, I, x, n_tok, y, 0);
+}
+
+void or_expert_ffn_act4(const uint8_t* blob, int H, int I, const double* x, int n_tok, double* y) {
+    or_expert_ffn_mode(blob, H, I, x, n_tok, y, 1);
 }
 
 /* out[t][c] = sum over j = 0..k-1 (in order) of w[t][j] * y[t*k + j][c]. */
@@ -243,8 +326,8 @@ void or_combine(const double* y, const double* w, int T, int k, int H, double* o
  * (blobs[e] points at expert e's bytes, wherever they live), then combine.
  * x_bf16: [T][H] bf16 bits.  Outputs ids/w/out; y is scratch [T*k][H].
  */
-int or_layer(const float* logits, const uint16_t* x_bf16, int T, int E, int k, int renorm, int H, int I,
-             const uint8_t* const* blobs, int32_t* ids, double* w, double* out) {
+static int or_layer_mode(const float* logits, const uint16_t* x_bf16, int T, int E, int k, int renorm, int H, int I,
+                         const uint8_t* const* blobs, int32_t* ids, double* w, double* out, int act4) {
     int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
     int32_t* offsets = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
     int32_t* entries = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T * k > 0 ? T * k : 1));
@@ -258,11 +341,22 @@ int or_layer(const float* logits, const uint16_t* x_bf16, int T, int E, int k, i
     for (int t = 0; t < T; ++t) {
         for (int c = 0; c < H; ++c) x[c] = or_bf16(x_bf16[(size_t)t * H + c]);
         for (int j = 0; j < k; ++j)
-            or_expert_ffn(blobs[ids[(size_t)t * k + j]], H, I, x, 1, y + ((size_t)t * k + j) * H);
+            or_expert_ffn_mode(blobs[ids[(size_t)t * k + j]], H, I, x, 1, y + ((size_t)t * k + j) * H, act4);
     }
     or_combine(y, w, T, k, H, out);
     free(x); free(y); free(counts); free(offsets); free(entries);
     return OR_OK;
+}
+
+int or_layer(const float* logits, const uint16_t* x_bf16, int T, int E, int k, int renorm, int H, int I,
+             const uint8_t* const* blobs, int32_t* ids, double* w, double* out) {
+    return or_layer_mode(logits, x_bf16, T, E, k, renorm, H, I, blobs, ids, w, out, 0);
+}
+
+/* The whole layer in the all-FP4 mode (or_expert_ffn_act4 for every pick). */
+int or_layer_act4(const float* logits, const uint16_t* x_bf16, int T, int E, int k, int renorm, int H, int I,
+                  const uint8_t* const* blobs, int32_t* ids, double* w, double* out) {
+    return or_layer_mode(logits, x_bf16, T, E, k, renorm, H, I, blobs, ids, w, out, 1);
 }
 
 /* ---- adaptive residency ------------------------------------------------------ */

@@ -347,8 +347,8 @@ def test_combine_identical_experts():
         np.testing.assert_allclose(out[t], w[t].sum() * y[t], rtol=1e-12, atol=1e-12 * np.abs(y).max())
 
 
-@pytest.mark.parametrize("renorm", [0, 1])
-def test_layer_distinct_experts_tagged_by_powers_of_two(renorm):
+@pytest.mark.parametrize("renorm,act4", [(0, False), (1, False), (0, True)])
+def test_layer_distinct_experts_tagged_by_powers_of_two(renorm, act4):
     """Expert e is one base expert with every down-projection scale byte raised by
     e, so its output is exactly 2^e times the base output: the layer's result then
     names which experts each token used and with which weights. Picks come from a
@@ -365,8 +365,8 @@ def test_layer_distinct_experts_tagged_by_powers_of_two(renorm):
     logits = rng.standard_normal((T, E)).astype(np.float32)
     x = synth.gen_x(T, H, seed=6)
     bits = x.view(torch.int16).numpy().view(np.uint16)
-    y = oracle.expert_ffn(base, H, I, oracle.bf16_bits_to_f64(bits))
-    rc, ids, w, out = oracle.layer(logits, bits, k, renorm, H, I, blobs)
+    y = oracle.expert_ffn(base, H, I, oracle.bf16_bits_to_f64(bits), act4=act4)
+    rc, ids, w, out = oracle.layer(logits, bits, k, renorm, H, I, blobs, act4=act4)
     assert rc == 0
     want_ids = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :k]
     assert np.array_equal(ids, want_ids)
@@ -380,6 +380,124 @@ def test_layer_distinct_experts_tagged_by_powers_of_two(renorm):
     tag = np.exp2(want_ids.astype(np.float64))
     want = (want_w * tag).sum(axis=1, keepdims=True) * y
     np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
+
+
+# ---------------------------------------------------------------- MXFP4 activations (all-FP4 mode)
+
+_E2M1_MAG = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # E2M1 magnitudes of codes 0..7 (pinned above)
+
+
+def _golden_quant():
+    for line in open(os.path.join(GOLDEN, "mxfp4_quant.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        sb, codes, vals = line.split("|")
+        v = [_num(x) for x in vals.split(",")]
+        v += [0.0] * (32 - len(v))
+        yield int(sb), [int(ch, 16) for ch in codes.strip()], np.array(v, np.float64)
+
+
+def _codes(nib, K):
+    return [int((int(nib[i // 2]) >> (4 * (i % 2))) & 15) for i in range(K)]
+
+
+def _brute_quant_block(v):
+    """The OCP conversion of one 32-block restated with exact rationals: the
+    exponent bracketed by exact powers of two, every E2M1 magnitude tried."""
+    amax = max(abs(float(x)) for x in v)
+    if amax == 0.0:
+        X = -127
+    else:
+        e = math.frexp(amax)[1] - 1
+        assert Fraction(2) ** e <= Fraction(amax) < Fraction(2) ** (e + 1)
+        X = min(127, max(-127, e - 2))
+    codes = []
+    for x in v:
+        r = Fraction(abs(float(x))) / Fraction(2) ** X
+        best = min(range(8), key=lambda c: (abs(Fraction(_E2M1_MAG[c]) - r), c % 2))
+        codes.append(best | (8 if math.copysign(1.0, float(x)) < 0 else 0))
+    return X + 127, codes
+
+
+def _brute_quant_dequant(row):
+    out = np.empty(row.size)
+    for b in range(row.size // 32):
+        sb, codes = _brute_quant_block(row[32 * b: 32 * b + 32])
+        for i, c in enumerate(codes):
+            mag = _E2M1_MAG[c & 7] * 2.0 ** (sb - 127)
+            out[32 * b + i] = -mag if c & 8 else mag
+    return out
+
+
+def test_quant_mxfp4_hand_worked():
+    n = 0
+    for sb, codes, v in _golden_quant():
+        nib, sc = oracle.quant_mxfp4(v)
+        assert sc.tolist() == [sb]
+        assert _codes(nib, 32) == codes
+        n += 1
+    assert n == 8
+
+
+def test_quant_mxfp4_matches_brute_force():
+    rng = np.random.default_rng(41)
+    blocks = []
+    for _ in range(150):
+        blocks.append(rng.standard_normal(32) * 2.0 ** rng.integers(-20, 21))
+    for _ in range(50):  # ties and near-ties of the E2M1 grid at scale 2^0
+        v = rng.choice([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 3.0], 32) * rng.choice([-1.0, 1.0], 32)
+        v[0] = 4.0
+        v[1:4] += rng.choice([0.0, 2.0 ** -40, -(2.0 ** -40)], 3)
+        blocks.append(v)
+    for _ in range(20):  # E8M0 clamps at both ends, sparse blocks
+        v = np.where(rng.random(32) < 0.3, rng.standard_normal(32), 0.0)
+        blocks.append(v * 2.0 ** rng.choice([-140, -128, 128, 140]))
+    K = 32 * len(blocks)
+    row = np.concatenate(blocks)
+    nib, sc = oracle.quant_mxfp4(row)
+    got = _codes(nib, K)
+    for b, v in enumerate(blocks):
+        sb, codes = _brute_quant_block(v)
+        assert int(sc[b]) == sb, b
+        assert got[32 * b: 32 * b + 32] == codes, b
+
+
+def test_quant_mxfp4_scaling_and_sign():
+    rng = np.random.default_rng(42)
+    v = rng.standard_normal(256)
+    nib, sc = oracle.quant_mxfp4(v)
+    for k in (-5, 1, 7):
+        n2, s2 = oracle.quant_mxfp4(v * 2.0 ** k)
+        assert np.array_equal(n2, nib) and np.array_equal(s2.astype(int), sc.astype(int) + k)
+    n3, s3 = oracle.quant_mxfp4(-v)
+    assert np.array_equal(s3, sc) and np.array_equal(n3, nib ^ 0x88)
+
+
+def test_ffn_act4_structured_closed_form():
+    """Gate row r reads x[r % H] (weight 1), up row r reads x[(r+5) % H] (weight 2),
+    down row r reads h[3r % I] (weight 1): with x and h quantised as the
+    all-FP4 mode prescribes, y[r] = hq[3r % I] exactly."""
+    H, I = 128, 256
+    w13 = np.zeros((2 * I, H), np.uint8)
+    for r in range(I):
+        w13[r, r % H] = 2
+        w13[I + r, (r + 5) % H] = 4
+    w2 = np.zeros((H, I), np.uint8)
+    for r in range(H):
+        w2[r, (3 * r) % I] = 2
+    blob = _blob(H, I, w13, np.full((2 * I, H // 32), 127), w2, np.full((H, I // 32), 127))
+    rng = np.random.default_rng(43)
+    x = rng.standard_normal((2, H)) * 3.0
+    y = oracle.expert_ffn(blob, H, I, x, act4=True)
+    for t in range(2):
+        xq = _brute_quant_dequant(x[t])
+        h = np.empty(I)
+        for r in range(I):
+            g, u = xq[r % H], 2.0 * xq[(r + 5) % H]
+            h[r] = g / (1.0 + math.exp(-g)) * u
+        hq = _brute_quant_dequant(h)
+        want = np.array([hq[(3 * r) % I] for r in range(H)])
+        assert np.array_equal(y[t], want)
 
 
 # ---------------------------------------------------------------- residency
