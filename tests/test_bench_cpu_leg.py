@@ -40,3 +40,36 @@ def test_first_tokens_route_as_in_the_whole_step():
     _, ids_head, w_head, _, _, _ = oracle.route(np.ascontiguousarray(full[:8]), k)
     assert np.array_equal(ids_full[:8], ids_head)
     assert np.array_equal(w_full[:8], w_head)
+
+
+def _args(*argv):
+    old = sys.argv
+    sys.argv = ["bench.py", *argv]
+    try:
+        return bench.parse()
+    finally:
+        sys.argv = old
+
+
+def test_default_run_is_the_batch1_decode_layer():
+    a = _args()
+    assert (a.gpus, a.config, a.impl) == (1, "c1", "ours")
+    assert a.warmup >= 3 and a.steps > 0
+    c = bench.workload(a)
+    assert (c["H"], c["I"], c["E"], c["n_hot"], c["n_cold"], c["k"], c["T"]) == (4096, 3072, 384, 255, 129, 6, 1)
+    assert c["routing"] == "uniform" and c["layers"] == 1
+    assert a.no_residency and not c["mirror"] and not c["zero_copy"]
+
+
+def test_workload_shapes_of_the_other_configs():
+    c = bench.workload(_args("--config", "c2", "--batch", "32", "--skew", "1.5"))
+    assert (c["T"], c["routing"], c["s"], c["E"], c["n_hot"]) == (32, "zipf", 1.5, 384, 255)
+    a = _args("--config", "c3")
+    c = bench.workload(a)
+    assert c["layers"] == 20 and c["swap_every"] == 16 and not a.no_residency
+    assert (c["swap_every_steps"], c["max_swaps"], c["hysteresis"]) == (16, 8, 3.0)
+    assert not c["mirror"]  # 20 layers keep the in-place exchange
+    c = bench.workload(_args("--config", "c4"))
+    assert (c["T"], c["n_hot"], c["n_cold"]) == (8192, 384, 0)
+    c = bench.workload(_args("--config", "v1"))
+    assert (c["T"], c["routing"]) == (6, "verify")
