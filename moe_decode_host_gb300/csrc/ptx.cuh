@@ -104,13 +104,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Generic-proxy writes to shared memory by this thread are ordered before later
 // async-proxy accesses (TMA, bulk copies) to the same bytes once a barrier follows.
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -124,8 +117,6 @@ __device__ __forceinline__ uint4 ld_host_v4(const void* p) {
                  : "l"(p));
     return v;
 }
-
-__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
     uint32_t v;
