@@ -37,10 +37,13 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_and_job_rate_on_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
-    mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
+    # the manager process is started with spawn too: no fork of a threaded process
+    with mp.get_context("spawn").Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = {r: out[r] for r in range(world)}
     for r in range(world):
-        m, rate = out[r]
+        m, rate = res[r]
         assert m == 40.0  # every rank sees the slowest replica's time
         assert rate == pytest.approx(2 * 100 * 4 / 0.040)  # all ranks' tokens over that time
 
