@@ -12,7 +12,10 @@
  *
  * Conventions
  *  - Every call returns an int status: MOE_OK (0) or a negative MOE_ERR_* code.
- *    A call that returns an error has launched nothing.
+ *    A call that returns MOE_ERR_INVALID_ARG has launched nothing; after
+ *    MOE_ERR_CUDA part of its work may already be enqueued.  Where a call lists no
+ *    errors, a null handle or pointer gives MOE_ERR_INVALID_ARG and a failed CUDA
+ *    call MOE_ERR_CUDA.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    All device work is enqueued on it; nothing synchronises except
  *    residency_update on an acting step (it reads the pick counters on the host),
