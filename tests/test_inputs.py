@@ -48,3 +48,68 @@ def test_zipf_skew_matches_the_pages_share():
         cnt = np.sort(np.bincount(ids.ravel(), minlength=E))[::-1]
         share = cnt[:int(0.73 * E)].sum() / cnt.sum()
         assert lo <= share <= hi, (s, share)
+
+
+def test_weight_codes_follow_rounded_normal():
+    """Nibble codes are draws of E2M1 round-to-nearest of N(0,1) (saturating at
+    +-6): the frequencies match the normal probabilities of each code's rounding
+    interval (scipy's normal CDF), every code occurs, scale bytes are 127 - U{0..8}."""
+    import pytest
+
+    stats = pytest.importorskip("scipy.stats")
+    H, I = 256, 512
+    blob = synth.gen_blobs(1, H, I, seed=5)[0].numpy()
+    sec = synth.blob_sections(H, I)
+    nib = np.concatenate([blob[sec["w13n"][0]:sec["w13n"][0] + sec["w13n"][1]],
+                          blob[sec["w2n"][0]:sec["w2n"][0] + sec["w2n"][1]]])
+    codes = np.concatenate([nib & 15, nib >> 4])
+    freq = np.bincount(codes, minlength=16) / codes.size
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    mid = [(a + b) / 2 for a, b in zip(mags[:-1], mags[1:])]
+    edges = np.array([0.0] + mid + [np.inf])
+    half = np.diff(stats.norm.cdf(edges))  # P(|z| in the rounding interval of each magnitude) / 2
+    want = np.concatenate([half, half])  # + and - codes
+    n = codes.size
+    assert np.all(np.bincount(codes, minlength=16) > 0)
+    sigma = np.sqrt(np.maximum(want, 1.0 / n) * (1 - want) / n)
+    assert np.all(np.abs(freq - want) < 6 * sigma + 2.0 ** -16)
+    sc = np.concatenate([blob[sec["w13s"][0]:sec["w13s"][0] + sec["w13s"][1]],
+                         blob[sec["w2s"][0]:sec["w2s"][0] + sec["w2s"][1]]])
+    assert sc.min() == 119 and sc.max() == 127
+    cnt = np.bincount(sc - 119, minlength=9) / sc.size
+    assert np.all(np.abs(cnt - 1 / 9) < 6 * np.sqrt((1 / 9) * (8 / 9) / sc.size))
+
+
+def test_zipf_first_pick_is_the_zipf_law():
+    """logits = log p(rank) + Gumbel(0,1): the top pick is a draw from p (the
+    Gumbel-max property), with rank 1 the first expert of the permutation."""
+    E, s, T = 16, 1.1, 60000
+    perm = synth.zipf_permutation(E, 3)
+    l = synth.gen_logits_zipf(T, E, s, perm, seed=4)
+    top = np.argmax(l, axis=1)
+    freq = np.bincount(top, minlength=E) / T
+    r = np.arange(1, E + 1, dtype=np.float64)
+    p = r ** -s / np.sum(r ** -s)
+    want = np.empty(E)
+    want[perm] = p
+    assert np.all(np.abs(freq - want) < 6 * np.sqrt(want * (1 - want) / T))
+
+
+def test_activations_are_bf16_standard_normal():
+    import torch
+
+    x = synth.gen_x(64, 4096, seed=9)
+    assert x.dtype == torch.bfloat16 and tuple(x.shape) == (64, 4096)
+    v = x.float().numpy().ravel()
+    assert abs(v.mean()) < 0.01 and abs(v.std() - 1.0) < 0.01
+    assert np.array_equal(synth.gen_x(64, 4096, seed=9).float().numpy(), x.float().numpy())  # seeded
+
+
+def test_starting_maps_are_placements():
+    E, n_hot = 384, 255
+    assert np.array_equal(synth.loc_identity(E, n_hot), np.arange(E))
+    hot = synth.zipf_permutation(E, 1)[:n_hot]
+    loc = synth.loc_from_hot_set(E, n_hot, hot)
+    assert np.array_equal(np.sort(loc), np.arange(E))  # a bijection
+    assert np.all(loc[hot] < n_hot)
+    assert np.array_equal(np.sort(hot), np.argsort(np.where(loc < n_hot, loc, E + loc))[:n_hot])
