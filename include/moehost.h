@@ -262,6 +262,21 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream);
 int moe_residency_plan(const int32_t* counts, const int32_t* loc, int E, int n_hot, int max_swaps, float hysteresis,
                        int32_t* loc_out, int32_t* promoted, int32_t* demoted);
 
+/* MXFP4 quantisation of bf16 activation rows, the first step of the all-FP4
+ * prefill mode (a block-scaled FP4 x FP4 tensor-core product takes both operands
+ * in MXFP4).  Each 32-element block of a row gets the shared exponent
+ * floor(log2(max |v|)) - 2 clamped to [-127, 127] (an all-zero block: -127),
+ * stored as scale byte exponent + 127; each element gets |v| / 2^exponent rounded
+ * to the nearest E2M1 magnitude {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to the even
+ * code, above 6 saturating to 6, with v's sign bit (the OCP Microscaling
+ * conversion for E2M1).  Output in the weights' row layout.
+ *  x_bf16  device bf16 [rows][K], finite values; K a positive multiple of 32.
+ *  nib     device uint8 [rows][K/2] out: element k of a row in byte k/2, low
+ *          nibble when k is even.
+ *  scales  device uint8 [rows][K/32] out.
+ * rows = 0 is valid.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+int moe_quant_mxfp4(const void* x_bf16, int rows, int K, uint8_t* nib, uint8_t* scales, void* stream);
+
 /* Copies the placement map to host int32 [E] (synchronous). */
 int moe_layer_get_loc(moe_layer* L, int32_t* loc_host);
 

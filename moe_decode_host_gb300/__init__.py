@@ -19,7 +19,7 @@ __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_by
            "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
            "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED", "MOE_ERR_SCRATCH_TOO_SMALL",
-           "moe_grouped_ffn_noalloc", "residency_plan"]
+           "moe_grouped_ffn_noalloc", "residency_plan", "quant_mxfp4"]
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -188,6 +188,12 @@ def residency_plan(counts, loc, n_hot: int, max_swaps: int, hysteresis: float):
     if n < 0:
         check(n, "moe_residency_plan")
     return out, pro[:n].copy(), dem[:n].copy()
+
+
+def quant_mxfp4(x, rows: int, K: int, nib, scales, stream=None):
+    """MXFP4 quantisation of bf16 rows x [rows, K] into nib [rows, K/2] and scales
+    [rows, K/32] (device tensors), on the GPU."""
+    check(lib.moe_quant_mxfp4(ptr(x), rows, K, ptr(nib), ptr(scales), stream_handle(stream)), "moe_quant_mxfp4")
 
 
 def link_probe(src_host, dst_dev, nbytes, ctas=0, stream=None):

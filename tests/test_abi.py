@@ -151,3 +151,12 @@ def test_residency_plan_rejects_bad_input(mlib):
     assert plan(ok_counts, np.arange(8, dtype=np.int32), max_swaps=65) == mlib.MOE_ERR_INVALID_ARG
     assert plan(ok_counts, np.arange(8, dtype=np.int32), hyst=float("nan")) == mlib.MOE_ERR_INVALID_ARG
     assert plan(ok_counts, np.arange(8, dtype=np.int32), hyst=-1.0) == mlib.MOE_ERR_INVALID_ARG
+
+
+def test_quant_mxfp4_host_checks(mlib):
+    lib = mlib.lib
+    assert lib.moe_quant_mxfp4(None, 0, 64, None, None, None) == mlib.MOE_OK  # nothing to do
+    assert lib.moe_quant_mxfp4(None, 2, 64, None, None, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mxfp4(None, 2, 48, None, None, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mxfp4(None, -1, 64, None, None, None) == mlib.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_mxfp4(None, 1, 0, None, None, None) == mlib.MOE_ERR_INVALID_ARG

@@ -4,7 +4,7 @@ during a global-mode stream capture, embedders with their own allocator).  Its
 workspace is a fixed array inside the library, so its results must match the
 regular entry point's, call after call, with nothing allocated by the call.
 
-This file is collected last on purpose; it also passes when run alone in a fresh
+This file is collected after the layer parity tests on purpose; it also passes when run alone in a fresh
 process (the first call on the device looks up the array's address)."""
 import numpy as np
 import pytest
