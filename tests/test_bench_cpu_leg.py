@@ -73,3 +73,18 @@ def test_workload_shapes_of_the_other_configs():
     assert (c["T"], c["n_hot"], c["n_cold"]) == (8192, 384, 0)
     c = bench.workload(_args("--config", "v1"))
     assert (c["T"], c["routing"]) == (6, "verify")
+
+
+def test_prefill_targets_on_the_8192_token_layer():
+    """At 8192 tokens x top-6 over 384 experts of H=4096, I=3072: 3.71 TFLOP on
+    7.70 GB of weights plus 134 MB of x and output, about 473 flop/B; at the
+    measured 6751.7 GB/s that caps any kernel near 3.19 PFLOP/s."""
+    flops = 2.0 * 3 * 4096 * 3072 * 8192 * 6
+    algo = 384 * 20054016 + 2 * 8192 * 4096 * 2
+    t = bench.prefill_targets(flops, algo, 3.78, 1691.1, 6751.7)
+    assert abs(flops - 3.71e12) < 0.01e12
+    assert abs(t["flop_per_byte"] - 473) < 2
+    assert abs(t["hbm_bound_cap_tflops"] - 3190) < 20
+    assert abs(t["achieved_tflops"] - 981.7) < 1
+    assert abs(t["mxfp4_peak_tflops"] - 6 * 1691.1) < 1e-6
+    assert abs(t["frac_of_mxfp4_peak"] - 981.7 / 10146.6) < 1e-3
