@@ -87,6 +87,17 @@ def prefill_targets(flops: float, algo_bytes: float, ms: float, tc_peak_tflops: 
             "flop_per_byte": flops / algo_bytes}
 
 
+def skew_share(counts, frac_experts: float = 0.73) -> float:
+    """Share of the picks that land on the most-picked `frac_experts` of the
+    experts (the skew statistic the pages quote: 98.7% of picks on 73% of
+    experts), per layer over all timed steps, pooled over layers.
+    counts: int [steps, layers, E] picks per expert."""
+    per_layer = np.asarray(counts, dtype=np.int64).sum(axis=0)  # [layers, E]
+    n_top = int(round(frac_experts * per_layer.shape[1]))
+    top = np.sort(per_layer, axis=1)[:, ::-1][:, :n_top].sum()
+    return float(top / max(1, per_layer.sum()))
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -633,6 +644,7 @@ def run_ours(args):
                               "hbm_peak_gbs": hbm_peak, "link_peak_gbs": link_peak, "link_probe": link_detail},
             "ffn_hbm_gbs": ffn_gbs, "ffn_kernel_ms_mean": ffn_k_tot_ms / (K * NL), "gather_link_gbs": gather_gbs,
             "distinct_experts_per_layer_step": float(distinct.mean()),
+            "picks_on_top_73pct_experts": skew_share(counts_h),
             "cold_experts_per_layer_step": float(ncold_h.mean()), "swaps": int(total_swaps),
             "clocks": clk, "gpu_launches": int(launches),
             "device_status": [int(L["layer"].status()) for L in layers]}

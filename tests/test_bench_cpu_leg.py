@@ -88,3 +88,19 @@ def test_prefill_targets_on_the_8192_token_layer():
     assert abs(t["achieved_tflops"] - 981.7) < 1
     assert abs(t["mxfp4_peak_tflops"] - 6 * 1691.1) < 1e-6
     assert abs(t["frac_of_mxfp4_peak"] - 981.7 / 10146.6) < 1e-3
+
+
+def test_skew_share_statistic():
+    import numpy as np
+
+    # 100 experts, 2 layers: picks only on experts 0..72 -> everything on the top 73%
+    c = np.zeros((3, 2, 100), np.int32)
+    c[:, :, :73] = 1
+    assert bench.skew_share(c) == 1.0
+    # uniform picks -> 73%
+    assert abs(bench.skew_share(np.ones((5, 1, 100), np.int32)) - 0.73) < 1e-12
+    # per layer: each layer's own top experts count (layer 0 on 0..72, layer 1 on 27..99)
+    c = np.zeros((1, 2, 100), np.int32)
+    c[0, 0, :73] = 2
+    c[0, 1, 27:] = 2
+    assert bench.skew_share(c) == 1.0
