@@ -87,6 +87,22 @@ def prefill_targets(flops: float, algo_bytes: float, ms: float, tc_peak_tflops: 
             "flop_per_byte": flops / algo_bytes}
 
 
+def repetition_bounds(K: int, n: int = 5) -> list:
+    """Step indices splitting K timed steps into n repetitions of (nearly) equal
+    length: [0, ..., K]; fewer repetitions when K < n (one step each)."""
+    n = max(1, min(n, K))
+    return [round(K * j / n) for j in range(n + 1)]
+
+
+def repetition_spread(bounds: list, rep_ms: list, tokens_per_step: int) -> dict:
+    """Throughput of each repetition (this rank's clock) and their median, min and
+    max, in the line's unit."""
+    vals = [tokens_per_step * (bounds[j + 1] - bounds[j]) / (ms * 1e-3) for j, ms in enumerate(rep_ms)]
+    return {"n": len(vals), "steps_each": [bounds[j + 1] - bounds[j] for j in range(len(vals))],
+            "tokens_per_s": vals, "median": float(np.median(vals)), "min": float(min(vals)),
+            "max": float(max(vals)), "note": "the timed region split at event marks; rank 0's clock"}
+
+
 def skew_share(counts, frac_experts: float = 0.73) -> float:
     """Share of the picks that land on the most-picked `frac_experts` of the
     experts (the skew statistic the pages quote: 98.7% of picks on 73% of
@@ -546,6 +562,10 @@ def run_ours(args):
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    # the timed steps also fall into five repetitions, marked by an event at each
+    # inner boundary (four records in the whole region), for the spread
+    bounds = repetition_bounds(K)
+    marks = {b: torch.cuda.Event(enable_timing=True) for b in bounds[1:-1]}
     torch.cuda.synchronize()
     t_start.record(st)
     total_swaps = 0
@@ -554,10 +574,18 @@ def run_ours(args):
         s, n = step(i, True)
         total_swaps += s
         launches += n
+        if i + 1 in marks:
+            marks[i + 1].record(st)
     t_end.record(st)
     torch.cuda.synchronize()
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
+    try:
+        evs = [t_start] + [marks[b] for b in bounds[1:-1]] + [t_end]
+        rep_ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(evs) - 1)]
+        repetitions = repetition_spread(bounds, rep_ms, T * world)
+    except Exception as exc:  # the spread is an addition; it never costs the line
+        repetitions = {"error": str(exc)[:200]}
     if dist:
         dist.barrier()
     copy_ms = [L["layer"].profile_read(K) for L in layers]
@@ -645,6 +673,7 @@ def run_ours(args):
             "ffn_hbm_gbs": ffn_gbs, "ffn_kernel_ms_mean": ffn_k_tot_ms / (K * NL), "gather_link_gbs": gather_gbs,
             "distinct_experts_per_layer_step": float(distinct.mean()),
             "picks_on_top_73pct_experts": skew_share(counts_h),
+            "repetitions": repetitions,
             "cold_experts_per_layer_step": float(ncold_h.mean()), "swaps": int(total_swaps),
             "clocks": clk, "gpu_launches": int(launches),
             "device_status": [int(L["layer"].status()) for L in layers]}

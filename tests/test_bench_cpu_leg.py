@@ -104,3 +104,14 @@ def test_skew_share_statistic():
     c[0, 0, :73] = 2
     c[0, 1, 27:] = 2
     assert bench.skew_share(c) == 1.0
+
+
+def test_repetition_split_and_spread():
+    assert bench.repetition_bounds(8000) == [0, 1600, 3200, 4800, 6400, 8000]
+    assert bench.repetition_bounds(7) == [0, 1, 3, 4, 6, 7]
+    assert bench.repetition_bounds(3) == [0, 1, 2, 3]
+    assert bench.repetition_bounds(1) == [0, 1]
+    b = bench.repetition_bounds(10)
+    r = bench.repetition_spread(b, [2.0, 2.0, 4.0, 1.0, 2.0], 4)  # 2 steps x 4 tokens each
+    assert r["tokens_per_s"] == [4000.0, 4000.0, 2000.0, 8000.0, 4000.0]
+    assert (r["median"], r["min"], r["max"], r["n"]) == (4000.0, 2000.0, 8000.0, 5)
