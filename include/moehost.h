@@ -328,6 +328,15 @@ int moe_layer_inject_fault(moe_layer* L, int what);
  * the link peak the cold gather is reported against. */
 int moe_link_probe(const void* src_host, void* dst_dev, size_t bytes, int ctas, void* stream);
 
+/* Test hook for the bounded device waits of the pipelined kernels: launches one
+ * thread that waits on an mbarrier phase that nothing completes.  The wait gives
+ * up at its deadline (2 s), writes its record to diag_dev (device int32 [16], the
+ * layout moe_get_diag describes; zero it first) and MOE_ERR_TIMEOUT to
+ * *status_dev (device int; the first error written wins, so zero it first), and
+ * the kernel returns, leaving the context usable: how a lost producer is reported
+ * without faulting or hanging the GPU. */
+int moe_debug_wait_timeout(int* status_dev, int32_t* diag_dev, void* stream);
+
 /* Lane-layout check of the E2M1 pair conversion used by the FFN kernels: writes
  * for every byte b (0..255) the two f16 values it decodes to (low nibble first)
  * as uint32 [256] to out_dev (device). */
