@@ -29,6 +29,11 @@
  *    handles and small internal tables (placement map, phys-id pointer table, pick
  *    counters, status word), freed by the destroy calls.
  *  - Shapes: H and I multiples of 128; 1 <= k <= 32; k <= E <= 1024.
+ *  - Host threads: a layer (and the scratch it shares) keeps host-side state
+ *    (placement map, pending-copy flag, step count), so calls on one layer, or on
+ *    layers sharing a scratch, must not run concurrently from several host
+ *    threads; distinct layers with distinct scratches may.  moe_combine,
+ *    moe_quant_mxfp4 and moe_residency_plan hold no state.
  *
  * Expert blob format (one contiguous blob per expert, every plane 16-byte aligned):
  *   w13 nibbles [2I][H/2] | w13 scales [2I][H/32] | w2 nibbles [H][I/2] | w2 scales [H][I/32]
