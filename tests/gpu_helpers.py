@@ -24,10 +24,10 @@ class LayerFixture:
         self.hot = torch.empty((max(1, n_hot), self.eb), dtype=torch.uint8, device=dev)
         if host_mirror:
             # a host copy of every expert, indexed by expert id
-            self.cold = torch.empty((E, self.eb), dtype=torch.uint8).pin_memory()
+            self.cold = torch.empty((E, self.eb), dtype=torch.uint8, pin_memory=True)
             synth.fill_layer(self.hot, None, self.loc0, H, I, seed, device=gen_device, mirror=self.cold)
         else:
-            self.cold = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8).pin_memory()
+            self.cold = torch.empty((max(1, n_cold), self.eb), dtype=torch.uint8, pin_memory=True)
             synth.fill_layer(self.hot, self.cold, self.loc0, H, I, seed, device=gen_device)
         n_host = E if host_mirror else n_cold
         if scratch is None:
@@ -65,3 +65,42 @@ def rel_l2(got, want) -> float:
     want = np.asarray(want, np.float64)
     den = np.linalg.norm(want)
     return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def oracle_pick_rows(blob_of, H, I, x_f64, picks, act4=False):
+    """Oracle expert outputs for the picks {(t, j): expert}: one oracle call per
+    expert with its tokens batched, the experts spread over the host's cores (the
+    oracle's expert FFN keeps no shared state, and ctypes releases the interpreter
+    lock during the call).  blob_of(e) returns expert e's bytes; x_f64 [T, H]."""
+    import concurrent.futures as cf
+    import os
+
+    import oracle
+
+    by_e = {}
+    for tj, e in picks.items():
+        by_e.setdefault(int(e), []).append(tj)
+
+    def one(e):
+        tj = by_e[e]
+        return e, oracle.expert_ffn(blob_of(e), H, I, np.stack([x_f64[t] for t, _ in tj]), act4=act4)
+
+    out = {}
+    workers = max(1, len(os.sched_getaffinity(0)))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        for e, yy in ex.map(one, sorted(by_e)):
+            for tj, row in zip(by_e[e], yy):
+                out[tj] = row
+    return out
+
+
+def fingerprints(blob_of, experts):
+    """FNV-1a-64 of each listed expert's current bytes (oracle), over host threads."""
+    import concurrent.futures as cf
+    import os
+
+    import oracle
+
+    workers = max(1, len(os.sched_getaffinity(0)))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        return dict(zip(experts, ex.map(lambda e: oracle.fnv1a64(blob_of(e)), experts)))

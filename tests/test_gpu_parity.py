@@ -433,41 +433,6 @@ def test_layer_verify_window(c1_layer, T):
     _gather_check(fx, logits, T)
 
 
-@pytest.fixture(scope="module")
-def c2_layer():
-    c = synth.CONFIGS["c2"]
-    perm = synth.zipf_permutation(c["E"], synth.sub_seed("c2", "perm"))
-    loc = synth.loc_from_hot_set(c["E"], c["n_hot"], perm[:c["n_hot"]])
-    fx = LayerFixture(H=c["H"], I=c["I"], E=c["E"], n_hot=c["n_hot"], n_cold=c["n_cold"], k=c["k"],
-                      seed=synth.sub_seed("c2", "blobs"), loc=loc)
-    fx.perm = perm
-    yield fx
-    fx.layer.close()
-
-
-@pytest.mark.parametrize("T,s", [(8, 1.1), (32, 1.1), (32, 1.5)])
-def test_layer_c2(c2_layer, T, s):
-    c = synth.CONFIGS["c2"]
-    fx = c2_layer
-    logits = synth.gen_logits_zipf(T, c["E"], s, fx.perm, seed=synth.sub_seed("c2", "logits", T, s))
-    x = synth.gen_x(T, c["H"], seed=synth.sub_seed("c2", "x", T))
-    buf = _run_layer(fx, logits, x, False)
-    _compare_layer(fx, buf, logits, x, [0, T - 1], False)
-    _gather_check(fx, logits, T)
-
-
-def test_layer_c4_prefill_shape():
-    c = synth.CONFIGS["c4"]
-    T = c["T"]
-    fx = LayerFixture(H=c["H"], I=c["I"], E=c["E"], n_hot=c["n_hot"], n_cold=0, k=c["k"],
-                      seed=synth.sub_seed("c4", "blobs"))
-    logits = synth.gen_logits_uniform(T, c["E"], seed=synth.sub_seed("c4", "logits"))
-    x = synth.gen_x(T, c["H"], seed=synth.sub_seed("c4", "x"))
-    buf = _run_layer(fx, logits, x, False)
-    _compare_layer(fx, buf, logits, x, [0, 4097, T - 1], False)
-    fx.layer.close()
-
-
 # ------------------------------------------------------------------ residency
 
 def _skewed_logits(T, E, step, hot_first):
