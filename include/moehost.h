@@ -221,8 +221,9 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
  * clears what must start at zero itself), so calls that overlap on the GPU race:
  * order them on one stream or otherwise serialise them.
  * Errors: MOE_ERR_SCRATCH_TOO_SMALL when T needs more than the array holds
- * (moe_ffn_workspace_bytes(L, T) > MOE_NOALLOC_SCRATCH_BYTES; about T = 70 at
- * H=4096, I=3072, k=6), MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+ * (moe_ffn_workspace_bytes(L, T) > MOE_NOALLOC_SCRATCH_BYTES; each of the T*k picks
+ * takes 2*max(H, I) + 4*I + 4 bytes, each section rounded up to 256 bytes, so
+ * T <= 68 at H=4096, I=3072, k=6), MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
 #define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int moe_grouped_ffn_noalloc(moe_layer* L, const void* x, int T, const int32_t* phys_ids, const int32_t* counts,
                             const int32_t* offsets, const int32_t* entries, float* y, void* stream);
