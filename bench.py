@@ -2,10 +2,12 @@
 
 One step = one pass of the whole path over one batch: moe_route -> cold_gather ->
 moe_grouped_ffn -> moe_combine -> residency_update (acting every 16 steps with
-hysteresis 3.0 and at most 8 swaps).  Default workload: one layer with H=4096,
-I=3072, 384 experts (255 in HBM, 129 in pinned host memory), top-6, one decode
-token per step, router logits N(0,1).  Steps cycle over a pool of 64 distinct
-routings; the 7.7 GB weight pool is far larger than L2, so no L2 flush is used.
+hysteresis 3.0 and at most 8 swaps where the workload runs the residency manager).
+Default workload: one layer with H=4096, I=3072, 384 experts (255 in HBM, 129 in
+pinned host memory), top-6, one decode token per step, router logits N(0,1); the
+same line also carries the layer at decode batches of 8 and 32 tokens with Zipf
+s=1.1 routing (`per_batch`).  Steps draw their routing from a pool of distinct
+steps; the 7.7 GB weight pool is far larger than L2, so no L2 flush is used.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
 """
@@ -27,33 +29,19 @@ import numpy as np  # noqa: E402
 
 HBM_NOMINAL_GBS = 8000.0
 
-
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work,
-# from the ncu captures summarised under profiles/ (a smaller layer of the same
-# expert shape; traffic scales with the experts processed).  An entry is set to
-# None whenever its kernel changes after the capture.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per unit of work, from
+# ncu captures of a smaller layer of the same expert shape (traffic scales with the
+# experts processed).  None once the kernel has changed since its capture.
 NCU_TRAFFIC = {
-    # per cold expert copied: the slot writes stay in L2 during the launch
-    "cold_copy": {"bytes_per_expert": (11520 + 15616) / 2,
-                  "source": "profiles/cold_copy_kernel_c1_small.md"},
-    # per distinct expert through the decode kernels (gate/up + down launches)
-    "ffn_decode": {"bytes_per_expert": (66931968 + 642560 + 33490432) / 5,
-                   "source": "profiles/ffn_decode_kernel_c1_small.md"},
-    # per expert through the tcgen05 kernels at about 128 tokens per expert: the
-    # capture (935596288 + 92993792 + 483277568 + 112975360 bytes over 64 experts)
-    # predates the converters' scale-word prefetch, so no figure is reported
-    "ffn_tc": {"bytes_per_expert": None,
-               "source": "profiles/ffn_tc_kernel_c4_small.md (counters of the previous kernel build)"},
+    "cold_copy": (11520 + 15616) / 2,                     # per cold expert copied
+    "ffn_decode": (66931968 + 642560 + 33490432) / 5,     # per distinct expert, both phases
+    "ffn_tc": None,                                       # per expert at ~128 tokens per expert
 }
 
 
-def _traffic(kind, experts_per_call):
-    t = NCU_TRAFFIC.get(kind)
-    if not t:
-        return None, None
-    if t.get("bytes_per_expert") is None:
-        return None, t.get("source")
-    return float(t["bytes_per_expert"] * experts_per_call), t["source"]
+def _traffic(kind, units):
+    b = NCU_TRAFFIC.get(kind)
+    return None if b is None else float(b * units)
 
 
 def _tensor_peak():
@@ -103,14 +91,19 @@ def repetition_spread(bounds: list, rep_ms: list, tokens_per_step: int) -> dict:
             "max": float(max(vals)), "note": "the timed region split at event marks; rank 0's clock"}
 
 
-def skew_share(counts, frac_experts: float = 0.73) -> float:
-    """Share of the picks that land on the most-picked `frac_experts` of the
-    experts (the skew statistic the pages quote: 98.7% of picks on 73% of
-    experts), per layer over all timed steps, pooled over layers.
-    counts: int [steps, layers, E] picks per expert."""
+def skew_share(counts, ranking, frac_experts: float = 0.73) -> float:
+    """Share of the picks that land on the `frac_experts` most popular experts of
+    the routing generator (the skew statistic the pages quote: 98.7% of picks on 73%
+    of experts), pooled over layers.  The popularity order is the generator's own
+    (the Zipf permutation; expert order for uniform routing, where every expert is
+    equally popular), not the order observed in the sample, so a short sample of
+    uniform routing reads about 0.73.
+    counts: int [steps, layers, E] picks per expert; ranking: int [layers, E], most
+    popular expert first."""
     per_layer = np.asarray(counts, dtype=np.int64).sum(axis=0)  # [layers, E]
+    ranking = np.asarray(ranking, dtype=np.int64)
     n_top = int(round(frac_experts * per_layer.shape[1]))
-    top = np.sort(per_layer, axis=1)[:, ::-1][:, :n_top].sum()
+    top = sum(int(per_layer[li, ranking[li, :n_top]].sum()) for li in range(per_layer.shape[0]))
     return float(top / max(1, per_layer.sum()))
 
 
@@ -126,21 +119,23 @@ def _peaks():
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=8000)
-    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c1", choices=["c1", "c2", "c3", "c4", "v1"])
     ap.add_argument("--batch", type=int, default=None, help="tokens per step (c2/c3: 8 or 32)")
     ap.add_argument("--skew", type=float, default=None, help="Zipf exponent for skewed routing")
     ap.add_argument("--layers", type=int, default=None, help="layers for c3")
-    ap.add_argument("--pool", type=int, default=64)
+    ap.add_argument("--pool", type=int, default=64, help="distinct steps of routing (at least)")
     ap.add_argument("--residency", dest="no_residency", action="store_false", default=None,
                     help="run the residency manager (default: only where the workload specifies it, the "
                          "20-layer stack)")
     ap.add_argument("--no-residency", dest="no_residency", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-per-batch", action="store_true",
+                    help="skip the decode batches of 8 and 32 tokens that the default line carries")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time of each CPU baseline leg")
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling on a smaller layer)")
     ap.add_argument("--hot", type=int, default=None, help="override n_hot (with --experts)")
     ap.add_argument("--no-link-probe", action="store_true")
@@ -158,28 +153,34 @@ def parse():
     return ap.parse_args()
 
 
-def workload(args):
+def workload(args, config=None, batch=None):
     import synth
 
-    c = dict(synth.CONFIGS[args.config])
-    if args.no_residency is None:
+    name = config or args.config
+    c = dict(synth.CONFIGS[name])
+    no_res = args.no_residency
+    if no_res is None:
         # residency only where the workload asks for it (the stacked-layer config)
-        args.no_residency = "swap_every" not in c
-    if args.batch is not None:
-        c["T"] = args.batch
-    if args.skew is not None:
-        c["s"] = args.skew
-    if args.layers is not None:
-        c["layers"] = args.layers
-    if args.experts is not None:
-        c["E"] = args.experts
-        c["n_hot"] = args.hot if args.hot is not None else min(c["n_hot"], args.experts)
-        c["n_cold"] = c["E"] - c["n_hot"]
-    c["name"] = args.config
+        no_res = "swap_every" not in c
+    c["no_res"] = no_res
+    if config is None:
+        if args.batch is not None:
+            c["T"] = args.batch
+        if args.skew is not None:
+            c["s"] = args.skew
+        if args.layers is not None:
+            c["layers"] = args.layers
+        if args.experts is not None:
+            c["E"] = args.experts
+            c["n_hot"] = args.hot if args.hot is not None else min(c["n_hot"], args.experts)
+            c["n_cold"] = c["E"] - c["n_hot"]
+    if batch is not None:
+        c["T"] = batch
+    c["name"] = name
     # host copies of every expert: default for one layer (7.7 GB pinned); a 20-layer
     # stack would need 154 GB of pinned host memory, so it keeps the in-place exchange
     c["mirror"] = args.mirror if args.mirror is not None else (
-        c.get("layers", 1) == 1 and c["n_cold"] > 0 and not args.no_residency)
+        c.get("layers", 1) == 1 and c["n_cold"] > 0 and not no_res)
     c["zero_copy"] = bool(args.zero_copy)
     if args.n_hot is not None and args.experts is None:
         c["n_hot"] = min(args.n_hot, c["E"])
@@ -209,6 +210,14 @@ def job_rate(world: int, steps: int, tokens_per_step: int, elapsed_ms: float) ->
     """Whole-job tokens/s: every replica processes its own steps, timed by the
     slowest replica."""
     return world * steps * tokens_per_step / (elapsed_ms * 1e-3)
+
+
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
 class Clocks:
@@ -261,33 +270,36 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ reference arm (CPU oracle)
+# ------------------------------------------------------------------ CPU oracle timing
 
 ORACLE_TOKENS_PER_CALL = 8  # one oracle token of the 384-expert layer takes about two seconds
+ORACLE_BLOB_POOL = 16       # distinct expert blobs the timed oracle calls read
+_BLOB_POOLS: dict = {}
 
 
-def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
-    """Times the CPU oracle on a bounded sample of the workload: whole tokens of
-    the layer (route + every pick's expert FFN + combine), expert bytes drawn by the
-    seeded generator on the CPU.  The oracle runs every pick on its own token, so
-    its time per token does not depend on the batch: each call takes the first
-    ORACLE_TOKENS_PER_CALL tokens of a seeded step of the workload (routing is per
-    token, so they route as they do in the whole step).  Returns (tokens/s, tokens,
-    seconds, sample text)."""
-    import torch
-
-    import oracle
+def _blob_pool(H, I, n):
+    """n seeded expert blobs of shape (H, I), drawn once per process."""
     import synth
 
-    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    key = (H, I, n)
+    if key not in _BLOB_POOLS:
+        b = synth.gen_blobs(n, H, I, seed=synth.sub_seed("oracle-timing", "blobs", H, I))
+        _BLOB_POOLS[key] = [b[i].numpy() for i in range(n)]
+    return _BLOB_POOLS[key]
+
+
+def _oracle_jobs(c, seed_tag, n_jobs):
+    """Inputs of n_jobs oracle calls: each the first ORACLE_TOKENS_PER_CALL tokens of
+    a seeded step of the workload (logits, x bits)."""
+    import torch
+
+    import synth
+
+    E, H = c["E"], c["H"]
     T_step = max(1, c["T"])
     T = min(T_step, ORACLE_TOKENS_PER_CALL)
-    oracle.build()
-    tok = 0
-    t_total = 0.0
-    blob_cache = {}
-    step = 0
-    while t_total < seconds or tok == 0:
+    jobs = []
+    for step in range(n_jobs):
         if c.get("routing") == "zipf":
             perm = synth.zipf_permutation(E, synth.sub_seed(c["name"], "perm"))
             logits = synth.gen_logits_zipf(T_step, E, c.get("s", 1.1), perm, seed=synth.sub_seed(seed_tag, step))
@@ -296,47 +308,86 @@ def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu"):
         else:
             logits = synth.gen_logits_uniform(T_step, E, seed=synth.sub_seed(seed_tag, step))
         x = synth.gen_x(T_step, H, seed=synth.sub_seed(seed_tag, "x", step))
-        logits = np.ascontiguousarray(logits[:T])
-        bits = np.ascontiguousarray(x[:T].view(torch.int16).numpy().view(np.uint16))
-        # expert bytes are generated outside the timed region (they are inputs)
-        _, ids, _, _, _, _ = oracle.route(logits, k)
-        blobs = []
-        picked = set(ids.ravel().tolist())
-        for e in range(E):
-            if e in picked:
-                if e not in blob_cache:
-                    blob_cache[e] = synth.gen_blobs(1, H, I, seed=synth.sub_seed(seed_tag, "blob", e))[0].numpy()
-                blobs.append(blob_cache[e])
-            else:
-                blobs.append(blob_cache.get(e, np.zeros(1, np.uint8)))
-        t0 = time.perf_counter()
-        rc, _, _, out = oracle.layer(logits, bits, k, 0, H, I, blobs)
-        t_total += time.perf_counter() - t0
+        jobs.append((np.ascontiguousarray(logits[:T]),
+                     np.ascontiguousarray(x[:T].view(torch.int16).numpy().view(np.uint16))))
+    return jobs, T, T_step
+
+
+def oracle_tokens_per_s(c, seconds: float, seed_tag="cpu", threads: int = 1):
+    """Times the CPU oracle on a bounded sample of the workload: whole tokens of the
+    layer (route + every pick's expert FFN + combine), on `threads` host threads
+    (the oracle's C calls run without the interpreter lock, each call on its own
+    tokens).  The oracle runs every pick on its own token, so its time per token
+    does not depend on the batch: each call takes the first ORACLE_TOKENS_PER_CALL
+    tokens of a seeded step of the workload (routing is per token, so they route as
+    they do in the whole step).  Expert e reads the bytes of blob e mod
+    ORACLE_BLOB_POOL of a seeded pool (drawn outside the timed region; the oracle's
+    time does not depend on the byte values).  Calls continue until `seconds` of
+    wall time have passed (at least one per thread).  Returns (tokens/s, tokens,
+    seconds, sample text)."""
+    import concurrent.futures as cf
+
+    import oracle
+    import synth
+
+    H, I, E, k = c["H"], c["I"], c["E"], c["k"]
+    oracle.build()
+    pool = _blob_pool(H, I, min(ORACLE_BLOB_POOL, E))
+    blobs = [pool[e % len(pool)] for e in range(E)]
+    batch = max(2, threads) * 2
+    jobs, T, T_step = _oracle_jobs(c, seed_tag, batch)
+
+    def call(j):
+        logits, bits = jobs[j % len(jobs)]
+        rc, _, _, _ = oracle.layer(logits, bits, k, 0, H, I, blobs)
         assert rc == 0
-        tok += T
-        step += 1
-        if len(blob_cache) > 64:
-            blob_cache.clear()
-    sample = (f"{tok} token(s) of the {c['name']} layer (the first {T} of a {T_step}-token step, {step} "
-              f"step(s)): route, {k} expert FFNs per token, combine; single-threaded C oracle, fp64")
-    return tok / t_total, tok, t_total, sample
+        return logits.shape[0]
+
+    tok = 0
+    calls = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max(1, threads)) as ex:
+        while True:
+            done = list(ex.map(call, range(calls, calls + max(1, threads))))
+            tok += sum(done)
+            calls += len(done)
+            if time.perf_counter() - t0 >= seconds:
+                break
+    secs = time.perf_counter() - t0
+    who = "single-threaded" if threads == 1 else f"{threads} host threads, one call each at a time"
+    sample = (f"{tok} token(s) of the {c['name']} layer (the first {T} of a {T_step}-token step, {calls} "
+              f"call(s)): route, {k} expert FFNs per token, combine; C oracle, fp64, {who}; expert bytes from "
+              f"a pool of {len(pool)} seeded blobs")
+    return tok / secs, tok, secs, sample
 
 
-def run_reference(args, budget_s: float = 150.0):
-    """The CPU oracle as the reference arm, on this arm's workload and metric.  Each
-    step is one batch of the workload's tokens through the whole oracle layer; the
-    number of timed steps is capped so the run ends within a few minutes (one
-    oracle token of the 384-expert layer takes seconds)."""
+def cpu_baseline(c, seconds: float, seed_tag="cpu") -> dict:
+    """The oracle on every host core this process may use (the reported value) and
+    on one core, each for about `seconds` of wall time."""
+    cores = host_cores()
+    v_all, tok_all, s_all, sample_all = oracle_tokens_per_s(c, seconds, seed_tag=seed_tag + "-all", threads=cores)
+    v_one, tok_one, s_one, sample_one = oracle_tokens_per_s(c, seconds, seed_tag=seed_tag + "-one", threads=1)
+    return {"value": v_all, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample_all,
+            "single_thread": {"value": v_one, "unit": "tokens/s", "cores": 1, "sample": sample_one}}
+
+
+def run_reference(args, budget_s: float = 120.0):
+    """The CPU oracle as the reference arm, on this arm's workload and metric: each
+    step is one batch of oracle calls on every host core this process may use (one
+    call per core), each call on the first tokens of a seeded step of the workload;
+    the number of timed steps is capped so the run ends within a few minutes."""
     rank, world, _ = _rank_env()
     if rank != 0:
         return
     c = workload(args)
-    oracle_tokens_per_s(c, 0.0, seed_tag="ref-warm") if args.warmup > 0 else None
+    cores = host_cores()
+    if args.warmup > 0:
+        oracle_tokens_per_s(c, 0.0, seed_tag="ref-warm", threads=cores)
     t_steps = []
     tok_total = 0
     sample = ""
     for s in range(max(1, args.steps)):
-        v, tok, secs, sample = oracle_tokens_per_s(c, 0.0, seed_tag=f"ref{s}")
+        v, tok, secs, sample = oracle_tokens_per_s(c, 0.0, seed_tag=f"ref{s}", threads=cores)
         t_steps.append(secs)
         tok_total += tok
         if sum(t_steps) + secs > budget_s:
@@ -344,31 +395,38 @@ def run_reference(args, budget_s: float = 150.0):
     total = sum(t_steps)
     value = tok_total / total
     n = len(t_steps)
-    sample = (f"{n} step(s) of {min(max(1, c['T']), ORACLE_TOKENS_PER_CALL)} token(s) (the first of each "
-              f"{c['T']}-token step) of the {c['name']} layer (of {args.steps} requested; capped "
-              f"at {budget_s:.0f} s of oracle time): route, {c['k']} expert FFNs per token, combine; "
-              f"single-threaded C oracle, fp64")
+    sample = (f"{n} step(s) of {cores} oracle call(s) on {cores} host threads, each call the first "
+              f"{min(max(1, c['T']), ORACLE_TOKENS_PER_CALL)} token(s) of a {c['T']}-token step of the "
+              f"{c['name']} layer (of {args.steps} requested; capped at {budget_s:.0f} s of oracle time): route, "
+              f"{c['k']} expert FFNs per token, combine; C oracle, fp64; expert bytes from a pool of "
+              f"{ORACLE_BLOB_POOL} seeded blobs")
     line = {"impl": "reference", "metric": "MoE layer tokens/s (decode)", "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": n, "steps_requested": args.steps, "warmup": min(args.warmup, 1),
             "ms_per_step": 1000.0 * total / n, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config_json(c, args),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def _config_json(c, args):
+def _routing_name(c):
+    if c.get("routing") == "zipf":
+        return "Zipf s=%.2f" % c.get("s", 1.1)
+    if c.get("routing") == "verify":
+        return "verify-window (6 tokens of one sequence, correlated)"
+    return "uniform"
+
+
+def _config_json(c, args, pool_steps=None):
     return {"workload": f"{c['name']}: MoE layer H={c['H']} I={c['I']} E={c['E']} ({c['n_hot']} HBM / "
-                        f"{c['n_cold']} pinned host) top-{c['k']}, {c['T']} token(s)/step, "
-                        f"{'Zipf s=%.2f' % c.get('s', 1.1) if c.get('routing') == 'zipf' else ('verify-window (6 tokens of one sequence, correlated)' if c.get('routing') == 'verify' else 'uniform')} routing"
+                        f"{c['n_cold']} pinned host) top-{c['k']}, {c['T']} token(s)/step, {_routing_name(c)} routing"
                         + (f", {c['layers']} layers sharing one slot scratch" if c.get("layers", 1) > 1 else ""),
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
-            "residency": "off" if args.no_residency else (
+            "residency": "off" if c["no_res"] else (
                 "every %d steps, hysteresis %g, <=%d swaps, " % (c["swap_every_steps"], c["hysteresis"], c["max_swaps"]) + (
                 "host copy of every expert" if c.get("mirror") else "in-place HBM/host exchange")),
-            "step_pool": (min(max(args.pool, args.steps + args.warmup), 2048)
-                          if (not args.no_residency and c["n_cold"] > 0) else args.pool),
+            "step_pool": pool_steps if pool_steps is not None else args.pool,
             "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
             "cold_experts": ("read in place from pinned host memory by the FFN (zero copy)"
                              if c.get("zero_copy") and c["T"] <= 64 else "copied into the HBM slot scratch"),
@@ -419,11 +477,17 @@ def build_layers(c, dev, seed_tag="bench"):
     return layers, scratch, slots
 
 
+def popularity(c, layers):
+    """Per layer, experts from most to least popular under the routing generator
+    (expert order for uniform routing)."""
+    E = c["E"]
+    return np.stack([L["perm"] if (L["perm"] is not None and c.get("routing") == "zipf") else np.arange(E)
+                     for L in layers])
+
+
 def gen_pool(c, layers, P, PL, dev):
     """Inputs of PL distinct steps: entry i holds, per layer, the logits of step i and
-    the activations of step i % P.  Routing never repeats within PL steps, so with
-    PL large the residency manager sees the workload's picking frequencies rather
-    than a short loop it could learn."""
+    the activations of step i % P.  Routing never repeats within PL steps."""
     import torch
 
     import synth
@@ -447,6 +511,27 @@ def gen_pool(c, layers, P, PL, dev):
     return pool
 
 
+def host_numa(dev_index: int) -> dict:
+    """The NUMA nodes this process sees and the GPU's node (sysfs): pinned host
+    memory lands on the node of the allocating thread, so with one node there is no
+    placement to choose."""
+    out = {}
+    try:
+        nodes = sorted(int(d[4:]) for d in os.listdir("/sys/devices/system/node")
+                       if d.startswith("node") and d[4:].isdigit())
+        out["nodes"] = nodes
+    except Exception:
+        out["nodes"] = None
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(dev_index), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().lower()
+        path = f"/sys/bus/pci/devices/{bus[-12:]}/numa_node"
+        out["gpu_node"] = int(open(path).read().strip())
+    except Exception:
+        out["gpu_node"] = None
+    return out
+
+
 def measure_link_peak(dev):
     """Host-link read peak: max of a pinned H2D cudaMemcpyAsync and the zero-copy
     16-byte-load probe kernel (the same loop as cold_gather), 1 GiB each."""
@@ -455,7 +540,7 @@ def measure_link_peak(dev):
     import moe_decode_host_gb300 as m
 
     n = 1 << 30
-    src = torch.empty(n, dtype=torch.uint8).pin_memory()
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     src.fill_(1)
     dst = torch.empty(n, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream()
@@ -478,32 +563,32 @@ def measure_link_peak(dev):
     return max(res.values()), res
 
 
-def run_ours(args):
+def step_launches(T, n_cold):
+    """Kernels one layer-step launches (residency swap kernel excluded)."""
+    route = 1 if T <= 64 else 2                      # one-CTA route, or top-k + bucketing
+    gather = 1 + (1 if n_cold > 0 else 0)            # remap, byte copy on the copy stream
+    calls = 4 if n_cold > 0 else 2                   # FFN phases: (gate/up, down) x (hot, cold)
+    per_call = 1 + (1 if T > 8 else 0) + (1 if T > 16 else 0) + (2 if T > 64 else 0)  # decode ranges, gather + tcgen05
+    ffn = 1 + calls * per_call + calls // 2          # activation prep, phases, h prescale per down phase
+    return route + gather + ffn + 1                  # + combine
+
+
+def measure(c, args, dev, dist, world, link_peak, link_detail, local):
+    """Builds the workload's layers, runs W warm-up steps, times K steps on the
+    device (events on the stream, max over ranks), then per-call breakdown steps and
+    the end-to-end leg, all on distinct steps of routing.  Returns the measurement
+    as a dict (the JSON line's fields) and frees the layers."""
     import torch
 
     import moe_decode_host_gb300 as m
 
-    rank, world, local = _rank_env()
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_mod
-
-        dist = dist_mod
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    c = workload(args)
-    c["no_res"] = args.no_residency
     hbm_peak, peak_kind = _peaks()
-    if args.no_link_probe:
-        link_peak, link_detail = None, {"skipped": True}
-    else:
-        link_peak, link_detail = measure_link_peak(dev)
     layers, scratch, slots = build_layers(c, dev)
-    # with residency on, routing comes from up to 2048 distinct steps (no short loop)
-    resid = not args.no_residency and c["n_cold"] > 0
-    P = min(max(args.pool, args.steps + args.warmup), 2048) if resid else args.pool
+    K, W = args.steps, args.warmup
+    Kb = min(K, 64)
+    Ke = 0 if args.no_e2e else K
+    # every phase of the run reads its own steps of routing (up to 2048 distinct)
+    P = min(max(args.pool, W + K + Kb + Ke), 2048)
     pool = gen_pool(c, layers, args.pool, P, dev)
     T, k, H, E = c["T"], c["k"], c["H"], c["E"]
     eb = m.expert_bytes(H, c["I"])
@@ -511,21 +596,20 @@ def run_ours(args):
     bufs = [m.StepBuffers(L["layer"], T) for L in layers]
     for L in layers:
         L["layer"].set_copy_ctas(args.copy_ctas)
-    K, W = args.steps, args.warmup
     counts_log = torch.zeros((K, NL, E), dtype=torch.int32, device=dev)
     ncold_log = torch.zeros((K, NL), dtype=torch.int32, device=dev)
     st = torch.cuda.current_stream()
     nev = 6
 
-    def step(i, timed, ev=None):
+    def step(i, log=None, ev=None):
         swaps = 0
         launches = 0
         for li, L in enumerate(layers):
             lg, x, _ = pool[i % P][li]
             b = bufs[li]
             layer = L["layer"]
-            counts = counts_log[i, li] if timed else b.counts
-            ncold = ncold_log[i, li] if timed else b.n_cold_picked
+            counts = counts_log[log, li] if log is not None else b.counts
+            ncold = ncold_log[log, li] if log is not None else b.n_cold_picked
             if ev is not None:
                 ev[li][0].record(st)
             m.moe_route(layer, lg, T, b.topk_ids, b.topk_w, counts, b.offsets, b.entries, st)
@@ -540,7 +624,7 @@ def run_ours(args):
             m.moe_combine(b.y, b.topk_w, T, k, H, b.out, False, st)
             if ev is not None:
                 ev[li][4].record(st)
-            n = m.residency_update(layer, st)
+            n = m.residency_update(layer, st) if not c["no_res"] else 0
             if ev is not None:
                 ev[li][5].record(st)
             swaps += n
@@ -548,16 +632,13 @@ def run_ours(args):
         return swaps, launches
 
     for i in range(W):
-        step(i, False)
+        step(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    # per-call events go in a separate pass after the timed region (below); inside it
-    # only the library's own events around the cold copy and the FFN kernels run
-    Kb = min(K, 256)
     events = [[[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(NL)] for _ in range(Kb)]
     for L in layers:
-        L["layer"].profile(K)  # events around each cold copy, on the layer's copy stream
+        L["layer"].profile(K)  # events around each cold copy (copy stream) and each FFN call
     clocks = Clocks(local)
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
@@ -571,7 +652,7 @@ def run_ours(args):
     total_swaps = 0
     launches = 0
     for i in range(K):
-        s, n = step(i, True)
+        s, n = step(W + i, log=i)
         total_swaps += s
         launches += n
         if i + 1 in marks:
@@ -594,7 +675,7 @@ def run_ours(args):
         L["layer"].profile(0)
     # per-call durations: Kb further steps with events around every call
     for i in range(Kb):
-        step(K + i, False, events[i])
+        step(W + K + i, ev=events[i])
     torch.cuda.synchronize()
     names = ["moe_route", "cold_gather", "moe_grouped_ffn", "moe_combine", "residency_update"]
     per = {n: [] for n in names}
@@ -617,8 +698,8 @@ def run_ours(args):
     ffn_tflops = ffn_flops / (ffn_k_tot_ms * 1e-3) / 1e12
     # the copy runs on the layer's copy stream, overlapped with the FFN: its duration
     # comes from the events the library records around it on that stream
-    copy_tot_ms = float(sum(float(np.sum(c)) for c in copy_ms))
-    n_copies = int(sum(len(c) for c in copy_ms))
+    copy_tot_ms = float(sum(float(np.sum(cm)) for cm in copy_ms))
+    n_copies = int(sum(len(cm) for cm in copy_ms))
     gather_gbs = float(gather_bytes.sum() / (copy_tot_ms * 1e-3) / 1e9) if copy_tot_ms > 0 else 0.0
     lp = link_peak if link_peak else float("inf")
     tstar_nom = np.maximum(hot_bytes / (HBM_NOMINAL_GBS * 1e9), gather_bytes / (lp * 1e9))
@@ -633,74 +714,64 @@ def run_ours(args):
     mean_cold = float(ncold_h.mean())
     if dom == "moe_grouped_ffn" and T > 64:
         tc_peak, tc_kind = _tensor_peak()
-        tr, src = _traffic("ffn_tc", mean_distinct)
         roof = {"kernel": "moe_grouped_ffn (tcgen05 kind::f16 grouped GEMM for buckets > 64 tokens)",
                 "bound": "tensor", "achieved": ffn_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": ffn_tflops / tc_peak, "traffic": tr, "traffic_source": src,
+                "frac": ffn_tflops / tc_peak, "traffic": _traffic("ffn_tc", mean_distinct),
                 "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
                 "ms_mean": ffn_k_tot_ms / (K * NL), "flops_per_call": ffn_flops / (K * NL), "peak_kind": tc_kind,
                 "hbm_gbs_same_calls": ffn_gbs,
                 "prefill_target": prefill_targets(ffn_flops, float((distinct * eb).sum()) + K * NL * 2.0 * T * H * 2,
                                                   ffn_k_tot_ms, tc_peak, hbm_peak)}
     elif dom == "moe_grouped_ffn":
-        tr, src = _traffic("ffn_decode", mean_distinct)
         roof = {"kernel": "moe_grouped_ffn (decode dequant-GEMV)", "bound": "hbm", "achieved": ffn_gbs,
-                "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak, "traffic": tr,
-                "traffic_source": src, "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
+                "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak,
+                "traffic": _traffic("ffn_decode", mean_distinct),
+                "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
                 "ms_mean": ffn_k_tot_ms / (K * NL), "peak_kind": peak_kind}
     else:
-        tr, src = _traffic("cold_copy", mean_cold)
         roof = {"kernel": "cold_copy_kernel (cold_gather's zero-copy host reads)", "bound": "link",
                 "achieved": gather_gbs, "launches": n_copies, "ms_mean": copy_tot_ms / max(1, n_copies),
                 "peak": link_peak, "unit": "GB/s", "frac": gather_gbs / link_peak if link_peak else None,
-                "traffic": tr, "traffic_source": src,
+                "traffic": _traffic("cold_copy", mean_cold),
                 "traffic_note": "DRAM bytes only: the copy reads host memory over the C2C link and its slot "
                                 "writes stay in L2 during the launch",
                 "algorithmic_bytes_per_launch": float(gather_bytes.sum() / max(1, n_copies)),
                 "peak_kind": "measured in this run (max of pinned cudaMemcpyAsync and zero-copy probe)"}
-    line = {"metric": "MoE layer tokens/s (decode)", "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": K, "warmup": W, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e2m1xf16->f32", "data": "synthetic", "config": _config_json(c, args),
-            "roofline": roof,
-            "kernels": {n: {"ms_mean": float(np.mean(per[n])), "share": tot[n] / max(1e-9, sum(tot.values()))}
-                        for n in names},
-            "kernels_note": "per-call CUDA events over %d further steps run after the timed region" % Kb,
-            "step_roofline": {"tstar_ms_nominal_hbm": float(1e3 * tstar_nom.sum() / K),
-                              "frac_nominal": float(1e3 * tstar_nom.sum() / K / step_ms),
-                              "tstar_ms_measured_hbm": float(1e3 * tstar_meas.sum() / K),
-                              "frac_measured": float(1e3 * tstar_meas.sum() / K / step_ms),
-                              "hbm_peak_gbs": hbm_peak, "link_peak_gbs": link_peak, "link_probe": link_detail},
-            "ffn_hbm_gbs": ffn_gbs, "ffn_kernel_ms_mean": ffn_k_tot_ms / (K * NL), "gather_link_gbs": gather_gbs,
-            "distinct_experts_per_layer_step": float(distinct.mean()),
-            "picks_on_top_73pct_experts": skew_share(counts_h),
-            "repetitions": repetitions,
-            "cold_experts_per_layer_step": float(ncold_h.mean()), "swaps": int(total_swaps),
-            "clocks": clk, "gpu_launches": int(launches),
-            "device_status": [int(L["layer"].status()) for L in layers]}
+    res = {"value": value, "ms_per_step": step_ms, "roofline": roof,
+           "kernels": {n: {"ms_mean": float(np.mean(per[n])), "share": tot[n] / max(1e-9, sum(tot.values()))}
+                       for n in names},
+           "kernels_note": "per-call CUDA events over %d further steps run after the timed region" % Kb,
+           "step_roofline": {"tstar_ms_nominal_hbm": float(1e3 * tstar_nom.sum() / K),
+                             "frac_nominal": float(1e3 * tstar_nom.sum() / K / step_ms),
+                             "tstar_ms_measured_hbm": float(1e3 * tstar_meas.sum() / K),
+                             "frac_measured": float(1e3 * tstar_meas.sum() / K / step_ms),
+                             "hbm_peak_gbs": hbm_peak, "link_peak_gbs": link_peak, "link_probe": link_detail},
+           "ffn_hbm_gbs": ffn_gbs, "ffn_kernel_ms_mean": ffn_k_tot_ms / (K * NL), "gather_link_gbs": gather_gbs,
+           "distinct_experts_per_layer_step": mean_distinct,
+           "picks_on_top_73pct_experts": skew_share(counts_h, popularity(c, layers)),
+           "picks_sampled": int(counts_h.sum()),
+           "repetitions": repetitions,
+           "cold_experts_per_layer_step": mean_cold, "swaps": int(total_swaps),
+           "clocks": clk, "gpu_launches": int(launches),
+           "device_status": [int(L["layer"].status()) for L in layers],
+           "pool_steps": P}
     if not args.no_e2e:
-        line["e2e"] = run_e2e(args, c, layers, pool, bufs, dev, dist, world)
-    if rank == 0 and not args.no_cpu:
-        v, tok, secs, sample = oracle_tokens_per_s(c, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+        res["e2e"] = run_e2e(args, c, layers, pool, bufs, dev, dist, world, first=W + K + Kb, K=Ke)
+    for L in layers:
+        L["layer"].close()
+    if scratch is not None:
+        scratch.close()
+    del layers, scratch, slots, pool, bufs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 
-def step_launches(T, n_cold):
-    """Kernels one layer-step launches (residency swap kernel excluded)."""
-    route = 1 if T <= 64 else 2                      # one-CTA route, or top-k + bucketing
-    gather = 1 + (1 if n_cold > 0 else 0)            # remap, byte copy on the copy stream
-    calls = 4 if n_cold > 0 else 2                   # FFN phases: (gate/up, down) x (hot, cold)
-    per_call = 1 + (1 if T > 8 else 0) + (1 if T > 16 else 0) + (2 if T > 64 else 0)  # decode ranges, gather + tcgen05
-    ffn = 1 + calls * per_call + calls // 2          # activation prep, phases, h prescale per down phase
-    return route + gather + ffn + 1                  # + combine
-
-
-def run_e2e(args, c, layers, pool, bufs, dev, dist, world):
-    """Same steps through the public API with host buffers: pinned host logits and x
-    copied in, the layer output copied back, every step, inside the timed region."""
+def run_e2e(args, c, layers, pool, bufs, dev, dist, world, first, K):
+    """Steps through the public API with host buffers, on routing steps the device-
+    timed region did not use: every step copies its logits and x in from pinned
+    host memory and the layer output back out, inside the timed region; timed with
+    the host clock from the first call to the end of a final synchronize."""
     import torch
 
     import moe_decode_host_gb300 as m
@@ -708,37 +779,91 @@ def run_e2e(args, c, layers, pool, bufs, dev, dist, world):
     T, k, H, E = c["T"], c["k"], c["H"], c["E"]
     P = len(pool)
     NL = len(layers)
-    host_in = [[(torch.from_numpy(pool[p][li][2]).pin_memory(), pool[p][li][1].cpu().pin_memory())
-                for li in range(NL)] for p in range(P)]
+    ids = [(first + i) % P for i in range(K)]
+    host_in = {p: [(torch.from_numpy(pool[p][li][2]).pin_memory(), pool[p][li][1].cpu().pin_memory())
+                   for li in range(NL)] for p in sorted(set(ids))}
     d_lg = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in range(NL)]
     d_x = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(NL)]
-    host_out = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(NL)]
+    host_out = [torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True) for _ in range(NL)]
     st = torch.cuda.current_stream()
-    K = max(1, args.steps)
 
-    def step(i):
+    def step(p):
         for li, L in enumerate(layers):
-            lg_h, x_h = host_in[i % P][li]
+            lg_h, x_h = host_in[p][li]
             d_lg[li].copy_(lg_h, non_blocking=True)
             d_x[li].copy_(x_h, non_blocking=True)
-            m.run_step(L["layer"], bufs[li], d_lg[li], d_x[li], st, residency=not args.no_residency)
+            m.run_step(L["layer"], bufs[li], d_lg[li], d_x[li], st, residency=not c["no_res"])
             host_out[li].copy_(bufs[li].out[:T], non_blocking=True)
 
-    for i in range(args.warmup):
-        step(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(K):
-        step(i)
-    e1.record(st)
+    t0 = time.perf_counter()
+    for p in ids:
+        step(p)
     torch.cuda.synchronize()
-    ms = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+    ms = max_over_ranks(dist, (time.perf_counter() - t0) * 1e3, dev)
     return {"value": job_rate(world, K, T, ms), "unit": "tokens/s",
-            "h2d_bytes_per_step": NL * (T * E * 4 + T * H * 2), "d2h_bytes_per_step": NL * T * H * 2}
+            "h2d_bytes_per_step": NL * (T * E * 4 + T * H * 2), "d2h_bytes_per_step": NL * T * H * 2,
+            "timing": "host clock around the steps, ending in a synchronize; routing steps disjoint from the "
+                      "device-timed region's"}
+
+
+PER_BATCH = ((8, "c2"), (32, "c2"))  # decode batches the default line also carries (Zipf s=1.1)
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = _rank_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    c = workload(args)
+    if args.no_link_probe:
+        link_peak, link_detail = None, {"skipped": True}
+    else:
+        link_peak, link_detail = measure_link_peak(dev)
+        link_detail["numa"] = host_numa(local)
+    res = measure(c, args, dev, dist, world, link_peak, link_detail, local)
+    pool_steps = res.pop("pool_steps")
+    line = {"metric": "MoE layer tokens/s (decode)", "value": res.pop("value"), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xf16->f32",
+            "data": "synthetic", "config": _config_json(c, args, pool_steps)}
+    line.update(res)
+    default_run = (args.config == "c1" and args.batch is None and args.experts is None and not args.zero_copy
+                   and args.n_hot is None)
+    if default_run and not args.no_per_batch:
+        per_batch = {}
+        for T, name in PER_BATCH:
+            cb = workload(args, config=name, batch=T)
+            r = measure(cb, args, dev, dist, world, link_peak, link_detail, local)
+            ps = r.pop("pool_steps")
+            per_batch[str(T)] = {"config": _config_json(cb, args, ps), "value": r["value"], "unit": "tokens/s",
+                                 "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
+                                 "step_roofline": {kk: v for kk, v in r["step_roofline"].items()
+                                                   if kk != "link_probe"},
+                                 "e2e": r.get("e2e"), "kernels": r["kernels"],
+                                 "ffn_hbm_gbs": r["ffn_hbm_gbs"], "gather_link_gbs": r["gather_link_gbs"],
+                                 "distinct_experts_per_layer_step": r["distinct_experts_per_layer_step"],
+                                 "cold_experts_per_layer_step": r["cold_experts_per_layer_step"],
+                                 "picks_on_top_73pct_experts": r["picks_on_top_73pct_experts"],
+                                 "repetitions": r["repetitions"], "clocks": r["clocks"],
+                                 "gpu_launches": r["gpu_launches"], "device_status": r["device_status"]}
+        line["per_batch"] = per_batch
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
 
 
 def main():

@@ -58,7 +58,12 @@ def test_default_run_is_the_batch1_decode_layer():
     c = bench.workload(a)
     assert (c["H"], c["I"], c["E"], c["n_hot"], c["n_cold"], c["k"], c["T"]) == (4096, 3072, 384, 255, 129, 6, 1)
     assert c["routing"] == "uniform" and c["layers"] == 1
-    assert a.no_residency and not c["mirror"] and not c["zero_copy"]
+    assert c["no_res"] and not c["mirror"] and not c["zero_copy"]
+    # the same line carries the skewed decode batches of 8 and 32 tokens
+    assert [(T, n) for T, n in bench.PER_BATCH] == [(8, "c2"), (32, "c2")]
+    cb = bench.workload(a, config="c2", batch=32)
+    assert (cb["T"], cb["routing"], cb["s"], cb["n_hot"], cb["n_cold"]) == (32, "zipf", 1.1, 255, 129)
+    assert cb["no_res"]
 
 
 def test_workload_shapes_of_the_other_configs():
@@ -66,7 +71,7 @@ def test_workload_shapes_of_the_other_configs():
     assert (c["T"], c["routing"], c["s"], c["E"], c["n_hot"]) == (32, "zipf", 1.5, 384, 255)
     a = _args("--config", "c3")
     c = bench.workload(a)
-    assert c["layers"] == 20 and c["swap_every"] == 16 and not a.no_residency
+    assert c["layers"] == 20 and c["swap_every"] == 16 and not c["no_res"]
     assert (c["swap_every_steps"], c["max_swaps"], c["hysteresis"]) == (16, 8, 3.0)
     assert not c["mirror"]  # 20 layers keep the in-place exchange
     c = bench.workload(_args("--config", "c4"))
@@ -93,17 +98,24 @@ def test_prefill_targets_on_the_8192_token_layer():
 def test_skew_share_statistic():
     import numpy as np
 
-    # 100 experts, 2 layers: picks only on experts 0..72 -> everything on the top 73%
-    c = np.zeros((3, 2, 100), np.int32)
+    ident = np.arange(100)[None, :]
+    # 100 experts: picks only on experts 0..72, ranked first by the generator -> all on the top 73%
+    c = np.zeros((3, 1, 100), np.int32)
     c[:, :, :73] = 1
-    assert bench.skew_share(c) == 1.0
+    assert bench.skew_share(c, ident) == 1.0
     # uniform picks -> 73%
-    assert abs(bench.skew_share(np.ones((5, 1, 100), np.int32)) - 0.73) < 1e-12
-    # per layer: each layer's own top experts count (layer 0 on 0..72, layer 1 on 27..99)
+    assert abs(bench.skew_share(np.ones((5, 1, 100), np.int32), ident) - 0.73) < 1e-12
+    # the generator's ranking decides, not the sample: a few picks on low-ranked experts
+    # count as off the top even though they are the only experts picked
+    c = np.zeros((1, 1, 100), np.int32)
+    c[0, 0, 90:96] = 1
+    assert bench.skew_share(c, ident) == 0.0
+    # per layer, each layer's own ranking (layer 1 ranks experts in reverse)
     c = np.zeros((1, 2, 100), np.int32)
     c[0, 0, :73] = 2
     c[0, 1, 27:] = 2
-    assert bench.skew_share(c) == 1.0
+    rank = np.stack([np.arange(100), np.arange(100)[::-1]])
+    assert bench.skew_share(c, rank) == 1.0
 
 
 def test_repetition_split_and_spread():
