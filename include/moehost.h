@@ -207,6 +207,25 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
                     const int32_t* offsets, const int32_t* entries, float* y, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Arithmetic of calls with more than 64 tokens (prefill-sized buckets).
+ *  kind 0 (default): weights expanded exactly from MXFP4 to f16 and multiplied with
+ *         f16 activations on tcgen05 kind::f16 tensor cores (buckets above 64
+ *         tokens; smaller ones on the decode kernel), fp32 accumulation: the result
+ *         of the unquantised layer within rounding.
+ *  kind 1 (all-FP4): x and h are converted to MXFP4 as well (each 32-element block
+ *         of a row gets the exponent floor(log2(max |v|)) - 2 clamped to
+ *         [-127, 127], each element the nearest E2M1 value, ties to the even code,
+ *         saturating at 6), and every bucket of the call runs on block-scaled
+ *         tcgen05 kind::mxf4 tensor cores with fp32 accumulation ("A 475 GB Model
+ *         Across Two Workstations, With the Table on Disk", Abstract: the experts
+ *         ship in MXFP4).  The result is the layer with both activations
+ *         quantised, which differs from the unquantised layer by the quantisation
+ *         of x and h.
+ * Calls of at most 64 tokens always run the decode kernel (unquantised
+ * activations).  moe_ffn_workspace_bytes follows the kind; set it before sizing
+ * the workspace.  Errors: MOE_ERR_INVALID_ARG (null, kind not 0 or 1). */
+int moe_layer_set_prefill_kind(moe_layer* L, int kind);
+
 /* moe_grouped_ffn for callers that cannot allocate device memory (an engine that
  * has given all free HBM to its own pools and forbids later allocations, code
  * running during a global-mode stream capture, embedders with their own

@@ -110,6 +110,11 @@ class Layer:
     def clear_status(self):
         check(lib.moe_clear_status(self.handle), "moe_clear_status")
 
+    def set_prefill_kind(self, kind: int):
+        """0: exact-weight f16 tensor-core path for calls of more than 64 tokens;
+        1: all-FP4 block-scaled path (x and h quantised to MXFP4)."""
+        check(lib.moe_layer_set_prefill_kind(self.handle, kind), "moe_layer_set_prefill_kind")
+
     def set_copy_ctas(self, ctas: int):
         check(lib.moe_layer_set_copy_ctas(self.handle, ctas), "moe_layer_set_copy_ctas")
 

@@ -11,32 +11,11 @@
 // the output layout: element k of a row in byte k/2, low nibble when k is even,
 // one scale byte per block.
 #include "internal.cuh"
+#include "mx.cuh"
 
 namespace {
 
 constexpr int kQuantThreads = 256;  // 8 warps, one 32-element block each
-
-// floor(log2(a)) of a positive finite float given by its bits.
-__device__ __forceinline__ int floor_log2_bits(uint32_t b) {
-    const int ef = (int)((b >> 23) & 0xffu);
-    if (ef != 0) return ef - 127;
-    const uint32_t m = b & 0x7fffffu;  // subnormal: m * 2^-149, m != 0
-    return (31 - __clz((int)m)) - 149;
-}
-
-// E2M1 code (sign clear) of r >= 0: round to nearest with the decision points at
-// the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5, where the even code wins;
-// anything above 5 takes the largest magnitude, 6.
-__device__ __forceinline__ uint32_t e2m1_code(float r) {
-    if (r <= 0.25f) return 0u;
-    if (r < 0.75f) return 1u;
-    if (r <= 1.25f) return 2u;
-    if (r < 1.75f) return 3u;
-    if (r <= 2.5f) return 4u;
-    if (r < 3.5f) return 5u;
-    if (r <= 5.0f) return 6u;
-    return 7u;
-}
 
 // One warp per block of 32 consecutive elements of the flattened [rows][K] input
 // (K a multiple of 32, so blocks never straddle rows): lane i takes element i.
@@ -49,12 +28,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_mxfp4_kernel(const uint16
     const uint16_t h = x[blk * 32 + lane];
     const uint32_t mag = (uint32_t)(h & 0x7fffu) << 16;  // |v| as fp32 bits (bf16 widens exactly)
     const uint32_t amax = __reduce_max_sync(0xffffffffu, mag);  // bit order = value order for |v|
-    int e = -127;
-    if (amax != 0u) e = max(-127, min(127, floor_log2_bits(amax) - 2));
-    // 2^-e as a float (e <= 125 for finite bf16 input, so 127 - e is in [2, 254]);
-    // the product is exact: a power of two times a bf16 value, below 8 in magnitude
-    const float r = __uint_as_float(mag) * __uint_as_float((uint32_t)(127 - e) << 23);
-    const uint32_t code = e2m1_code(r) | ((uint32_t)(h >> 15) << 3);
+    const int e = moe::mx_block_exp(amax);
+    const uint32_t code = moe::e2m1_code(moe::mx_scaled(mag, e)) | ((uint32_t)(h >> 15) << 3);
     const uint32_t odd = __shfl_down_sync(0xffffffffu, code, 1);
     if ((lane & 1) == 0) nib[blk * 16 + (lane >> 1)] = (uint8_t)(code | (odd << 4));
     if (lane == 0) scale[blk] = (uint8_t)(e + 127);

@@ -56,6 +56,7 @@ struct moe_layer {
     int fprof_n = 0;
     long steps = 0;
     int fault = 0;
+    int prefill_kind = 0;  // moe_layer_set_prefill_kind
 };
 
 namespace {
@@ -383,9 +384,28 @@ int moe_gather_join(moe_layer* L, void* stream) {
     return cuda_status(join_copy(L, S(stream)));
 }
 
+namespace {
+// Calls with more tokens than a decode-sized bucket can hold run the block-scaled
+// (all-FP4) path when the layer asks for it.
+bool use_mx(const moe_layer* L, int T) { return L->prefill_kind == 1 && T > kTcMinTokens; }
+
+size_t ffn_workspace(const moe_layer* L, int T) {
+    const size_t d = ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I);
+    if (!use_mx(L, T)) return d;
+    const size_t m = ffn_mx_workspace(T, L->p.k, L->p.H, L->p.I);
+    return d > m ? d : m;
+}
+}  // namespace
+
 int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes) {
     if (!L || T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
-    *bytes = ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I);
+    *bytes = ffn_workspace(L, T);
+    return MOE_OK;
+}
+
+int moe_layer_set_prefill_kind(moe_layer* L, int kind) {
+    if (!L || kind < 0 || kind > 1) return MOE_ERR_INVALID_ARG;
+    L->prefill_kind = kind;
     return MOE_OK;
 }
 
@@ -396,7 +416,7 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     if (T == 0) return MOE_OK;
     if (!x || !phys_ids || !counts || !offsets || !entries || !y || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(workspace, 256) || !aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
-    if (workspace_bytes < ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < ffn_workspace(L, T)) return MOE_ERR_INVALID_ARG;
     FfnArgs a;
     memset(&a, 0, sizeof a);
     a.ptr = L->d_ptr;
@@ -425,6 +445,28 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     // join, end (the two middle events coincide when no copy is pending)
     cudaEvent_t* pe = L->fprof_n < (int)L->fprof_ev.size() / 4 ? &L->fprof_ev[4 * L->fprof_n++] : nullptr;
     cudaError_t err = pe ? cudaEventRecord(pe[0], st) : cudaSuccess;
+    if (use_mx(L, T)) {
+        // block-scaled path: x converted to MXFP4 once, then per placement class the
+        // gate/up kernel (h converted in its epilogue) and the down kernel; experts in
+        // HBM first while a cold copy is in flight
+        if (err == cudaSuccess) err = launch_ffn_mx_prep(a, workspace, st);
+        if (err == cudaSuccess && L->copy_pending) {
+            err = launch_ffn_mx(a, 0, 1, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 1, L->sm_count, st);
+            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+            if (err == cudaSuccess) err = join_copy(L, st);
+            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 2, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 2, L->sm_count, st);
+        } else {
+            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 0, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 0, L->sm_count, st);
+        }
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[3], st);
+        return cuda_status(err);
+    }
     if (err == cudaSuccess) err = launch_ffn_prep(a, workspace, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (L->p.zero_copy && L->p.n_cold > 0 && T <= kTcMinTokens) {

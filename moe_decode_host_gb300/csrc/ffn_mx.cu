@@ -1,0 +1,705 @@
+// Grouped SwiGLU expert FFN on block-scaled FP4 tensor cores (the all-FP4 prefill
+// mode): tcgen05.mma kind::mxf4 with both operands in MXFP4.
+//
+// "DeepSeek-V4.1-Flash on One GB300 Without the Second GPU", section 1: the layer
+// runs all experts in one call; "A 475 GB Model Across Two Workstations, With the
+// Table on Disk", Abstract: the routed experts ship in MXFP4 (E2M1 elements, one
+// E8M0 scale per 32 elements along the reduction dimension).  The weights feed the
+// tensor cores as they are stored; the activations are converted to the same
+// format: x once per call (mx_xprep_kernel, bucket order), h by the gate/up
+// kernel's epilogue, which owns whole 32-element blocks of h (one 32-row slice of
+// the I dimension per warp and token).  The scale factors reach tensor memory
+// through tcgen05.st, so the MMA applies them per 32-element block:
+//   D[128 weight rows x N tokens] (+)= sum over blocks of (A_blk * 2^sa) (B_blk * 2^sb)^T
+// with fp32 accumulation in tensor memory.
+//
+// Tensor-memory layout of the scale factors (kind::mxf4, M = 128, scale_vec::2X;
+// established with in-bounds checks on this GPU against a CPU product): the MMA
+// reads the two block scales of weight row m from lane m at column sfa + m / 32,
+// bytes sf_id and sf_id + 1; for token column n, a row of D in lane quarter q
+// reads them from quarter q, lane n % 32, column sfb + n / 32, so the token scales
+// are written to all four quarters.  One 32-bit word holds four blocks (the K
+// range of two MMAs, sf_id 0 and 2).
+//
+// Warp roles of one persistent CTA per SM (12 warps):
+//   warp 0       takes tasks (an expert and a 128-row tile) from a launch-wide
+//                counter, experts with the most tokens first, publishes them in a
+//                shared-memory queue, and loads the tile's E2M1 rows by TMA, 256
+//                elements of K per stage (128-byte swizzle; gate and up rows in the
+//                gate/up phase, w2 rows in the down phase);
+//   warp 1       loads the tokens' E2M1 activation rows of each stage by TMA (up to
+//                192 bucket rows, 32 per box);
+//   warp 2       owns tensor memory; one thread issues the MMAs (four of K = 64 per
+//                matrix and stage);
+//   warps 4-7    scale writers: each thread reads its weight row's scale words and
+//                the tokens' activation scale words of a stage and stores them into
+//                a ring of scale slots in tensor memory;
+//   warps 8-11   epilogue: tensor memory -> registers; gate/up phase: h = SiLU(g) u
+//                with the accurate exponential (so that the quantisation of h takes
+//                the same decisions as an exact evaluation except within rounding of
+//                a decision point), converted to MXFP4 across the warp's 32 rows and
+//                stored in bucket order; down phase: y rows.
+// Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT, and the CTA
+// drains its copies and MMAs before it frees tensor memory and returns.
+#include <cuda.h>
+
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMxBM = 128;                     // weight rows per tile = tensor-memory lanes
+constexpr int kMxBK = 256;                     // K elements per stage
+constexpr int kMxRowB = kMxBK / 2;             // bytes of a row per stage
+constexpr int kMxTile = kMxBM * kMxRowB;       // 16 KB: one matrix's rows of a stage
+constexpr int kMxNMax = 192;                   // token columns per pass
+constexpr int kMxBox = 32;                     // activation rows per TMA box
+constexpr int kMxBStage = kMxNMax * kMxRowB;   // 24 KB
+constexpr int kMxBStages = 3;
+constexpr int kMxSfStages = 3;
+constexpr int kMxThreads = 384;
+constexpr int kMxFirstSf = 4;
+constexpr int kMxFirstEpi = 8;
+constexpr int kMxMaxE = 1024;
+constexpr int kMxTaskQ = 4;
+// Tensor memory: accumulators in [0, 384) -- gate and up (192 columns each) in the
+// gate/up phase, two buffers in the down phase -- and the scale slots from 384.
+constexpr uint32_t kMxAccCols = 192;
+constexpr uint32_t kMxSf0 = 384;
+constexpr uint32_t kMxTmemCols = 512;
+constexpr int kMxTakers = 1 + 1 + 4 + 4;  // activation producer, issuer, scale writers, epilogue
+constexpr int kMxEpiStage = 16 * 16;      // epilogue staging per warp: 16 tokens x 16 bytes of h
+
+template <int P>
+__host__ __device__ constexpr int mx_mats() { return P == 0 ? 2 : 1; }  // weight matrices per stage
+template <int P>
+__host__ __device__ constexpr int mx_astages() { return P == 0 ? 4 : 6; }
+// scale slot: weight words (8 columns per matrix: two words x four quarter columns),
+// then token words (16 columns: word j of the stage at 8j + token group)
+template <int P>
+__host__ __device__ constexpr uint32_t mx_sfb_col() { return P == 0 ? 16u : 8u; }
+template <int P>
+__host__ __device__ constexpr uint32_t mx_sf_cols() { return mx_sfb_col<P>() + 16u; }
+static_assert(kMxSf0 + kMxSfStages * mx_sf_cols<0>() <= kMxTmemCols, "tensor memory budget");
+
+struct MxTask {
+    const uint8_t* blob;
+    int e, rb, cnt, off, phys;
+    bool valid;
+};
+
+struct alignas(16) MxHead {
+    uint64_t a_full[6], a_empty[6];
+    uint64_t b_full[kMxBStages], b_empty[kMxBStages];
+    uint64_t sf_full[kMxSfStages], sf_empty[kMxSfStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t tq_full[kMxTaskQ], tq_empty[kMxTaskQ];
+    int tq[kMxTaskQ];
+    MxTask tqt[kMxTaskQ];
+    uint32_t tmem_base;
+    int abort;
+    int D;
+    alignas(16) int key[kMxMaxE];  // tokens of each active expert, -1 when inactive
+    int list[kMxMaxE];             // active experts, most tokens first
+};
+
+template <int P>
+struct MxSmem {
+    static constexpr size_t kB = (size_t)mx_astages<P>() * mx_mats<P>() * kMxTile;  // after the weight ring
+    static constexpr size_t kStg = kB + (size_t)kMxBStages * kMxBStage;
+    static constexpr size_t kHead = kStg + 4 * kMxEpiStage;
+    static constexpr size_t kTotal = 1024 + kHead + sizeof(MxHead);
+};
+static_assert(MxSmem<0>::kTotal <= 232448 && MxSmem<1>::kTotal <= 232448, "shared memory budget of one CTA");
+
+// kind::mxf4 instruction descriptor: A and B E2M1 (format 1), both K-major, UE8M0
+// scales, M = 128, N tokens, scale-factor byte selector sf for both operands.
+__device__ __forceinline__ uint32_t mx_idesc(int N, uint32_t sf) {
+    return (sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(kMxBM >> 4) << 24) | (sf << 29);
+}
+
+__device__ __forceinline__ void mx_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mx_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void mx_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
+    uint32_t v;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ MxTask mx_task(const FfnArgs& a, const MxHead& hd, int task, int tiles) {
+    MxTask t;
+    t.e = hd.list[task / tiles];
+    t.rb = task % tiles;
+    t.cnt = __ldg(a.counts + t.e);
+    t.off = __ldg(a.offsets + t.e);
+    t.phys = __ldg(a.phys_ids + __ldg(a.entries + t.off));
+    t.valid = t.phys >= 0 && t.phys < a.n_phys;
+    t.blob = t.valid ? a.ptr[t.phys] : nullptr;
+    return t;
+}
+
+__device__ __forceinline__ int mx_take(MxHead& hd, int k, const FfnArgs& a, volatile int* abort, int who, MxTask& t) {
+    const int j = k % kMxTaskQ;
+    if (!mbar_wait_fast(&hd.tq_full[j], (unsigned)(k / kMxTaskQ) & 1u, abort, a.status, a.diag, 30, j, k, who))
+        return -1;
+    const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    t = hd.tqt[j];
+    mbar_arrive(&hd.tq_empty[j]);
+    return task;
+}
+
+__device__ __forceinline__ int mx_warp_take(MxHead& hd, int k, const FfnArgs& a, volatile int* abort, int who,
+                                            MxTask& t) {
+    const int j = k % kMxTaskQ;
+    if (!warp_wait(&hd.tq_full[j], (unsigned)(k / kMxTaskQ) & 1u, a, abort, 30, j, k, who)) return -1;
+    const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
+    t = hd.tqt[j];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&hd.tq_empty[j]);
+    return task;
+}
+
+// MMA width of a pass over nb tokens: a multiple of 16 (the M = 128 shape's step).
+__device__ __forceinline__ int mx_ncols(int nb) { return (nb + 15) & ~15; }
+
+// Scale words of one stage for one thread of a scale-writer warp: its weight row's
+// two words (blocks 8s..8s+7) per matrix and, for token columns lane + 32c, the two
+// words of each (clamped to the last bucket row; columns past the pass are unused).
+template <int P>
+struct MxScales {
+    uint32_t wa[2][2];  // [matrix][word]
+    uint32_t wb[2][6];  // [word][token group]
+};
+
+template <int P>
+__device__ __forceinline__ void mx_load_scales(MxScales<P>& v, const uint8_t* const (&sa)[2], const uint32_t* sfb,
+                                               int R, int row0, int s, int nj) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int mt = 0; mt < mx_mats<P>(); ++mt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) v.wa[mt][j] = j < nj ? ld_u32(sa[mt] + 8 * s + 4 * j) : 0u;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+            const int row = min(row0 + 32 * c + lane, R - 1);
+            v.wb[j][c] = j < nj ? ld_word(sfb + (size_t)(2 * s + j) * R + row) : 0u;
+        }
+}
+
+template <int P>
+__global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
+                                                               int sel, int ctr) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = base;
+    uint8_t* sB = base + MxSmem<P>::kB;
+    MxHead& hd = *reinterpret_cast<MxHead*>(base + MxSmem<P>::kHead);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, I = a.I;
+    const int K = P == 0 ? H : I;
+    const int nks = (K + kMxBK - 1) / kMxBK;  // stages per pass; the last may hold 128 elements
+    const int tiles = (P == 0 ? I : H) / kMxBM;
+    const int R = a.T * a.k;  // bucket rows
+    constexpr int AS = mx_astages<P>();
+    constexpr int MATS = mx_mats<P>();
+    volatile int* abort = &hd.abort;
+
+    // active experts (at least one token, in the selected placement class), most
+    // tokens first (ties by id): every thread keys some experts, then ranks its own
+    for (int e = threadIdx.x; e < a.E; e += kMxThreads) {
+        const int c = __ldg(a.counts + e);
+        bool act = c > 0;
+        if (act && sel != 0) {
+            const bool hot = __ldg(a.loc + e) < a.n_hot;
+            act = (sel == 1) ? hot : !hot;
+        }
+        hd.key[e] = act ? c : -1;
+    }
+    for (int e = a.E + threadIdx.x; e < ((a.E + 3) & ~3); e += kMxThreads) hd.key[e] = -1;  // pad to 4
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += kMxThreads) {
+        const int ke = hd.key[e];
+        if (ke < 0) continue;
+        int r = 0;
+        for (int f = 0; f < a.E; f += 4) {
+            const int4 k4 = *reinterpret_cast<const int4*>(&hd.key[f]);
+            r += (k4.x > ke || (k4.x == ke && f < e)) + (k4.y > ke || (k4.y == ke && f + 1 < e)) +
+                 (k4.z > ke || (k4.z == ke && f + 2 < e)) + (k4.w > ke || (k4.w == ke && f + 3 < e));
+        }
+        hd.list[r] = e;
+    }
+    if (warp == 0) {
+        int cnt = 0;
+        for (int b0 = 0; b0 < a.E; b0 += 32) {
+            const int e = b0 + lane;
+            cnt += __popc(__ballot_sync(0xffffffffu, e < a.E && hd.key[e] >= 0));
+        }
+        if (lane == 0) {
+            hd.D = cnt;
+            hd.abort = 0;
+            for (int s = 0; s < AS; ++s) {
+                mbar_init(&hd.a_full[s], 1);
+                mbar_init(&hd.a_empty[s], 1);
+            }
+            for (int s = 0; s < kMxBStages; ++s) {
+                mbar_init(&hd.b_full[s], 1);
+                mbar_init(&hd.b_empty[s], 1);
+            }
+            for (int s = 0; s < kMxSfStages; ++s) {
+                mbar_init(&hd.sf_full[s], 4);
+                mbar_init(&hd.sf_empty[s], 1);
+            }
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&hd.acc_full[s], 1);
+                mbar_init(&hd.acc_empty[s], 4);
+            }
+            for (int j = 0; j < kMxTaskQ; ++j) {
+                mbar_init(&hd.tq_full[j], 1);
+                mbar_init(&hd.tq_empty[j], kMxTakers);
+            }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
+    if (warp == 2) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&hd.tmem_base)),
+                     "r"(kMxTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // the quantised activations and the outputs belong to the previous kernel until it completes
+    grid_dep_wait();
+    const uint32_t tmem = hd.tmem_base;
+    const int ntask = hd.D * tiles;
+
+    if (warp == 0) {
+        // ---------------- task fetcher, weight producer (lane 0) ----------------
+        if (lane == 0) {
+            int as = 0;
+            unsigned aph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int j = k % kMxTaskQ;
+                if (!mbar_wait_fast(&hd.tq_empty[j], ((unsigned)(k / kMxTaskQ) & 1u) ^ 1u, abort, a.status, a.diag,
+                                    31, j, k, 0))
+                    break;
+                int task = atomicAdd(a.task_ctr + ctr, 1);
+                if (task >= ntask) task = -1;
+                MxTask t{};
+                if (task >= 0) t = mx_task(a, hd, task, tiles);
+                *reinterpret_cast<volatile int*>(&hd.tq[j]) = task;
+                hd.tqt[j] = t;
+                mbar_arrive(&hd.tq_full[j]);
+                if (task < 0) break;
+                if (!t.valid) continue;
+                // the decode kernel's views of the two planes: 128-byte boxes of 32 (w13)
+                // or 64 (w2) rows with the 128-byte swizzle, stacked to 128 rows
+                const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13n : &a.tmaps[t.phys].w2n;
+                constexpr int box_rows = P == 0 ? 32 : 64;
+                asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                const int r0 = t.rb * kMxBM;
+                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.a_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&hd.a_full[as], (unsigned)(MATS * kMxTile));
+#pragma unroll
+                        for (int mt = 0; mt < MATS; ++mt)
+#pragma unroll
+                            for (int i = 0; i < kMxBM / box_rows; ++i)
+                                tma_load_2d(sA + (size_t)(as * MATS + mt) * kMxTile + i * box_rows * kMxRowB, map,
+                                            s * kMxRowB, (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as]);
+                        advance(as, aph, AS);
+                    }
+                }
+            }
+            for (int s = 0; s < AS; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- activation producer (lane 0) ----------------
+        if (lane == 0) {
+            int bs = 0;
+            unsigned bph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                MxTask t;
+                const int task = mx_take(hd, k, a, abort, 1, t);
+                if (task < 0) break;
+                if (!t.valid) continue;
+                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                    const int boxes = (mx_ncols(min(kMxNMax, t.cnt - tb)) + kMxBox - 1) / kMxBox;
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB));
+                        for (int bx = 0; bx < boxes; ++bx)
+                            tma_load_2d(sB + (size_t)bs * kMxBStage + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB,
+                                        t.off + tb + kMxBox * bx, &hd.b_full[bs]);
+                        advance(bs, bph, kMxBStages);
+                    }
+                }
+            }
+            for (int s = 0; s < kMxBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------- MMA issuer (lane 0) ----------------
+        if (lane == 0) {
+            int as = 0, bs = 0, ss = 0, buf = 0;
+            unsigned aph = 0, bph = 0, sph = 0, accph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                MxTask t;
+                const int task = mx_take(hd, k, a, abort, 2, t);
+                if (task < 0) break;
+                if (!t.valid) continue;
+                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                    const int N = mx_ncols(min(kMxNMax, t.cnt - tb));
+                    const uint32_t id0 = mx_idesc(N, 0u), id2 = mx_idesc(N, 2u);
+                    if (!mbar_wait_fast(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, abort, a.status, a.diag, 34,
+                                        buf, 0, task)) {
+                        ok = false;
+                        break;
+                    }
+                    accph ^= 1u << buf;
+                    tc_fence_after();
+                    for (int s = 0; s < nks; ++s) {
+                        if (!mbar_wait_fast(&hd.a_full[as], aph, abort, a.status, a.diag, 35, as, s, task) ||
+                            !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 36, bs, s, task) ||
+                            !mbar_wait_fast(&hd.sf_full[ss], sph, abort, a.status, a.diag, 37, ss, s, task)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int nkk = min(4, (K - s * kMxBK) / 64);  // K steps of 64 in this stage
+                        const uint32_t sf = tmem + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
+                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * kMxBStage));
+#pragma unroll
+                        for (int mt = 0; mt < MATS; ++mt) {
+                            const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * kMxAccCols;
+                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxTile));
+                            for (int kk = 0; kk < nkk; ++kk) {
+                                // a K step of 64 elements advances both start addresses by 32 bytes;
+                                // its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2
+                                const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                                mx_mma(d, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id2 : id0,
+                                       sf + 8u * mt + 4u * (uint32_t)(kk >> 1),
+                                       sf + mx_sfb_col<P>() + 8u * (uint32_t)(kk >> 1), acc);
+                            }
+                        }
+                        tc_commit(&hd.a_empty[as]);
+                        tc_commit(&hd.b_empty[bs]);
+                        tc_commit(&hd.sf_empty[ss]);
+                        advance(as, aph, AS);
+                        advance(bs, bph, kMxBStages);
+                        advance(ss, sph, kMxSfStages);
+                    }
+                    if (!ok) break;
+                    tc_commit(&hd.acc_full[buf]);
+                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 384)
+                }
+            }
+            // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
+            // last commit of every slot
+            for (int s = 0; s < AS; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
+            for (int s = 0; s < kMxBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < kMxSfStages; ++s) mbar_drain(&hd.sf_empty[s], (s < ss) ? sph : (sph ^ 1u));
+        }
+        __syncwarp();
+    } else if (warp >= kMxFirstSf && warp < kMxFirstSf + 4) {
+        // ---------------- scale writers ----------------
+        // thread = weight row 32 q + lane of the tile (q = lane quarter); every quarter
+        // also stores the token words, which each quarter's rows read from their own
+        const int q = warp & 3;
+        const uint32_t qaddr = tmem + ((uint32_t)(q * 32) << 16);
+        const uint32_t* sfb = P == 0 ? a.xs : a.hs;
+        int ss = 0;
+        unsigned sph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            MxTask t;
+            const int task = mx_warp_take(hd, k, a, abort, 3, t);
+            if (task < 0) break;
+            if (!t.valid) continue;
+            const int r0 = t.rb * kMxBM;
+            const size_t srl = (size_t)K / 32;  // scale bytes per weight row
+            const uint8_t* sa[2];
+            sa[0] = t.blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + 32 * q + lane) * srl;
+            sa[1] = P == 0 ? t.blob + a.w13s + (size_t)(I + r0 + 32 * q + lane) * srl : sa[0];
+            for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                const int row0 = t.off + tb;
+                MxScales<P> cur, nxt;
+                mx_load_scales<P>(cur, sa, sfb, R, row0, 0, min(2, K / 128));
+                for (int s = 0; s < nks; ++s) {
+                    // the next stage's words are in flight while this one waits for its slot
+                    if (s + 1 < nks) mx_load_scales<P>(nxt, sa, sfb, R, row0, s + 1, min(2, (K - (s + 1) * kMxBK) / 128));
+                    if (!warp_wait(&hd.sf_empty[ss], sph ^ 1u, a, abort, 38, ss, s, task)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t col = qaddr + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
+                    // weight words: matrix mt, word j at column 8 mt + 4 j + q (this lane = row 32 q + lane)
+                    uint32_t va[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int mt = i >> 3, j = (i >> 2) & 1;
+                        va[i] = (mt < MATS && (i & 3) == q) ? cur.wa[mt][j] : 0u;
+                    }
+                    if constexpr (P == 0) {
+                        mx_st16(col, va);
+                    } else {
+                        uint32_t v8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v8[i] = va[i];
+                        mx_st8(col, v8);
+                    }
+                    // token words: word j of token group c at column 8 j + c
+                    uint32_t vb[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) vb[i] = (i & 7) < 6 ? cur.wb[i >> 3][i & 7] : 0u;
+                    mx_st16(col + mx_sfb_col<P>(), vb);
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&hd.sf_full[ss]);
+                    advance(ss, sph, kMxSfStages);
+                    cur = nxt;
+                }
+            }
+        }
+    } else if (warp >= kMxFirstEpi) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // tensor-memory lane quarter: weight rows 32 q ..
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        uint8_t* stg = base + MxSmem<P>::kStg + (size_t)q * kMxEpiStage;
+        int buf = 0;
+        unsigned accph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            MxTask t;
+            const int task = mx_warp_take(hd, k, a, abort, 4, t);
+            if (task < 0) break;
+            const int r0 = t.rb * kMxBM;
+            if (!t.valid) {
+                // zero outputs for an expert whose physical id is out of range (its h is
+                // never read: the down phase sees the same id)
+                if (t.rb == 0 && threadIdx.x == kMxFirstEpi * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
+                if (P == 1)
+                    for (int c = 0; c < t.cnt; ++c) a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + 32 * q + lane] = 0.f;
+                continue;
+            }
+            for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                const int nb = min(kMxNMax, t.cnt - tb);
+                if (!warp_wait(&hd.acc_full[buf], (accph >> buf) & 1u, a, abort, 39, buf, tb, task)) {
+                    ok = false;
+                    break;
+                }
+                accph ^= 1u << buf;
+                tc_fence_after();
+                const uint32_t d = lane_addr + (uint32_t)buf * kMxAccCols;
+                for (int cb = 0; cb < nb; cb += 16) {
+                    if constexpr (P == 0) {
+                        float g[16], u[16];
+                        tc_ld16x2(d + cb, d + kMxAccCols + cb, g, u);
+                        int es[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float h = g[i] / (1.0f + expf(-g[i])) * u[i];
+                            const uint32_t bits = __float_as_uint(h);
+                            const uint32_t mag = bits & 0x7fffffffu;
+                            // one 32-element block of h per token: this warp's 32 rows
+                            const int e = mx_block_exp(__reduce_max_sync(0xffffffffu, mag));
+                            const uint32_t code = e2m1_code(mx_scaled(mag, e)) | ((bits >> 31) << 3);
+                            const uint32_t odd = __shfl_down_sync(0xffffffffu, code, 1);
+                            if ((lane & 1) == 0) stg[i * 16 + (lane >> 1)] = (uint8_t)(code | (odd << 4));
+                            es[i] = e;
+                        }
+                        __syncwarp();
+                        int my_e = es[0];
+#pragma unroll
+                        for (int i = 1; i < 16; ++i) my_e = lane == i ? es[i] : my_e;
+                        if (lane < 16 && cb + lane < nb) {
+                            const int row = t.off + tb + cb + lane;  // bucket row of this token
+                            *reinterpret_cast<uint4*>(a.hq + (size_t)row * (I / 2) + (r0 + 32 * q) / 2) =
+                                *reinterpret_cast<const uint4*>(stg + lane * 16);
+                            // block (r0 + 32 q) / 32 is byte q of word r0 / 128
+                            reinterpret_cast<uint8_t*>(a.hs)[((size_t)(r0 / 128) * R + row) * 4 + q] =
+                                (uint8_t)(my_e + 127);
+                        }
+                        __syncwarp();
+                    } else {
+                        float v[16];
+                        tc_ld16(d + cb, v);
+                        int pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = cb + i < nb ? __ldg(a.entries + t.off + tb + cb + i) : 0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (cb + i < nb) a.y[(size_t)pk[i] * H + r0 + 32 * q + lane] = v[i];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hd.acc_empty[buf]);
+                if (P == 1) buf ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kMxTmemCols) : "memory");
+    }
+}
+
+// One CTA per bucket row i: x of token entries[i] / k converted to MXFP4 into row i
+// of xq, and its block scales into the words of xs (word g of row i at g * R + i).
+// Thread b takes block b (32 elements, 64 bytes of bf16).
+__global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k, int R,
+                                                       const int32_t* __restrict__ entries, uint8_t* __restrict__ xq,
+                                                       uint32_t* __restrict__ xs, int32_t* __restrict__ task_ctr) {
+    const int i = blockIdx.x;
+    if (i == 0 && threadIdx.x < kTaskCounters) task_ctr[threadIdx.x] = 0;
+    const int t = __ldg(entries + i) / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int nblk = H / 32;  // a multiple of 4: a word's four blocks sit in four consecutive lanes
+    for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+        const int lane = threadIdx.x & 31;
+        const int active = min(32, nblk - (b - lane));
+        const unsigned mask = active >= 32 ? 0xffffffffu : ((1u << active) - 1u);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 v = __ldg(src + 4 * b + j);
+            w[4 * j] = v.x, w[4 * j + 1] = v.y, w[4 * j + 2] = v.z, w[4 * j + 3] = v.w;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            amax = max(amax, (w[j] & 0x7fffu) << 16);
+            amax = max(amax, (w[j] >> 16 & 0x7fffu) << 16);
+        }
+        const int e = mx_block_exp(amax);
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            // elements 2j (low half) and 2j + 1 (high half) -> byte j, low nibble first
+            const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
+            const uint32_t c0 = e2m1_code(mx_scaled((lo & 0x7fffu) << 16, e)) | ((lo >> 15) << 3);
+            const uint32_t c1 = e2m1_code(mx_scaled((hi & 0x7fffu) << 16, e)) | ((hi >> 15) << 3);
+            o[j >> 2] |= (c0 | (c1 << 4)) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint4*>(xq + (size_t)i * (H / 2) + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
+        uint32_t word = (uint32_t)(e + 127) << (8 * (b & 3));
+        word |= __shfl_xor_sync(mask, word, 1);
+        word |= __shfl_xor_sync(mask, word, 2);
+        if ((b & 3) == 0) xs[(size_t)(b >> 2) * R + i] = word;
+    }
+}
+
+inline size_t mx_align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct MxWs {
+    size_t ctr, xq, xs, hq, hs, total;
+};
+
+MxWs mx_ws(int T, int k, int H, int I) {
+    MxWs w;
+    const size_t R = (size_t)T * k;
+    size_t o = 0;
+    w.ctr = o;
+    o = mx_align256(o + kTaskCounters * sizeof(int32_t));
+    w.xq = o;
+    o = mx_align256(o + R * (size_t)(H / 2));
+    w.xs = o;
+    o = mx_align256(o + (size_t)(H / 128) * R * 4);
+    w.hq = o;
+    o = mx_align256(o + R * (size_t)(I / 2));
+    w.hs = o;
+    o = mx_align256(o + (size_t)(I / 128) * R * 4);
+    w.total = o;
+    return w;
+}
+
+}  // namespace
+
+size_t ffn_mx_workspace(int T, int k, int H, int I) { return mx_ws(T, k, H, I).total; }
+
+cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
+    const MxWs w = mx_ws(a.T, a.k, a.H, a.I);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.task_ctr = reinterpret_cast<int32_t*>(ws + w.ctr);
+    a.xq = ws + w.xq;
+    a.xs = reinterpret_cast<uint32_t*>(ws + w.xs);
+    a.hq = ws + w.hq;
+    a.hs = reinterpret_cast<uint32_t*>(ws + w.hs);
+    if (a.T == 0) return cudaSuccess;
+    const int R = a.T * a.k;
+    mx_xprep_kernel<<<R, 128, 0, st>>>(a.x, a.H, a.k, R, a.entries, a.xq, a.xs, a.task_ctr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st) {
+    const int R = a.T * a.k;
+    if (R == 0) return cudaSuccess;
+    // activations of the phase: [R rows][K/2 bytes] E2M1, boxes of 128 bytes x 32 rows, 128-byte swizzle
+    CUtensorMap map;
+    const int K = phase == 0 ? a.H : a.I;
+    if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, phase == 0 ? a.xq : a.hq, (uint64_t)(K / 2), (uint64_t)R,
+                        (uint64_t)(K / 2), kMxRowB, kMxBox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const long dmax = (long)(a.E < R ? a.E : R);
+    const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kMxBM);
+    const int grid = (int)(tasks < sm_count ? tasks : sm_count);
+    if (grid <= 0) return cudaSuccess;
+    static std::atomic<uint64_t> configured[2];
+    const size_t smem = phase == 0 ? MxSmem<0>::kTotal : MxSmem<1>::kTotal;
+    cudaError_t err = ensure_smem_limit(phase == 0 ? (const void*)ffn_mx_kernel<0> : (const void*)ffn_mx_kernel<1>,
+                                        (int)smem, configured[phase]);
+    if (err != cudaSuccess) return err;
+    // task counters 12-15 of the call's workspace (zeroed by the prep kernel): one per
+    // phase and placement class
+    const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;
+    if (phase == 0) return launch_pdl(ffn_mx_kernel<0>, dim3(grid), dim3(kMxThreads), smem, st, a, map, sel, ctr);
+    return launch_pdl(ffn_mx_kernel<1>, dim3(grid), dim3(kMxThreads), smem, st, a, map, sel, ctr);
+}
+
+}  // namespace moe

@@ -133,6 +133,14 @@ struct FfnArgs {
     // zero-copy launches: cold slot c's blob read in place from pinned host memory
     // (device-mapped pointers), no scratch copy
     const uint8_t* const* cold_host;
+    // block-scaled (all-FP4) prefill, in bucket order (row i = entries[i]): x and h
+    // quantised to MXFP4, element k of a row in byte k/2, and their E8M0 block
+    // scales as 32-bit words of four blocks, word (g, i) = blocks 4g..4g+3 of row i
+    // at index g * T*k + i
+    uint8_t* xq;   // [T*k][H/2]
+    uint32_t* xs;  // [H/128][T*k]
+    uint8_t* hq;   // [T*k][I/2]
+    uint32_t* hs;  // [I/128][T*k]
 };
 
 size_t ffn_decode_workspace(int T, int k, int H, int I);
@@ -150,6 +158,14 @@ cudaError_t launch_ffn_prep(FfnArgs& a, void* workspace, cudaStream_t st);
 cudaError_t launch_ffn_phase(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st, bool zc = false);
 // The tensor-core kernel of one phase over the selected experts with more than lo tokens.
 cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_count, cudaStream_t st);
+
+// Block-scaled (all-FP4) prefill path: workspace bytes for T tokens; the prep that
+// points the workspace fields of `a` at `workspace`, zeroes the task counters and
+// quantises x into bucket order; one phase (0: gate/up -> h quantised, 1: down -> y)
+// over every selected expert with at least one token.
+size_t ffn_mx_workspace(int T, int k, int H, int I);
+cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st);
+cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st);
 
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
                            cudaStream_t st);

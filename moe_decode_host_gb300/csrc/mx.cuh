@@ -1,0 +1,48 @@
+// MXFP4 conversion of activations (the OCP Microscaling rule for E2M1 elements),
+// shared by the stand-alone quantiser and the block-scaled prefill kernels: each
+// 32-element block gets the exponent floor(log2(max |v|)) - 2 (2 = the exponent of
+// E2M1's largest value, 6 = 1.5 * 2^2), clamped to the E8M0 range [-127, 127] (an
+// all-zero block takes -127); each element gets |v| / 2^exp rounded to the nearest
+// E2M1 magnitude {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to the even code, above 6
+// saturating to 6, with v's sign bit.
+#pragma once
+
+#include <stdint.h>
+
+namespace moe {
+
+// floor(log2(a)) of a positive finite float given by its bits.
+__device__ __forceinline__ int floor_log2_bits(uint32_t b) {
+    const int ef = (int)((b >> 23) & 0xffu);
+    if (ef != 0) return ef - 127;
+    const uint32_t m = b & 0x7fffffu;  // subnormal: m * 2^-149, m != 0
+    return (31 - __clz((int)m)) - 149;
+}
+
+// Shared block exponent from the largest magnitude's bits (0 for an all-zero block).
+__device__ __forceinline__ int mx_block_exp(uint32_t amax_bits) {
+    return amax_bits == 0u ? -127 : max(-127, min(127, floor_log2_bits(amax_bits) - 2));
+}
+
+// |v| / 2^e for the bits of |v| and a block exponent e of its block: exact (a
+// power-of-two scaling; e <= 125 for finite fp32 input, so 127 - e is in [2, 254]),
+// and below 8 because |v| < 2^(e + 3).
+__device__ __forceinline__ float mx_scaled(uint32_t mag_bits, int e) {
+    return __uint_as_float(mag_bits) * __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// E2M1 code (sign clear) of r >= 0: round to nearest with the decision points at
+// the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5, where the even code wins;
+// anything above 5 takes the largest magnitude, 6.
+__device__ __forceinline__ uint32_t e2m1_code(float r) {
+    if (r <= 0.25f) return 0u;
+    if (r < 0.75f) return 1u;
+    if (r <= 1.25f) return 2u;
+    if (r < 1.75f) return 3u;
+    if (r <= 2.5f) return 4u;
+    if (r < 3.5f) return 5u;
+    if (r <= 5.0f) return 6u;
+    return 7u;
+}
+
+}  // namespace moe
