@@ -56,23 +56,45 @@ def _tensor_peak():
         return 1700.0, "fallback (sustained bf16)"
 
 
-FP4_OVER_BF16 = 6.0  # nominal dense tensor rates per GPU: 13.5 PFLOP/s MXFP4 over 2.25 bf16
-
-
-def prefill_targets(flops: float, algo_bytes: float, ms: float, tc_peak_tflops: float, hbm_gbs: float) -> dict:
+def prefill_targets(flops: float, algo_bytes: float, ms: float, mxfp4_peak_tflops: float, mxfp4_kind: str,
+                    hbm_gbs: float) -> dict:
     """The prefill config against its own target, a fraction of the dense MXFP4
-    tensor peak: that peak is not measured here, so it is the measured bf16 peak
-    times the nominal FP4/bf16 ratio. The workload's irreducible bytes (each
-    picked expert's weights once, x in and the output out) cap what any kernel can
-    reach: flops / (bytes / HBM peak)."""
+    tensor peak. The workload's irreducible bytes (each picked expert's weights
+    once, x in and the per-pick outputs out) cap what any kernel can reach:
+    flops / (bytes / HBM peak)."""
     achieved = flops / (ms * 1e-3) / 1e12
-    mxfp4_peak = tc_peak_tflops * FP4_OVER_BF16
     cap = flops / (algo_bytes / (hbm_gbs * 1e9)) / 1e12
-    return {"achieved_tflops": achieved, "mxfp4_peak_tflops": mxfp4_peak,
-            "mxfp4_peak_kind": "measured bf16 x 6 (nominal dense FP4/bf16 ratio)",
-            "frac_of_mxfp4_peak": achieved / mxfp4_peak,
+    return {"achieved_tflops": achieved, "mxfp4_peak_tflops": mxfp4_peak_tflops, "mxfp4_peak_kind": mxfp4_kind,
+            "frac_of_mxfp4_peak": achieved / mxfp4_peak_tflops,
             "hbm_bound_cap_tflops": cap, "frac_of_hbm_bound_cap": achieved / cap,
+            "cap_frac_of_mxfp4_peak": cap / mxfp4_peak_tflops,
             "flop_per_byte": flops / algo_bytes}
+
+
+def measure_mxfp4_peak(dev, iters: int = 4096, reps: int = 5):
+    """Dense block-scaled FP4 rate of this GPU from the library's probe (one CTA per
+    SM issuing kind::mxf4 MMAs on shared-memory operands): best of `reps` launches,
+    TFLOP/s."""
+    import torch
+
+    import moe_decode_host_gb300 as m
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st = torch.cuda.current_stream()
+    m.mxf4_peak_probe(64, status, 0, st)  # warm-up
+    best = 0.0
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        m.mxf4_peak_probe(iters, status, 0, st)
+        e1.record(st)
+        e1.synchronize()
+        flops = sms * iters * 2.0 * 128 * 256 * 64
+        best = max(best, flops / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    assert int(status.item()) == 0
+    return best
 
 
 def repetition_bounds(K: int, n: int = 5) -> list:
@@ -148,6 +170,9 @@ def parse():
     ap.add_argument("--swap-every", type=int, default=16, help="residency update interval in steps")
     ap.add_argument("--max-swaps", type=int, default=8, help="swaps per residency update")
     ap.add_argument("--n-hot", type=int, default=None, help="HBM-resident experts per layer (rest cold)")
+    ap.add_argument("--prefill", default=None, choices=["f16", "fp4"],
+                    help="arithmetic of calls above 64 tokens: exact-weight f16 tensor cores, or block-scaled "
+                         "FP4 with x and h in MXFP4 (default for the 8192-token config)")
     ap.add_argument("--zero-copy", action="store_true",
                     help="the FFN reads picked cold experts in place from host memory (no slot copy)")
     return ap.parse_args()
@@ -182,6 +207,7 @@ def workload(args, config=None, batch=None):
     c["mirror"] = args.mirror if args.mirror is not None else (
         c.get("layers", 1) == 1 and c["n_cold"] > 0 and not no_res)
     c["zero_copy"] = bool(args.zero_copy)
+    c["prefill"] = args.prefill or ("fp4" if c["T"] > 64 else "f16")
     if args.n_hot is not None and args.experts is None:
         c["n_hot"] = min(args.n_hot, c["E"])
         c["n_cold"] = c["E"] - c["n_hot"]
@@ -430,6 +456,9 @@ def _config_json(c, args, pool_steps=None):
             "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
             "cold_experts": ("read in place from pinned host memory by the FFN (zero copy)"
                              if c.get("zero_copy") and c["T"] <= 64 else "copied into the HBM slot scratch"),
+            "prefill_arithmetic": (None if c["T"] <= 64 else (
+                "block-scaled FP4 tensor cores (tcgen05 kind::mxf4), x and h quantised to MXFP4"
+                if c.get("prefill") == "fp4" else "f16 tensor cores (tcgen05 kind::f16), weights expanded exactly")),
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -473,6 +502,7 @@ def build_layers(c, dev, seed_tag="bench"):
                         init_loc=loc, swap_every=0 if c.get("no_res") else c["swap_every_steps"],
                         max_swaps=c["max_swaps"], hysteresis=c["hysteresis"],
                         host_mirror=mirror, zero_copy=bool(c.get("zero_copy")))
+        layer.set_prefill_kind(1 if c.get("prefill") == "fp4" else 0)
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
 
@@ -573,7 +603,7 @@ def step_launches(T, n_cold):
     return route + gather + ffn + 1                  # + combine
 
 
-def measure(c, args, dev, dist, world, link_peak, link_detail, local):
+def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=None):
     """Builds the workload's layers, runs W warm-up steps, times K steps on the
     device (events on the stream, max over ranks), then per-call breakdown steps and
     the end-to-end leg, all on distinct steps of routing.  Returns the measurement
@@ -687,7 +717,7 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local):
     counts_h = counts_log.cpu().numpy()
     ncold_h = ncold_log.cpu().numpy()
     distinct = (counts_h > 0).sum(axis=2)  # [K, NL]
-    act_bytes = T * H * 2 + T * k * (H * 4 + c["I"] * 4 * 2) + T * H * 2  # x, y, h write+read, x16
+    act_bytes = T * H * 2 + T * k * H * 4  # x read (bf16), y written (fp32 per pick)
     ffn_bytes = distinct * eb + act_bytes
     gather_bytes = ncold_h * eb
     hot_bytes = (distinct - ncold_h) * eb
@@ -713,15 +743,28 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local):
     mean_distinct = float(distinct.mean())
     mean_cold = float(ncold_h.mean())
     if dom == "moe_grouped_ffn" and T > 64:
-        tc_peak, tc_kind = _tensor_peak()
-        roof = {"kernel": "moe_grouped_ffn (tcgen05 kind::f16 grouped GEMM for buckets > 64 tokens)",
-                "bound": "tensor", "achieved": ffn_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": ffn_tflops / tc_peak, "traffic": _traffic("ffn_tc", mean_distinct),
+        fp4 = c.get("prefill") == "fp4"
+        if fp4:
+            tc_peak, tc_kind = mx_peak, "measured in this run (dense kind::mxf4 probe)"
+            kern = "moe_grouped_ffn (tcgen05 kind::mxf4 block-scaled grouped GEMM, x and h in MXFP4)"
+        else:
+            tc_peak, tc_kind = _tensor_peak()
+            kern = "moe_grouped_ffn (tcgen05 kind::f16 grouped GEMM for buckets > 64 tokens)"
+        t_tensor = ffn_flops / (tc_peak * 1e12)
+        t_hbm = float(ffn_bytes.sum()) / (hbm_peak * 1e9)
+        roof = {"kernel": kern, "ms_mean": ffn_k_tot_ms / (K * NL), "flops_per_call": ffn_flops / (K * NL),
                 "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
-                "ms_mean": ffn_k_tot_ms / (K * NL), "flops_per_call": ffn_flops / (K * NL), "peak_kind": tc_kind,
-                "hbm_gbs_same_calls": ffn_gbs,
-                "prefill_target": prefill_targets(ffn_flops, float((distinct * eb).sum()) + K * NL * 2.0 * T * H * 2,
-                                                  ffn_k_tot_ms, tc_peak, hbm_peak)}
+                "tensor_tflops": ffn_tflops, "tensor_peak_tflops": tc_peak, "tensor_peak_kind": tc_kind,
+                "tensor_frac": ffn_tflops / tc_peak, "hbm_gbs": ffn_gbs, "hbm_frac": ffn_gbs / hbm_peak,
+                "traffic": None if fp4 else _traffic("ffn_tc", mean_distinct),
+                "prefill_target": prefill_targets(ffn_flops, float(ffn_bytes.sum()), ffn_k_tot_ms, mx_peak,
+                                                  "measured in this run (dense kind::mxf4 probe)", hbm_peak)}
+        if t_hbm >= t_tensor:  # the call's bytes take longer than its flops at the kind's peak
+            roof.update({"bound": "hbm", "achieved": ffn_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": ffn_gbs / hbm_peak, "peak_kind": peak_kind})
+        else:
+            roof.update({"bound": "tensor", "achieved": ffn_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": ffn_tflops / tc_peak, "peak_kind": tc_kind})
     elif dom == "moe_grouped_ffn":
         roof = {"kernel": "moe_grouped_ffn (decode dequant-GEMV)", "bound": "hbm", "achieved": ffn_gbs,
                 "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak,
@@ -831,11 +874,13 @@ def run_ours(args):
     else:
         link_peak, link_detail = measure_link_peak(dev)
         link_detail["numa"] = host_numa(local)
-    res = measure(c, args, dev, dist, world, link_peak, link_detail, local)
+    mx_peak = measure_mxfp4_peak(dev) if c["T"] > 64 else None
+    res = measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak)
     pool_steps = res.pop("pool_steps")
     line = {"metric": "MoE layer tokens/s (decode)", "value": res.pop("value"), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xf16->f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e2m1xe2m1->f32" if (c["T"] > 64 and c["prefill"] == "fp4") else "e2m1xf16->f32",
             "data": "synthetic", "config": _config_json(c, args, pool_steps)}
     line.update(res)
     default_run = (args.config == "c1" and args.batch is None and args.experts is None and not args.zero_copy

@@ -353,6 +353,15 @@ int moe_layer_inject_fault(moe_layer* L, int what);
  * the link peak the cold gather is reported against. */
 int moe_link_probe(const void* src_host, void* dst_dev, size_t bytes, int ctas, void* stream);
 
+/* Dense block-scaled FP4 tensor-core rate probe (the denominator the all-FP4
+ * prefill path is reported against): `ctas` CTAs (0 = one per SM) each issue
+ * `iters` back-to-back tcgen05 kind::mxf4 MMAs of M = 128, N = 256, K = 64
+ * (2 * 128 * 256 * 64 flops each) on operands resident in shared memory; the
+ * caller times the launch on `stream`.  status_dev: device int, set to
+ * MOE_ERR_TIMEOUT if the kernel's bounded wait for its MMAs ran out (zero it
+ * first).  1 <= iters <= 2^20.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+int moe_mxf4_peak_probe(int iters, int ctas, int* status_dev, void* stream);
+
 /* Test hook for the bounded device waits of the pipelined kernels: launches one
  * thread that waits on an mbarrier phase that nothing completes.  The wait gives
  * up at its deadline (2 s), writes its record to diag_dev (device int32 [16], the

@@ -19,7 +19,7 @@ __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_by
            "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
            "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED", "MOE_ERR_SCRATCH_TOO_SMALL",
-           "moe_grouped_ffn_noalloc", "residency_plan", "quant_mxfp4"]
+           "moe_grouped_ffn_noalloc", "residency_plan", "quant_mxfp4", "mxf4_peak_probe"]
 
 
 def expert_bytes(H: int, I: int) -> int:
@@ -203,6 +203,12 @@ def quant_mxfp4(x, rows: int, K: int, nib, scales, stream=None):
 
 def link_probe(src_host, dst_dev, nbytes, ctas=0, stream=None):
     check(lib.moe_link_probe(ptr(src_host), ptr(dst_dev), nbytes, ctas, stream_handle(stream)), "moe_link_probe")
+
+
+def mxf4_peak_probe(iters, status_dev, ctas=0, stream=None):
+    """Launches the dense block-scaled FP4 rate probe (time it on `stream`):
+    ctas x iters MMAs of 2 * 128 * 256 * 64 flops each."""
+    check(lib.moe_mxf4_peak_probe(iters, ctas, ptr(status_dev), stream_handle(stream)), "moe_mxf4_peak_probe")
 
 
 def debug_e2m1_pairs(out_dev, stream=None):

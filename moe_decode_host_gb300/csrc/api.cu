@@ -139,6 +139,12 @@ bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, siz
                           CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Scale plane [rows][row_bytes] for the block-scaled kernels: 16-byte x 128-row boxes.
+bool encode_scales(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 16, 128,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // Makes `st` wait for the layer's cold copy in flight, if any.
 cudaError_t join_copy(moe_layer* L, cudaStream_t st) {
     if (!L->copy_pending) return cudaSuccess;
@@ -308,7 +314,15 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     err = err ? err : cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
     if (err == cudaSuccess) {
         std::vector<ExpertMaps> maps(p.E);
+        memset(maps.data(), 0, sizeof(ExpertMaps) * maps.size());
         for (int i = 0; i < p.E; ++i) {
+            if ((mx_scale_maps(p.H) && !encode_scales(&maps[i].w13s, ptr[i] + L->lay.w13s, (size_t)p.H / 32,
+                                                      (size_t)2 * p.I)) ||
+                (mx_scale_maps(p.I) && !encode_scales(&maps[i].w2s, ptr[i] + L->lay.w2s, (size_t)p.I / 32,
+                                                      (size_t)p.H))) {
+                free_layer(L);
+                return MOE_ERR_CUDA;
+            }
             if (!encode_plane(&maps[i].w13n, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I, 32) ||
                 !encode_plane(&maps[i].w2n, ptr[i] + L->lay.w2n, (size_t)p.I / 2, (size_t)p.H, 64) ||
                 !encode_plane_raw(&maps[i].w13r, ptr[i] + L->lay.w13n, (size_t)p.H / 2, (size_t)2 * p.I) ||

@@ -21,23 +21,28 @@
 // are written to all four quarters.  One 32-bit word holds four blocks (the K
 // range of two MMAs, sf_id 0 and 2).
 //
-// Warp roles of one persistent CTA per SM (12 warps):
-//   warp 0       takes tasks (an expert and a 128-row tile) from a launch-wide
-//                counter, experts with the most tokens first, publishes them in a
-//                shared-memory queue, and loads the tile's E2M1 rows by TMA, 256
-//                elements of K per stage (128-byte swizzle; gate and up rows in the
-//                gate/up phase, w2 rows in the down phase);
+// Warp roles of one persistent CTA per SM (17 warps), each task an expert and a
+// 128-row tile:
+//   warp 0       loads the tile's E2M1 rows by TMA, 256 elements of K per stage
+//                (128-byte swizzle; gate and up rows in the gate/up phase, w2 rows
+//                in the down phase), with the rows' scale bytes of the stage;
 //   warp 1       loads the tokens' E2M1 activation rows of each stage by TMA (up to
-//                192 bucket rows, 32 per box);
+//                192 bucket rows, 32 per box), with their scale words;
 //   warp 2       owns tensor memory; one thread issues the MMAs (four of K = 64 per
-//                matrix and stage);
-//   warps 4-7    scale writers: each thread reads its weight row's scale words and
-//                the tokens' activation scale words of a stage and stores them into
-//                a ring of scale slots in tensor memory;
-//   warps 8-11   epilogue: tensor memory -> registers; gate/up phase: h = SiLU(g) u
-//                with the accurate exponential (so that the quantisation of h takes
-//                the same decisions as an exact evaluation except within rounding of
-//                a decision point), converted to MXFP4 across the warp's 32 rows and
+//                matrix and stage); in the gate/up phase it issues the gate matrix's
+//                and a thread of warp 16 the up matrix's, each into its accumulator;
+//   warp 3       takes tasks from a launch-wide counter, experts with the most
+//                tokens first, and publishes them with their routing values in a
+//                shared-memory queue, up to the queue's depth ahead;
+//   warps 4-7    scale writers: each thread takes its weight row's scale words and
+//                the tokens' activation scale words of a stage from shared memory
+//                (loaded by TMA with the stage's operands) and stores them into a
+//                ring of scale slots in tensor memory;
+//   warps 8-15   epilogue, two warps per lane quarter taking alternate 16-token
+//                chunks: tensor memory -> registers; gate/up phase: h = SiLU(g) u
+//                (relative error about 1e-6, so the quantisation of h takes the
+//                decisions of an exact evaluation except within that distance of a
+//                decision point), converted to MXFP4 across the warp's 32 rows and
 //                stored in bucket order; down phase: y rows.
 // Every wait is bounded; a wait that runs out sets MOE_ERR_TIMEOUT, and the CTA
 // drains its copies and MMAs before it frees tensor memory and returns.
@@ -55,12 +60,19 @@ constexpr int kMxRowB = kMxBK / 2;             // bytes of a row per stage
 constexpr int kMxTile = kMxBM * kMxRowB;       // 16 KB: one matrix's rows of a stage
 constexpr int kMxNMax = 192;                   // token columns per pass
 constexpr int kMxBox = 32;                     // activation rows per TMA box
-constexpr int kMxBStage = kMxNMax * kMxRowB;   // 24 KB
-constexpr int kMxBStages = 3;
+constexpr int kMxBTile = kMxNMax * kMxRowB;    // 24 KB of activation rows
+// activation scale words of a stage, loaded by TMA from a 4-aligned bucket row (the
+// box's start must be a whole 16 bytes): 2 rows (the stage's two words) x 200
+constexpr int kMxSfbBox = 200;
+constexpr int kMxBStage = kMxBTile + 2048;     // rows, then the 1600 bytes of scale words
+constexpr int kMxWsc = kMxBM * 16;             // a matrix's scale box: 128 rows x 16 bytes
+constexpr int kMxASlot = kMxTile + kMxWsc;     // per matrix: E2M1 rows, then their scales
 constexpr int kMxSfStages = 3;
-constexpr int kMxThreads = 384;
+constexpr int kMxThreads = 544;
+constexpr int kMxUpIssuer = 16;  // gate/up phase: the warp that issues the up matrix's MMAs
 constexpr int kMxFirstSf = 4;
 constexpr int kMxFirstEpi = 8;
+constexpr int kMxEpiWarps = 8;  // two per lane quarter, taking alternate 16-token chunks
 constexpr int kMxMaxE = 1024;
 constexpr int kMxTaskQ = 4;
 // Tensor memory: accumulators in [0, 384) -- gate and up (192 columns each) in the
@@ -68,13 +80,19 @@ constexpr int kMxTaskQ = 4;
 constexpr uint32_t kMxAccCols = 192;
 constexpr uint32_t kMxSf0 = 384;
 constexpr uint32_t kMxTmemCols = 512;
-constexpr int kMxTakers = 1 + 1 + 4 + 4;  // activation producer, issuer, scale writers, epilogue
 constexpr int kMxEpiStage = 16 * 16;      // epilogue staging per warp: 16 tokens x 16 bytes of h
 
 template <int P>
 __host__ __device__ constexpr int mx_mats() { return P == 0 ? 2 : 1; }  // weight matrices per stage
+// roles that take each task from the queue: producers, issuers, scale writers, epilogue
 template <int P>
-__host__ __device__ constexpr int mx_astages() { return P == 0 ? 4 : 6; }
+__host__ __device__ constexpr int mx_takers() { return 2 + mx_mats<P>() + 4 + kMxEpiWarps; }
+// Rings: per task an expert's activations are read (from L2) in about as many bytes
+// as its weights (from HBM), so both rings need depth against their latency.
+template <int P>
+__host__ __device__ constexpr int mx_astages() { return P == 0 ? 3 : 4; }
+template <int P>
+__host__ __device__ constexpr int mx_bstages() { return P == 0 ? 4 : 5; }
 // scale slot: weight words (8 columns per matrix: two words x four quarter columns),
 // then token words (16 columns: word j of the stage at 8j + token group)
 template <int P>
@@ -90,8 +108,8 @@ struct MxTask {
 };
 
 struct alignas(16) MxHead {
-    uint64_t a_full[6], a_empty[6];
-    uint64_t b_full[kMxBStages], b_empty[kMxBStages];
+    uint64_t a_full[8], a_empty[8];
+    uint64_t b_full[8], b_empty[8];
     uint64_t sf_full[kMxSfStages], sf_empty[kMxSfStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t tq_full[kMxTaskQ], tq_empty[kMxTaskQ];
@@ -100,15 +118,14 @@ struct alignas(16) MxHead {
     uint32_t tmem_base;
     int abort;
     int D;
-    alignas(16) int key[kMxMaxE];  // tokens of each active expert, -1 when inactive
-    int list[kMxMaxE];             // active experts, most tokens first
+    int list[kMxMaxE];  // active experts, most tokens first
 };
 
 template <int P>
 struct MxSmem {
-    static constexpr size_t kB = (size_t)mx_astages<P>() * mx_mats<P>() * kMxTile;  // after the weight ring
-    static constexpr size_t kStg = kB + (size_t)kMxBStages * kMxBStage;
-    static constexpr size_t kHead = kStg + 4 * kMxEpiStage;
+    static constexpr size_t kB = (size_t)mx_astages<P>() * mx_mats<P>() * kMxASlot;  // after the weight ring
+    static constexpr size_t kStg = kB + (size_t)mx_bstages<P>() * kMxBStage;
+    static constexpr size_t kHead = kStg + kMxEpiWarps * kMxEpiStage;
     static constexpr size_t kTotal = 1024 + kHead + sizeof(MxHead);
 };
 static_assert(MxSmem<0>::kTotal <= 232448 && MxSmem<1>::kTotal <= 232448, "shared memory budget of one CTA");
@@ -188,35 +205,10 @@ __device__ __forceinline__ int mx_warp_take(MxHead& hd, int k, const FfnArgs& a,
 // MMA width of a pass over nb tokens: a multiple of 16 (the M = 128 shape's step).
 __device__ __forceinline__ int mx_ncols(int nb) { return (nb + 15) & ~15; }
 
-// Scale words of one stage for one thread of a scale-writer warp: its weight row's
-// two words (blocks 8s..8s+7) per matrix and, for token columns lane + 32c, the two
-// words of each (clamped to the last bucket row; columns past the pass are unused).
-template <int P>
-struct MxScales {
-    uint32_t wa[2][2];  // [matrix][word]
-    uint32_t wb[2][6];  // [word][token group]
-};
-
-template <int P>
-__device__ __forceinline__ void mx_load_scales(MxScales<P>& v, const uint8_t* const (&sa)[2], const uint32_t* sfb,
-                                               int R, int row0, int s, int nj) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int mt = 0; mt < mx_mats<P>(); ++mt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) v.wa[mt][j] = j < nj ? ld_u32(sa[mt] + 8 * s + 4 * j) : 0u;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int c = 0; c < 6; ++c) {
-            const int row = min(row0 + 32 * c + lane, R - 1);
-            v.wb[j][c] = j < nj ? ld_word(sfb + (size_t)(2 * s + j) * R + row) : 0u;
-        }
-}
-
 template <int P>
 __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
-                                                               int sel, int ctr) {
+                                                               const __grid_constant__ CUtensorMap sfb_map, int sel,
+                                                               int ctr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = base;
@@ -228,9 +220,17 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     const int nks = (K + kMxBK - 1) / kMxBK;  // stages per pass; the last may hold 128 elements
     const int tiles = (P == 0 ? I : H) / kMxBM;
     const int R = a.T * a.k;  // bucket rows
+    const int Rs = (R + 3) & ~3;  // row stride of the activation scale words
+    // the weight scales arrive by TMA with their stage where the plane's rows are whole
+    // 16-byte units, else the scale writers read them from global memory
+    const bool wsc_tma = mx_scale_maps(K);
     constexpr int AS = mx_astages<P>();
+    constexpr int BS = mx_bstages<P>();
     constexpr int MATS = mx_mats<P>();
     volatile int* abort = &hd.abort;
+    // tokens of each active expert (-1: inactive), in the weight ring until the
+    // producers start
+    int* key = reinterpret_cast<int*>(sA);
 
     // active experts (at least one token, in the selected placement class), most
     // tokens first (ties by id): every thread keys some experts, then ranks its own
@@ -241,16 +241,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             const bool hot = __ldg(a.loc + e) < a.n_hot;
             act = (sel == 1) ? hot : !hot;
         }
-        hd.key[e] = act ? c : -1;
+        key[e] = act ? c : -1;
     }
-    for (int e = a.E + threadIdx.x; e < ((a.E + 3) & ~3); e += kMxThreads) hd.key[e] = -1;  // pad to 4
+    for (int e = a.E + threadIdx.x; e < ((a.E + 3) & ~3); e += kMxThreads) key[e] = -1;  // pad to 4
     __syncthreads();
     for (int e = threadIdx.x; e < a.E; e += kMxThreads) {
-        const int ke = hd.key[e];
+        const int ke = key[e];
         if (ke < 0) continue;
         int r = 0;
         for (int f = 0; f < a.E; f += 4) {
-            const int4 k4 = *reinterpret_cast<const int4*>(&hd.key[f]);
+            const int4 k4 = *reinterpret_cast<const int4*>(&key[f]);
             r += (k4.x > ke || (k4.x == ke && f < e)) + (k4.y > ke || (k4.y == ke && f + 1 < e)) +
                  (k4.z > ke || (k4.z == ke && f + 2 < e)) + (k4.w > ke || (k4.w == ke && f + 3 < e));
         }
@@ -260,30 +260,31 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         int cnt = 0;
         for (int b0 = 0; b0 < a.E; b0 += 32) {
             const int e = b0 + lane;
-            cnt += __popc(__ballot_sync(0xffffffffu, e < a.E && hd.key[e] >= 0));
+            cnt += __popc(__ballot_sync(0xffffffffu, e < a.E && key[e] >= 0));
         }
         if (lane == 0) {
             hd.D = cnt;
             hd.abort = 0;
+            // every consumed slot is released by each issuer's commit (one per matrix)
             for (int s = 0; s < AS; ++s) {
                 mbar_init(&hd.a_full[s], 1);
-                mbar_init(&hd.a_empty[s], 1);
+                mbar_init(&hd.a_empty[s], MATS);
             }
-            for (int s = 0; s < kMxBStages; ++s) {
+            for (int s = 0; s < BS; ++s) {
                 mbar_init(&hd.b_full[s], 1);
-                mbar_init(&hd.b_empty[s], 1);
+                mbar_init(&hd.b_empty[s], MATS);
             }
             for (int s = 0; s < kMxSfStages; ++s) {
                 mbar_init(&hd.sf_full[s], 4);
-                mbar_init(&hd.sf_empty[s], 1);
+                mbar_init(&hd.sf_empty[s], MATS);
             }
             for (int s = 0; s < 2; ++s) {
-                mbar_init(&hd.acc_full[s], 1);
-                mbar_init(&hd.acc_empty[s], 4);
+                mbar_init(&hd.acc_full[s], MATS);
+                mbar_init(&hd.acc_empty[s], kMxEpiWarps);
             }
             for (int j = 0; j < kMxTaskQ; ++j) {
                 mbar_init(&hd.tq_full[j], 1);
-                mbar_init(&hd.tq_empty[j], kMxTakers);
+                mbar_init(&hd.tq_empty[j], mx_takers<P>());
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
@@ -294,6 +295,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // the weight ring is rewritten by the async proxy (TMA) from here on
+    fence_proxy_async_shared();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -302,13 +305,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     const uint32_t tmem = hd.tmem_base;
     const int ntask = hd.D * tiles;
 
-    if (warp == 0) {
-        // ---------------- task fetcher, weight producer (lane 0) ----------------
+    if (warp == 3) {
+        // ---------------- task fetcher (lane 0) ----------------
+        // runs up to a queue's depth ahead of the roles, so the chain of loads behind a
+        // task (its expert's picks, first entry, physical id and blob) stays off the
+        // operand streams
         if (lane == 0) {
-            int as = 0;
-            unsigned aph = 0;
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
+            for (int k = 0;; ++k) {
                 const int j = k % kMxTaskQ;
                 if (!mbar_wait_fast(&hd.tq_empty[j], ((unsigned)(k / kMxTaskQ) & 1u) ^ 1u, abort, a.status, a.diag,
                                     31, j, k, 0))
@@ -321,12 +324,28 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 hd.tqt[j] = t;
                 mbar_arrive(&hd.tq_full[j]);
                 if (task < 0) break;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
+        // ---------------- weight producer (lane 0) ----------------
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();  // each weight byte is read once
+            int as = 0;
+            unsigned aph = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                MxTask t;
+                const int task = mx_take(hd, k, a, abort, 0, t);
+                if (task < 0) break;
                 if (!t.valid) continue;
                 // the decode kernel's views of the two planes: 128-byte boxes of 32 (w13)
                 // or 64 (w2) rows with the 128-byte swizzle, stacked to 128 rows
                 const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13n : &a.tmaps[t.phys].w2n;
+                const CUtensorMap* smap = P == 0 ? &a.tmaps[t.phys].w13s : &a.tmaps[t.phys].w2s;
                 constexpr int box_rows = P == 0 ? 32 : 64;
                 asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                if (wsc_tma) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(smap) : "memory");
                 const int r0 = t.rb * kMxBM;
                 for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
                     for (int s = 0; s < nks; ++s) {
@@ -334,13 +353,19 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&hd.a_full[as], (unsigned)(MATS * kMxTile));
+                        mbar_arrive_expect_tx(&hd.a_full[as], (unsigned)(MATS * (wsc_tma ? kMxASlot : kMxTile)));
 #pragma unroll
-                        for (int mt = 0; mt < MATS; ++mt)
+                        for (int mt = 0; mt < MATS; ++mt) {
+                            uint8_t* dst = sA + (size_t)(as * MATS + mt) * kMxASlot;
 #pragma unroll
                             for (int i = 0; i < kMxBM / box_rows; ++i)
-                                tma_load_2d(sA + (size_t)(as * MATS + mt) * kMxTile + i * box_rows * kMxRowB, map,
-                                            s * kMxRowB, (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as]);
+                                tma_load_2d_hint(dst + i * box_rows * kMxRowB, map, s * kMxRowB,
+                                                 (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as], pol);
+                            // the 16 scale bytes of each row that hold this stage's 8 blocks
+                            if (wsc_tma)
+                                tma_load_2d_hint(dst + kMxTile, smap, 16 * (s >> 1), (mt ? I : 0) + r0, &hd.a_full[as],
+                                                 pol);
+                        }
                         advance(as, aph, AS);
                     }
                 }
@@ -351,6 +376,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     } else if (warp == 1) {
         // ---------------- activation producer (lane 0) ----------------
         if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();  // read once per row tile of the expert
             int bs = 0;
             unsigned bph = 0;
             bool ok = true;
@@ -366,26 +392,35 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB));
+                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB + 2 * kMxSfbBox * 4));
+                        uint8_t* dst = sB + (size_t)bs * kMxBStage;
                         for (int bx = 0; bx < boxes; ++bx)
-                            tma_load_2d(sB + (size_t)bs * kMxBStage + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB,
-                                        t.off + tb + kMxBox * bx, &hd.b_full[bs]);
-                        advance(bs, bph, kMxBStages);
+                            tma_load_2d_hint(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB,
+                                             t.off + tb + kMxBox * bx, &hd.b_full[bs], pol);
+                        // the stage's two scale words of the pass's tokens, from the 4-aligned
+                        // bucket row at or below the first (x is a whole 16 bytes)
+                        tma_load_2d_hint(dst + kMxBTile, &sfb_map, (t.off + tb) & ~3, 2 * s, &hd.b_full[bs], pol);
+                        advance(bs, bph, BS);
                     }
                 }
             }
-            for (int s = 0; s < kMxBStages; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < BS; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // ---------------- MMA issuer (lane 0) ----------------
+    } else if (warp == 2 || (P == 0 && warp == kMxUpIssuer)) {
+        // ---------------- MMA issuers (lane 0) ----------------
+        // a thread needs about 100 ns to issue one block-scaled MMA, so the gate/up
+        // phase issues from two threads, warp 2 the gate matrix's MMAs into the gate
+        // accumulator and warp 16 the up matrix's into the up accumulator; the down
+        // phase has one matrix and one issuer
+        const int mt = warp == 2 ? 0 : 1;
         if (lane == 0) {
             int as = 0, bs = 0, ss = 0, buf = 0;
             unsigned aph = 0, bph = 0, sph = 0, accph = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 MxTask t;
-                const int task = mx_take(hd, k, a, abort, 2, t);
+                const int task = mx_take(hd, k, a, abort, 2 + mt, t);
                 if (task < 0) break;
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
@@ -408,11 +443,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                         tc_fence_after();
                         const int nkk = min(4, (K - s * kMxBK) / 64);  // K steps of 64 in this stage
                         const uint32_t sf = tmem + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
-                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * kMxBStage));
-#pragma unroll
-                        for (int mt = 0; mt < MATS; ++mt) {
+                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * kMxBStage));  // its rows
+                        {
                             const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * kMxAccCols;
-                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxTile));
+                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxASlot));
                             for (int kk = 0; kk < nkk; ++kk) {
                                 // a K step of 64 elements advances both start addresses by 32 bytes;
                                 // its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2
@@ -426,7 +460,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                         tc_commit(&hd.b_empty[bs]);
                         tc_commit(&hd.sf_empty[ss]);
                         advance(as, aph, AS);
-                        advance(bs, bph, kMxBStages);
+                        advance(bs, bph, BS);
                         advance(ss, sph, kMxSfStages);
                     }
                     if (!ok) break;
@@ -437,19 +471,21 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
             // last commit of every slot
             for (int s = 0; s < AS; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
-            for (int s = 0; s < kMxBStages; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < BS; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
             for (int s = 0; s < kMxSfStages; ++s) mbar_drain(&hd.sf_empty[s], (s < ss) ? sph : (sph ^ 1u));
         }
         __syncwarp();
     } else if (warp >= kMxFirstSf && warp < kMxFirstSf + 4) {
         // ---------------- scale writers ----------------
         // thread = weight row 32 q + lane of the tile (q = lane quarter); every quarter
-        // also stores the token words, which each quarter's rows read from their own
+        // also stores the token words, which each quarter's rows read from their own.
+        // The words arrive in shared memory with their stage (the writers follow the
+        // weight and activation rings as the MMA issuer does).
         const int q = warp & 3;
+        const int rr = 32 * q + lane;
         const uint32_t qaddr = tmem + ((uint32_t)(q * 32) << 16);
-        const uint32_t* sfb = P == 0 ? a.xs : a.hs;
-        int ss = 0;
-        unsigned sph = 0;
+        int ss = 0, as = 0, bs = 0;
+        unsigned sph = 0, aph = 0, bph = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
             MxTask t;
@@ -458,16 +494,39 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             if (!t.valid) continue;
             const int r0 = t.rb * kMxBM;
             const size_t srl = (size_t)K / 32;  // scale bytes per weight row
-            const uint8_t* sa[2];
-            sa[0] = t.blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + 32 * q + lane) * srl;
-            sa[1] = P == 0 ? t.blob + a.w13s + (size_t)(I + r0 + 32 * q + lane) * srl : sa[0];
+            const uint8_t* sg0 = t.blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + rr) * srl;
+            const uint8_t* sg1 = P == 0 ? t.blob + a.w13s + (size_t)(I + r0 + rr) * srl : sg0;
             for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
-                const int row0 = t.off + tb;
-                MxScales<P> cur, nxt;
-                mx_load_scales<P>(cur, sa, sfb, R, row0, 0, min(2, K / 128));
+                const int d0 = (t.off + tb) & 3;  // first token's place in the loaded words
                 for (int s = 0; s < nks; ++s) {
-                    // the next stage's words are in flight while this one waits for its slot
-                    if (s + 1 < nks) mx_load_scales<P>(nxt, sa, sfb, R, row0, s + 1, min(2, (K - (s + 1) * kMxBK) / 128));
+                    const int nj = min(2, (K - s * kMxBK) / 128);  // words of this stage
+                    uint32_t wa[2][2] = {{0u, 0u}, {0u, 0u}};
+                    if (!wsc_tma) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            wa[0][j] = j < nj ? ld_u32(sg0 + 8 * s + 4 * j) : 0u;
+                            if (P == 0) wa[1][j] = j < nj ? ld_u32(sg1 + 8 * s + 4 * j) : 0u;
+                        }
+                    }
+                    if ((wsc_tma && !warp_wait(&hd.a_full[as], aph, a, abort, 40, as, s, task)) ||
+                        !warp_wait(&hd.b_full[bs], bph, a, abort, 41, bs, s, task)) {
+                        ok = false;
+                        break;
+                    }
+                    if (wsc_tma) {
+#pragma unroll
+                        for (int mt = 0; mt < MATS; ++mt) {
+                            const uint8_t* row = sA + (size_t)(as * MATS + mt) * kMxASlot + kMxTile + rr * 16 + 8 * (s & 1);
+                            wa[mt][0] = *reinterpret_cast<const uint32_t*>(row);
+                            wa[mt][1] = nj > 1 ? *reinterpret_cast<const uint32_t*>(row + 4) : 0u;
+                        }
+                    }
+                    const uint32_t* wsb = reinterpret_cast<const uint32_t*>(sB + (size_t)bs * kMxBStage + kMxBTile);
+                    uint32_t wb[2][6];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int c = 0; c < 6; ++c) wb[j][c] = j < nj ? wsb[j * kMxSfbBox + d0 + 32 * c + lane] : 0u;
                     if (!warp_wait(&hd.sf_empty[ss], sph ^ 1u, a, abort, 38, ss, s, task)) {
                         ok = false;
                         break;
@@ -479,7 +538,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int mt = i >> 3, j = (i >> 2) & 1;
-                        va[i] = (mt < MATS && (i & 3) == q) ? cur.wa[mt][j] : 0u;
+                        va[i] = (mt < MATS && (i & 3) == q) ? wa[mt][j] : 0u;
                     }
                     if constexpr (P == 0) {
                         mx_st16(col, va);
@@ -492,22 +551,24 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     // token words: word j of token group c at column 8 j + c
                     uint32_t vb[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) vb[i] = (i & 7) < 6 ? cur.wb[i >> 3][i & 7] : 0u;
+                    for (int i = 0; i < 16; ++i) vb[i] = (i & 7) < 6 ? wb[i >> 3][i & 7] : 0u;
                     mx_st16(col + mx_sfb_col<P>(), vb);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&hd.sf_full[ss]);
                     advance(ss, sph, kMxSfStages);
-                    cur = nxt;
+                    advance(as, aph, AS);
+                    advance(bs, bph, BS);
                 }
             }
         }
-    } else if (warp >= kMxFirstEpi) {
+    } else if (warp >= kMxFirstEpi && warp < kMxFirstEpi + kMxEpiWarps) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // tensor-memory lane quarter: weight rows 32 q ..
+        const int half = (warp - kMxFirstEpi) >> 2;  // this warp's 16-token chunks: 2 i + half
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        uint8_t* stg = base + MxSmem<P>::kStg + (size_t)q * kMxEpiStage;
+        uint8_t* stg = base + MxSmem<P>::kStg + (size_t)(warp - kMxFirstEpi) * kMxEpiStage;
         int buf = 0;
         unsigned accph = 0;
         bool ok = true;
@@ -521,7 +582,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 // never read: the down phase sees the same id)
                 if (t.rb == 0 && threadIdx.x == kMxFirstEpi * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
                 if (P == 1)
-                    for (int c = 0; c < t.cnt; ++c) a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + 32 * q + lane] = 0.f;
+                    for (int c = half; c < t.cnt; c += 2)
+                        a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + 32 * q + lane] = 0.f;
                 continue;
             }
             for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
@@ -533,14 +595,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 accph ^= 1u << buf;
                 tc_fence_after();
                 const uint32_t d = lane_addr + (uint32_t)buf * kMxAccCols;
-                for (int cb = 0; cb < nb; cb += 16) {
+                for (int cb = 16 * half; cb < nb; cb += 32) {
                     if constexpr (P == 0) {
                         float g[16], u[16];
                         tc_ld16x2(d + cb, d + kMxAccCols + cb, g, u);
                         int es[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float h = g[i] / (1.0f + expf(-g[i])) * u[i];
+                            // the fast exponential and division: relative error about 1e-6 for
+                            // |g| up to 10, far below the quantisation step of h
+                            const float h = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
                             const uint32_t bits = __float_as_uint(h);
                             const uint32_t mag = bits & 0x7fffffffu;
                             // one 32-element block of h per token: this warp's 32 rows
@@ -559,7 +623,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                             *reinterpret_cast<uint4*>(a.hq + (size_t)row * (I / 2) + (r0 + 32 * q) / 2) =
                                 *reinterpret_cast<const uint4*>(stg + lane * 16);
                             // block (r0 + 32 q) / 32 is byte q of word r0 / 128
-                            reinterpret_cast<uint8_t*>(a.hs)[((size_t)(r0 / 128) * R + row) * 4 + q] =
+                            reinterpret_cast<uint8_t*>(a.hs)[((size_t)(r0 / 128) * Rs + row) * 4 + q] =
                                 (uint8_t)(my_e + 127);
                         }
                         __syncwarp();
@@ -591,9 +655,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
 }
 
 // One CTA per bucket row i: x of token entries[i] / k converted to MXFP4 into row i
-// of xq, and its block scales into the words of xs (word g of row i at g * R + i).
+// of xq, and its block scales into the words of xs (word g of row i at g * Rs + i).
 // Thread b takes block b (32 elements, 64 bytes of bf16).
-__global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k, int R,
+__global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k, int Rs,
                                                        const int32_t* __restrict__ entries, uint8_t* __restrict__ xq,
                                                        uint32_t* __restrict__ xs, int32_t* __restrict__ task_ctr) {
     const int i = blockIdx.x;
@@ -631,7 +695,7 @@ __global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __re
         uint32_t word = (uint32_t)(e + 127) << (8 * (b & 3));
         word |= __shfl_xor_sync(mask, word, 1);
         word |= __shfl_xor_sync(mask, word, 2);
-        if ((b & 3) == 0) xs[(size_t)(b >> 2) * R + i] = word;
+        if ((b & 3) == 0) xs[(size_t)(b >> 2) * Rs + i] = word;
     }
 }
 
@@ -643,18 +707,18 @@ struct MxWs {
 
 MxWs mx_ws(int T, int k, int H, int I) {
     MxWs w;
-    const size_t R = (size_t)T * k;
+    const size_t R = (size_t)T * k, Rs = (R + 3) & ~(size_t)3;
     size_t o = 0;
     w.ctr = o;
     o = mx_align256(o + kTaskCounters * sizeof(int32_t));
     w.xq = o;
     o = mx_align256(o + R * (size_t)(H / 2));
     w.xs = o;
-    o = mx_align256(o + (size_t)(H / 128) * R * 4);
+    o = mx_align256(o + (size_t)(H / 128) * Rs * 4);
     w.hq = o;
     o = mx_align256(o + R * (size_t)(I / 2));
     w.hs = o;
-    o = mx_align256(o + (size_t)(I / 128) * R * 4);
+    o = mx_align256(o + (size_t)(I / 128) * Rs * 4);
     w.total = o;
     return w;
 }
@@ -673,7 +737,7 @@ cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     a.hs = reinterpret_cast<uint32_t*>(ws + w.hs);
     if (a.T == 0) return cudaSuccess;
     const int R = a.T * a.k;
-    mx_xprep_kernel<<<R, 128, 0, st>>>(a.x, a.H, a.k, R, a.entries, a.xq, a.xs, a.task_ctr);
+    mx_xprep_kernel<<<R, 128, 0, st>>>(a.x, a.H, a.k, (R + 3) & ~3, a.entries, a.xq, a.xs, a.task_ctr);
     return cudaGetLastError();
 }
 
@@ -685,6 +749,12 @@ cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cu
     const int K = phase == 0 ? a.H : a.I;
     if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, phase == 0 ? a.xq : a.hq, (uint64_t)(K / 2), (uint64_t)R,
                         (uint64_t)(K / 2), kMxRowB, kMxBox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // their scale words [K/128 rows][Rs words], boxes of 200 words x 2 rows
+    CUtensorMap smap;
+    const int Rs = (R + 3) & ~3;
+    if (!encode_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, phase == 0 ? a.xs : a.hs, (uint64_t)Rs,
+                        (uint64_t)(K / 128), (uint64_t)Rs * 4, kMxSfbBox, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const long dmax = (long)(a.E < R ? a.E : R);
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kMxBM);
@@ -698,8 +768,9 @@ cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cu
     // task counters 12-15 of the call's workspace (zeroed by the prep kernel): one per
     // phase and placement class
     const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;
-    if (phase == 0) return launch_pdl(ffn_mx_kernel<0>, dim3(grid), dim3(kMxThreads), smem, st, a, map, sel, ctr);
-    return launch_pdl(ffn_mx_kernel<1>, dim3(grid), dim3(kMxThreads), smem, st, a, map, sel, ctr);
+    if (phase == 0)
+        return launch_pdl(ffn_mx_kernel<0>, dim3(grid), dim3(kMxThreads), smem, st, a, map, smap, sel, ctr);
+    return launch_pdl(ffn_mx_kernel<1>, dim3(grid), dim3(kMxThreads), smem, st, a, map, smap, sel, ctr);
 }
 
 }  // namespace moe

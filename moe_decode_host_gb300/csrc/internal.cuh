@@ -96,7 +96,16 @@ struct ExpertMaps {
     CUtensorMap w2n;   // [H rows][I/2 bytes], box 128 B x 64 rows, 128-byte swizzle
     CUtensorMap w13r;  // [2I rows][H/2 bytes], box 64 B x 128 rows, 64-byte swizzle
     CUtensorMap w2r;   // [H rows][I/2 bytes], same box
+    // the two scale planes for the block-scaled kernels, box 16 B x 128 rows: encoded
+    // only where a row is a multiple of 16 bytes (H, resp. I, a multiple of 512),
+    // else zero and unused (see mx_scale_maps)
+    CUtensorMap w13s;  // [2I rows][H/32 bytes]
+    CUtensorMap w2s;   // [H rows][I/32 bytes]
 };
+
+// Whether the scale plane of a matrix with reduction length K has a tensor map
+// (TMA needs row strides that are multiples of 16 bytes).
+__host__ __device__ inline bool mx_scale_maps(int K) { return (K / 32) % 16 == 0; }
 
 // Buckets with more than this many tokens run on the tensor-core prefill kernel.
 constexpr int kTcMinTokens = 64;
@@ -136,11 +145,12 @@ struct FfnArgs {
     // block-scaled (all-FP4) prefill, in bucket order (row i = entries[i]): x and h
     // quantised to MXFP4, element k of a row in byte k/2, and their E8M0 block
     // scales as 32-bit words of four blocks, word (g, i) = blocks 4g..4g+3 of row i
-    // at index g * T*k + i
+    // at index g * Rs + i
     uint8_t* xq;   // [T*k][H/2]
-    uint32_t* xs;  // [H/128][T*k]
+    uint32_t* xs;  // [H/128][Rs], Rs = T*k rounded up to a multiple of 4 (row stride of
+                   // whole 16-byte units, so the words can be loaded by TMA)
     uint8_t* hq;   // [T*k][I/2]
-    uint32_t* hs;  // [I/128][T*k]
+    uint32_t* hs;  // [I/128][Rs]
 };
 
 size_t ffn_decode_workspace(int T, int k, int H, int I);

@@ -33,16 +33,12 @@ __device__ __forceinline__ float mx_scaled(uint32_t mag_bits, int e) {
 
 // E2M1 code (sign clear) of r >= 0: round to nearest with the decision points at
 // the midpoints 0.25, 0.75, 1.25, 1.75, 2.5, 3.5 and 5, where the even code wins;
-// anything above 5 takes the largest magnitude, 6.
+// anything above 5 takes the largest magnitude, 6.  The code counts the decision
+// points r has passed (strictly for those where the lower code is the even one),
+// without branches, so the lanes of a warp never diverge.
 __device__ __forceinline__ uint32_t e2m1_code(float r) {
-    if (r <= 0.25f) return 0u;
-    if (r < 0.75f) return 1u;
-    if (r <= 1.25f) return 2u;
-    if (r < 1.75f) return 3u;
-    if (r <= 2.5f) return 4u;
-    if (r < 3.5f) return 5u;
-    if (r <= 5.0f) return 6u;
-    return 7u;
+    return (uint32_t)(r > 0.25f) + (uint32_t)(r >= 0.75f) + (uint32_t)(r > 1.25f) + (uint32_t)(r >= 1.75f) +
+           (uint32_t)(r > 2.5f) + (uint32_t)(r >= 3.5f) + (uint32_t)(r > 5.0f);
 }
 
 }  // namespace moe

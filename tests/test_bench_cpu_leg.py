@@ -75,24 +75,26 @@ def test_workload_shapes_of_the_other_configs():
     assert (c["swap_every_steps"], c["max_swaps"], c["hysteresis"]) == (16, 8, 3.0)
     assert not c["mirror"]  # 20 layers keep the in-place exchange
     c = bench.workload(_args("--config", "c4"))
-    assert (c["T"], c["n_hot"], c["n_cold"]) == (8192, 384, 0)
+    assert (c["T"], c["n_hot"], c["n_cold"], c["prefill"]) == (8192, 384, 0, "fp4")
+    assert bench.workload(_args("--config", "c4", "--prefill", "f16"))["prefill"] == "f16"
     c = bench.workload(_args("--config", "v1"))
     assert (c["T"], c["routing"]) == (6, "verify")
 
 
 def test_prefill_targets_on_the_8192_token_layer():
     """At 8192 tokens x top-6 over 384 experts of H=4096, I=3072: 3.71 TFLOP on
-    7.70 GB of weights plus 134 MB of x and output, about 473 flop/B; at the
-    measured 6751.7 GB/s that caps any kernel near 3.19 PFLOP/s."""
+    7.70 GB of weights, 67 MB of x in and 805 MB of per-pick fp32 outputs, about
+    433 flop/B; at the measured 6751.7 GB/s that caps any kernel near 2.92 PFLOP/s."""
     flops = 2.0 * 3 * 4096 * 3072 * 8192 * 6
-    algo = 384 * 20054016 + 2 * 8192 * 4096 * 2
-    t = bench.prefill_targets(flops, algo, 3.78, 1691.1, 6751.7)
+    algo = 384 * 20054016 + 8192 * 4096 * 2 + 8192 * 6 * 4096 * 4
+    t = bench.prefill_targets(flops, algo, 1.5, 12000.0, "probe", 6751.7)
     assert abs(flops - 3.71e12) < 0.01e12
-    assert abs(t["flop_per_byte"] - 473) < 2
-    assert abs(t["hbm_bound_cap_tflops"] - 3190) < 20
-    assert abs(t["achieved_tflops"] - 981.7) < 1
-    assert abs(t["mxfp4_peak_tflops"] - 6 * 1691.1) < 1e-6
-    assert abs(t["frac_of_mxfp4_peak"] - 981.7 / 10146.6) < 1e-3
+    assert abs(t["flop_per_byte"] - 433) < 2
+    assert abs(t["hbm_bound_cap_tflops"] - 2924) < 20
+    assert abs(t["achieved_tflops"] - 2473.9) < 1
+    assert t["mxfp4_peak_tflops"] == 12000.0 and t["mxfp4_peak_kind"] == "probe"
+    assert abs(t["frac_of_mxfp4_peak"] - 2473.9 / 12000.0) < 1e-4
+    assert abs(t["cap_frac_of_mxfp4_peak"] - t["hbm_bound_cap_tflops"] / 12000.0) < 1e-12
 
 
 def test_skew_share_statistic():
