@@ -21,7 +21,7 @@
 // are written to all four quarters.  One 32-bit word holds four blocks (the K
 // range of two MMAs, sf_id 0 and 2).
 //
-// Warp roles of one persistent CTA per SM (17 warps), each task an expert and a
+// Warp roles of one persistent CTA per SM (25 warps), each task an expert and a
 // 128-row tile:
 //   warp 0       loads the tile's E2M1 rows by TMA, 256 elements of K per stage
 //                (128-byte swizzle; gate and up rows in the gate/up phase, w2 rows
@@ -30,7 +30,7 @@
 //                192 bucket rows, 32 per box), with their scale words;
 //   warp 2       owns tensor memory; one thread issues the MMAs (four of K = 64 per
 //                matrix and stage); in the gate/up phase it issues the gate matrix's
-//                and a thread of warp 16 the up matrix's, each into its accumulator;
+//                and a thread of warp 24 the up matrix's, each into its accumulator;
 //   warp 3       takes tasks from a launch-wide counter, experts with the most
 //                tokens first, and publishes them with their routing values in a
 //                shared-memory queue, up to the queue's depth ahead;
@@ -38,8 +38,8 @@
 //                the tokens' activation scale words of a stage from shared memory
 //                (loaded by TMA with the stage's operands) and stores them into a
 //                ring of scale slots in tensor memory;
-//   warps 8-15   epilogue, two warps per lane quarter taking alternate 16-token
-//                chunks: tensor memory -> registers; gate/up phase: h = SiLU(g) u
+//   warps 8-23   epilogue, four warps per lane quarter taking every fourth 16-token
+//                chunk: tensor memory -> registers; gate/up phase: h = SiLU(g) u
 //                (relative error about 1e-6, so the quantisation of h takes the
 //                decisions of an exact evaluation except within that distance of a
 //                decision point), converted to MXFP4 across the warp's 32 rows and
@@ -67,12 +67,11 @@ constexpr int kMxSfbBox = 200;
 constexpr int kMxBStage = kMxBTile + 2048;     // rows, then the 1600 bytes of scale words
 constexpr int kMxWsc = kMxBM * 16;             // a matrix's scale box: 128 rows x 16 bytes
 constexpr int kMxASlot = kMxTile + kMxWsc;     // per matrix: E2M1 rows, then their scales
-constexpr int kMxSfStages = 3;
-constexpr int kMxThreads = 544;
-constexpr int kMxUpIssuer = 16;  // gate/up phase: the warp that issues the up matrix's MMAs
+constexpr int kMxThreads = 800;
+constexpr int kMxUpIssuer = 24;  // gate/up phase: the warp that issues the up matrix's MMAs
 constexpr int kMxFirstSf = 4;
 constexpr int kMxFirstEpi = 8;
-constexpr int kMxEpiWarps = 8;  // two per lane quarter, taking alternate 16-token chunks
+constexpr int kMxEpiWarps = 16;  // four per lane quarter, taking every fourth 16-token chunk
 constexpr int kMxMaxE = 1024;
 constexpr int kMxTaskQ = 4;
 // Tensor memory: accumulators in [0, 384) -- gate and up (192 columns each) in the
@@ -87,19 +86,19 @@ __host__ __device__ constexpr int mx_mats() { return P == 0 ? 2 : 1; }  // weigh
 // roles that take each task from the queue: producers, issuers, scale writers, epilogue
 template <int P>
 __host__ __device__ constexpr int mx_takers() { return 2 + mx_mats<P>() + 4 + kMxEpiWarps; }
-// Rings: per task an expert's activations are read (from L2) in about as many bytes
-// as its weights (from HBM), so both rings need depth against their latency.
+// One ring of stage slots: slot i holds a stage's weight rows, activation rows and
+// (in tensor memory) scale words; the MMA issuers release all three at once.
 template <int P>
-__host__ __device__ constexpr int mx_astages() { return P == 0 ? 3 : 4; }
-template <int P>
-__host__ __device__ constexpr int mx_bstages() { return P == 0 ? 4 : 5; }
+__host__ __device__ constexpr int mx_stages() { return P == 0 ? 3 : 4; }
 // scale slot: weight words (8 columns per matrix: two words x four quarter columns),
 // then token words (16 columns: word j of the stage at 8j + token group)
 template <int P>
 __host__ __device__ constexpr uint32_t mx_sfb_col() { return P == 0 ? 16u : 8u; }
 template <int P>
 __host__ __device__ constexpr uint32_t mx_sf_cols() { return mx_sfb_col<P>() + 16u; }
-static_assert(kMxSf0 + kMxSfStages * mx_sf_cols<0>() <= kMxTmemCols, "tensor memory budget");
+static_assert(kMxSf0 + mx_stages<0>() * mx_sf_cols<0>() <= kMxTmemCols &&
+                  kMxSf0 + mx_stages<1>() * mx_sf_cols<1>() <= kMxTmemCols,
+              "tensor memory budget");
 
 struct MxTask {
     const uint8_t* blob;
@@ -108,9 +107,8 @@ struct MxTask {
 };
 
 struct alignas(16) MxHead {
-    uint64_t a_full[8], a_empty[8];
-    uint64_t b_full[8], b_empty[8];
-    uint64_t sf_full[kMxSfStages], sf_empty[kMxSfStages];
+    uint64_t a_full[4], b_full[4], sf_full[4];
+    uint64_t st_empty[4];  // the slot's MMAs have completed (one commit per issuer)
     uint64_t acc_full[2], acc_empty[2];
     uint64_t tq_full[kMxTaskQ], tq_empty[kMxTaskQ];
     int tq[kMxTaskQ];
@@ -123,8 +121,8 @@ struct alignas(16) MxHead {
 
 template <int P>
 struct MxSmem {
-    static constexpr size_t kB = (size_t)mx_astages<P>() * mx_mats<P>() * kMxASlot;  // after the weight ring
-    static constexpr size_t kStg = kB + (size_t)mx_bstages<P>() * kMxBStage;
+    static constexpr size_t kB = (size_t)mx_stages<P>() * mx_mats<P>() * kMxASlot;  // after the weight ring
+    static constexpr size_t kStg = kB + (size_t)mx_stages<P>() * kMxBStage;
     static constexpr size_t kHead = kStg + kMxEpiWarps * kMxEpiStage;
     static constexpr size_t kTotal = 1024 + kHead + sizeof(MxHead);
 };
@@ -224,8 +222,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     // the weight scales arrive by TMA with their stage where the plane's rows are whole
     // 16-byte units, else the scale writers read them from global memory
     const bool wsc_tma = mx_scale_maps(K);
-    constexpr int AS = mx_astages<P>();
-    constexpr int BS = mx_bstages<P>();
+    constexpr int NS = mx_stages<P>();
     constexpr int MATS = mx_mats<P>();
     volatile int* abort = &hd.abort;
     // tokens of each active expert (-1: inactive), in the weight ring until the
@@ -266,17 +263,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             hd.D = cnt;
             hd.abort = 0;
             // every consumed slot is released by each issuer's commit (one per matrix)
-            for (int s = 0; s < AS; ++s) {
+            for (int s = 0; s < NS; ++s) {
                 mbar_init(&hd.a_full[s], 1);
-                mbar_init(&hd.a_empty[s], MATS);
-            }
-            for (int s = 0; s < BS; ++s) {
                 mbar_init(&hd.b_full[s], 1);
-                mbar_init(&hd.b_empty[s], MATS);
-            }
-            for (int s = 0; s < kMxSfStages; ++s) {
                 mbar_init(&hd.sf_full[s], 4);
-                mbar_init(&hd.sf_empty[s], MATS);
+                mbar_init(&hd.st_empty[s], MATS);
             }
             for (int s = 0; s < 2; ++s) {
                 mbar_init(&hd.acc_full[s], MATS);
@@ -349,7 +340,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 const int r0 = t.rb * kMxBM;
                 for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.a_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
+                        if (!mbar_wait_fast(&hd.st_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
                             ok = false;
                             break;
                         }
@@ -366,11 +357,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                                 tma_load_2d_hint(dst + kMxTile, smap, 16 * (s >> 1), (mt ? I : 0) + r0, &hd.a_full[as],
                                                  pol);
                         }
-                        advance(as, aph, AS);
+                        advance(as, aph, NS);
                     }
                 }
             }
-            for (int s = 0; s < AS; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
+            for (int s = 0; s < NS; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -388,7 +379,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
                     const int boxes = (mx_ncols(min(kMxNMax, t.cnt - tb)) + kMxBox - 1) / kMxBox;
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
+                        if (!mbar_wait_fast(&hd.st_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
                             ok = false;
                             break;
                         }
@@ -400,23 +391,23 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                         // the stage's two scale words of the pass's tokens, from the 4-aligned
                         // bucket row at or below the first (x is a whole 16 bytes)
                         tma_load_2d_hint(dst + kMxBTile, &sfb_map, (t.off + tb) & ~3, 2 * s, &hd.b_full[bs], pol);
-                        advance(bs, bph, BS);
+                        advance(bs, bph, NS);
                     }
                 }
             }
-            for (int s = 0; s < BS; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < NS; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 2 || (P == 0 && warp == kMxUpIssuer)) {
         // ---------------- MMA issuers (lane 0) ----------------
         // a thread needs about 100 ns to issue one block-scaled MMA, so the gate/up
         // phase issues from two threads, warp 2 the gate matrix's MMAs into the gate
-        // accumulator and warp 16 the up matrix's into the up accumulator; the down
+        // accumulator and warp 24 the up matrix's into the up accumulator; the down
         // phase has one matrix and one issuer
         const int mt = warp == 2 ? 0 : 1;
         if (lane == 0) {
-            int as = 0, bs = 0, ss = 0, buf = 0;
-            unsigned aph = 0, bph = 0, sph = 0, accph = 0;
+            int ss = 0, buf = 0;
+            unsigned sph = 0, accph = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 MxTask t;
@@ -434,19 +425,18 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     accph ^= 1u << buf;
                     tc_fence_after();
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.a_full[as], aph, abort, a.status, a.diag, 35, as, s, task) ||
-                            !mbar_wait_fast(&hd.b_full[bs], bph, abort, a.status, a.diag, 36, bs, s, task) ||
-                            !mbar_wait_fast(&hd.sf_full[ss], sph, abort, a.status, a.diag, 37, ss, s, task)) {
+                        // the scale writers arrive only after both of the stage's loads landed
+                        if (!mbar_wait_fast(&hd.sf_full[ss], sph, abort, a.status, a.diag, 37, ss, s, task)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const int nkk = min(4, (K - s * kMxBK) / 64);  // K steps of 64 in this stage
                         const uint32_t sf = tmem + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
-                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * kMxBStage));  // its rows
+                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)ss * kMxBStage));  // its rows
                         {
                             const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * kMxAccCols;
-                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxASlot));
+                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(ss * MATS + mt) * kMxASlot));
                             for (int kk = 0; kk < nkk; ++kk) {
                                 // a K step of 64 elements advances both start addresses by 32 bytes;
                                 // its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2
@@ -456,12 +446,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                                        sf + mx_sfb_col<P>() + 8u * (uint32_t)(kk >> 1), acc);
                             }
                         }
-                        tc_commit(&hd.a_empty[as]);
-                        tc_commit(&hd.b_empty[bs]);
-                        tc_commit(&hd.sf_empty[ss]);
-                        advance(as, aph, AS);
-                        advance(bs, bph, BS);
-                        advance(ss, sph, kMxSfStages);
+                        tc_commit(&hd.st_empty[ss]);
+                        advance(ss, sph, NS);
                     }
                     if (!ok) break;
                     tc_commit(&hd.acc_full[buf]);
@@ -470,9 +456,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             }
             // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
             // last commit of every slot
-            for (int s = 0; s < AS; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
-            for (int s = 0; s < BS; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
-            for (int s = 0; s < kMxSfStages; ++s) mbar_drain(&hd.sf_empty[s], (s < ss) ? sph : (sph ^ 1u));
+            for (int s = 0; s < NS; ++s) mbar_drain(&hd.st_empty[s], (s < ss) ? sph : (sph ^ 1u));
         }
         __syncwarp();
     } else if (warp >= kMxFirstSf && warp < kMxFirstSf + 4) {
@@ -484,8 +468,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         const int q = warp & 3;
         const int rr = 32 * q + lane;
         const uint32_t qaddr = tmem + ((uint32_t)(q * 32) << 16);
-        int ss = 0, as = 0, bs = 0;
-        unsigned sph = 0, aph = 0, bph = 0;
+        int ss = 0;
+        unsigned sph = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
             MxTask t;
@@ -508,29 +492,27 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                             if (P == 0) wa[1][j] = j < nj ? ld_u32(sg1 + 8 * s + 4 * j) : 0u;
                         }
                     }
-                    if ((wsc_tma && !warp_wait(&hd.a_full[as], aph, a, abort, 40, as, s, task)) ||
-                        !warp_wait(&hd.b_full[bs], bph, a, abort, 41, bs, s, task)) {
+                    // both loads of the stage landed: the producers reused the slot only after
+                    // its previous MMAs completed, so its scale slot is free as well
+                    if (!warp_wait(&hd.a_full[ss], sph, a, abort, 40, ss, s, task) ||
+                        !warp_wait(&hd.b_full[ss], sph, a, abort, 41, ss, s, task)) {
                         ok = false;
                         break;
                     }
                     if (wsc_tma) {
 #pragma unroll
                         for (int mt = 0; mt < MATS; ++mt) {
-                            const uint8_t* row = sA + (size_t)(as * MATS + mt) * kMxASlot + kMxTile + rr * 16 + 8 * (s & 1);
+                            const uint8_t* row = sA + (size_t)(ss * MATS + mt) * kMxASlot + kMxTile + rr * 16 + 8 * (s & 1);
                             wa[mt][0] = *reinterpret_cast<const uint32_t*>(row);
                             wa[mt][1] = nj > 1 ? *reinterpret_cast<const uint32_t*>(row + 4) : 0u;
                         }
                     }
-                    const uint32_t* wsb = reinterpret_cast<const uint32_t*>(sB + (size_t)bs * kMxBStage + kMxBTile);
+                    const uint32_t* wsb = reinterpret_cast<const uint32_t*>(sB + (size_t)ss * kMxBStage + kMxBTile);
                     uint32_t wb[2][6];
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
 #pragma unroll
                         for (int c = 0; c < 6; ++c) wb[j][c] = j < nj ? wsb[j * kMxSfbBox + d0 + 32 * c + lane] : 0u;
-                    if (!warp_wait(&hd.sf_empty[ss], sph ^ 1u, a, abort, 38, ss, s, task)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
                     const uint32_t col = qaddr + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
                     // weight words: matrix mt, word j at column 8 mt + 4 j + q (this lane = row 32 q + lane)
@@ -557,16 +539,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&hd.sf_full[ss]);
-                    advance(ss, sph, kMxSfStages);
-                    advance(as, aph, AS);
-                    advance(bs, bph, BS);
+                    advance(ss, sph, NS);
                 }
             }
         }
     } else if (warp >= kMxFirstEpi && warp < kMxFirstEpi + kMxEpiWarps) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // tensor-memory lane quarter: weight rows 32 q ..
-        const int half = (warp - kMxFirstEpi) >> 2;  // this warp's 16-token chunks: 2 i + half
+        const int half = (warp - kMxFirstEpi) >> 2;  // this warp's 16-token chunks: 4 i + half
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         uint8_t* stg = base + MxSmem<P>::kStg + (size_t)(warp - kMxFirstEpi) * kMxEpiStage;
         int buf = 0;
@@ -582,7 +562,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 // never read: the down phase sees the same id)
                 if (t.rb == 0 && threadIdx.x == kMxFirstEpi * 32) set_status(a.status, MOE_ERR_BAD_EXPERT);
                 if (P == 1)
-                    for (int c = half; c < t.cnt; c += 2)
+                    for (int c = half; c < t.cnt; c += 4)
                         a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + 32 * q + lane] = 0.f;
                 continue;
             }
@@ -595,7 +575,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 accph ^= 1u << buf;
                 tc_fence_after();
                 const uint32_t d = lane_addr + (uint32_t)buf * kMxAccCols;
-                for (int cb = 16 * half; cb < nb; cb += 32) {
+                for (int cb = 16 * half; cb < nb; cb += 64) {
                     if constexpr (P == 0) {
                         float g[16], u[16];
                         tc_ld16x2(d + cb, d + kMxAccCols + cb, g, u);
