@@ -139,9 +139,10 @@ bool encode_plane_raw(CUtensorMap* m, const uint8_t* base, size_t row_bytes, siz
                           CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// Scale plane [rows][row_bytes] for the block-scaled kernels: 16-byte x 128-row boxes.
+// Scale plane [rows][row_bytes]: 16-byte x 32-row boxes (a decode task's gate or up
+// rows; four of them make a prefill tile).
 bool encode_scales(CUtensorMap* m, const uint8_t* base, size_t row_bytes, size_t rows) {
-    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 16, 128,
+    return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, 16, 32,
                           CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 

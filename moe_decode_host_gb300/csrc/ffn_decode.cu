@@ -76,7 +76,10 @@ template <int P, int NT>
 struct Layout {
     static constexpr int kWBytes = kStageRows * 128;
     static constexpr int kABytes = 8 * NT * kActRow;
-    static constexpr int kStageBytes = ((kWBytes + kABytes) + 1023) & ~1023;
+    // the stage rows' scale bytes (16 per row: this stage's 8 blocks and its
+    // neighbour's), by TMA where the scale plane allows it
+    static constexpr int kSBytes = kStageRows * 16;
+    static constexpr int kStageBytes = ((kWBytes + kABytes + kSBytes) + 1023) & ~1023;
     // one partial-sum fragment per consumer warp, reduced once per task
     static constexpr int kFrag = NT * 4 * 32;
     static constexpr int kRedBytes = (int)sizeof(float) * kConsumers * kFrag;
@@ -192,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
     const int ngroups = K / 128;
     const int nst = (ngroups + 1) / 2;
     const int tiles = (P == 0 ? I : H) / C::kTaskRows;
+    // scale words reach the stage by TMA (copy path, scale rows a whole number of
+    // 16-byte units), else the consumers read them from the blob
+    const bool smem_sc = !ZC && mx_scale_maps(K);
 
     // active experts in this launch's token-count range and placement class: every
     // thread takes some experts and, for the active ones, follows the chain to the
@@ -388,9 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                 const TaskInfo ti = task_info(a, hd, task, tiles);
                 if (!ti.valid) continue;
                 const CUtensorMap* map = P == 0 ? &a.tmaps[ti.phys].w13n : &a.tmaps[ti.phys].w2n;
+                const CUtensorMap* smap = P == 0 ? &a.tmaps[ti.phys].w13s : &a.tmaps[ti.phys].w2s;
                 // descriptors live in global memory and a layer's table may reuse the
                 // address of a destroyed one: acquire the current contents for the async proxy
                 asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+                if (smem_sc) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(smap) : "memory");
                 const int r0 = ti.rt * C::kTaskRows;
                 for (int tb = 0; tb < ti.cnt && ok; tb += 8 * NT) {
                     for (int s = 0; s < nst; ++s) {
@@ -402,13 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                             }
                             uint8_t* dst = stages + slot * L::kStageBytes;
                             // full boxes land even past the tensor's edge (zero filled)
-                            mbar_arrive_expect_tx(&hd.full[slot], (unsigned)(L::kWBytes + L::kABytes));
+                            mbar_arrive_expect_tx(&hd.full[slot],
+                                                  (unsigned)(L::kWBytes + L::kABytes + (smem_sc ? L::kSBytes : 0)));
                             if (P == 0) {
                                 tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
                                 tma_load_2d(dst + C::kTaskRows * kSliceBytes, map, s * kSliceBytes, I + r0,
                                             &hd.full[slot]);
                             } else {
                                 tma_load_2d(dst, map, s * kSliceBytes, r0, &hd.full[slot]);
+                            }
+                            if (smem_sc) {
+                                // 16 scale bytes per row (this stage's 8 blocks and the neighbour
+                                // stage's), 32 rows per box: gate then up rows, or two w2 boxes
+                                uint8_t* sdst = dst + L::kWBytes + L::kABytes;
+                                tma_load_2d(sdst, smap, 16 * (s >> 1), r0, &hd.full[slot]);
+                                tma_load_2d(sdst + 32 * 16, smap, 16 * (s >> 1), P == 0 ? I + r0 : r0 + 32,
+                                            &hd.full[slot]);
                             }
                             tma_load_2d(dst + L::kWBytes, &act_map, s * 256, ti.off + tb, &hd.full[slot]);
                         }
@@ -503,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
             // after use for the stage two own stages later
             uint32_t scA[2], scB[2];
             auto load_sc = [&](int s, uint32_t(&dst)[2]) {
+                if (smem_sc) return;  // read from the stage once it has landed
                 const int grp = 2 * s + gl;
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
@@ -527,6 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tma_kernel(FfnArgs a, const _
                     return false;
                 if (2 * s + gl < ngroups) {  // (an odd K tail leaves group 1 of the last stage empty)
                     const uint8_t* stage = stages + sl * L::kStageBytes;
+                    if (smem_sc) {
+                        // word gl of the stage's 8 blocks in each of this lane's two rows
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            sc[r] = *reinterpret_cast<const uint32_t*>(stage + L::kWBytes + L::kABytes + srow[r] * 16 +
+                                                                       8 * (s & 1) + 4 * gl);
+                    }
                     SmemB<NT> bl;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {

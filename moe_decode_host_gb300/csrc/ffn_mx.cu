@@ -354,8 +354,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                                                  (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as], pol);
                             // the 16 scale bytes of each row that hold this stage's 8 blocks
                             if (wsc_tma)
-                                tma_load_2d_hint(dst + kMxTile, smap, 16 * (s >> 1), (mt ? I : 0) + r0, &hd.a_full[as],
-                                                 pol);
+#pragma unroll
+                                for (int i = 0; i < kMxBM / 32; ++i)
+                                    tma_load_2d_hint(dst + kMxTile + i * 32 * 16, smap, 16 * (s >> 1),
+                                                     (mt ? I : 0) + r0 + 32 * i, &hd.a_full[as], pol);
                         }
                         advance(as, aph, NS);
                     }

@@ -96,9 +96,9 @@ struct ExpertMaps {
     CUtensorMap w2n;   // [H rows][I/2 bytes], box 128 B x 64 rows, 128-byte swizzle
     CUtensorMap w13r;  // [2I rows][H/2 bytes], box 64 B x 128 rows, 64-byte swizzle
     CUtensorMap w2r;   // [H rows][I/2 bytes], same box
-    // the two scale planes for the block-scaled kernels, box 16 B x 128 rows: encoded
-    // only where a row is a multiple of 16 bytes (H, resp. I, a multiple of 512),
-    // else zero and unused (see mx_scale_maps)
+    // the two scale planes, box 16 B x 32 rows: encoded only where a row is a multiple
+    // of 16 bytes (H, resp. I, a multiple of 512), else zero and unused (see
+    // mx_scale_maps); the kernels then read the scales from global memory
     CUtensorMap w13s;  // [2I rows][H/32 bytes]
     CUtensorMap w2s;   // [H rows][I/32 bytes]
 };
