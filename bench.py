@@ -173,6 +173,9 @@ def parse():
     ap.add_argument("--prefill", default=None, choices=["f16", "fp4"],
                     help="arithmetic of calls above 64 tokens: exact-weight f16 tensor cores, or block-scaled "
                          "FP4 with x and h in MXFP4 (default for the 8192-token config)")
+    ap.add_argument("--decode-kind", type=int, default=0, choices=[0, 1, 2],
+                    help="arithmetic of calls of at most 64 tokens: 1 the dequant-GEMV kernel, 2 block-scaled "
+                         "tensor cores with 4-term MXFP4 activations, 0 (default) kind 1 at 1-2 tokens, else 2")
     ap.add_argument("--zero-copy", action="store_true",
                     help="the FFN reads picked cold experts in place from host memory (no slot copy)")
     return ap.parse_args()
@@ -208,6 +211,7 @@ def workload(args, config=None, batch=None):
         c.get("layers", 1) == 1 and c["n_cold"] > 0 and not no_res)
     c["zero_copy"] = bool(args.zero_copy)
     c["prefill"] = args.prefill or ("fp4" if c["T"] > 64 else "f16")
+    c["decode_kind"] = args.decode_kind
     if args.n_hot is not None and args.experts is None:
         c["n_hot"] = min(args.n_hot, c["E"])
         c["n_cold"] = c["E"] - c["n_hot"]
@@ -456,6 +460,7 @@ def _config_json(c, args, pool_steps=None):
             "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
             "cold_experts": ("read in place from pinned host memory by the FFN (zero copy)"
                              if c.get("zero_copy") and c["T"] <= 64 else "copied into the HBM slot scratch"),
+            "decode_arithmetic": (None if c["T"] > 64 else decode_arithmetic(c)),
             "prefill_arithmetic": (None if c["T"] <= 64 else (
                 "block-scaled FP4 tensor cores (tcgen05 kind::mxf4), x and h quantised to MXFP4"
                 if c.get("prefill") == "fp4" else "f16 tensor cores (tcgen05 kind::f16), weights expanded exactly")),
@@ -503,6 +508,7 @@ def build_layers(c, dev, seed_tag="bench"):
                         max_swaps=c["max_swaps"], hysteresis=c["hysteresis"],
                         host_mirror=mirror, zero_copy=bool(c.get("zero_copy")))
         layer.set_prefill_kind(1 if c.get("prefill") == "fp4" else 0)
+        layer.set_decode_kind(c.get("decode_kind", 0))
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
 
@@ -601,6 +607,18 @@ def step_launches(T, n_cold):
     per_call = 1 + (1 if T > 8 else 0) + (1 if T > 16 else 0) + (2 if T > 64 else 0)  # decode ranges, gather + tcgen05
     ffn = 1 + calls * per_call + calls // 2          # activation prep, phases, h prescale per down phase
     return route + gather + ffn + 1                  # + combine
+
+
+def decode_arithmetic(c):
+    """What the FFN of a decode-sized call computes in, as the library picks it."""
+    kind = c.get("decode_kind", 0)
+    if c.get("zero_copy") and c.get("n_cold", 0) > 0:
+        kind = 1
+    if kind == 0:
+        kind = 1 if c["T"] < 3 else 2
+    if kind == 2:
+        return "block-scaled FP4 tensor cores (tcgen05 kind::mxf4), activations as sums of 4 MXFP4 terms"
+    return "dequant-GEMV (E2M1 -> f16 in registers, mma.sync)"
 
 
 def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=None):

@@ -221,10 +221,26 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
  *         ship in MXFP4).  The result is the layer with both activations
  *         quantised, which differs from the unquantised layer by the quantisation
  *         of x and h.
- * Calls of at most 64 tokens always run the decode kernel (unquantised
- * activations).  moe_ffn_workspace_bytes follows the kind; set it before sizing
- * the workspace.  Errors: MOE_ERR_INVALID_ARG (null, kind not 0 or 1). */
+ * Calls of at most 64 tokens follow moe_layer_set_decode_kind.
+ * moe_ffn_workspace_bytes follows the kinds; set them before sizing the workspace.
+ * Errors: MOE_ERR_INVALID_ARG (null, kind not 0 or 1). */
 int moe_layer_set_prefill_kind(moe_layer* L, int kind);
+
+/* Arithmetic of calls with at most 64 tokens (decode-sized).
+ *  kind 1: the dequant-GEMV kernel (E2M1 weights expanded to f16 in registers, f16
+ *         activations, mma.sync).
+ *  kind 2: every bucket on block-scaled tcgen05 kind::mxf4 tensor cores, which
+ *         decode the MXFP4 weights themselves; each activation (x, then h) is
+ *         written as a sum of four MXFP4 terms, the first the activation rounded to
+ *         MXFP4 and each further one the remainder of those before, with block
+ *         exponents chosen so that no element saturates (each remainder is exact in
+ *         fp32), so the result is the unquantised layer's to about 2e-4 relative.
+ *  kind 0 (default): kind 1 for calls of 1 or 2 tokens, kind 2 from 3 tokens up
+ *         (on a GB300 the block-scaled kernels are the faster from 4 tokens of
+ *         H = 4096, I = 3072, k = 6 up, the GEMV at 1 and 2).
+ * Layers that read cold experts in place (moe_params.zero_copy) run kind 1 for
+ * calls with cold experts.  Errors: MOE_ERR_INVALID_ARG (null, kind not 0, 1 or 2). */
+int moe_layer_set_decode_kind(moe_layer* L, int kind);
 
 /* moe_grouped_ffn for callers that cannot allocate device memory (an engine that
  * has given all free HBM to its own pools and forbids later allocations, code

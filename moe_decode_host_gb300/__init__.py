@@ -115,6 +115,12 @@ class Layer:
         1: all-FP4 block-scaled path (x and h quantised to MXFP4)."""
         check(lib.moe_layer_set_prefill_kind(self.handle, kind), "moe_layer_set_prefill_kind")
 
+    def set_decode_kind(self, kind: int):
+        """Arithmetic of calls of at most 64 tokens: 1 the dequant-GEMV kernel; 2
+        block-scaled tensor cores with 4-term MXFP4 activations; 0 (default) kind 1
+        for 1 or 2 tokens, kind 2 from 3 up."""
+        check(lib.moe_layer_set_decode_kind(self.handle, kind), "moe_layer_set_decode_kind")
+
     def set_copy_ctas(self, ctas: int):
         check(lib.moe_layer_set_copy_ctas(self.handle, ctas), "moe_layer_set_copy_ctas")
 

@@ -57,6 +57,7 @@ struct moe_layer {
     long steps = 0;
     int fault = 0;
     int prefill_kind = 0;  // moe_layer_set_prefill_kind
+    int decode_kind = 0;   // moe_layer_set_decode_kind
 };
 
 namespace {
@@ -400,14 +401,26 @@ int moe_gather_join(moe_layer* L, void* stream) {
 }
 
 namespace {
-// Calls with more tokens than a decode-sized bucket can hold run the block-scaled
-// (all-FP4) path when the layer asks for it.
-bool use_mx(const moe_layer* L, int T) { return L->prefill_kind == 1 && T > kTcMinTokens; }
+// The kernels a call runs.  Prefill-sized calls (more than 64 tokens): the all-FP4
+// block-scaled kernels when the layer asks for them (1 activation term), else the
+// dequant-GEMV kernel for buckets of at most 64 tokens and the f16 tensor-core kernel
+// above.  Decode-sized calls: the block-scaled kernels with activations as sums of
+// four MXFP4 terms from kBlockScaledMinTokens tokens up (or always, kind 2), the
+// dequant-GEMV kernel below that (or always, kind 1) and whenever the layer reads cold
+// experts in place (zero copy), which only that kernel does.
+constexpr int kBlockScaledMinTokens = 3;
+int mx_terms(const moe_layer* L, int T) {
+    if (T > kTcMinTokens) return L->prefill_kind == 1 ? 1 : 0;
+    if (L->decode_kind == 1 || (L->p.zero_copy && L->p.n_cold > 0)) return 0;
+    if (L->decode_kind == 0 && T < kBlockScaledMinTokens) return 0;
+    return 4;
+}
 
 size_t ffn_workspace(const moe_layer* L, int T) {
     const size_t d = ffn_decode_workspace(T, L->p.k, L->p.H, L->p.I);
-    if (!use_mx(L, T)) return d;
-    const size_t m = ffn_mx_workspace(T, L->p.k, L->p.H, L->p.I);
+    const int terms = mx_terms(L, T);
+    if (terms == 0) return d;
+    const size_t m = ffn_mx_workspace(T, L->p.k, L->p.H, L->p.I, terms);
     return d > m ? d : m;
 }
 }  // namespace
@@ -421,6 +434,12 @@ int moe_ffn_workspace_bytes(const moe_layer* L, int T, size_t* bytes) {
 int moe_layer_set_prefill_kind(moe_layer* L, int kind) {
     if (!L || kind < 0 || kind > 1) return MOE_ERR_INVALID_ARG;
     L->prefill_kind = kind;
+    return MOE_OK;
+}
+
+int moe_layer_set_decode_kind(moe_layer* L, int kind) {
+    if (!L || kind < 0 || kind > 2) return MOE_ERR_INVALID_ARG;
+    L->decode_kind = kind;
     return MOE_OK;
 }
 
@@ -460,24 +479,33 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     // join, end (the two middle events coincide when no copy is pending)
     cudaEvent_t* pe = L->fprof_n < (int)L->fprof_ev.size() / 4 ? &L->fprof_ev[4 * L->fprof_n++] : nullptr;
     cudaError_t err = pe ? cudaEventRecord(pe[0], st) : cudaSuccess;
-    if (use_mx(L, T)) {
-        // block-scaled path: x converted to MXFP4 once, then per placement class the
-        // gate/up kernel (h converted in its epilogue) and the down kernel; experts in
-        // HBM first while a cold copy is in flight
-        if (err == cudaSuccess) err = launch_ffn_mx_prep(a, workspace, st);
+    // While the cold experts stream over the link (copy, or zero-copy chain) on the
+    // layer's copy stream, that stream's CTAs hold copy_ctas SMs: the persistent FFN
+    // launches that run meanwhile take the other SMs, so that all their CTAs are
+    // resident and they complete as soon as their work does (a launch with CTAs
+    // waiting for an SM would end only when the copy frees one, and the next kernel
+    // waits for it).
+    const int hot_sms = L->sm_count > L->copy_ctas ? L->sm_count - L->copy_ctas : L->sm_count;
+    const int terms = mx_terms(L, T);
+    if (terms > 0) {
+        // block-scaled path: x converted to MXFP4 terms once, then per placement class
+        // the gate/up kernel (h converted in its epilogue) and the down kernel; experts
+        // in HBM first while a cold copy is in flight
+        const int lo = 0, hi = 1 << 30;
+        if (err == cudaSuccess) err = launch_ffn_mx_prep(a, workspace, terms, st);
         if (err == cudaSuccess && L->copy_pending) {
-            err = launch_ffn_mx(a, 0, 1, L->sm_count, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 1, L->sm_count, st);
+            err = launch_ffn_mx(a, 0, 1, lo, hi, terms, hot_sms, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 1, lo, hi, terms, hot_sms, st);
             if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
             if (err == cudaSuccess) err = join_copy(L, st);
             if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 2, L->sm_count, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 2, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 2, lo, hi, terms, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 2, lo, hi, terms, L->sm_count, st);
         } else {
             if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
             if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 0, L->sm_count, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 0, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 0, lo, hi, terms, L->sm_count, st);
+            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 0, lo, hi, terms, L->sm_count, st);
         }
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[3], st);
         return cuda_status(err);
@@ -501,18 +529,15 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
             ++L->prof_n;
         }
         if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 1, hot_sms, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(st, L->ev_join, 0);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
     } else if (L->copy_pending) {
-        // experts in HBM first, while the cold copy is in flight; then the cold ones.
-        // An FFN CTA leaves no room on its SM for a copy CTA; the decode kernel's CTAs
-        // take tasks from a shared counter, so those that start only when the copy
-        // frees their SM simply take fewer
-        err = launch_ffn_phase(a, 0, 1, L->sm_count, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, L->sm_count, st);
+        // experts in HBM first, on the SMs the cold copy leaves free; then the cold ones
+        err = launch_ffn_phase(a, 0, 1, hot_sms, st);
+        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
         if (err == cudaSuccess) err = join_copy(L, st);
         if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);

@@ -203,10 +203,17 @@ __device__ __forceinline__ int mx_warp_take(MxHead& hd, int k, const FfnArgs& a,
 // MMA width of a pass over nb tokens: a multiple of 16 (the M = 128 shape's step).
 __device__ __forceinline__ int mx_ncols(int nb) { return (nb + 15) & ~15; }
 
-template <int P>
+// TERMS: activation rows per token.  1: x and h converted to MXFP4 by the OCP rule
+// (the all-FP4 mode).  4: each activation written as a sum of four MXFP4 terms, the
+// first the activation, each further one the residual of those before (exponent
+// rule mx_term_exp, so nothing saturates and every residual is exact in fp32), so
+// the products reproduce the unquantised layer to about 2e-4; the terms of a token
+// are consecutive rows and consecutive accumulator columns, summed in the epilogue.
+// The launch takes the experts with lo < tokens <= hi.
+template <int P, int TERMS>
 __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const __grid_constant__ CUtensorMap act_map,
                                                                const __grid_constant__ CUtensorMap sfb_map, int sel,
-                                                               int ctr) {
+                                                               int ctr, int lo, int hi) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = base;
@@ -217,8 +224,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     const int K = P == 0 ? H : I;
     const int nks = (K + kMxBK - 1) / kMxBK;  // stages per pass; the last may hold 128 elements
     const int tiles = (P == 0 ? I : H) / kMxBM;
-    const int R = a.T * a.k;  // bucket rows
-    const int Rs = (R + 3) & ~3;  // row stride of the activation scale words
+    const int R = a.T * a.k * TERMS;  // activation rows: TERMS per bucket row
+    const int Rs = (R + 3) & ~3;      // row stride of the activation scale words
+    constexpr int TPP = kMxNMax / TERMS;  // tokens per column pass
     // the weight scales arrive by TMA with their stage where the plane's rows are whole
     // 16-byte units, else the scale writers read them from global memory
     const bool wsc_tma = mx_scale_maps(K);
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     // tokens first (ties by id): every thread keys some experts, then ranks its own
     for (int e = threadIdx.x; e < a.E; e += kMxThreads) {
         const int c = __ldg(a.counts + e);
-        bool act = c > 0;
+        bool act = c > lo && c <= hi;
         if (act && sel != 0) {
             const bool hot = __ldg(a.loc + e) < a.n_hot;
             act = (sel == 1) ? hot : !hot;
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
                 if (wsc_tma) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(smap) : "memory");
                 const int r0 = t.rb * kMxBM;
-                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
+                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
                     for (int s = 0; s < nks; ++s) {
                         if (!mbar_wait_fast(&hd.st_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
                             ok = false;
@@ -378,8 +386,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 const int task = mx_take(hd, k, a, abort, 1, t);
                 if (task < 0) break;
                 if (!t.valid) continue;
-                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
-                    const int boxes = (mx_ncols(min(kMxNMax, t.cnt - tb)) + kMxBox - 1) / kMxBox;
+                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                    const int row0 = TERMS * (t.off + tb);  // first activation row of the pass
+                    const int boxes = (mx_ncols(TERMS * min(TPP, t.cnt - tb)) + kMxBox - 1) / kMxBox;
                     for (int s = 0; s < nks; ++s) {
                         if (!mbar_wait_fast(&hd.st_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
                             ok = false;
@@ -388,11 +397,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                         mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB + 2 * kMxSfbBox * 4));
                         uint8_t* dst = sB + (size_t)bs * kMxBStage;
                         for (int bx = 0; bx < boxes; ++bx)
-                            tma_load_2d_hint(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB,
-                                             t.off + tb + kMxBox * bx, &hd.b_full[bs], pol);
+                            tma_load_2d_hint(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB, row0 + kMxBox * bx,
+                                             &hd.b_full[bs], pol);
                         // the stage's two scale words of the pass's tokens, from the 4-aligned
                         // bucket row at or below the first (x is a whole 16 bytes)
-                        tma_load_2d_hint(dst + kMxBTile, &sfb_map, (t.off + tb) & ~3, 2 * s, &hd.b_full[bs], pol);
+                        tma_load_2d_hint(dst + kMxBTile, &sfb_map, row0 & ~3, 2 * s, &hd.b_full[bs], pol);
                         advance(bs, bph, NS);
                     }
                 }
@@ -416,8 +425,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 const int task = mx_take(hd, k, a, abort, 2 + mt, t);
                 if (task < 0) break;
                 if (!t.valid) continue;
-                for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
-                    const int N = mx_ncols(min(kMxNMax, t.cnt - tb));
+                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                    const int N = mx_ncols(TERMS * min(TPP, t.cnt - tb));
                     const uint32_t id0 = mx_idesc(N, 0u), id2 = mx_idesc(N, 2u);
                     if (!mbar_wait_fast(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, abort, a.status, a.diag, 34,
                                         buf, 0, task)) {
@@ -482,8 +491,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             const size_t srl = (size_t)K / 32;  // scale bytes per weight row
             const uint8_t* sg0 = t.blob + (P == 0 ? a.w13s : a.w2s) + (size_t)(r0 + rr) * srl;
             const uint8_t* sg1 = P == 0 ? t.blob + a.w13s + (size_t)(I + r0 + rr) * srl : sg0;
-            for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
-                const int d0 = (t.off + tb) & 3;  // first token's place in the loaded words
+            for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                const int d0 = (TERMS * (t.off + tb)) & 3;  // first row's place in the loaded words
                 for (int s = 0; s < nks; ++s) {
                     const int nj = min(2, (K - s * kMxBK) / 128);  // words of this stage
                     uint32_t wa[2][2] = {{0u, 0u}, {0u, 0u}};
@@ -568,8 +577,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                         a.y[(size_t)__ldg(a.entries + t.off + c) * H + r0 + 32 * q + lane] = 0.f;
                 continue;
             }
-            for (int tb = 0; tb < t.cnt && ok; tb += kMxNMax) {
-                const int nb = min(kMxNMax, t.cnt - tb);
+            for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                const int nb = min(TPP, t.cnt - tb);  // tokens of the pass
+                const int ncol = TERMS * nb;          // accumulator columns (activation rows)
                 if (!warp_wait(&hd.acc_full[buf], (accph >> buf) & 1u, a, abort, 39, buf, tb, task)) {
                     ok = false;
                     break;
@@ -577,31 +587,44 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 accph ^= 1u << buf;
                 tc_fence_after();
                 const uint32_t d = lane_addr + (uint32_t)buf * kMxAccCols;
-                for (int cb = 16 * half; cb < nb; cb += 64) {
+                for (int cb = 16 * half; cb < ncol; cb += 64) {
+                    constexpr int TOK = 16 / TERMS;  // tokens of a 16-column chunk
                     if constexpr (P == 0) {
                         float g[16], u[16];
                         tc_ld16x2(d + cb, d + kMxAccCols + cb, g, u);
                         int es[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
+                        for (int n = 0; n < TOK; ++n) {
+                            float gs = 0.f, us = 0.f;
+#pragma unroll
+                            for (int tt = 0; tt < TERMS; ++tt) {
+                                gs += g[n * TERMS + tt];
+                                us += u[n * TERMS + tt];
+                            }
                             // the fast exponential and division: relative error about 1e-6 for
                             // |g| up to 10, far below the quantisation step of h
-                            const float h = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
-                            const uint32_t bits = __float_as_uint(h);
-                            const uint32_t mag = bits & 0x7fffffffu;
-                            // one 32-element block of h per token: this warp's 32 rows
-                            const int e = mx_block_exp(__reduce_max_sync(0xffffffffu, mag));
-                            const uint32_t code = e2m1_code(mx_scaled(mag, e)) | ((bits >> 31) << 3);
-                            const uint32_t odd = __shfl_down_sync(0xffffffffu, code, 1);
-                            if ((lane & 1) == 0) stg[i * 16 + (lane >> 1)] = (uint8_t)(code | (odd << 4));
-                            es[i] = e;
+                            float r = __fdividef(gs, 1.0f + __expf(-gs)) * us;
+#pragma unroll
+                            for (int tt = 0; tt < TERMS; ++tt) {
+                                const int i = n * TERMS + tt;
+                                const uint32_t bits = __float_as_uint(r);
+                                const uint32_t mag = bits & 0x7fffffffu;
+                                // one 32-element block of h per token: this warp's 32 rows
+                                const uint32_t amax = __reduce_max_sync(0xffffffffu, mag);
+                                const int e = TERMS == 1 ? mx_block_exp(amax) : mx_term_exp(amax);
+                                const uint32_t code = e2m1_code(mx_scaled(mag, e)) | ((bits >> 31) << 3);
+                                const uint32_t odd = __shfl_down_sync(0xffffffffu, code, 1);
+                                if ((lane & 1) == 0) stg[i * 16 + (lane >> 1)] = (uint8_t)(code | (odd << 4));
+                                es[i] = e;
+                                if (TERMS > 1) r -= mx_decode(code, e);  // exact: the next term's input
+                            }
                         }
                         __syncwarp();
                         int my_e = es[0];
 #pragma unroll
                         for (int i = 1; i < 16; ++i) my_e = lane == i ? es[i] : my_e;
-                        if (lane < 16 && cb + lane < nb) {
-                            const int row = t.off + tb + cb + lane;  // bucket row of this token
+                        if (lane < 16 && cb + lane < ncol) {
+                            const int row = TERMS * (t.off + tb) + cb + lane;  // activation row of this column
                             *reinterpret_cast<uint4*>(a.hq + (size_t)row * (I / 2) + (r0 + 32 * q) / 2) =
                                 *reinterpret_cast<const uint4*>(stg + lane * 16);
                             // block (r0 + 32 q) / 32 is byte q of word r0 / 128
@@ -612,13 +635,19 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     } else {
                         float v[16];
                         tc_ld16(d + cb, v);
-                        int pk[16];
+                        int pk[TOK];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = cb + i < nb ? __ldg(a.entries + t.off + tb + cb + i) : 0;
+                        for (int n = 0; n < TOK; ++n) {
+                            const int tok = cb / TERMS + n;
+                            pk[n] = tok < nb ? __ldg(a.entries + t.off + tb + tok) : 0;
+                        }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (cb + i < nb) a.y[(size_t)pk[i] * H + r0 + 32 * q + lane] = v[i];
+                        for (int n = 0; n < TOK; ++n) {
+                            float sum = 0.f;
+#pragma unroll
+                            for (int tt = 0; tt < TERMS; ++tt) sum += v[n * TERMS + tt];
+                            if (cb / TERMS + n < nb) a.y[(size_t)pk[n] * H + r0 + 32 * q + lane] = sum;
+                        }
                     }
                 }
                 tc_fence_before();
@@ -636,9 +665,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     }
 }
 
-// One CTA per bucket row i: x of token entries[i] / k converted to MXFP4 into row i
-// of xq, and its block scales into the words of xs (word g of row i at g * Rs + i).
-// Thread b takes block b (32 elements, 64 bytes of bf16).
+// One CTA per bucket row i: x of token entries[i] / k converted to TERMS rows of
+// MXFP4 (rows TERMS i .. TERMS i + TERMS - 1 of xq; see ffn_mx_kernel), and their block
+// scales into the words of xs (word g of row j at g * Rs + j).  Thread b takes block
+// b (32 elements, 64 bytes of bf16).
+template <int TERMS>
 __global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __restrict__ x, int H, int k, int Rs,
                                                        const int32_t* __restrict__ entries, uint8_t* __restrict__ xq,
                                                        uint32_t* __restrict__ xs, int32_t* __restrict__ task_ctr) {
@@ -651,33 +682,39 @@ __global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __re
         const int lane = threadIdx.x & 31;
         const int active = min(32, nblk - (b - lane));
         const unsigned mask = active >= 32 ? 0xffffffffu : ((1u << active) - 1u);
-        uint32_t w[16];
+        float r[32];  // the block (bf16 widens exactly), then each term's residual
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint4 v = __ldg(src + 4 * b + j);
-            w[4 * j] = v.x, w[4 * j + 1] = v.y, w[4 * j + 2] = v.z, w[4 * j + 3] = v.w;
-        }
-        uint32_t amax = 0;
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            amax = max(amax, (w[j] & 0x7fffu) << 16);
-            amax = max(amax, (w[j] >> 16 & 0x7fffu) << 16);
+            for (int q = 0; q < 4; ++q) {
+                r[8 * j + 2 * q] = __uint_as_float(w4[q] << 16);
+                r[8 * j + 2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+            }
         }
-        const int e = mx_block_exp(amax);
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            // elements 2j (low half) and 2j + 1 (high half) -> byte j, low nibble first
-            const uint32_t lo = w[j] & 0xffffu, hi = w[j] >> 16;
-            const uint32_t c0 = e2m1_code(mx_scaled((lo & 0x7fffu) << 16, e)) | ((lo >> 15) << 3);
-            const uint32_t c1 = e2m1_code(mx_scaled((hi & 0x7fffu) << 16, e)) | ((hi >> 15) << 3);
-            o[j >> 2] |= (c0 | (c1 << 4)) << (8 * (j & 3));
+        for (int tt = 0; tt < TERMS; ++tt) {
+            uint32_t amax = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = max(amax, __float_as_uint(r[j]) & 0x7fffffffu);
+            const int e = TERMS == 1 ? mx_block_exp(amax) : mx_term_exp(amax);
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                // element j -> byte j / 2, low nibble when j is even
+                const uint32_t bits = __float_as_uint(r[j]);
+                const uint32_t c = e2m1_code(mx_scaled(bits & 0x7fffffffu, e)) | ((bits >> 31) << 3);
+                o[j >> 3] |= c << (4 * (j & 7));
+                if (TERMS > 1) r[j] -= mx_decode(c, e);  // exact: the next term's input
+            }
+            const size_t row = (size_t)TERMS * i + tt;
+            *reinterpret_cast<uint4*>(xq + row * (H / 2) + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
+            uint32_t word = (uint32_t)(e + 127) << (8 * (b & 3));
+            word |= __shfl_xor_sync(mask, word, 1);
+            word |= __shfl_xor_sync(mask, word, 2);
+            if ((b & 3) == 0) xs[(size_t)(b >> 2) * Rs + row] = word;
         }
-        *reinterpret_cast<uint4*>(xq + (size_t)i * (H / 2) + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
-        uint32_t word = (uint32_t)(e + 127) << (8 * (b & 3));
-        word |= __shfl_xor_sync(mask, word, 1);
-        word |= __shfl_xor_sync(mask, word, 2);
-        if ((b & 3) == 0) xs[(size_t)(b >> 2) * Rs + i] = word;
     }
 }
 
@@ -687,9 +724,9 @@ struct MxWs {
     size_t ctr, xq, xs, hq, hs, total;
 };
 
-MxWs mx_ws(int T, int k, int H, int I) {
+MxWs mx_ws(int T, int k, int H, int I, int terms) {
     MxWs w;
-    const size_t R = (size_t)T * k, Rs = (R + 3) & ~(size_t)3;
+    const size_t R = (size_t)T * k * terms, Rs = (R + 3) & ~(size_t)3;
     size_t o = 0;
     w.ctr = o;
     o = mx_align256(o + kTaskCounters * sizeof(int32_t));
@@ -705,12 +742,25 @@ MxWs mx_ws(int T, int k, int H, int I) {
     return w;
 }
 
+template <int P, int TERMS>
+cudaError_t launch_mx(const FfnArgs& a, const CUtensorMap& map, const CUtensorMap& smap, int sel, int lo, int hi,
+                      int grid, cudaStream_t st) {
+    static std::atomic<uint64_t> configured{0};
+    const size_t smem = MxSmem<P>::kTotal;
+    cudaError_t err = ensure_smem_limit((const void*)ffn_mx_kernel<P, TERMS>, (int)smem, configured);
+    if (err != cudaSuccess) return err;
+    // task counters 12-15 of the call's workspace (zeroed by the prep kernel): one per
+    // phase and placement class
+    const int ctr = 12 + (sel == 2 ? 2 : 0) + P;
+    return launch_pdl(ffn_mx_kernel<P, TERMS>, dim3(grid), dim3(kMxThreads), smem, st, a, map, smap, sel, ctr, lo, hi);
+}
+
 }  // namespace
 
-size_t ffn_mx_workspace(int T, int k, int H, int I) { return mx_ws(T, k, H, I).total; }
+size_t ffn_mx_workspace(int T, int k, int H, int I, int terms) { return mx_ws(T, k, H, I, terms).total; }
 
-cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
-    const MxWs w = mx_ws(a.T, a.k, a.H, a.I);
+cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, int terms, cudaStream_t st) {
+    const MxWs w = mx_ws(a.T, a.k, a.H, a.I, terms);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.task_ctr = reinterpret_cast<int32_t*>(ws + w.ctr);
     a.xq = ws + w.xq;
@@ -719,12 +769,17 @@ cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st) {
     a.hs = reinterpret_cast<uint32_t*>(ws + w.hs);
     if (a.T == 0) return cudaSuccess;
     const int R = a.T * a.k;
-    mx_xprep_kernel<<<R, 128, 0, st>>>(a.x, a.H, a.k, (R + 3) & ~3, a.entries, a.xq, a.xs, a.task_ctr);
+    const int Rs = (R * terms + 3) & ~3;
+    if (terms == 1)
+        mx_xprep_kernel<1><<<R, 128, 0, st>>>(a.x, a.H, a.k, Rs, a.entries, a.xq, a.xs, a.task_ctr);
+    else
+        mx_xprep_kernel<4><<<R, 128, 0, st>>>(a.x, a.H, a.k, Rs, a.entries, a.xq, a.xs, a.task_ctr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st) {
-    const int R = a.T * a.k;
+cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int lo, int hi, int terms, int sm_count,
+                          cudaStream_t st) {
+    const int R = a.T * a.k * terms;
     if (R == 0) return cudaSuccess;
     // activations of the phase: [R rows][K/2 bytes] E2M1, boxes of 128 bytes x 32 rows, 128-byte swizzle
     CUtensorMap map;
@@ -738,21 +793,16 @@ cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cu
     if (!encode_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT32, phase == 0 ? a.xs : a.hs, (uint64_t)Rs,
                         (uint64_t)(K / 128), (uint64_t)Rs * 4, kMxSfbBox, 2, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    const long dmax = (long)(a.E < R ? a.E : R);
+    const long picks = (long)a.T * a.k;
+    const long dmax = a.E < picks ? a.E : picks;
     const long tasks = dmax * ((phase == 0 ? a.I : a.H) / kMxBM);
     const int grid = (int)(tasks < sm_count ? tasks : sm_count);
     if (grid <= 0) return cudaSuccess;
-    static std::atomic<uint64_t> configured[2];
-    const size_t smem = phase == 0 ? MxSmem<0>::kTotal : MxSmem<1>::kTotal;
-    cudaError_t err = ensure_smem_limit(phase == 0 ? (const void*)ffn_mx_kernel<0> : (const void*)ffn_mx_kernel<1>,
-                                        (int)smem, configured[phase]);
-    if (err != cudaSuccess) return err;
-    // task counters 12-15 of the call's workspace (zeroed by the prep kernel): one per
-    // phase and placement class
-    const int ctr = 12 + (sel == 2 ? 2 : 0) + phase;
-    if (phase == 0)
-        return launch_pdl(ffn_mx_kernel<0>, dim3(grid), dim3(kMxThreads), smem, st, a, map, smap, sel, ctr);
-    return launch_pdl(ffn_mx_kernel<1>, dim3(grid), dim3(kMxThreads), smem, st, a, map, smap, sel, ctr);
+    if (terms == 1)
+        return phase == 0 ? launch_mx<0, 1>(a, map, smap, sel, lo, hi, grid, st)
+                          : launch_mx<1, 1>(a, map, smap, sel, lo, hi, grid, st);
+    return phase == 0 ? launch_mx<0, 4>(a, map, smap, sel, lo, hi, grid, st)
+                      : launch_mx<1, 4>(a, map, smap, sel, lo, hi, grid, st);
 }
 
 }  // namespace moe

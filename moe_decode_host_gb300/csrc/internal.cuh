@@ -173,9 +173,13 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, int phase, int sel, int lo, int sm_c
 // points the workspace fields of `a` at `workspace`, zeroes the task counters and
 // quantises x into bucket order; one phase (0: gate/up -> h quantised, 1: down -> y)
 // over every selected expert with at least one token.
-size_t ffn_mx_workspace(int T, int k, int H, int I);
-cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, cudaStream_t st);
-cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int sm_count, cudaStream_t st);
+// terms: activation rows per token (1: the all-FP4 mode; 4: a sum of four MXFP4
+// terms that reproduces the activation, the decode path); lo < tokens <= hi selects
+// the experts of a launch.
+size_t ffn_mx_workspace(int T, int k, int H, int I, int terms);
+cudaError_t launch_ffn_mx_prep(FfnArgs& a, void* workspace, int terms, cudaStream_t st);
+cudaError_t launch_ffn_mx(const FfnArgs& a, int phase, int sel, int lo, int hi, int terms, int sm_count,
+                          cudaStream_t st);
 
 cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, void* out, int out_fp32,
                            cudaStream_t st);

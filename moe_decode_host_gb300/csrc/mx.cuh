@@ -42,3 +42,31 @@ __device__ __forceinline__ uint32_t e2m1_code(float r) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// 2^k as a float, exactly, for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float mx_pow2(int k) {
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(1u << (k + 149));
+}
+
+// Exponent of one term of an activation written as a sum of MXFP4 terms (the
+// decode path, where the sum must reproduce the activation closely): the smallest
+// e with max |v| <= 6 * 2^e, so no element saturates, clamped to [-127, 127].  For a
+// normal max of 2^f * (1 + m) that is f - 2 when m <= 1/2, else f - 1; a subnormal
+// max takes -127.
+__device__ __forceinline__ int mx_term_exp(uint32_t amax_bits) {
+    if ((amax_bits >> 23) == 0u) return -127;
+    const int f = (int)(amax_bits >> 23) - 127;
+    const int e = (amax_bits & 0x7fffffu) > 0x400000u ? f - 1 : f - 2;
+    return max(-127, min(127, e));
+}
+
+// Value of E2M1 code c (sign bit 3) at block exponent e: twice the magnitudes
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6} are the nibbles of 0xC8643210.
+__device__ __forceinline__ float mx_decode(uint32_t c, int e) {
+    const float m = (float)((0xC8643210u >> (4 * (c & 7u))) & 0xFu) * mx_pow2(e - 1);
+    return (c & 8u) ? -m : m;
+}
+
+}  // namespace moe

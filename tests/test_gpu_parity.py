@@ -246,10 +246,11 @@ def _compare_layer(fx, buf, logits, x, tokens, out_fp32):
 @pytest.mark.parametrize("T,dist", [(1, "uniform"), (8, "zipf1.1"), (33, "zipf1.5"), (64, "uniform")])
 def test_layer_zero_copy_matches_copy_path(T, dist):
     """Zero copy: the cold experts' weights are read in place from host memory and
-    their slots stay untouched; the outputs match the copy path's to rounding (the
-    same arithmetic in the same order; the two kernel variants are compiled
-    separately, so the compiler's fused multiply-adds may differ in the last bit)
-    and the oracle within the bar."""
+    their slots stay untouched; the outputs match the copy path's on the same
+    dequant-GEMV kernel to rounding (the same arithmetic in the same order; the two
+    kernel variants are compiled separately, so the compiler's fused multiply-adds
+    may differ in the last bit), and the oracle within the bar; the copy path on the
+    block-scaled decode kernels matches the oracle too."""
     H, I, E, n_hot, k = 1024, 768, 32, 24, 6
     loc = np.random.default_rng(T).permutation(E).astype(np.int32)
     if dist == "uniform":
@@ -260,6 +261,7 @@ def test_layer_zero_copy_matches_copy_path(T, dist):
     outs = []
     for zc in (False, True):
         fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=E - n_hot, k=k, seed=77, loc=loc, zero_copy=zc)
+        fx.layer.set_decode_kind(1)  # the copy path on the same kernel as the zero-copy path
         fx.slots.fill_(0xAB)
         buf = _run_layer(fx, logits, x, True)
         outs.append((buf.y.cpu().clone(), buf.out.cpu().clone()))
@@ -270,6 +272,11 @@ def test_layer_zero_copy_matches_copy_path(T, dist):
         fx.layer.close()
     assert rel_l2(outs[1][0].numpy(), outs[0][0].numpy()) <= 1e-6
     assert rel_l2(outs[1][1].numpy(), outs[0][1].numpy()) <= 1e-6
+    # the default decode kernels on the copy path
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=E - n_hot, k=k, seed=77, loc=loc)
+    buf = _run_layer(fx, logits, x, True)
+    _compare_layer(fx, buf, logits, x, list(range(0, T, max(1, T // 8))), True)
+    fx.layer.close()
 
 
 def test_layer_zero_copy_large_call_copies():
@@ -302,16 +309,23 @@ def test_layer_c0(out_fp32):
     _compare_layer(fx, buf, logits, x, list(range(c["T"])), out_fp32)
 
 
+@pytest.mark.parametrize("decode_kind", [0, 1, 2])
 @pytest.mark.parametrize("H,I,E,n_hot,k,T,dist", [
-    (384, 640, 40, 30, 5, 13, "uniform"),   # uneven split of the reduction over warps
+    (384, 640, 40, 30, 5, 13, "uniform"),   # uneven split of the reduction over warps; K stages of 128
     (128, 128, 8, 5, 8, 3, "uniform"),      # k == E, a single 128-group per row
-    (512, 256, 64, 48, 6, 40, "zipf1.5"),   # buckets above 8, 16 and 32 tokens
+    (512, 256, 64, 48, 6, 40, "zipf1.5"),   # buckets above 8, 16, 32 and 48 tokens (two column passes)
     (256, 512, 16, 0, 2, 17, "uniform"),    # everything cold
+    (256, 512, 16, 8, 4, 1, "uniform"),     # one token (default: dequant-GEMV)
+    (384, 640, 40, 30, 5, 2, "uniform"),    # two tokens
 ])
-def test_layer_ragged_shapes(H, I, E, n_hot, k, T, dist):
+def test_layer_ragged_shapes(H, I, E, n_hot, k, T, dist, decode_kind):
+    """Decode-sized calls on both decode kernels: the dequant-GEMV kernel (kind 1),
+    block-scaled tensor cores with four-term activations (kind 2) and the default
+    choice between them by call size (kind 0)."""
     n_cold = E - n_hot
     loc = np.random.default_rng(E).permutation(E).astype(np.int32)
     fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=E + T, loc=loc)
+    fx.layer.set_decode_kind(decode_kind)
     if dist == "uniform":
         logits = synth.gen_logits_uniform(T, E, seed=T)
     else:
