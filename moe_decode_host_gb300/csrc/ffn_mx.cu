@@ -25,9 +25,11 @@
 // 128-row tile:
 //   warp 0       loads the tile's E2M1 rows by TMA, 256 elements of K per stage
 //                (128-byte swizzle; gate and up rows in the gate/up phase, w2 rows
-//                in the down phase), with the rows' scale bytes of the stage;
+//                in the down phase), with the rows' scale bytes of the stage, into
+//                the weight ring;
 //   warp 1       loads the tokens' E2M1 activation rows of each stage by TMA (up to
-//                192 bucket rows, 32 per box), with their scale words;
+//                192 bucket rows with one term per token, 128 with four; 32 per
+//                box), with their scale words, into the shallower activation ring;
 //   warp 2       owns tensor memory; one thread issues the MMAs (four of K = 64 per
 //                matrix and stage); in the gate/up phase it issues the gate matrix's
 //                and a thread of warp 24 the up matrix's, each into its accumulator;
@@ -58,13 +60,10 @@ constexpr int kMxBM = 128;                     // weight rows per tile = tensor-
 constexpr int kMxBK = 256;                     // K elements per stage
 constexpr int kMxRowB = kMxBK / 2;             // bytes of a row per stage
 constexpr int kMxTile = kMxBM * kMxRowB;       // 16 KB: one matrix's rows of a stage
-constexpr int kMxNMax = 192;                   // token columns per pass
 constexpr int kMxBox = 32;                     // activation rows per TMA box
-constexpr int kMxBTile = kMxNMax * kMxRowB;    // 24 KB of activation rows
 // activation scale words of a stage, loaded by TMA from a 4-aligned bucket row (the
 // box's start must be a whole 16 bytes): 2 rows (the stage's two words) x 200
 constexpr int kMxSfbBox = 200;
-constexpr int kMxBStage = kMxBTile + 2048;     // rows, then the 1600 bytes of scale words
 constexpr int kMxWsc = kMxBM * 16;             // a matrix's scale box: 128 rows x 16 bytes
 constexpr int kMxASlot = kMxTile + kMxWsc;     // per matrix: E2M1 rows, then their scales
 constexpr int kMxThreads = 800;
@@ -74,31 +73,54 @@ constexpr int kMxFirstEpi = 8;
 constexpr int kMxEpiWarps = 16;  // four per lane quarter, taking every fourth 16-token chunk
 constexpr int kMxMaxE = 1024;
 constexpr int kMxTaskQ = 4;
-// Tensor memory: accumulators in [0, 384) -- gate and up (192 columns each) in the
-// gate/up phase, two buffers in the down phase -- and the scale slots from 384.
-constexpr uint32_t kMxAccCols = 192;
-constexpr uint32_t kMxSf0 = 384;
 constexpr uint32_t kMxTmemCols = 512;
 constexpr int kMxEpiStage = 16 * 16;      // epilogue staging per warp: 16 tokens x 16 bytes of h
 
 template <int P>
 __host__ __device__ constexpr int mx_mats() { return P == 0 ? 2 : 1; }  // weight matrices per stage
+// MMA issuing threads: the gate/up phase issues each matrix from its own thread
+// (issuing one block-scaled MMA takes a thread about 100 cycles whatever N is).
+template <int P, int TERMS>
+__host__ __device__ constexpr int mx_issuers() { return P == 0 ? 2 : 1; }
 // roles that take each task from the queue: producers, issuers, scale writers, epilogue
-template <int P>
-__host__ __device__ constexpr int mx_takers() { return 2 + mx_mats<P>() + 4 + kMxEpiWarps; }
-// One ring of stage slots: slot i holds a stage's weight rows, activation rows and
-// (in tensor memory) scale words; the MMA issuers release all three at once.
-template <int P>
-__host__ __device__ constexpr int mx_stages() { return P == 0 ? 3 : 4; }
+template <int P, int TERMS>
+__host__ __device__ constexpr int mx_takers() { return 2 + mx_issuers<P, TERMS>() + 4 + kMxEpiWarps; }
+// Activation rows (token columns of the MMA) per pass: 192 with one term per token;
+// 128 (32 tokens) with four, which leaves shared memory to a deeper weight ring
+// (decode-sized calls read far more weight bytes than activation bytes).
+template <int TERMS>
+__host__ __device__ constexpr int mx_nmax() { return TERMS == 1 ? 192 : 128; }
+template <int TERMS>
+__host__ __device__ constexpr int mx_bstage() { return mx_nmax<TERMS>() * kMxRowB + 2048; }  // rows, then scale words
+// Two rings of stage slots, each the K range of one stage: weight slots (a matrix's
+// E2M1 rows and their scale bytes per matrix) and activation slots (rows and scale
+// words, with a scale slot in tensor memory); the MMA issuers release both.  The
+// weight ring is the deeper: its bytes come from DRAM, the activations mostly from L2.
+template <int P, int TERMS>
+__host__ __device__ constexpr int mx_astages() { return TERMS == 1 ? (P == 0 ? 3 : 4) : (P == 0 ? 4 : 8); }
+template <int P, int TERMS>
+__host__ __device__ constexpr int mx_bstages() { return TERMS == 1 ? (P == 0 ? 3 : 4) : 3; }
+constexpr int kMxMaxStages = 8;
+// Tensor memory: accumulators (gate and up in the gate/up phase, two buffers in the
+// down phase) in [0, 2 nmax), then the scale slots.
+template <int TERMS>
+__host__ __device__ constexpr uint32_t mx_acc_cols() { return (uint32_t)mx_nmax<TERMS>(); }
+template <int TERMS>
+__host__ __device__ constexpr uint32_t mx_sf0() { return 2u * mx_acc_cols<TERMS>(); }
 // scale slot: weight words (8 columns per matrix: two words x four quarter columns),
 // then token words (16 columns: word j of the stage at 8j + token group)
 template <int P>
 __host__ __device__ constexpr uint32_t mx_sfb_col() { return P == 0 ? 16u : 8u; }
 template <int P>
 __host__ __device__ constexpr uint32_t mx_sf_cols() { return mx_sfb_col<P>() + 16u; }
-static_assert(kMxSf0 + mx_stages<0>() * mx_sf_cols<0>() <= kMxTmemCols &&
-                  kMxSf0 + mx_stages<1>() * mx_sf_cols<1>() <= kMxTmemCols,
-              "tensor memory budget");
+template <int P, int TERMS>
+__host__ __device__ constexpr bool mx_budget_ok() {
+    return mx_sf0<TERMS>() + mx_bstages<P, TERMS>() * mx_sf_cols<P>() <= kMxTmemCols &&
+           mx_astages<P, TERMS>() <= kMxMaxStages && mx_bstages<P, TERMS>() <= kMxMaxStages &&
+           mx_nmax<TERMS>() + 8 <= kMxSfbBox;
+}
+static_assert(mx_budget_ok<0, 1>() && mx_budget_ok<1, 1>() && mx_budget_ok<0, 4>() && mx_budget_ok<1, 4>(),
+              "tensor memory and ring budget");
 
 struct MxTask {
     const uint8_t* blob;
@@ -107,8 +129,9 @@ struct MxTask {
 };
 
 struct alignas(16) MxHead {
-    uint64_t a_full[4], b_full[4], sf_full[4];
-    uint64_t st_empty[4];  // the slot's MMAs have completed (one commit per issuer)
+    uint64_t a_full[kMxMaxStages], a_empty[kMxMaxStages];  // weight ring
+    uint64_t b_full[kMxMaxStages], b_empty[kMxMaxStages];  // activation ring (and scale slots)
+    uint64_t sf_full[kMxMaxStages];  // scale slot written; empties: one commit per issuer
     uint64_t acc_full[2], acc_empty[2];
     uint64_t tq_full[kMxTaskQ], tq_empty[kMxTaskQ];
     int tq[kMxTaskQ];
@@ -119,14 +142,16 @@ struct alignas(16) MxHead {
     int list[kMxMaxE];  // active experts, most tokens first
 };
 
-template <int P>
+template <int P, int TERMS>
 struct MxSmem {
-    static constexpr size_t kB = (size_t)mx_stages<P>() * mx_mats<P>() * kMxASlot;  // after the weight ring
-    static constexpr size_t kStg = kB + (size_t)mx_stages<P>() * kMxBStage;
+    static constexpr size_t kB = (size_t)mx_astages<P, TERMS>() * mx_mats<P>() * kMxASlot;  // after the weight ring
+    static constexpr size_t kStg = kB + (size_t)mx_bstages<P, TERMS>() * mx_bstage<TERMS>();
     static constexpr size_t kHead = kStg + kMxEpiWarps * kMxEpiStage;
     static constexpr size_t kTotal = 1024 + kHead + sizeof(MxHead);
 };
-static_assert(MxSmem<0>::kTotal <= 232448 && MxSmem<1>::kTotal <= 232448, "shared memory budget of one CTA");
+static_assert(MxSmem<0, 1>::kTotal <= 232448 && MxSmem<1, 1>::kTotal <= 232448 && MxSmem<0, 4>::kTotal <= 232448 &&
+                  MxSmem<1, 4>::kTotal <= 232448,
+              "shared memory budget of one CTA");
 
 // kind::mxf4 instruction descriptor: A and B E2M1 (format 1), both K-major, UE8M0
 // scales, M = 128, N tokens, scale-factor byte selector sf for both operands.
@@ -159,12 +184,6 @@ __device__ __forceinline__ void mx_st16(uint32_t taddr, const uint32_t (&v)[16])
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
         "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_word(const uint32_t* p) {
-    uint32_t v;
-    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
 }
 
 __device__ __forceinline__ MxTask mx_task(const FfnArgs& a, const MxHead& hd, int task, int tiles) {
@@ -217,8 +236,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = base;
-    uint8_t* sB = base + MxSmem<P>::kB;
-    MxHead& hd = *reinterpret_cast<MxHead*>(base + MxSmem<P>::kHead);
+    uint8_t* sB = base + MxSmem<P, TERMS>::kB;
+    MxHead& hd = *reinterpret_cast<MxHead*>(base + MxSmem<P, TERMS>::kHead);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = a.H, I = a.I;
     const int K = P == 0 ? H : I;
@@ -226,12 +245,15 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
     const int tiles = (P == 0 ? I : H) / kMxBM;
     const int R = a.T * a.k * TERMS;  // activation rows: TERMS per bucket row
     const int Rs = (R + 3) & ~3;      // row stride of the activation scale words
-    constexpr int TPP = kMxNMax / TERMS;  // tokens per column pass
+    constexpr int TPP = mx_nmax<TERMS>() / TERMS;  // tokens per column pass
+    constexpr uint32_t ACC = mx_acc_cols<TERMS>(), SF0 = mx_sf0<TERMS>();
+    constexpr int BSTAGE = mx_bstage<TERMS>(), BTILE = mx_nmax<TERMS>() * kMxRowB;
     // the weight scales arrive by TMA with their stage where the plane's rows are whole
     // 16-byte units, else the scale writers read them from global memory
     const bool wsc_tma = mx_scale_maps(K);
-    constexpr int NS = mx_stages<P>();
+    constexpr int NA = mx_astages<P, TERMS>(), NB = mx_bstages<P, TERMS>();
     constexpr int MATS = mx_mats<P>();
+    constexpr int ISS = mx_issuers<P, TERMS>();
     volatile int* abort = &hd.abort;
     // tokens of each active expert (-1: inactive), in the weight ring until the
     // producers start
@@ -271,19 +293,22 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
             hd.D = cnt;
             hd.abort = 0;
             // every consumed slot is released by each issuer's commit (one per matrix)
-            for (int s = 0; s < NS; ++s) {
+            for (int s = 0; s < NA; ++s) {
                 mbar_init(&hd.a_full[s], 1);
+                mbar_init(&hd.a_empty[s], ISS);
+            }
+            for (int s = 0; s < NB; ++s) {
                 mbar_init(&hd.b_full[s], 1);
+                mbar_init(&hd.b_empty[s], ISS);
                 mbar_init(&hd.sf_full[s], 4);
-                mbar_init(&hd.st_empty[s], MATS);
             }
             for (int s = 0; s < 2; ++s) {
-                mbar_init(&hd.acc_full[s], MATS);
+                mbar_init(&hd.acc_full[s], ISS);
                 mbar_init(&hd.acc_empty[s], kMxEpiWarps);
             }
             for (int j = 0; j < kMxTaskQ; ++j) {
                 mbar_init(&hd.tq_full[j], 1);
-                mbar_init(&hd.tq_empty[j], mx_takers<P>());
+                mbar_init(&hd.tq_empty[j], mx_takers<P, TERMS>());
             }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
@@ -348,7 +373,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 const int r0 = t.rb * kMxBM;
                 for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.st_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
+                        if (!mbar_wait_fast(&hd.a_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
                             ok = false;
                             break;
                         }
@@ -367,11 +392,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                                     tma_load_2d_hint(dst + kMxTile + i * 32 * 16, smap, 16 * (s >> 1),
                                                      (mt ? I : 0) + r0 + 32 * i, &hd.a_full[as], pol);
                         }
-                        advance(as, aph, NS);
+                        advance(as, aph, NA);
                     }
                 }
             }
-            for (int s = 0; s < NS; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
+            for (int s = 0; s < NA; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -390,39 +415,40 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     const int row0 = TERMS * (t.off + tb);  // first activation row of the pass
                     const int boxes = (mx_ncols(TERMS * min(TPP, t.cnt - tb)) + kMxBox - 1) / kMxBox;
                     for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.st_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
+                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB + 2 * kMxSfbBox * 4));
-                        uint8_t* dst = sB + (size_t)bs * kMxBStage;
+                        uint8_t* dst = sB + (size_t)bs * BSTAGE;
                         for (int bx = 0; bx < boxes; ++bx)
                             tma_load_2d_hint(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB, row0 + kMxBox * bx,
                                              &hd.b_full[bs], pol);
                         // the stage's two scale words of the pass's tokens, from the 4-aligned
                         // bucket row at or below the first (x is a whole 16 bytes)
-                        tma_load_2d_hint(dst + kMxBTile, &sfb_map, row0 & ~3, 2 * s, &hd.b_full[bs], pol);
-                        advance(bs, bph, NS);
+                        tma_load_2d_hint(dst + BTILE, &sfb_map, row0 & ~3, 2 * s, &hd.b_full[bs], pol);
+                        advance(bs, bph, NB);
                     }
                 }
             }
-            for (int s = 0; s < NS; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
+            for (int s = 0; s < NB; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
-    } else if (warp == 2 || (P == 0 && warp == kMxUpIssuer)) {
+    } else if (warp == 2 || (ISS == 2 && warp == kMxUpIssuer)) {
         // ---------------- MMA issuers (lane 0) ----------------
-        // a thread needs about 100 ns to issue one block-scaled MMA, so the gate/up
+        // a thread takes about 100 cycles to issue one block-scaled MMA, so the gate/up
         // phase issues from two threads, warp 2 the gate matrix's MMAs into the gate
         // accumulator and warp 24 the up matrix's into the up accumulator; the down
         // phase has one matrix and one issuer
-        const int mt = warp == 2 ? 0 : 1;
+        const int mt0 = warp == 2 ? 0 : 1;
+        const int mt1 = ISS == 2 ? mt0 + 1 : MATS;  // matrices [mt0, mt1) of each stage
         if (lane == 0) {
-            int ss = 0, buf = 0;
-            unsigned sph = 0, accph = 0;
+            int as = 0, bs = 0, buf = 0;
+            unsigned aph = 0, bph = 0, accph = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 MxTask t;
-                const int task = mx_take(hd, k, a, abort, 2 + mt, t);
+                const int task = mx_take(hd, k, a, abort, 2 + mt0, t);
                 if (task < 0) break;
                 if (!t.valid) continue;
                 for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
@@ -437,17 +463,17 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     tc_fence_after();
                     for (int s = 0; s < nks; ++s) {
                         // the scale writers arrive only after both of the stage's loads landed
-                        if (!mbar_wait_fast(&hd.sf_full[ss], sph, abort, a.status, a.diag, 37, ss, s, task)) {
+                        if (!mbar_wait_fast(&hd.sf_full[bs], bph, abort, a.status, a.diag, 37, bs, s, task)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const int nkk = min(4, (K - s * kMxBK) / 64);  // K steps of 64 in this stage
-                        const uint32_t sf = tmem + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
-                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)ss * kMxBStage));  // its rows
-                        {
-                            const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * kMxAccCols;
-                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(ss * MATS + mt) * kMxASlot));
+                        const uint32_t sf = tmem + SF0 + (uint32_t)bs * mx_sf_cols<P>();
+                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * BSTAGE));  // its rows
+                        for (int mt = mt0; mt < mt1; ++mt) {
+                            const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * ACC;
+                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxASlot));
                             for (int kk = 0; kk < nkk; ++kk) {
                                 // a K step of 64 elements advances both start addresses by 32 bytes;
                                 // its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2
@@ -457,17 +483,20 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                                        sf + mx_sfb_col<P>() + 8u * (uint32_t)(kk >> 1), acc);
                             }
                         }
-                        tc_commit(&hd.st_empty[ss]);
-                        advance(ss, sph, NS);
+                        tc_commit(&hd.a_empty[as]);
+                        tc_commit(&hd.b_empty[bs]);
+                        advance(as, aph, NA);
+                        advance(bs, bph, NB);
                     }
                     if (!ok) break;
                     tc_commit(&hd.acc_full[buf]);
-                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 384)
+                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 2 ACC)
                 }
             }
             // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
             // last commit of every slot
-            for (int s = 0; s < NS; ++s) mbar_drain(&hd.st_empty[s], (s < ss) ? sph : (sph ^ 1u));
+            for (int s = 0; s < NA; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
+            for (int s = 0; s < NB; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
         }
         __syncwarp();
     } else if (warp >= kMxFirstSf && warp < kMxFirstSf + 4) {
@@ -479,8 +508,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         const int q = warp & 3;
         const int rr = 32 * q + lane;
         const uint32_t qaddr = tmem + ((uint32_t)(q * 32) << 16);
-        int ss = 0;
-        unsigned sph = 0;
+        int as = 0, bs = 0;
+        unsigned aph = 0, bph = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
             MxTask t;
@@ -505,27 +534,28 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     }
                     // both loads of the stage landed: the producers reused the slot only after
                     // its previous MMAs completed, so its scale slot is free as well
-                    if (!warp_wait(&hd.a_full[ss], sph, a, abort, 40, ss, s, task) ||
-                        !warp_wait(&hd.b_full[ss], sph, a, abort, 41, ss, s, task)) {
+                    if (!warp_wait(&hd.a_full[as], aph, a, abort, 40, as, s, task) ||
+                        !warp_wait(&hd.b_full[bs], bph, a, abort, 41, bs, s, task)) {
                         ok = false;
                         break;
                     }
                     if (wsc_tma) {
 #pragma unroll
                         for (int mt = 0; mt < MATS; ++mt) {
-                            const uint8_t* row = sA + (size_t)(ss * MATS + mt) * kMxASlot + kMxTile + rr * 16 + 8 * (s & 1);
+                            const uint8_t* row = sA + (size_t)(as * MATS + mt) * kMxASlot + kMxTile + rr * 16 + 8 * (s & 1);
                             wa[mt][0] = *reinterpret_cast<const uint32_t*>(row);
                             wa[mt][1] = nj > 1 ? *reinterpret_cast<const uint32_t*>(row + 4) : 0u;
                         }
                     }
-                    const uint32_t* wsb = reinterpret_cast<const uint32_t*>(sB + (size_t)ss * kMxBStage + kMxBTile);
-                    uint32_t wb[2][6];
+                    const uint32_t* wsb = reinterpret_cast<const uint32_t*>(sB + (size_t)bs * BSTAGE + BTILE);
+                    constexpr int NG = mx_nmax<TERMS>() / 32;  // token groups of a pass
+                    uint32_t wb[2][NG];
 #pragma unroll
                     for (int j = 0; j < 2; ++j)
 #pragma unroll
-                        for (int c = 0; c < 6; ++c) wb[j][c] = j < nj ? wsb[j * kMxSfbBox + d0 + 32 * c + lane] : 0u;
+                        for (int c = 0; c < NG; ++c) wb[j][c] = j < nj ? wsb[j * kMxSfbBox + d0 + 32 * c + lane] : 0u;
                     tc_fence_after();
-                    const uint32_t col = qaddr + kMxSf0 + (uint32_t)ss * mx_sf_cols<P>();
+                    const uint32_t col = qaddr + SF0 + (uint32_t)bs * mx_sf_cols<P>();
                     // weight words: matrix mt, word j at column 8 mt + 4 j + q (this lane = row 32 q + lane)
                     uint32_t va[16];
 #pragma unroll
@@ -544,13 +574,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                     // token words: word j of token group c at column 8 j + c
                     uint32_t vb[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) vb[i] = (i & 7) < 6 ? wb[i >> 3][i & 7] : 0u;
+                    for (int i = 0; i < 16; ++i) vb[i] = (i & 7) < NG ? wb[i >> 3][(i & 7) % NG] : 0u;
                     mx_st16(col + mx_sfb_col<P>(), vb);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&hd.sf_full[ss]);
-                    advance(ss, sph, NS);
+                    if (lane == 0) mbar_arrive(&hd.sf_full[bs]);
+                    advance(as, aph, NA);
+                    advance(bs, bph, NB);
                 }
             }
         }
@@ -559,7 +590,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         const int q = warp & 3;  // tensor-memory lane quarter: weight rows 32 q ..
         const int half = (warp - kMxFirstEpi) >> 2;  // this warp's 16-token chunks: 4 i + half
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        uint8_t* stg = base + MxSmem<P>::kStg + (size_t)(warp - kMxFirstEpi) * kMxEpiStage;
+        uint8_t* stg = base + MxSmem<P, TERMS>::kStg + (size_t)(warp - kMxFirstEpi) * kMxEpiStage;
         int buf = 0;
         unsigned accph = 0;
         bool ok = true;
@@ -586,12 +617,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 }
                 accph ^= 1u << buf;
                 tc_fence_after();
-                const uint32_t d = lane_addr + (uint32_t)buf * kMxAccCols;
+                const uint32_t d = lane_addr + (uint32_t)buf * ACC;
                 for (int cb = 16 * half; cb < ncol; cb += 64) {
                     constexpr int TOK = 16 / TERMS;  // tokens of a 16-column chunk
                     if constexpr (P == 0) {
                         float g[16], u[16];
-                        tc_ld16x2(d + cb, d + kMxAccCols + cb, g, u);
+                        tc_ld16x2(d + cb, d + ACC + cb, g, u);
                         int es[16];
 #pragma unroll
                         for (int n = 0; n < TOK; ++n) {
@@ -746,7 +777,7 @@ template <int P, int TERMS>
 cudaError_t launch_mx(const FfnArgs& a, const CUtensorMap& map, const CUtensorMap& smap, int sel, int lo, int hi,
                       int grid, cudaStream_t st) {
     static std::atomic<uint64_t> configured{0};
-    const size_t smem = MxSmem<P>::kTotal;
+    const size_t smem = MxSmem<P, TERMS>::kTotal;
     cudaError_t err = ensure_smem_limit((const void*)ffn_mx_kernel<P, TERMS>, (int)smem, configured);
     if (err != cudaSuccess) return err;
     // task counters 12-15 of the call's workspace (zeroed by the prep kernel): one per
