@@ -169,6 +169,9 @@ def parse():
     ap.add_argument("--hysteresis", type=float, default=3.0, help="residency threshold ratio")
     ap.add_argument("--swap-every", type=int, default=16, help="residency update interval in steps")
     ap.add_argument("--max-swaps", type=int, default=8, help="swaps per residency update")
+    ap.add_argument("--residency-sync", action="store_true",
+                    help="synchronous residency (plan and move at the closing call, draining the stream) "
+                         "instead of the default deferred mode")
     ap.add_argument("--n-hot", type=int, default=None, help="HBM-resident experts per layer (rest cold)")
     ap.add_argument("--prefill", default=None, choices=["f16", "fp4"],
                     help="arithmetic of calls above 64 tokens: exact-weight f16 tensor cores, or block-scaled "
@@ -216,6 +219,7 @@ def workload(args, config=None, batch=None):
         c["n_hot"] = min(args.n_hot, c["E"])
         c["n_cold"] = c["E"] - c["n_hot"]
     c["hysteresis"], c["swap_every_steps"], c["max_swaps"] = args.hysteresis, args.swap_every, args.max_swaps
+    c["residency_sync"] = bool(args.residency_sync)
     return c
 
 
@@ -454,7 +458,9 @@ def _config_json(c, args, pool_steps=None):
                         + (f", {c['layers']} layers sharing one slot scratch" if c.get("layers", 1) > 1 else ""),
             "tokens_per_step": c["T"], "layers": c.get("layers", 1),
             "residency": "off" if c["no_res"] else (
-                "every %d steps, hysteresis %g, <=%d swaps, " % (c["swap_every_steps"], c["hysteresis"], c["max_swaps"]) + (
+                "every %d steps, hysteresis %g, <=%d swaps, %s, " % (
+                    c["swap_every_steps"], c["hysteresis"], c["max_swaps"],
+                    "synchronous" if c.get("residency_sync") else "deferred one step (no stream sync)") + (
                 "host copy of every expert" if c.get("mirror") else "in-place HBM/host exchange")),
             "step_pool": pool_steps if pool_steps is not None else args.pool,
             "l2": "inputs larger than L2 (7.7 GB expert pool per layer), no flush",
@@ -509,6 +515,7 @@ def build_layers(c, dev, seed_tag="bench"):
                         host_mirror=mirror, zero_copy=bool(c.get("zero_copy")))
         layer.set_prefill_kind(1 if c.get("prefill") == "fp4" else 0)
         layer.set_decode_kind(c.get("decode_kind", 0))
+        layer.set_residency_defer(not c.get("residency_sync", False))
         layers.append(dict(layer=layer, hot=hot, cold=cold, perm=perm))
     return layers, scratch, slots
 
@@ -705,6 +712,10 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
         launches += n
         if i + 1 in marks:
             marks[i + 1].record(st)
+    # the timed work includes each layer's last residency move (deferred moves run on
+    # the layers' copy streams)
+    for L in layers:
+        m.moe_gather_join(L["layer"], st)
     t_end.record(st)
     torch.cuda.synchronize()
     clk = clocks.stop()

@@ -17,9 +17,11 @@
  *    errors, a null handle or pointer gives MOE_ERR_INVALID_ARG and a failed CUDA
  *    call MOE_ERR_CUDA.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *    All device work is enqueued on it; nothing synchronises except
- *    residency_update on an acting step (it reads the pick counters on the host),
- *    moe_get_status, moe_layer_get_loc and moe_layer_get_counts.
+ *    All device work is enqueued on it; nothing synchronises the stream except
+ *    residency_update on an acting step in the synchronous residency mode (it
+ *    reads the pick counters on the host), moe_get_status, moe_layer_get_loc and
+ *    moe_layer_get_counts.  In the default deferred mode residency_update waits
+ *    (host side) only for the previous acting call's counter copy.
  *  - Errors found by a kernel after launch (non-finite logits, an expert id out of
  *    range) are written to the layer's device status word (first error wins);
  *    moe_get_status reads it.
@@ -181,8 +183,10 @@ int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float
 int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids, int32_t* cold_list,
                 int32_t* n_cold_picked, void* stream);
 
-/* Makes `stream` wait for the layer's cold copy in flight (no-op when none).
- * Needed only to read the scratch slots without calling moe_grouped_ffn. */
+/* Makes `stream` wait for the layer's work in flight on its copy stream: the cold
+ * copy, and a deferred residency move with its map upload (no-op when none).
+ * Needed only to read the scratch slots, the expert bytes or the placement
+ * without calling cold_gather or moe_grouped_ffn. */
 int moe_gather_join(moe_layer* L, void* stream);
 
 /* Device workspace bytes moe_grouped_ffn needs for T tokens. */
@@ -273,19 +277,44 @@ int moe_combine(const float* y, const float* topk_w, int T, int k, int H, void* 
 
 /* Adaptive residency ("DeepSeek-V4.1-Flash on One GB300 ...", section 1: between
  * steps a manager swaps often-picked experts into the hot set and quiet ones out;
- * section 3: hysteresis 3.0 as the published default).  Call once per step.  On
- * every swap_every-th call it synchronises `stream`, reads the window counters,
- * pairs cold experts picked at least once (count desc, id asc) with hot experts
- * (count asc, id asc), swaps pair i while count(cold) > hysteresis * count(hot)
- * (at most max_swaps, stopping at the first pair that fails), moves the bytes
- * (host_mirror 0: exchanges the two experts' bytes in place between the HBM slot
- * and the host blob; host_mirror 1: copies the promoted expert into the HBM slot,
- * see moe_params), rewrites the placement map and clears the counters.  Other
- * calls only count the step.  Layers sharing a scratch must make this call before
- * a later layer's cold_gather on the same stream order (it may read a slot).
- *  n_swaps_out host int32 [1] out (0 on non-acting calls).
- * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_INJECTED (test hook). */
+ * section 3: hysteresis 3.0 as the published default).  Call once per step, after
+ * the layer's moe_grouped_ffn (and moe_combine) on the same stream.  Every
+ * swap_every-th call closes a window of pick counts; the plan pairs cold experts
+ * picked at least once (count desc, id asc) with hot experts (count asc, id asc)
+ * and swaps pair i while count(cold) > hysteresis * count(hot) (at most
+ * max_swaps, stopping at the first pair that fails); applying a pair moves the
+ * bytes (host_mirror 0: exchanges the two experts' bytes in place between the
+ * HBM slot and the host blob; host_mirror 1: copies the promoted expert into the
+ * HBM slot, see moe_params) and rewrites the placement map.  Each expert is in at
+ * most one pair, so any prefix of a plan is a valid placement.
+ *  Deferred mode (default, moe_layer_set_residency_defer 1): the closing call
+ *  enqueues a copy of the window's counters to the host and starts the next
+ *  window in a second counter buffer, without synchronising; the layer's next
+ *  call (one step later) makes the plan from those counts and the current
+ *  placement.  The plan's n pairs land in plan order, paced over the calls
+ *  before the next window closes: pair i at the plan's call floor(i * span / n)
+ *  (call 0 being the one that made it, span = max(1, swap_every - 1)); pairs
+ *  still unapplied when the next plan is made land first.  Each landing moves
+ *  its bytes on the layer's copy stream, after the work already on `stream`,
+ *  while later layers run; the layer's next cold_gather or moe_grouped_ffn waits
+ *  for the move.  The promoted expert is read from its host blob (host copy),
+ *  never from the shared scratch.  The counts and plans are those of the
+ *  synchronous mode; only the times at which the pairs land differ.
+ *  Synchronous mode (0): the closing call synchronises `stream`, reads the
+ *  counters, and moves the bytes on `stream` at once; with host copies it
+ *  promotes from the scratch slot while that slot still holds this layer's copy.
+ *  Layers sharing a scratch must make this call before a later layer's
+ *  cold_gather on the same stream order (it may read a slot).
+ *  n_swaps_out host int32 [1] out: the swaps applied by this call (deferred: by
+ *  the plan of the previous closing call).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, MOE_ERR_INJECTED (test hook: on a
+ * closing call, before anything is enqueued or applied). */
 int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream);
+
+/* Selects the residency mode of residency_update: 1 deferred (default), 0
+ * synchronous.  A plan already pending is applied at the next call either way.
+ * Errors: MOE_ERR_INVALID_ARG (null, defer not 0 or 1). */
+int moe_layer_set_residency_defer(moe_layer* L, int defer);
 
 /* The plan one acting residency_update applies, computed on the host with no
  * device work (callable without a GPU): the same ranking, pairing and stopping

@@ -121,6 +121,11 @@ class Layer:
         for 1 or 2 tokens, kind 2 from 3 up."""
         check(lib.moe_layer_set_decode_kind(self.handle, kind), "moe_layer_set_decode_kind")
 
+    def set_residency_defer(self, defer: bool):
+        """True (default): residency plans are made and applied one step after their
+        window closes, with no stream synchronisation; False: at once, synchronously."""
+        check(lib.moe_layer_set_residency_defer(self.handle, 1 if defer else 0), "moe_layer_set_residency_defer")
+
     def set_copy_ctas(self, ctas: int):
         check(lib.moe_layer_set_copy_ctas(self.handle, ctas), "moe_layer_set_copy_ctas")
 

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_layer_set_prefill_kind": (_I, [_P, _I]),
     "moe_mxf4_peak_probe": (_I, [_I, _I, _P, _P]),
     "moe_layer_set_decode_kind": (_I, [_P, _I]),
+    "moe_layer_set_residency_defer": (_I, [_P, _I]),
     "moe_residency_plan": (_I, [_P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P]),
     "moe_quant_mxfp4": (_I, [_P, _I, _I, _P, _P, _P]),
     "moe_layer_get_loc": (_I, [_P, _P]),

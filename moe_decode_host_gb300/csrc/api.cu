@@ -41,14 +41,26 @@ struct moe_layer {
     const uint8_t** d_ptr = nullptr;  // [n_hot + n_cold] phys id -> blob base
     const uint8_t** d_cold_src = nullptr;  // [n_cold] host blobs (device-mapped)
     int32_t* d_window = nullptr;      // [E] picks in the current window
+    int32_t* d_window_alt = nullptr;  // [E] the other window buffer (deferred residency snapshots)
     int* d_status = nullptr;
     int* d_diag = nullptr;            // [16] record of the first device-side wait that timed out
     int32_t* h_counts = nullptr;      // pinned [E]
     int32_t* h_loc = nullptr;         // pinned [E]
+    const uint8_t** h_cold_src = nullptr;  // pinned [n_cold] staging of d_cold_src updates
     ExpertMaps* d_tmaps = nullptr;      // [E] TMA descriptors per physical id
     cudaStream_t copy_stream = nullptr;  // cold slot copies run here, joined by moe_grouped_ffn
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     bool copy_pending = false;
+    // residency (moe_layer_set_residency_defer): ev_counts follows the D2H copy of a
+    // window snapshot; ev_swap follows the last exchange and map upload
+    cudaEvent_t ev_counts = nullptr, ev_swap = nullptr;
+    int residency_defer = 1;
+    bool plan_pending = false;   // a snapshot in h_counts awaits its plan
+    std::vector<int32_t> plan_pro, plan_dem;  // the current plan's pairs (deferred: paced)
+    int plan_next = 0;  // pairs [0, plan_next) have been applied
+    int plan_age = 0;   // calls since the current plan was made
+    bool swap_recorded = false;  // ev_swap has been recorded (the staging buffers may be in use)
+    bool swap_pending = false;   // the caller's stream has not yet waited for ev_swap
     int copy_ctas = 0;
     std::vector<cudaEvent_t> prof_ev;  // pairs of events around recorded cold copies
     int prof_n = 0;
@@ -154,6 +166,20 @@ cudaError_t join_copy(moe_layer* L, cudaStream_t st) {
     return cudaStreamWaitEvent(st, L->ev_join, 0);
 }
 
+// Makes `st` wait for a residency exchange (and its map upload) that ran on the
+// layer's copy stream, if the caller's stream has not waited for it yet.
+cudaError_t join_swap(moe_layer* L, cudaStream_t st) {
+    if (!L->swap_pending) return cudaSuccess;
+    L->swap_pending = false;
+    return cudaStreamWaitEvent(st, L->ev_swap, 0);
+}
+
+// Blocks the host until the copies that read the pinned staging buffers (h_loc,
+// h_cold_src) of the last exchange have completed, before they are rewritten.
+cudaError_t settle_staging(moe_layer* L) {
+    return L->swap_recorded ? cudaEventSynchronize(L->ev_swap) : cudaSuccess;
+}
+
 void free_prof(moe_layer* L) {
     for (cudaEvent_t e : L->prof_ev) cudaEventDestroy(e);
     L->prof_ev.clear();
@@ -172,15 +198,19 @@ void free_layer(moe_layer* L) {
     if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
     if (L->ev_fork) cudaEventDestroy(L->ev_fork);
     if (L->ev_join) cudaEventDestroy(L->ev_join);
+    if (L->ev_counts) cudaEventDestroy(L->ev_counts);
+    if (L->ev_swap) cudaEventDestroy(L->ev_swap);
     cudaFree(L->d_tmaps);
     cudaFree(L->d_loc);
     cudaFree(L->d_ptr);
     cudaFree(L->d_cold_src);
     cudaFree(L->d_window);
+    cudaFree(L->d_window_alt);
     cudaFree(L->d_status);
     cudaFree(L->d_diag);
     cudaFreeHost(L->h_counts);
     cudaFreeHost(L->h_loc);
+    cudaFreeHost(L->h_cold_src);
     delete L;
 }
 
@@ -299,21 +329,27 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     err = err ? err : cudaMalloc(&L->d_ptr, sizeof(uint8_t*) * p.E);
     err = err ? err : cudaMalloc(&L->d_cold_src, sizeof(uint8_t*) * (p.n_cold > 0 ? p.n_cold : 1));
     err = err ? err : cudaMalloc(&L->d_window, sizeof(int32_t) * p.E);
+    err = err ? err : cudaMalloc(&L->d_window_alt, sizeof(int32_t) * p.E);
     err = err ? err : cudaMalloc(&L->d_status, sizeof(int));
     err = err ? err : cudaMalloc(&L->d_diag, sizeof(int) * 16);
     err = err ? err : cudaMemset(L->d_diag, 0, sizeof(int) * 16);
     err = err ? err : cudaHostAlloc(&L->h_counts, sizeof(int32_t) * p.E, cudaHostAllocDefault);
     err = err ? err : cudaHostAlloc(&L->h_loc, sizeof(int32_t) * p.E, cudaHostAllocDefault);
+    err = err ? err
+              : cudaHostAlloc(&L->h_cold_src, sizeof(uint8_t*) * (p.n_cold > 0 ? p.n_cold : 1), cudaHostAllocDefault);
     err = err ? err : cudaMemcpy(L->d_loc, init_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice);
     err = err ? err : cudaMemcpy(L->d_ptr, ptr.data(), sizeof(uint8_t*) * p.E, cudaMemcpyHostToDevice);
     if (p.n_cold > 0)
         err = err ? err
                   : cudaMemcpy(L->d_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold, cudaMemcpyHostToDevice);
     err = err ? err : cudaMemset(L->d_window, 0, sizeof(int32_t) * p.E);
+    err = err ? err : cudaMemset(L->d_window_alt, 0, sizeof(int32_t) * p.E);
     err = err ? err : cudaMemset(L->d_status, 0, sizeof(int));
     err = err ? err : cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
+    err = err ? err : cudaEventCreateWithFlags(&L->ev_counts, cudaEventDisableTiming);
+    err = err ? err : cudaEventCreateWithFlags(&L->ev_swap, cudaEventDisableTiming);
     if (err == cudaSuccess) {
         std::vector<ExpertMaps> maps(p.E);
         memset(maps.data(), 0, sizeof(ExpertMaps) * maps.size());
@@ -367,7 +403,8 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
     if (T > 0 && (!topk_ids || !phys_ids)) return MOE_ERR_INVALID_ARG;
     if (L->p.n_cold > 0 && T > 0 && !cold_list) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
-    cudaError_t err = cudaSuccess;
+    // the remap reads the placement map, which a deferred residency exchange updates
+    cudaError_t err = join_swap(L, st);
     // zero copy (decode-sized calls): the FFN reads the cold experts in place, no copy
     const bool zc = L->p.zero_copy && T <= kTcMinTokens;
     if (L->p.n_cold > 0 && T > 0 && !zc) {
@@ -397,7 +434,9 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
 
 int moe_gather_join(moe_layer* L, void* stream) {
     if (!L) return MOE_ERR_INVALID_ARG;
-    return cuda_status(join_copy(L, S(stream)));
+    cudaError_t err = join_copy(L, S(stream));
+    if (err == cudaSuccess) err = join_swap(L, S(stream));
+    return cuda_status(err);
 }
 
 namespace {
@@ -451,6 +490,7 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     if (!x || !phys_ids || !counts || !offsets || !entries || !y || !workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(workspace, 256) || !aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
     if (workspace_bytes < ffn_workspace(L, T)) return MOE_ERR_INVALID_ARG;
+    if (join_swap(L, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
     FfnArgs a;
     memset(&a, 0, sizeof a);
     a.ptr = L->d_ptr;
@@ -607,18 +647,158 @@ int moe_residency_plan(const int32_t* counts, const int32_t* loc, int E, int n_h
     return plan_residency(counts, loc, E, n_hot, max_swaps, hysteresis, loc_out, promoted, demoted);
 }
 
+namespace {
+// The plan of the window counts in h_counts from the current placement, kept in
+// plan_pro / plan_dem (pair i: promoted, demoted); returns the number of pairs.
+int make_plan(moe_layer* L) {
+    const moe_params& p = L->p;
+    int32_t promoted[kMaxSwaps], demoted[kMaxSwaps];
+    std::vector<int32_t> loc(p.E);
+    const int n = plan_residency(L->h_counts, L->loc.data(), p.E, p.n_hot, p.max_swaps, p.hysteresis, loc.data(),
+                                 promoted, demoted);
+    L->plan_pro.assign(promoted, promoted + (n > 0 ? n : 0));
+    L->plan_dem.assign(demoted, demoted + (n > 0 ? n : 0));
+    L->plan_next = 0;
+    L->plan_age = 0;
+    return n > 0 ? n : 0;
+}
+
+// Applies pairs [i0, i1) of the current plan: the byte moves (in-place exchange, or
+// with host copies a copy of the promoted expert into the HBM slot), the cold-source
+// table and the placement map.  Every expert is in at most one pair, so the pairs
+// commute and any prefix of the plan is a valid placement.  Deferred: on the layer's
+// copy stream, forked from `st` (after this layer's FFN, which read the slots) and
+// recorded in ev_swap, which the layer's next cold_gather or moe_grouped_ffn waits
+// for; the promoted expert is read from its host blob, never from the shared
+// scratch (a later layer's copy may overwrite its slot meanwhile).  Otherwise on
+// `st`, with h_tag read and the scratch slot used while it holds this layer's copy.
+int apply_pairs(moe_layer* L, cudaStream_t st, bool deferred, int i0, int i1) {
+    const moe_params& p = L->p;
+    if (i1 <= i0) return MOE_OK;
+    // the pinned staging buffers are rewritten below
+    if (settle_staging(L) != cudaSuccess) return MOE_ERR_CUDA;
+    std::vector<int32_t> loc = L->loc;
+    SwapList sw;
+    sw.n = 0;
+    std::vector<int> moved_slots;  // host_mirror: cold slots whose expert changes
+    for (int i = i0; i < i1; ++i) {
+        const int a = L->plan_pro[i], b = L->plan_dem[i];
+        const int slot_h = loc[b];            // HBM slot of the demoted expert
+        const int slot_c = loc[a] - p.n_hot;  // cold slot of the promoted expert
+        sw.hot[sw.n] = L->hot[slot_h];
+        if (p.host_mirror) {
+            // promote from the scratch slot if this layer's copy of the expert is still
+            // there (synchronous mode only), else from the expert's host copy; the
+            // demoted expert's bytes are already in its host copy
+            const bool in_scratch = !deferred && L->scratch->h_tag[slot_c] == L->uid;
+            sw.host[sw.n] = in_scratch ? L->scratch->base + (size_t)slot_c * L->lay.total : L->mirror_dev[a];
+            moved_slots.push_back(slot_c);
+        } else {
+            sw.host[sw.n] = L->cold_dev[slot_c];
+        }
+        ++sw.n;
+        loc[a] = slot_h;
+        loc[b] = p.n_hot + slot_c;
+    }
+    cudaStream_t xs = deferred ? L->copy_stream : st;
+    cudaError_t err = cudaSuccess;
+    if (deferred) {
+        err = cudaEventRecord(L->ev_fork, st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(xs, L->ev_fork, 0);
+    }
+    // deferred moves run in the background of later layers' steps, beside their cold
+    // copies on the same host link: a quarter of a cold copy's CTAs (about a quarter
+    // of its link rate) still finishes a move long before this layer's next step and
+    // leaves the critical-path copies most of the link
+    const int ctas = deferred ? (L->copy_ctas / 4 > 0 ? L->copy_ctas / 4 : 1) : 2 * L->sm_count;
+    if (err == cudaSuccess)
+        err = p.host_mirror ? launch_copy_list(sw, L->lay.total, ctas, xs) : launch_swap(sw, L->lay.total, ctas, xs);
+    if (err == cudaSuccess && p.host_mirror) {
+        // each moved cold slot now belongs to the demoted expert: point the copy at its
+        // host copy and drop the slot's tag (the scratch holds the promoted one)
+        for (int i = i0; i < i1; ++i) {
+            const int c = moved_slots[i - i0];
+            L->cold_dev[c] = L->mirror_dev[L->plan_dem[i]];
+            if (err == cudaSuccess) err = cudaMemsetAsync(L->scratch->d_tag + c, 0xff, sizeof(int32_t), xs);
+        }
+        std::memcpy(L->h_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(L->d_cold_src, L->h_cold_src, sizeof(uint8_t*) * p.n_cold, cudaMemcpyHostToDevice,
+                                  xs);
+    }
+    std::memcpy(L->h_loc, loc.data(), sizeof(int32_t) * p.E);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(L->d_loc, L->h_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice, xs);
+    if (err == cudaSuccess) err = cudaEventRecord(L->ev_swap, xs);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    L->swap_recorded = true;
+    L->swap_pending = deferred;
+    L->loc = loc;
+    L->plan_next = i1;
+    return MOE_OK;
+}
+}  // namespace
+
 int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
     if (!L || !n_swaps_out) return MOE_ERR_INVALID_ARG;
     *n_swaps_out = 0;
     const moe_params& p = L->p;
+    cudaStream_t st = S(stream);
     L->steps += 1;
-    if (p.swap_every <= 0 || (L->steps % p.swap_every) != 0) return MOE_OK;
-    if (L->fault == 1) {
+    const bool acting = p.swap_every > 0 && (L->steps % p.swap_every) == 0;
+    if (acting && L->fault == 1) {
         L->fault = 0;
         return MOE_ERR_INJECTED;
     }
-    cudaStream_t st = S(stream);
-    cudaError_t err = join_copy(L, st);
+    int applied = 0;
+    if (L->plan_pending) {
+        // the previous closing call's snapshot: its copy to h_counts completes behind that
+        // call's step, so by now the host rarely waits here, and the GPU never idles.
+        // Pairs of the plan before it that are still unapplied land first.
+        L->plan_pending = false;
+        const int rest = (int)L->plan_pro.size() - L->plan_next;
+        int rc = apply_pairs(L, st, true, L->plan_next, (int)L->plan_pro.size());
+        if (rc != MOE_OK) return rc;
+        applied += rest;
+        if (cudaEventSynchronize(L->ev_counts) != cudaSuccess) return MOE_ERR_CUDA;
+        make_plan(L);
+    }
+    const int n_plan = (int)L->plan_pro.size();
+    if (L->plan_next < n_plan) {
+        // paced: pair i lands at the plan's call floor(i * span / n), span the calls
+        // before the next window closes, so that each call moves a few experts while
+        // later layers run instead of every layer moving its whole plan at once
+        const int span = p.swap_every > 1 ? p.swap_every - 1 : 1;
+        const int i0 = L->plan_next;
+        int i1 = i0;
+        while (i1 < n_plan && (long)i1 * span / n_plan <= L->plan_age) ++i1;
+        const int rc = apply_pairs(L, st, true, i0, i1);
+        if (rc != MOE_OK) return rc;
+        applied += i1 - i0;
+    }
+    ++L->plan_age;
+    if (!acting) {
+        *n_swaps_out = applied;
+        return MOE_OK;
+    }
+    cudaError_t err = cudaSuccess;
+    if (L->residency_defer) {
+        // snapshot the window (its counts go to the host behind this step's work) and
+        // count the next window in the other buffer; the plan follows at the next call
+        err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
+        if (err == cudaSuccess) err = cudaEventRecord(L->ev_counts, st);
+        if (err == cudaSuccess) {
+            std::swap(L->d_window, L->d_window_alt);
+            err = cudaMemsetAsync(L->d_window, 0, sizeof(int32_t) * p.E, st);
+        }
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
+        L->plan_pending = true;
+        *n_swaps_out = applied;
+        return MOE_OK;
+    }
+    // synchronous: read the counters now (this drains the caller's stream), move the
+    // bytes on it and clear the window
+    err = join_copy(L, st);
+    if (err == cudaSuccess) err = join_swap(L, st);
     if (err == cudaSuccess)
         err = cudaMemcpyAsync(L->h_counts, L->d_window, sizeof(int32_t) * p.E, cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess && p.host_mirror && p.n_cold > 0)
@@ -626,64 +806,25 @@ int residency_update(moe_layer* L, int32_t* n_swaps_out, void* stream) {
                               cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    int32_t promoted[kMaxSwaps], demoted[kMaxSwaps];
-    std::vector<int32_t> loc(p.E);
-    const int n_plan = plan_residency(L->h_counts, L->loc.data(), p.E, p.n_hot, p.max_swaps, p.hysteresis, loc.data(),
-                                      promoted, demoted);
-    SwapList sw;
-    sw.n = 0;
-    std::vector<int> moved_slots;  // host_mirror: cold slots whose expert changes
-    for (int i = 0; i < n_plan; ++i) {
-        // every expert is in at most one pair, so the old map gives both slots
-        const int a = promoted[i], b = demoted[i];
-        const int slot_h = L->loc[b];            // HBM slot of the demoted expert
-        const int slot_c = L->loc[a] - p.n_hot;  // cold slot of the promoted expert
-        sw.hot[sw.n] = L->hot[slot_h];
-        if (p.host_mirror) {
-            // promote from the scratch slot if this layer's copy of the expert is still
-            // there, else from the expert's host copy; the demoted expert's bytes are
-            // already in its host copy
-            const bool in_scratch = L->scratch->h_tag[slot_c] == L->uid;
-            sw.host[sw.n] = in_scratch ? L->scratch->base + (size_t)slot_c * L->lay.total : L->mirror_dev[a];
-            moved_slots.push_back(slot_c);
-        } else {
-            sw.host[sw.n] = L->cold_dev[slot_c];
-        }
-        ++sw.n;
-    }
-    if (sw.n > 0) {
-        err = p.host_mirror ? launch_copy_list(sw, L->lay.total, L->sm_count, st)
-                            : launch_swap(sw, L->lay.total, L->sm_count, st);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-        if (p.host_mirror) {
-            // each moved cold slot now belongs to the demoted expert: point the copy at
-            // its host copy and drop the slot's tag (the scratch holds the promoted one)
-            for (int c : moved_slots) {
-                int e = -1;
-                for (int x = 0; x < p.E; ++x)
-                    if (loc[x] == p.n_hot + c) e = x;
-                L->cold_dev[c] = L->mirror_dev[e];
-                err = cudaMemsetAsync(L->scratch->d_tag + c, 0xff, sizeof(int32_t), st);
-                if (err != cudaSuccess) return MOE_ERR_CUDA;
-            }
-            err = cudaMemcpyAsync(L->d_cold_src, L->cold_dev.data(), sizeof(uint8_t*) * p.n_cold,
-                                  cudaMemcpyHostToDevice, st);
-            if (err == cudaSuccess) err = cudaStreamSynchronize(st);  // the host vector is the copy's source
-            if (err != cudaSuccess) return MOE_ERR_CUDA;
-        }
-        std::memcpy(L->h_loc, loc.data(), sizeof(int32_t) * p.E);
-        err = cudaMemcpyAsync(L->d_loc, L->h_loc, sizeof(int32_t) * p.E, cudaMemcpyHostToDevice, st);
-        if (err != cudaSuccess) return MOE_ERR_CUDA;
-        L->loc = loc;
-    }
+    const int n = make_plan(L);
+    const int rc = apply_pairs(L, st, false, 0, n);
+    if (rc != MOE_OK) return rc;
     err = cudaMemsetAsync(L->d_window, 0, sizeof(int32_t) * p.E, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    *n_swaps_out = sw.n;
+    *n_swaps_out = applied + n;
+    return MOE_OK;
+}
+
+int moe_layer_set_residency_defer(moe_layer* L, int defer) {
+    if (!L || defer < 0 || defer > 1) return MOE_ERR_INVALID_ARG;
+    L->residency_defer = defer;
     return MOE_OK;
 }
 
 int moe_layer_get_loc(moe_layer* L, int32_t* loc_host) {
     if (!L || !loc_host) return MOE_ERR_INVALID_ARG;
+    // a deferred exchange uploads the map on the layer's copy stream
+    if (settle_staging(L) != cudaSuccess) return MOE_ERR_CUDA;
     return cuda_status(cudaMemcpy(loc_host, L->d_loc, sizeof(int32_t) * L->p.E, cudaMemcpyDeviceToHost));
 }
 

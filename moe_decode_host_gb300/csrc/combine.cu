@@ -115,18 +115,18 @@ cudaError_t launch_combine(const float* y, const float* w, int T, int k, int H, 
     return launch_pdl(combine_kernel<false>, grid, dim3(256), 0, st, y, w, T, k, H, out);
 }
 
-cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st) {
+cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int ctas, cudaStream_t st) {
     if (s.n == 0) return cudaSuccess;
-    int ctas = 2 * sm_count;
+    if (ctas < 1) ctas = 1;
     int seg = ctas / s.n;
     if (seg < 1) seg = 1;
     swap_kernel<<<ctas, kSwapThreads, 0, st>>>(s, blob_bytes, seg);
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st) {
+cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int ctas, cudaStream_t st) {
     if (s.n <= 0) return cudaSuccess;
-    int ctas = 2 * sm_count;
+    if (ctas < 1) ctas = 1;
     int seg = ctas / s.n;
     if (seg < 1) seg = 1;
     copy_list_kernel<<<ctas, kSwapThreads, 0, st>>>(s, blob_bytes, seg);

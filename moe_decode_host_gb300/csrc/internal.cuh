@@ -189,10 +189,10 @@ struct SwapList {
     uint8_t* hot[kMaxSwaps];   // device blob of the HBM slot
     uint8_t* host[kMaxSwaps];  // device-mapped pointer of the host blob
 };
-// Exchanges hot[i] and host[i] in place for every pair.
-cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st);
-// Copies src[i] -> dst[i] (blob_bytes each) for every pair.
-cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int sm_count, cudaStream_t st);
+// Exchanges hot[i] and host[i] in place for every pair, with `ctas` CTAs.
+cudaError_t launch_swap(const SwapList& s, size_t blob_bytes, int ctas, cudaStream_t st);
+// Copies host[i] -> hot[i] (blob_bytes each) for every pair, with `ctas` CTAs.
+cudaError_t launch_copy_list(const SwapList& s, size_t blob_bytes, int ctas, cudaStream_t st);
 
 cudaError_t launch_debug_e2m1(uint32_t* out, cudaStream_t st);
 

@@ -12,7 +12,7 @@ import synth
 class LayerFixture:
     def __init__(self, *, H, I, E, n_hot, n_cold, k, seed, loc=None, swap_every=0, max_swaps=8,
                  hysteresis=3.0, renorm=0, scratch=None, slots=None, gen_device="cuda", host_mirror=False,
-                 zero_copy=False):
+                 zero_copy=False, residency_defer=True):
         import moe_decode_host_gb300 as m
 
         self.m = m
@@ -40,6 +40,8 @@ class LayerFixture:
                              cold_ptrs=[self.cold[c] for c in range(n_host)], init_loc=self.loc0,
                              renorm=renorm, swap_every=swap_every, max_swaps=max_swaps, hysteresis=hysteresis,
                              host_mirror=host_mirror, zero_copy=zero_copy)
+        if not residency_defer:
+            self.layer.set_residency_defer(False)
 
     def expert_bytes_now(self, e: int, loc=None) -> np.ndarray:
         """Current bytes of expert e (from its HBM slot or its host blob)."""

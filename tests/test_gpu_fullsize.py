@@ -7,7 +7,9 @@ through the C ABI, against the CPU oracle.
   another), with skewed routing over starting hot sets drawn from a different
   permutation, so the residency manager swaps within the test.  After every step:
   routing, physical ids, cold lists and gathered slot bytes bit-exact; the
-  placement map equal to the oracle's residency rule after every update; the
+  placement map equal to the oracle's residency rule after every update (in the
+  deferred mode one step after each window closes, in the synchronous mode at
+  once); the
   fingerprint of every moved expert and of 64 random ones per layer unchanged
   wherever the expert now lives (same page, section 4: the byte audit); every
   token's output within the relative-L2 bar.
@@ -61,8 +63,8 @@ def _check_outputs(fx, buf, ids, w, x, tokens, loc):
 
 # ------------------------------------------------------------------ stacked layers
 
-@pytest.mark.parametrize("host_mirror", [False, True])
-def test_shared_scratch_full_shape(host_mirror):
+@pytest.mark.parametrize("host_mirror,defer", [(False, True), (True, True), (False, False)])
+def test_shared_scratch_full_shape(host_mirror, defer):
     import moe_decode_host_gb300 as m
 
     c = synth.CONFIGS["c3"]
@@ -78,9 +80,11 @@ def test_shared_scratch_full_shape(host_mirror):
         loc = synth.loc_from_hot_set(E, n_hot, other[:n_hot])
         fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=synth.sub_seed("c3", "blobs", li),
                           loc=loc, scratch=scratch, slots=slots, swap_every=swap_every, max_swaps=max_swaps,
-                          hysteresis=hyst, host_mirror=host_mirror)
+                          hysteresis=hyst, host_mirror=host_mirror, residency_defer=defer)
         fx.perm = perm
-        fx.loc_o = loc.copy()
+        fx.loc_o = loc.copy()    # the oracle's placement after every plan so far
+        fx.loc_now = loc.copy()  # the placement the layer should hold now
+        fx.pending = None        # deferred: (placement, promoted, demoted) of a closed window
         fx.window = np.zeros(E, np.int64)
         fx.fp0 = fingerprints(lambda e, fx=fx, l0=loc: fx.expert_bytes_now(e, l0), list(range(E)))
         layers.append(fx)
@@ -91,7 +95,7 @@ def test_shared_scratch_full_shape(host_mirror):
             logits = synth.gen_logits_zipf(T, E, c["s"], fx.perm, seed=synth.sub_seed("c3", "logits", li, step))
             x = synth.gen_x(T, H, seed=synth.sub_seed("c3", "x", li, step))
             loc = fx.layer.get_loc()
-            assert np.array_equal(loc, fx.loc_o)
+            assert np.array_equal(loc, fx.loc_now)
             buf = m.StepBuffers(fx.layer, T, out_fp32=True)
             m.moe_route(fx.layer, torch.from_numpy(logits).cuda(), T, buf.topk_ids, buf.topk_w, buf.counts,
                         buf.offsets, buf.entries)
@@ -118,18 +122,28 @@ def test_shared_scratch_full_shape(host_mirror):
             torch.cuda.synchronize()
             assert fx.layer.status() == 0, fx.layer.diag().tolist()
             fx.window += counts
+            landed = None
+            if defer and fx.pending is not None:
+                landed, fx.pending = fx.pending, None
             if (step + 1) % swap_every == 0:
                 fx.loc_o, pro, dem = oracle.residency(fx.window.astype(np.int32), fx.loc_o, n_hot, max_swaps, hyst)
                 fx.window[:] = 0
+                if defer:
+                    fx.pending = (fx.loc_o.copy(), pro, dem)
+                else:
+                    landed = (fx.loc_o.copy(), pro, dem)
+            now = fx.layer.get_loc()
+            if landed is not None:
+                fx.loc_now, pro, dem = landed
                 assert nsw == pro.size, (step, li)
                 total_swaps += nsw
-                now = fx.layer.get_loc()
-                assert np.array_equal(now, fx.loc_o), (step, li)
+                assert np.array_equal(now, fx.loc_now), (step, li)
                 audit = sorted(set(pro.tolist()) | set(dem.tolist()) | set(rng.choice(E, 64, replace=False).tolist()))
                 fp = fingerprints(lambda e, fx=fx, l1=now: fx.expert_bytes_now(e, l1), audit)
                 assert all(fp[e] == fx.fp0[e] for e in audit), (step, li)
             else:
                 assert nsw == 0
+                assert np.array_equal(now, fx.loc_now), (step, li)
             # outputs: the bytes each expert had when the FFN ran are its bytes now
             _check_outputs(fx, buf, ids, w, x, list(range(T)), fx.layer.get_loc())
     assert total_swaps > 0

@@ -457,22 +457,39 @@ def _skewed_logits(T, E, step, hot_first):
     return l
 
 
+def paced_landing(n: int, swap_every: int) -> list:
+    """Deferred residency: the call (counted from the one after the window closes)
+    at which each of a plan's n pairs lands -- pair i at floor(i * span / n), span
+    the calls before the next window closes (at least 1)."""
+    span = max(1, swap_every - 1)
+    return [i * span // n for i in range(n)]
+
+
+@pytest.mark.parametrize("defer", [True, False])
 @pytest.mark.parametrize("host_mirror", [False, True])
-def test_residency_matches_oracle_and_keeps_bytes(host_mirror):
+def test_residency_matches_oracle_and_keeps_bytes(host_mirror, defer):
+    """Maps equal the oracle's rule on every window's counts.  Synchronous mode: the
+    whole plan lands at the call that closes the window.  Deferred mode: the plan is
+    made at the next call and its pairs land in plan order, paced over the calls
+    before the next window closes.  Every expert keeps its bytes and the outputs
+    equal a frozen layer's."""
     import moe_decode_host_gb300 as m
 
     H, I, E, n_hot, n_cold, k, T = 256, 512, 16, 12, 4, 2, 4
+    swap_every, max_swaps, steps = 4, 3, 16
     seed = synth.sub_seed("residency")
-    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=3, max_swaps=2,
-                      host_mirror=host_mirror)
+    fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=swap_every,
+                      max_swaps=max_swaps, host_mirror=host_mirror, residency_defer=defer)
     frozen = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=seed, swap_every=0)
     fp0 = [oracle.fnv1a64(b) for b in fx.all_blobs_now()]
     host0 = [oracle.fnv1a64(fx.cold[i].numpy()) for i in range(fx.cold.shape[0])]
-    loc_o = fx.loc0.copy()
+    loc_o = fx.loc0.copy()      # the oracle's placement after every plan so far
+    loc_now = fx.loc0.copy()    # the placement the layer should hold now
+    landing = {}                # step -> pairs (promoted, demoted) landing then
     window = np.zeros(E, np.int64)
-    total_swaps = 0
-    for step in range(12):
-        favoured = [12, 13, 14, 15] if step < 6 else [0, 1, 2, 3]
+    total_swaps, spread = 0, 0
+    for step in range(steps):
+        favoured = [12, 13, 14, 15] if step < steps // 2 else [0, 1, 2, 3]
         logits = _skewed_logits(T, E, step, favoured)
         x = synth.gen_x(T, H, seed=step)
         buf = m.StepBuffers(fx.layer, T, out_fp32=True)
@@ -485,31 +502,44 @@ def test_residency_matches_oracle_and_keeps_bytes(host_mirror):
         assert torch.equal(buf.out, bufz.out), step
         rc, ids, w, counts, _, _ = oracle.route(logits, k)
         window += counts
-        if (step + 1) % 3 == 0:
-            loc_o, pro, dem = oracle.residency(window.astype(np.int32), loc_o, n_hot, 2, 3.0)
-            assert nsw == pro.size, step
-            total_swaps += nsw
+        if (step + 1) % swap_every == 0:
+            loc_o, pro, dem = oracle.residency(window.astype(np.int32), loc_o, n_hot, max_swaps, 3.0)
             window[:] = 0
-            assert np.array_equal(fx.layer.get_loc(), loc_o), step
+            when = paced_landing(pro.size, swap_every) if defer else [None] * pro.size
+            spread += len(set(when)) > 1
+            for i, j in enumerate(when):
+                landing.setdefault(step if j is None else step + 1 + j, []).append((int(pro[i]), int(dem[i])))
+        pairs = landing.pop(step, [])
+        assert nsw == len(pairs), step
+        if pairs:
+            for a, b in pairs:
+                loc_now[a], loc_now[b] = loc_now[b], loc_now[a]
+            total_swaps += nsw
             # byte audit: every expert, wherever it now lives
             fp = [oracle.fnv1a64(b) for b in fx.all_blobs_now()]
             assert fp == fp0, step
-        else:
-            assert nsw == 0
+        assert np.array_equal(fx.layer.get_loc(), loc_now), step
         assert np.array_equal(fx.layer.get_counts(), window.astype(np.int32)), step
         rc, ids, w, want = oracle.layer(logits, bf16_bits(x), k, 0, H, I, fx.all_blobs_now())
         assert rel_l2(buf.out.cpu().numpy(), want) <= OUT_TOL
     assert total_swaps > 0
+    if defer:
+        assert spread > 0  # some plan landed over several calls
+    # at the end the placement is the oracle's but for pairs still to land
+    for a, b in sum(landing.values(), []):
+        loc_now[a], loc_now[b] = loc_now[b], loc_now[a]
+    assert np.array_equal(loc_now, loc_o)
     assert sorted(fx.layer.get_loc().tolist()) == list(range(E))
     if host_mirror:
         # with host copies nothing is ever written to host memory
         assert [oracle.fnv1a64(fx.cold[i].numpy()) for i in range(E)] == host0
 
 
-def test_residency_injected_fault_leaves_map():
+@pytest.mark.parametrize("defer", [True, False])
+def test_residency_injected_fault_leaves_map(defer):
     import moe_decode_host_gb300 as m
 
-    fx = LayerFixture(H=256, I=512, E=16, n_hot=12, n_cold=4, k=2, seed=4, swap_every=1)
+    fx = LayerFixture(H=256, I=512, E=16, n_hot=12, n_cold=4, k=2, seed=4, swap_every=1, residency_defer=defer)
     logits = _skewed_logits(4, 16, 0, [12, 13])
     buf = m.StepBuffers(fx.layer, 4)
     m.moe_route(fx.layer, torch.from_numpy(logits).cuda(), 4, buf.topk_ids, buf.topk_w, buf.counts, buf.offsets,
@@ -520,11 +550,17 @@ def test_residency_injected_fault_leaves_map():
         m.residency_update(fx.layer)
     assert ei.value.code == m.MOE_ERR_INJECTED
     assert np.array_equal(fx.layer.get_loc(), loc_before)
+    if defer:
+        # the next call closes the window (its plan lands at the call after)
+        assert m.residency_update(fx.layer) == 0
+        assert np.array_equal(fx.layer.get_loc(), loc_before)
     assert m.residency_update(fx.layer) > 0
+    assert not np.array_equal(fx.layer.get_loc(), loc_before)
 
 
+@pytest.mark.parametrize("defer", [True, False])
 @pytest.mark.parametrize("host_mirror", [False, True])
-def test_shared_scratch_across_layers(host_mirror):
+def test_shared_scratch_across_layers(host_mirror, defer):
     """Several layers share one slot scratch and run one after another (the c3
     structure at c0 size), swapping every other step: each layer's output still
     matches the oracle and every expert keeps its bytes (with host copies a
@@ -540,7 +576,7 @@ def test_shared_scratch_across_layers(host_mirror):
         loc = synth.loc_from_hot_set(E, n_hot, np.random.default_rng(L).permutation(E)[:n_hot])
         layers.append(LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=100 + L, loc=loc,
                                    scratch=scratch, slots=slots, swap_every=2, max_swaps=2, hysteresis=0.5,
-                                   host_mirror=host_mirror))
+                                   host_mirror=host_mirror, residency_defer=defer))
     fp0 = [[oracle.fnv1a64(b) for b in fx.all_blobs_now()] for fx in layers]
     x = synth.gen_x(T, H, seed=5).cuda()
     swaps = 0
