@@ -33,9 +33,11 @@ HBM_NOMINAL_GBS = 8000.0
 # ncu captures of a smaller layer of the same expert shape (traffic scales with the
 # experts processed).  None once the kernel has changed since its capture.
 NCU_TRAFFIC = {
-    "cold_copy": (11520 + 15616) / 2,                     # per cold expert copied
-    "ffn_decode": (66931968 + 642560 + 33490432) / 5,     # per distinct expert, both phases
-    "ffn_tc": None,                                       # per expert at ~128 tokens per expert
+    "cold_copy": (11520 + 15616) / 2,                       # per cold expert copied
+    "ffn_decode": (66936832 + 754944 + 33493504) / 5,      # dequant-GEMV, per distinct expert, both phases
+    "ffn_mx_decode": (537065728 + 3808000 + 268754176 + 4258048) / 40,  # 4-term block-scaled, per distinct expert
+    "ffn_mx": (904207616 + 6353152 + 482149888 + 79283712) / 64,       # all-FP4 prefill, per expert at ~128 tokens
+    "ffn_tc": (934021120 + 93158656 + 482610432 + 114407680) / 64,     # f16 prefill, per expert at ~128 tokens
 }
 
 
@@ -765,6 +767,9 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
     tstar_meas = np.maximum(hot_bytes / (hbm_peak * 1e9), gather_bytes / (lp * 1e9))
     step_ms = elapsed_ms / K
     value = job_rate(world, K, T, elapsed_ms)
+    # the residency moves' own link reads (one expert per swap, host to HBM) on top of
+    # the cold copies: the bound the policy's churn leaves
+    tstar_res_ms = float(1e3 * tstar_meas.sum() / K) + (total_swaps * eb / (lp * 1e9) * 1e3 / K)
     # dominant kernel: the one with the most GPU time over the timed region, the cold
     # copy (on the copy stream) or the FFN call's kernels (wait for the copy excluded)
     tot = {n: float(np.sum(per[n])) for n in names}
@@ -785,7 +790,7 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
                 "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
                 "tensor_tflops": ffn_tflops, "tensor_peak_tflops": tc_peak, "tensor_peak_kind": tc_kind,
                 "tensor_frac": ffn_tflops / tc_peak, "hbm_gbs": ffn_gbs, "hbm_frac": ffn_gbs / hbm_peak,
-                "traffic": None if fp4 else _traffic("ffn_tc", mean_distinct),
+                "traffic": _traffic("ffn_mx" if fp4 else "ffn_tc", mean_distinct),
                 "prefill_target": prefill_targets(ffn_flops, float(ffn_bytes.sum()), ffn_k_tot_ms, mx_peak,
                                                   "measured in this run (dense kind::mxf4 probe)", hbm_peak)}
         if t_hbm >= t_tensor:  # the call's bytes take longer than its flops at the kind's peak
@@ -795,9 +800,10 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
             roof.update({"bound": "tensor", "achieved": ffn_tflops, "peak": tc_peak, "unit": "TFLOP/s",
                          "frac": ffn_tflops / tc_peak, "peak_kind": tc_kind})
     elif dom == "moe_grouped_ffn":
-        roof = {"kernel": "moe_grouped_ffn (decode dequant-GEMV)", "bound": "hbm", "achieved": ffn_gbs,
+        arith = decode_arithmetic(c)
+        roof = {"kernel": "moe_grouped_ffn (decode: %s)" % arith, "bound": "hbm", "achieved": ffn_gbs,
                 "peak": hbm_peak, "unit": "GB/s", "frac": ffn_gbs / hbm_peak,
-                "traffic": _traffic("ffn_decode", mean_distinct),
+                "traffic": _traffic("ffn_decode" if arith.startswith("dequant") else "ffn_mx_decode", mean_distinct),
                 "algorithmic_bytes_per_call": float(ffn_bytes.sum() / (K * NL)),
                 "ms_mean": ffn_k_tot_ms / (K * NL), "peak_kind": peak_kind}
     else:
@@ -817,6 +823,8 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
                              "frac_nominal": float(1e3 * tstar_nom.sum() / K / step_ms),
                              "tstar_ms_measured_hbm": float(1e3 * tstar_meas.sum() / K),
                              "frac_measured": float(1e3 * tstar_meas.sum() / K / step_ms),
+                             "tstar_ms_with_residency_moves": tstar_res_ms,
+                             "frac_with_residency_moves": tstar_res_ms / step_ms,
                              "hbm_peak_gbs": hbm_peak, "link_peak_gbs": link_peak, "link_probe": link_detail},
            "ffn_hbm_gbs": ffn_gbs, "ffn_kernel_ms_mean": ffn_k_tot_ms / (K * NL), "gather_link_gbs": gather_gbs,
            "distinct_experts_per_layer_step": mean_distinct,
