@@ -608,24 +608,36 @@ def measure_link_peak(dev):
     return max(res.values()), res
 
 
-def step_launches(T, n_cold):
-    """Kernels one layer-step launches (residency swap kernel excluded)."""
-    route = 1 if T <= 64 else 2                      # one-CTA route, or top-k + bucketing
-    gather = 1 + (1 if n_cold > 0 else 0)            # remap, byte copy on the copy stream
-    calls = 4 if n_cold > 0 else 2                   # FFN phases: (gate/up, down) x (hot, cold)
-    per_call = 1 + (1 if T > 8 else 0) + (1 if T > 16 else 0) + (2 if T > 64 else 0)  # decode ranges, gather + tcgen05
-    ffn = 1 + calls * per_call + calls // 2          # activation prep, phases, h prescale per down phase
-    return route + gather + ffn + 1                  # + combine
+def ffn_terms(c):
+    """Activation terms of the library's block-scaled FFN for this workload's calls
+    (0: the dequant-GEMV / f16 tensor-core kernels), by the library's rule."""
+    T = c["T"]
+    if T > 64:
+        return 1 if c.get("prefill") == "fp4" else 0
+    kind = c.get("decode_kind", 0)
+    if kind == 1 or (c.get("zero_copy") and c.get("n_cold", 0) > 0) or (kind == 0 and T < 3):
+        return 0
+    return 4
+
+
+def step_launches(c):
+    """Kernels one layer-step launches (residency move kernels excluded)."""
+    T, n_cold = c["T"], c["n_cold"]
+    zc = bool(c.get("zero_copy")) and n_cold > 0 and T <= 64
+    route = 1 if T <= 64 else 2                          # one-CTA route, or top-k + bucketing
+    gather = 1 + (0 if (n_cold == 0 or zc) else 2)      # remap; gate/up planes, down planes
+    classes = 2 if n_cold > 0 else 1                    # HBM-resident and cold experts
+    if ffn_terms(c) > 0:
+        ffn = 1 + 2 * classes                           # activation prep, gate/up and down per class
+    else:
+        per_phase = 1 + (T > 8) + (T > 16) + (T > 64)   # decode token ranges, tcgen05 kernel
+        ffn = 1 + classes * (2 * per_phase + 1)         # activation prep, phases, h prescale per down phase
+    return route + gather + ffn + 1                     # + combine
 
 
 def decode_arithmetic(c):
     """What the FFN of a decode-sized call computes in, as the library picks it."""
-    kind = c.get("decode_kind", 0)
-    if c.get("zero_copy") and c.get("n_cold", 0) > 0:
-        kind = 1
-    if kind == 0:
-        kind = 1 if c["T"] < 3 else 2
-    if kind == 2:
+    if ffn_terms(c) == 4:
         return "block-scaled FP4 tensor cores (tcgen05 kind::mxf4), activations as sums of 4 MXFP4 terms"
     return "dequant-GEMV (E2M1 -> f16 in registers, mma.sync)"
 
@@ -685,7 +697,7 @@ def measure(c, args, dev, dist, world, link_peak, link_detail, local, mx_peak=No
             if ev is not None:
                 ev[li][5].record(st)
             swaps += n
-            launches += step_launches(T, c["n_cold"]) + (1 if n > 0 else 0)
+            launches += step_launches(c) + (1 if n > 0 else 0)
         return swaps, launches
 
     for i in range(W):

@@ -176,8 +176,11 @@ int moe_route(moe_layer* L, const float* logits, int T, int32_t* topk_ids, float
  * phys_ids, cold_list and n_cold_picked are ready in `stream` order.  The byte
  * copy itself runs on the layer's own copy stream, forked from `stream` at this
  * call, so that moe_grouped_ffn can work on the experts in HBM while the link
- * streams the cold ones; moe_grouped_ffn and residency_update on this layer join
- * it, and so does moe_gather_join.  A layer sharing the scratch must not call
+ * streams the cold ones; it moves every picked blob's gate/up planes (w13 nibbles
+ * and scales) first and its down planes second, so that moe_grouped_ffn can run
+ * the cold experts' gate/up phase while the down planes stream.
+ * moe_grouped_ffn and residency_update on this layer join it, and so does
+ * moe_gather_join.  A layer sharing the scratch must not call
  * cold_gather before this layer's copy has been joined into `stream`.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
 int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids, int32_t* cold_list,
@@ -382,8 +385,9 @@ int moe_layer_set_copy_ctas(moe_layer* L, int ctas);
  * moe_layer_profile_read waits for the copy records and writes up to `max`
  * durations in ms to host float copy_ms[] and their number to *n_out.
  * moe_layer_profile_read_ffn does the same for the FFN calls: each duration is the
- * call's kernel time without the wait for the cold copy (start to the join, plus
- * the join to the end).  0 <= n <= 2^20, else MOE_ERR_INVALID_ARG. */
+ * call's kernel time without the waits for the cold copy (the work before the join
+ * of the cold gate/up planes, between that join and the join of the rest, and
+ * after it).  0 <= n <= 2^20, else MOE_ERR_INVALID_ARG. */
 int moe_layer_profile(moe_layer* L, int max_records);
 int moe_layer_profile_read(moe_layer* L, float* copy_ms, int max, int* n_out);
 int moe_layer_profile_read_ffn(moe_layer* L, float* ffn_ms, int max, int* n_out);

@@ -50,7 +50,9 @@ struct moe_layer {
     ExpertMaps* d_tmaps = nullptr;      // [E] TMA descriptors per physical id
     cudaStream_t copy_stream = nullptr;  // cold slot copies run here, joined by moe_grouped_ffn
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    cudaEvent_t ev_join_w13 = nullptr;  // the copy's first launch (the gate/up planes) has completed
     bool copy_pending = false;
+    bool copy_pending_w13 = false;
     // residency (moe_layer_set_residency_defer): ev_counts follows the D2H copy of a
     // window snapshot; ev_swap follows the last exchange and map upload
     cudaEvent_t ev_counts = nullptr, ev_swap = nullptr;
@@ -64,7 +66,7 @@ struct moe_layer {
     int copy_ctas = 0;
     std::vector<cudaEvent_t> prof_ev;  // pairs of events around recorded cold copies
     int prof_n = 0;
-    std::vector<cudaEvent_t> fprof_ev;  // quadruples around recorded FFN calls (see moe_layer_profile_read_ffn)
+    std::vector<cudaEvent_t> fprof_ev;  // six per recorded FFN call (see moe_layer_profile_read_ffn)
     int fprof_n = 0;
     long steps = 0;
     int fault = 0;
@@ -169,7 +171,17 @@ int default_copy_ctas(int sm_count) { return sm_count * 3 / 16 > 0 ? sm_count * 
 cudaError_t join_copy(moe_layer* L, cudaStream_t st) {
     if (!L->copy_pending) return cudaSuccess;
     L->copy_pending = false;
+    L->copy_pending_w13 = false;
     return cudaStreamWaitEvent(st, L->ev_join, 0);
+}
+
+// Makes `st` wait for the first half of the cold copy in flight (every picked cold
+// expert's gate/up planes), if any: the gate/up phase over the cold experts can then
+// run while their down planes still stream.
+cudaError_t join_copy_w13(moe_layer* L, cudaStream_t st) {
+    if (!L->copy_pending_w13) return cudaSuccess;
+    L->copy_pending_w13 = false;
+    return cudaStreamWaitEvent(st, L->ev_join_w13, 0);
 }
 
 // Makes `st` wait for a residency exchange (and its map upload) that ran on the
@@ -204,6 +216,7 @@ void free_layer(moe_layer* L) {
     if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
     if (L->ev_fork) cudaEventDestroy(L->ev_fork);
     if (L->ev_join) cudaEventDestroy(L->ev_join);
+    if (L->ev_join_w13) cudaEventDestroy(L->ev_join_w13);
     if (L->ev_counts) cudaEventDestroy(L->ev_counts);
     if (L->ev_swap) cudaEventDestroy(L->ev_swap);
     cudaFree(L->d_tmaps);
@@ -354,6 +367,7 @@ int moe_layer_create(const moe_params* pp, moe_scratch* scratch, void* const* ho
     err = err ? err : cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_fork, cudaEventDisableTiming);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_join, cudaEventDisableTiming);
+    err = err ? err : cudaEventCreateWithFlags(&L->ev_join_w13, cudaEventDisableTiming);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_counts, cudaEventDisableTiming);
     err = err ? err : cudaEventCreateWithFlags(&L->ev_swap, cudaEventDisableTiming);
     if (err == cudaSuccess) {
@@ -416,21 +430,32 @@ int cold_gather(moe_layer* L, const int32_t* topk_ids, int T, int32_t* phys_ids,
     if (L->p.n_cold > 0 && T > 0 && !zc) {
         // the byte copy forks onto the layer's copy stream first, so that it starts
         // while the remap kernel runs and the FFN over HBM-resident experts can run
-        // while the link streams the cold ones
+        // while the link streams the cold ones.  It moves every picked blob's gate/up
+        // planes first, then its down planes, with an event between, so that the
+        // gate/up phase over the cold experts overlaps the second launch.
         err = cudaEventRecord(L->ev_fork, st);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
         const bool prof = L->prof_n < (int)L->prof_ev.size() / 2;
         if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
+        const size_t split = L->lay.w2n;  // the gate/up planes (nibbles, scales) end where w2 begins
         if (err == cudaSuccess)
             err = launch_cold_copy(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, L->d_cold_src,
-                                   L->scratch->base, L->lay.total, L->scratch->d_tag, L->uid, L->copy_ctas,
+                                   L->scratch->base, L->lay.total, 0, split, L->scratch->d_tag, L->uid, L->copy_ctas,
                                    L->copy_stream);
+        if (err == cudaSuccess) err = cudaEventRecord(L->ev_join_w13, L->copy_stream);
+        if (err == cudaSuccess)
+            err = launch_cold_copy(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, L->d_cold_src,
+                                   L->scratch->base, L->lay.total, split, L->lay.total, L->scratch->d_tag, L->uid,
+                                   L->copy_ctas, L->copy_stream);
         if (err == cudaSuccess && prof) {
             err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
             ++L->prof_n;
         }
         if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
-        if (err == cudaSuccess) L->copy_pending = true;
+        if (err == cudaSuccess) {
+            L->copy_pending = true;
+            L->copy_pending_w13 = true;
+        }
     }
     if (err == cudaSuccess)
         err = launch_cold_remap(topk_ids, T * L->p.k, L->d_loc, L->p.E, L->p.n_hot, L->p.n_cold, phys_ids, cold_list,
@@ -521,10 +546,16 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     a.w2n = L->lay.w2n;
     a.w2s = L->lay.w2s;
     cudaStream_t st = S(stream);
-    // profiled calls record: start, end of the work before the join, after the
-    // join, end (the two middle events coincide when no copy is pending)
-    cudaEvent_t* pe = L->fprof_n < (int)L->fprof_ev.size() / 4 ? &L->fprof_ev[4 * L->fprof_n++] : nullptr;
-    cudaError_t err = pe ? cudaEventRecord(pe[0], st) : cudaSuccess;
+    // profiled calls record six events: start, end of the work over HBM-resident
+    // experts, after the join of the cold gate/up planes, after the cold gate/up
+    // phase, after the join of the rest of the copy, end (the events between the
+    // joins coincide when no copy is pending)
+    cudaEvent_t* pe = L->fprof_n < (int)L->fprof_ev.size() / 6 ? &L->fprof_ev[6 * L->fprof_n++] : nullptr;
+    cudaError_t err = cudaSuccess;
+    auto mark = [&](int i) {
+        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[i], st);
+    };
+    mark(0);
     // While the cold experts stream over the link (copy, or zero-copy chain) on the
     // layer's copy stream, that stream's CTAs hold copy_ctas SMs: the persistent FFN
     // launches that run meanwhile take the other SMs, so that all their CTAs are
@@ -532,33 +563,18 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     // waiting for an SM would end only when the copy frees one, and the next kernel
     // waits for it).
     const int hot_sms = L->sm_count > L->copy_ctas ? L->sm_count - L->copy_ctas : L->sm_count;
+    // block-scaled path: x converted to MXFP4 terms once, then per placement class the
+    // gate/up kernel (h converted in its epilogue) and the down kernel; otherwise the
+    // dequant-GEMV / f16 tensor-core kernels, whose down phase starts with its own h
+    // prescale
     const int terms = mx_terms(L, T);
-    if (terms > 0) {
-        // block-scaled path: x converted to MXFP4 terms once, then per placement class
-        // the gate/up kernel (h converted in its epilogue) and the down kernel; experts
-        // in HBM first while a cold copy is in flight
-        const int lo = 0, hi = 1 << 30;
-        if (err == cudaSuccess) err = launch_ffn_mx_prep(a, workspace, terms, st);
-        if (err == cudaSuccess && L->copy_pending) {
-            err = launch_ffn_mx(a, 0, 1, lo, hi, terms, hot_sms, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 1, lo, hi, terms, hot_sms, st);
-            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
-            if (err == cudaSuccess) err = join_copy(L, st);
-            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 2, lo, hi, terms, L->sm_count, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 2, lo, hi, terms, L->sm_count, st);
-        } else {
-            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
-            if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 0, 0, lo, hi, terms, L->sm_count, st);
-            if (err == cudaSuccess) err = launch_ffn_mx(a, 1, 0, lo, hi, terms, L->sm_count, st);
-        }
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[3], st);
-        return cuda_status(err);
-    }
-    if (err == cudaSuccess) err = launch_ffn_prep(a, workspace, st);
+    auto phase = [&](int ph, int sel, int grid, cudaStream_t s, bool zc) -> cudaError_t {
+        return terms > 0 ? launch_ffn_mx(a, ph, sel, 0, 1 << 30, terms, grid, s)
+                         : launch_ffn_phase(a, ph, sel, grid, s, zc);
+    };
+    if (err == cudaSuccess) err = terms > 0 ? launch_ffn_mx_prep(a, workspace, terms, st) : launch_ffn_prep(a, workspace, st);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    if (L->p.zero_copy && L->p.n_cold > 0 && T <= kTcMinTokens) {
+    if (terms == 0 && L->p.zero_copy && L->p.n_cold > 0 && T <= kTcMinTokens) {
         // zero copy: the cold experts' chain (gate/up, prescale, down) reads their
         // weights in place over the host link on the layer's copy stream, with as
         // many CTAs as the cold copy would use, while the experts in HBM run here;
@@ -568,34 +584,43 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
         if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
         const bool prof = L->prof_n < (int)L->prof_ev.size() / 2;
         if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 2, L->copy_ctas, L->copy_stream, true);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 2, L->copy_ctas, L->copy_stream, true);
+        if (err == cudaSuccess) err = phase(0, 2, L->copy_ctas, L->copy_stream, true);
+        if (err == cudaSuccess) err = phase(1, 2, L->copy_ctas, L->copy_stream, true);
         if (err == cudaSuccess && prof) {
             err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
             ++L->prof_n;
         }
         if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 1, hot_sms, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+        if (err == cudaSuccess) err = phase(0, 1, hot_sms, st, false);
+        if (err == cudaSuccess) err = phase(1, 1, hot_sms, st, false);
+        mark(1);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(st, L->ev_join, 0);
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
+        mark(2);
+        mark(3);
+        mark(4);
     } else if (L->copy_pending) {
-        // experts in HBM first, on the SMs the cold copy leaves free; then the cold ones
-        err = launch_ffn_phase(a, 0, 1, hot_sms, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 1, hot_sms, st);
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
+        // experts in HBM first, on the SMs the cold copy leaves free; then the cold
+        // experts' gate/up phase once their gate/up planes have landed (beside the copy
+        // of their down planes), and their down phase after the whole copy
+        err = phase(0, 1, hot_sms, st, false);
+        if (err == cudaSuccess) err = phase(1, 1, hot_sms, st, false);
+        mark(1);
+        if (err == cudaSuccess) err = join_copy_w13(L, st);
+        mark(2);
+        if (err == cudaSuccess) err = phase(0, 2, hot_sms, st, false);
+        mark(3);
         if (err == cudaSuccess) err = join_copy(L, st);
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 2, L->sm_count, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 2, L->sm_count, st);
+        mark(4);
+        if (err == cudaSuccess) err = phase(1, 2, L->sm_count, st, false);
     } else {
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[1], st);
-        if (err == cudaSuccess && pe) err = cudaEventRecord(pe[2], st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 0, 0, L->sm_count, st);
-        if (err == cudaSuccess) err = launch_ffn_phase(a, 1, 0, L->sm_count, st);
+        mark(1);
+        mark(2);
+        mark(3);
+        mark(4);
+        if (err == cudaSuccess) err = phase(0, 0, L->sm_count, st, false);
+        if (err == cudaSuccess) err = phase(1, 0, L->sm_count, st, false);
     }
-    if (err == cudaSuccess && pe) err = cudaEventRecord(pe[3], st);
+    mark(5);
     return cuda_status(err);
 }
 
@@ -883,7 +908,7 @@ int moe_layer_profile(moe_layer* L, int max_records) {
     if (L->copy_stream && cudaStreamSynchronize(L->copy_stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
     free_prof(L);
-    for (int i = 0; i < 6 * max_records; ++i) {
+    for (int i = 0; i < 8 * max_records; ++i) {
         cudaEvent_t e;
         if (cudaEventCreate(&e) != cudaSuccess) {
             cudaGetLastError();
@@ -913,14 +938,15 @@ int moe_layer_profile_read_ffn(moe_layer* L, float* ffn_ms, int max, int* n_out)
     if (!L || !n_out || max < 0 || (max > 0 && !ffn_ms)) return MOE_ERR_INVALID_ARG;
     const int n = L->fprof_n < max ? L->fprof_n : max;
     for (int i = 0; i < n; ++i) {
-        const cudaEvent_t* e = &L->fprof_ev[4 * i];
-        float before = 0.f, after = 0.f;
-        if (cudaEventSynchronize(e[3]) != cudaSuccess || cudaEventElapsedTime(&before, e[0], e[1]) != cudaSuccess ||
-            cudaEventElapsedTime(&after, e[2], e[3]) != cudaSuccess) {
+        const cudaEvent_t* e = &L->fprof_ev[6 * i];
+        float part[3] = {0.f, 0.f, 0.f};
+        if (cudaEventSynchronize(e[5]) != cudaSuccess || cudaEventElapsedTime(&part[0], e[0], e[1]) != cudaSuccess ||
+            cudaEventElapsedTime(&part[1], e[2], e[3]) != cudaSuccess ||
+            cudaEventElapsedTime(&part[2], e[4], e[5]) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ERR_CUDA;
         }
-        ffn_ms[i] = before + after;
+        ffn_ms[i] = part[0] + part[1] + part[2];
     }
     *n_out = n;
     return MOE_OK;

@@ -95,14 +95,16 @@ __global__ void __launch_bounds__(kRemapThreads) cold_remap_kernel(
 // Streams every picked cold expert's host blob into its scratch slot.  Each CTA
 // derives the ascending list of picked cold slots from the picks itself (the same
 // marking and ballot compaction as the remap kernel), so the copy needs nothing
-// from the remap kernel and the two run concurrently.  Each picked slot is cut
-// into `seg` contiguous pieces spread over the grid.  CTA 0 also marks every
+// from the remap kernel and the two run concurrently.  A launch copies bytes
+// [part_lo, part_hi) of every picked blob (a call copies a blob in two launches:
+// the gate/up planes, then the down planes), each picked slot's range cut into
+// `seg` contiguous pieces spread over the grid.  CTA 0 also marks every
 // picked slot with the copying layer's id (slot_tag), which tells the residency
 // manager which slots hold this layer's copy of their expert.
 __global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(
     const int32_t* __restrict__ ids, int n_picks, const int32_t* __restrict__ loc, int E, int n_hot, int n_cold,
     const uint8_t* const* __restrict__ cold_src, uint8_t* __restrict__ slot_base, size_t blob_bytes,
-    int32_t* __restrict__ slot_tag, int uid) {
+    size_t part_lo, size_t part_hi, int32_t* __restrict__ slot_tag, int uid) {
     __shared__ unsigned char flag[kMaxColdSlots];
     __shared__ int32_t list[kMaxColdSlots];
     __shared__ int s_cnt;
@@ -133,15 +135,15 @@ __global__ void __launch_bounds__(kGatherThreads) cold_copy_kernel(
     if (cnt <= 0) return;
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < cnt; i += blockDim.x) slot_tag[list[i]] = uid;
-    const size_t chunks = blob_bytes / 16;
+    const size_t first = part_lo / 16, chunks = (part_hi - part_lo) / 16;
     int seg = (int)gridDim.x / cnt;
     if (seg < 1) seg = 1;
     const int items = cnt * seg;
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int c = list[it / seg];
         const int s = it % seg;
-        const size_t c0 = chunks * (size_t)s / (size_t)seg;
-        const size_t c1 = chunks * (size_t)(s + 1) / (size_t)seg;
+        const size_t c0 = first + chunks * (size_t)s / (size_t)seg;
+        const size_t c1 = first + chunks * (size_t)(s + 1) / (size_t)seg;
         copy_range(reinterpret_cast<const uint4*>(cold_src[c]),
                    reinterpret_cast<uint4*>(slot_base + (size_t)c * blob_bytes), c0, c1);
     }
@@ -166,11 +168,12 @@ cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* lo
 }
 
 cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int32_t* slot_tag,
-                             int uid, int ctas, cudaStream_t st) {
-    if (n_cold > kMaxColdSlots) return cudaErrorInvalidValue;
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, size_t part_lo,
+                             size_t part_hi, int32_t* slot_tag, int uid, int ctas, cudaStream_t st) {
+    if (n_cold > kMaxColdSlots || part_lo % 16 || part_hi % 16 || part_lo > part_hi || part_hi > blob_bytes)
+        return cudaErrorInvalidValue;
     cold_copy_kernel<<<ctas, kGatherThreads, 0, st>>>(ids, n_picks, loc, E, n_hot, n_cold, cold_src, slot_base,
-                                                      blob_bytes, slot_tag, uid);
+                                                      blob_bytes, part_lo, part_hi, slot_tag, uid);
     return cudaGetLastError();
 }
 

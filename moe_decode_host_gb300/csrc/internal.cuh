@@ -83,9 +83,11 @@ cudaError_t launch_cold_remap(const int32_t* ids, int n_picks, const int32_t* lo
                               int32_t* phys, int32_t* cold_list, int32_t* n_picked, int* status, cudaStream_t st);
 // Byte copy of the picked cold slots (derives the slot list from the picks itself);
 // marks each copied slot's tag with uid.
+// Copies bytes [part_lo, part_hi) (multiples of 16) of every picked cold expert's
+// host blob into its scratch slot.
 cudaError_t launch_cold_copy(const int32_t* ids, int n_picks, const int32_t* loc, int E, int n_hot, int n_cold,
-                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, int32_t* slot_tag,
-                             int uid, int ctas, cudaStream_t st);
+                             const uint8_t* const* cold_src, uint8_t* slot_base, size_t blob_bytes, size_t part_lo,
+                             size_t part_hi, int32_t* slot_tag, int uid, int ctas, cudaStream_t st);
 
 cudaError_t launch_link_probe(const uint8_t* src, uint8_t* dst, size_t bytes, int ctas, cudaStream_t st);
 

@@ -129,3 +129,28 @@ def test_repetition_split_and_spread():
     r = bench.repetition_spread(b, [2.0, 2.0, 4.0, 1.0, 2.0], 4)  # 2 steps x 4 tokens each
     assert r["tokens_per_s"] == [4000.0, 4000.0, 2000.0, 8000.0, 4000.0]
     assert (r["median"], r["min"], r["max"], r["n"]) == (4000.0, 2000.0, 8000.0, 5)
+
+
+def test_step_launches_follow_the_library_paths():
+    """The launch count the bench claims per layer-step: route, remap and the two
+    copy launches, the FFN's prep and phases on the kernels the library picks, the
+    combine."""
+    import bench
+
+    c1 = dict(T=1, n_cold=129)             # GEMV: prep, (gate/up + h prescale + down) x 2 classes
+    assert bench.ffn_terms(c1) == 0
+    assert bench.step_launches(c1) == 1 + 3 + (1 + 2 * 3) + 1
+    c2 = dict(T=32, n_cold=129)            # block-scaled 4-term: prep, 2 phases x 2 classes
+    assert bench.ffn_terms(c2) == 4
+    assert bench.step_launches(c2) == 1 + 3 + 5 + 1
+    assert bench.ffn_terms(dict(T=32, n_cold=129, decode_kind=1)) == 0
+    assert bench.ffn_terms(dict(T=32, n_cold=129, zero_copy=True)) == 0
+    zc = dict(T=1, n_cold=129, zero_copy=True)  # no copy launches
+    assert bench.step_launches(zc) == 1 + 1 + (1 + 2 * 3) + 1
+    c4 = dict(T=8192, n_cold=0, prefill="fp4")  # route in two kernels, no copy, one class
+    assert bench.ffn_terms(c4) == 1
+    assert bench.step_launches(c4) == 2 + 1 + 3 + 1
+    c4f = dict(T=8192, n_cold=0, prefill="f16")  # three decode ranges + tcgen05 per phase
+    assert bench.step_launches(c4f) == 2 + 1 + (1 + 1 * (2 * 4 + 1)) + 1
+    assert bench.decode_arithmetic(c2).startswith("block-scaled")
+    assert bench.decode_arithmetic(c1).startswith("dequant")
