@@ -33,7 +33,7 @@ HBM_NOMINAL_GBS = 8000.0
 # ncu captures of a smaller layer of the same expert shape (traffic scales with the
 # experts processed).  None once the kernel has changed since its capture.
 NCU_TRAFFIC = {
-    "cold_copy": (11520 + 15616) / 2,                       # per cold expert copied
+    "cold_copy": (11776 + 11776) / 1,                       # per cold expert copied (both launches)
     "ffn_decode": (66936832 + 754944 + 33493504) / 5,      # dequant-GEMV, per distinct expert, both phases
     "ffn_mx_decode": (537065728 + 3808000 + 268754176 + 4258048) / 40,  # 4-term block-scaled, per distinct expert
     "ffn_mx": (904207616 + 6353152 + 482149888 + 79283712) / 64,       # all-FP4 prefill, per expert at ~128 tokens
