@@ -160,15 +160,32 @@ __device__ __forceinline__ uint32_t mx_idesc(int N, uint32_t sf) {
            ((uint32_t)(kMxBM >> 4) << 24) | (sf << 29);
 }
 
+// One block-scaled MMA, issued by one elected lane of a converged warp.  Issued this
+// way, from straight-line code, a thread issues one every ~40 cycles and the
+// commits cost nothing; a lone lane in a loop with run-time bounds took ~165 cycles
+// per MMA (measured on this GPU).
 __device__ __forceinline__ void mx_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d),
         "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
         : "memory");
+}
+
+// The MMAs of one matrix for one stage: NKK steps of K = 64 (4 for a full stage of
+// 256, 2 for a tail of 128).  A step of 64 elements advances both start addresses
+// by 32 bytes; its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2.
+template <int NKK>
+__device__ __forceinline__ void mx_stage_mmas(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id0, uint32_t id2,
+                                              uint32_t sfa, uint32_t sfb, bool first) {
+#pragma unroll
+    for (int kk = 0; kk < NKK; ++kk)
+        mx_mma(d, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id2 : id0, sfa + 4u * (uint32_t)(kk >> 1),
+               sfb + 8u * (uint32_t)(kk >> 1), (first && kk == 0) ? 0u : 1u);
 }
 
 __device__ __forceinline__ void mx_st8(uint32_t taddr, const uint32_t (&v)[8]) {
@@ -435,66 +452,58 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         }
         __syncwarp();
     } else if (warp == 2 || (ISS == 2 && warp == kMxUpIssuer)) {
-        // ---------------- MMA issuers (lane 0) ----------------
-        // a thread takes about 100 cycles to issue one block-scaled MMA, so the gate/up
-        // phase issues from two threads, warp 2 the gate matrix's MMAs into the gate
-        // accumulator and warp 24 the up matrix's into the up accumulator; the down
-        // phase has one matrix and one issuer
-        const int mt0 = warp == 2 ? 0 : 1;
-        const int mt1 = ISS == 2 ? mt0 + 1 : MATS;  // matrices [mt0, mt1) of each stage
-        if (lane == 0) {
-            int as = 0, bs = 0, buf = 0;
-            unsigned aph = 0, bph = 0, accph = 0;
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                MxTask t;
-                const int task = mx_take(hd, k, a, abort, 2 + mt0, t);
-                if (task < 0) break;
-                if (!t.valid) continue;
-                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
-                    const int N = mx_ncols(TERMS * min(TPP, t.cnt - tb));
-                    const uint32_t id0 = mx_idesc(N, 0u), id2 = mx_idesc(N, 2u);
-                    if (!mbar_wait_fast(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, abort, a.status, a.diag, 34,
-                                        buf, 0, task)) {
+        // ---------------- MMA issuers ----------------
+        // the gate/up phase issues from two warps, warp 2 the gate matrix's MMAs into
+        // the gate accumulator and warp 24 the up matrix's into the up accumulator; the
+        // down phase has one matrix and one issuer.  Each issuing warp runs its loop
+        // converged and one elected lane issues.
+        const int mt = warp == 2 ? 0 : 1;
+        int as = 0, bs = 0, buf = 0;
+        unsigned aph = 0, bph = 0, accph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            MxTask t;
+            const int task = mx_warp_take(hd, k, a, abort, 2 + mt, t);
+            if (task < 0) break;
+            if (!t.valid) continue;
+            for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                const int N = mx_ncols(TERMS * min(TPP, t.cnt - tb));
+                const uint32_t id0 = mx_idesc(N, 0u), id2 = mx_idesc(N, 2u);
+                if (!warp_wait(&hd.acc_empty[buf], ((accph >> buf) & 1u) ^ 1u, a, abort, 34, buf, 0, task)) {
+                    ok = false;
+                    break;
+                }
+                accph ^= 1u << buf;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * ACC;
+                for (int s = 0; s < nks; ++s) {
+                    // the scale writers arrive only after both of the stage's loads landed
+                    if (!warp_wait(&hd.sf_full[bs], bph, a, abort, 37, bs, s, task)) {
                         ok = false;
                         break;
                     }
-                    accph ^= 1u << buf;
                     tc_fence_after();
-                    for (int s = 0; s < nks; ++s) {
-                        // the scale writers arrive only after both of the stage's loads landed
-                        if (!mbar_wait_fast(&hd.sf_full[bs], bph, abort, a.status, a.diag, 37, bs, s, task)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const int nkk = min(4, (K - s * kMxBK) / 64);  // K steps of 64 in this stage
-                        const uint32_t sf = tmem + SF0 + (uint32_t)bs * mx_sf_cols<P>();
-                        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * BSTAGE));  // its rows
-                        for (int mt = mt0; mt < mt1; ++mt) {
-                            const uint32_t d = tmem + (uint32_t)(P == 0 ? mt : buf) * ACC;
-                            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxASlot));
-                            for (int kk = 0; kk < nkk; ++kk) {
-                                // a K step of 64 elements advances both start addresses by 32 bytes;
-                                // its two blocks are bytes 2 (kk % 2) .. +1 of the stage's word kk / 2
-                                const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                                mx_mma(d, ad + 2 * kk, bd + 2 * kk, (kk & 1) ? id2 : id0,
-                                       sf + 8u * mt + 4u * (uint32_t)(kk >> 1),
-                                       sf + mx_sfb_col<P>() + 8u * (uint32_t)(kk >> 1), acc);
-                            }
-                        }
-                        tc_commit(&hd.a_empty[as]);
-                        tc_commit(&hd.b_empty[bs]);
-                        advance(as, aph, NA);
-                        advance(bs, bph, NB);
-                    }
-                    if (!ok) break;
-                    tc_commit(&hd.acc_full[buf]);
-                    if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 2 ACC)
+                    const uint32_t sf = tmem + SF0 + (uint32_t)bs * mx_sf_cols<P>();
+                    const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)bs * BSTAGE));  // its rows
+                    const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)(as * MATS + mt) * kMxASlot));
+                    const uint32_t sfa = sf + 8u * mt, sfb = sf + mx_sfb_col<P>();
+                    if (K - s * kMxBK >= kMxBK)
+                        mx_stage_mmas<4>(d, ad, bd, id0, id2, sfa, sfb, s == 0);
+                    else  // a K tail of 128 elements (K a multiple of 128)
+                        mx_stage_mmas<2>(d, ad, bd, id0, id2, sfa, sfb, s == 0);
+                    tc_commit_elect(&hd.a_empty[as]);
+                    tc_commit_elect(&hd.b_empty[bs]);
+                    advance(as, aph, NA);
+                    advance(bs, bph, NB);
                 }
+                if (!ok) break;
+                tc_commit_elect(&hd.acc_full[buf]);
+                if (P == 1) buf ^= 1;  // the gate/up phase's two accumulators fill [0, 2 ACC)
             }
-            // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
-            // last commit of every slot
+        }
+        // no MMA may be in flight when tensor memory is freed: wait (bounded) for the
+        // last commit of every slot
+        if (lane == 0) {
             for (int s = 0; s < NA; ++s) mbar_drain(&hd.a_empty[s], (s < as) ? aph : (aph ^ 1u));
             for (int s = 0; s < NB; ++s) mbar_drain(&hd.b_empty[s], (s < bs) ? bph : (bph ^ 1u));
         }
