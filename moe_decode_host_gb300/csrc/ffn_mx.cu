@@ -215,16 +215,6 @@ __device__ __forceinline__ MxTask mx_task(const FfnArgs& a, const MxHead& hd, in
     return t;
 }
 
-__device__ __forceinline__ int mx_take(MxHead& hd, int k, const FfnArgs& a, volatile int* abort, int who, MxTask& t) {
-    const int j = k % kMxTaskQ;
-    if (!mbar_wait_fast(&hd.tq_full[j], (unsigned)(k / kMxTaskQ) & 1u, abort, a.status, a.diag, 30, j, k, who))
-        return -1;
-    const int task = *reinterpret_cast<volatile int*>(&hd.tq[j]);
-    t = hd.tqt[j];
-    mbar_arrive(&hd.tq_empty[j]);
-    return task;
-}
-
 __device__ __forceinline__ int mx_warp_take(MxHead& hd, int k, const FfnArgs& a, volatile int* abort, int who,
                                             MxTask& t) {
     const int j = k % kMxTaskQ;
@@ -369,87 +359,91 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         }
         __syncwarp();
     } else if (warp == 0) {
-        // ---------------- weight producer (lane 0) ----------------
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();  // each weight byte is read once
-            int as = 0;
-            unsigned aph = 0;
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                MxTask t;
-                const int task = mx_take(hd, k, a, abort, 0, t);
-                if (task < 0) break;
-                if (!t.valid) continue;
-                // the decode kernel's views of the two planes: 128-byte boxes of 32 (w13)
-                // or 64 (w2) rows with the 128-byte swizzle, stacked to 128 rows
-                const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13n : &a.tmaps[t.phys].w2n;
-                const CUtensorMap* smap = P == 0 ? &a.tmaps[t.phys].w13s : &a.tmaps[t.phys].w2s;
-                constexpr int box_rows = P == 0 ? 32 : 64;
-                asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
-                if (wsc_tma) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(smap) : "memory");
-                const int r0 = t.rb * kMxBM;
-                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
-                    for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.a_empty[as], aph ^ 1u, abort, a.status, a.diag, 32, as, s, task)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&hd.a_full[as], (unsigned)(MATS * (wsc_tma ? kMxASlot : kMxTile)));
-#pragma unroll
-                        for (int mt = 0; mt < MATS; ++mt) {
-                            uint8_t* dst = sA + (size_t)(as * MATS + mt) * kMxASlot;
-#pragma unroll
-                            for (int i = 0; i < kMxBM / box_rows; ++i)
-                                tma_load_2d_hint(dst + i * box_rows * kMxRowB, map, s * kMxRowB,
-                                                 (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as], pol);
-                            // the 16 scale bytes of each row that hold this stage's 8 blocks
-                            if (wsc_tma)
-#pragma unroll
-                                for (int i = 0; i < kMxBM / 32; ++i)
-                                    tma_load_2d_hint(dst + kMxTile + i * 32 * 16, smap, 16 * (s >> 1),
-                                                     (mt ? I : 0) + r0 + 32 * i, &hd.a_full[as], pol);
-                        }
-                        advance(as, aph, NA);
+        // ---------------- weight producer ----------------
+        // the warp runs converged; one elected lane issues the barrier and TMA operations
+        const uint64_t pol = l2_policy_evict_first();  // each weight byte is read once
+        int as = 0;
+        unsigned aph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            MxTask t;
+            const int task = mx_warp_take(hd, k, a, abort, 0, t);
+            if (task < 0) break;
+            if (!t.valid) continue;
+            // the decode kernel's views of the two planes: 128-byte boxes of 32 (w13)
+            // or 64 (w2) rows with the 128-byte swizzle, stacked to 128 rows
+            const CUtensorMap* map = P == 0 ? &a.tmaps[t.phys].w13n : &a.tmaps[t.phys].w2n;
+            const CUtensorMap* smap = P == 0 ? &a.tmaps[t.phys].w13s : &a.tmaps[t.phys].w2s;
+            constexpr int box_rows = P == 0 ? 32 : 64;
+            asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+            if (wsc_tma) asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(smap) : "memory");
+            const int r0 = t.rb * kMxBM;
+            for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                for (int s = 0; s < nks; ++s) {
+                    if (!warp_wait(&hd.a_empty[as], aph ^ 1u, a, abort, 32, as, s, task)) {
+                        ok = false;
+                        break;
                     }
+                    mbar_arrive_expect_tx_elect(&hd.a_full[as], (unsigned)(MATS * (wsc_tma ? kMxASlot : kMxTile)));
+#pragma unroll
+                    for (int mt = 0; mt < MATS; ++mt) {
+                        uint8_t* dst = sA + (size_t)(as * MATS + mt) * kMxASlot;
+#pragma unroll
+                        for (int i = 0; i < kMxBM / box_rows; ++i)
+                            tma_load_2d_hint_elect(dst + i * box_rows * kMxRowB, map, s * kMxRowB,
+                                                   (mt ? I : 0) + r0 + i * box_rows, &hd.a_full[as], pol);
+                        // the 16 scale bytes of each row that hold this stage's 8 blocks
+                        if (wsc_tma)
+#pragma unroll
+                            for (int i = 0; i < kMxBM / 32; ++i)
+                                tma_load_2d_hint_elect(dst + kMxTile + i * 32 * 16, smap, 16 * (s >> 1),
+                                                       (mt ? I : 0) + r0 + 32 * i, &hd.a_full[as], pol);
+                    }
+                    advance(as, aph, NA);
                 }
             }
-            for (int s = 0; s < NA; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
         }
+        if (lane == 0)
+            for (int s = 0; s < NA; ++s) mbar_drain(&hd.a_full[s], (s < as) ? aph : (aph ^ 1u));
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- activation producer (lane 0) ----------------
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_last();  // read once per row tile of the expert
-            int bs = 0;
-            unsigned bph = 0;
-            bool ok = true;
-            for (int k = 0; ok; ++k) {
-                MxTask t;
-                const int task = mx_take(hd, k, a, abort, 1, t);
-                if (task < 0) break;
-                if (!t.valid) continue;
-                for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
-                    const int row0 = TERMS * (t.off + tb);  // first activation row of the pass
-                    const int boxes = (mx_ncols(TERMS * min(TPP, t.cnt - tb)) + kMxBox - 1) / kMxBox;
-                    for (int s = 0; s < nks; ++s) {
-                        if (!mbar_wait_fast(&hd.b_empty[bs], bph ^ 1u, abort, a.status, a.diag, 33, bs, s, task)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&hd.b_full[bs], (unsigned)(boxes * kMxBox * kMxRowB + 2 * kMxSfbBox * 4));
-                        uint8_t* dst = sB + (size_t)bs * BSTAGE;
-                        for (int bx = 0; bx < boxes; ++bx)
-                            tma_load_2d_hint(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB, row0 + kMxBox * bx,
-                                             &hd.b_full[bs], pol);
-                        // the stage's two scale words of the pass's tokens, from the 4-aligned
-                        // bucket row at or below the first (x is a whole 16 bytes)
-                        tma_load_2d_hint(dst + BTILE, &sfb_map, row0 & ~3, 2 * s, &hd.b_full[bs], pol);
-                        advance(bs, bph, NB);
+        // ---------------- activation producer ----------------
+        // the warp runs converged; one elected lane issues the barrier and TMA operations
+        const uint64_t pol = l2_policy_evict_last();  // read once per row tile of the expert
+        constexpr int kMaxBoxes = (mx_nmax<TERMS>() + kMxBox - 1) / kMxBox;
+        int bs = 0;
+        unsigned bph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            MxTask t;
+            const int task = mx_warp_take(hd, k, a, abort, 1, t);
+            if (task < 0) break;
+            if (!t.valid) continue;
+            for (int tb = 0; tb < t.cnt && ok; tb += TPP) {
+                const int row0 = TERMS * (t.off + tb);  // first activation row of the pass
+                const int boxes = (mx_ncols(TERMS * min(TPP, t.cnt - tb)) + kMxBox - 1) / kMxBox;
+                for (int s = 0; s < nks; ++s) {
+                    if (!warp_wait(&hd.b_empty[bs], bph ^ 1u, a, abort, 33, bs, s, task)) {
+                        ok = false;
+                        break;
                     }
+                    mbar_arrive_expect_tx_elect(&hd.b_full[bs],
+                                                (unsigned)(boxes * kMxBox * kMxRowB + 2 * kMxSfbBox * 4));
+                    uint8_t* dst = sB + (size_t)bs * BSTAGE;
+#pragma unroll
+                    for (int bx = 0; bx < kMaxBoxes; ++bx)
+                        if (bx < boxes)
+                            tma_load_2d_hint_elect(dst + bx * kMxBox * kMxRowB, &act_map, s * kMxRowB,
+                                                   row0 + kMxBox * bx, &hd.b_full[bs], pol);
+                    // the stage's two scale words of the pass's tokens, from the 4-aligned
+                    // bucket row at or below the first (x is a whole 16 bytes)
+                    tma_load_2d_hint_elect(dst + BTILE, &sfb_map, row0 & ~3, 2 * s, &hd.b_full[bs], pol);
+                    advance(bs, bph, NB);
                 }
             }
-            for (int s = 0; s < NB; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         }
+        if (lane == 0)
+            for (int s = 0; s < NB; ++s) mbar_drain(&hd.b_full[s], (s < bs) ? bph : (bph ^ 1u));
         __syncwarp();
     } else if (warp == 2 || (ISS == 2 && warp == kMxUpIssuer)) {
         // ---------------- MMA issuers ----------------

@@ -114,6 +114,26 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// The same for a converged warp: one elected lane issues.
+__device__ __forceinline__ void tma_load_2d_hint_elect(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                       uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// mbarrier.arrive.expect_tx by one elected lane of a converged warp.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, unsigned bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
 // L2 policies: data read once (streamed weights) goes first when L2 needs room;
 // data read many times (activations) stays.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
