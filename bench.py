@@ -180,7 +180,7 @@ def parse():
                          "FP4 with x and h in MXFP4 (default for the 8192-token config)")
     ap.add_argument("--decode-kind", type=int, default=0, choices=[0, 1, 2],
                     help="arithmetic of calls of at most 64 tokens: 1 the dequant-GEMV kernel, 2 block-scaled "
-                         "tensor cores with 4-term MXFP4 activations, 0 (default) kind 1 at 1-2 tokens, else 2")
+                         "tensor cores with 4-term MXFP4 activations, 0 (default) the library's choice (2)")
     ap.add_argument("--zero-copy", action="store_true",
                     help="the FFN reads picked cold experts in place from host memory (no slot copy)")
     return ap.parse_args()
@@ -615,7 +615,7 @@ def ffn_terms(c):
     if T > 64:
         return 1 if c.get("prefill") == "fp4" else 0
     kind = c.get("decode_kind", 0)
-    if kind == 1 or (c.get("zero_copy") and c.get("n_cold", 0) > 0) or (kind == 0 and T < 3):
+    if kind == 1 or (c.get("zero_copy") and c.get("n_cold", 0) > 0):
         return 0
     return 4
 

@@ -242,9 +242,8 @@ int moe_layer_set_prefill_kind(moe_layer* L, int kind);
  *         MXFP4 and each further one the remainder of those before, with block
  *         exponents chosen so that no element saturates (each remainder is exact in
  *         fp32), so the result is the unquantised layer's to about 2e-4 relative.
- *  kind 0 (default): kind 1 for calls of 1 or 2 tokens, kind 2 from 3 tokens up
- *         (on a GB300 the block-scaled kernels are the faster from 4 tokens of
- *         H = 4096, I = 3072, k = 6 up, the GEMV at 1 and 2).
+ *  kind 0 (default): kind 2 (on a GB300 the block-scaled kernels are the faster at
+ *         every decode size of H = 4096, I = 3072, k = 6, from one token up).
  * Layers that read cold experts in place (moe_params.zero_copy) run kind 1 for
  * calls with cold experts.  Errors: MOE_ERR_INVALID_ARG (null, kind not 0, 1 or 2). */
 int moe_layer_set_decode_kind(moe_layer* L, int kind);

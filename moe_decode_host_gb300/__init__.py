@@ -117,8 +117,8 @@ class Layer:
 
     def set_decode_kind(self, kind: int):
         """Arithmetic of calls of at most 64 tokens: 1 the dequant-GEMV kernel; 2
-        block-scaled tensor cores with 4-term MXFP4 activations; 0 (default) kind 1
-        for 1 or 2 tokens, kind 2 from 3 up."""
+        block-scaled tensor cores with 4-term MXFP4 activations; 0 (default) the
+        library's choice (kind 2)."""
         check(lib.moe_layer_set_decode_kind(self.handle, kind), "moe_layer_set_decode_kind")
 
     def set_residency_defer(self, defer: bool):

@@ -475,14 +475,12 @@ namespace {
 // block-scaled kernels when the layer asks for them (1 activation term), else the
 // dequant-GEMV kernel for buckets of at most 64 tokens and the f16 tensor-core kernel
 // above.  Decode-sized calls: the block-scaled kernels with activations as sums of
-// four MXFP4 terms from kBlockScaledMinTokens tokens up (or always, kind 2), the
-// dequant-GEMV kernel below that (or always, kind 1) and whenever the layer reads cold
+// four MXFP4 terms (kinds 0 and 2; measured faster than the dequant-GEMV kernel from
+// one token up), the dequant-GEMV kernel for kind 1 and whenever the layer reads cold
 // experts in place (zero copy), which only that kernel does.
-constexpr int kBlockScaledMinTokens = 3;
 int mx_terms(const moe_layer* L, int T) {
     if (T > kTcMinTokens) return L->prefill_kind == 1 ? 1 : 0;
     if (L->decode_kind == 1 || (L->p.zero_copy && L->p.n_cold > 0)) return 0;
-    if (L->decode_kind == 0 && T < kBlockScaledMinTokens) return 0;
     return 4;
 }
 

@@ -137,15 +137,16 @@ def test_step_launches_follow_the_library_paths():
     combine."""
     import bench
 
-    c1 = dict(T=1, n_cold=129)             # GEMV: prep, (gate/up + h prescale + down) x 2 classes
+    c1 = dict(T=1, n_cold=129, decode_kind=1)  # GEMV: prep, (gate/up + h prescale + down) x 2 classes
     assert bench.ffn_terms(c1) == 0
     assert bench.step_launches(c1) == 1 + 3 + (1 + 2 * 3) + 1
+    assert bench.ffn_terms(dict(T=1, n_cold=129)) == 4  # the default at one token
     c2 = dict(T=32, n_cold=129)            # block-scaled 4-term: prep, 2 phases x 2 classes
     assert bench.ffn_terms(c2) == 4
     assert bench.step_launches(c2) == 1 + 3 + 5 + 1
     assert bench.ffn_terms(dict(T=32, n_cold=129, decode_kind=1)) == 0
     assert bench.ffn_terms(dict(T=32, n_cold=129, zero_copy=True)) == 0
-    zc = dict(T=1, n_cold=129, zero_copy=True)  # no copy launches
+    zc = dict(T=1, n_cold=129, zero_copy=True)  # GEMV, no copy launches
     assert bench.step_launches(zc) == 1 + 1 + (1 + 2 * 3) + 1
     c4 = dict(T=8192, n_cold=0, prefill="fp4")  # route in two kernels, no copy, one class
     assert bench.ffn_terms(c4) == 1

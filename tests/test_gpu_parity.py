@@ -315,13 +315,13 @@ def test_layer_c0(out_fp32):
     (128, 128, 8, 5, 8, 3, "uniform"),      # k == E, a single 128-group per row
     (512, 256, 64, 48, 6, 40, "zipf1.5"),   # buckets above 8, 16, 32 and 48 tokens (two column passes)
     (256, 512, 16, 0, 2, 17, "uniform"),    # everything cold
-    (256, 512, 16, 8, 4, 1, "uniform"),     # one token (default: dequant-GEMV)
+    (256, 512, 16, 8, 4, 1, "uniform"),     # one token
     (384, 640, 40, 30, 5, 2, "uniform"),    # two tokens
 ])
 def test_layer_ragged_shapes(H, I, E, n_hot, k, T, dist, decode_kind):
     """Decode-sized calls on both decode kernels: the dequant-GEMV kernel (kind 1),
     block-scaled tensor cores with four-term activations (kind 2) and the default
-    choice between them by call size (kind 0)."""
+    (kind 0)."""
     n_cold = E - n_hot
     loc = np.random.default_rng(E).permutation(E).astype(np.int32)
     fx = LayerFixture(H=H, I=I, E=E, n_hot=n_hot, n_cold=n_cold, k=k, seed=E + T, loc=loc)
