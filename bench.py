@@ -34,9 +34,9 @@ HBM_NOMINAL_GBS = 8000.0
 # experts processed).  None once the kernel has changed since its capture.
 NCU_TRAFFIC = {
     "cold_copy": (11776 + 11776) / 1,                       # per cold expert copied (both launches)
-    "ffn_decode": (66936832 + 754944 + 33493504) / 5,      # dequant-GEMV, per distinct expert, both phases
-    "ffn_mx_decode": (537065728 + 3808000 + 268754176 + 4258048) / 40,  # 4-term block-scaled, per distinct expert
-    "ffn_mx": (904207616 + 6353152 + 482149888 + 79283712) / 64,       # all-FP4 prefill, per expert at ~128 tokens
+    "ffn_decode": (66932992 + 728576 + 33495040) / 5,      # dequant-GEMV, per distinct expert, both phases
+    "ffn_mx_decode": (536729344 + 3894528 + 268741632 + 4389120) / 40,  # 4-term block-scaled, per distinct expert
+    "ffn_mx": (895477248 + 5763840 + 473281536 + 80008960) / 64,       # all-FP4 prefill, per expert at ~128 tokens
     "ffn_tc": (934021120 + 93158656 + 482610432 + 114407680) / 64,     # f16 prefill, per expert at ~128 tokens
 }
 
