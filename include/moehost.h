@@ -425,6 +425,13 @@ int moe_debug_wait_timeout(int* status_dev, int32_t* diag_dev, void* stream);
  * as uint32 [256] to out_dev (device). */
 int moe_debug_e2m1_pairs(uint32_t* out_dev, void* stream);
 
+/* Test hook: both E2M1 roundings of n fp32 values |v| < 8 (already divided by their
+ * block scale).  out_dev uint32 [2n]: out[2i] from the hardware pair conversion the
+ * block-scaled kernels use (round to nearest, ties to the even code, saturating at
+ * 6), out[2i + 1] from the comparison rule of the stand-alone quantiser; both with
+ * the sign in bit 3.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA. */
+int moe_debug_e2m1_round(const float* v_dev, int n, uint32_t* out_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,7 @@ from ._lib import (LIB_PATH, MOE_ERR_BAD_EXPERT, MOE_ERR_CUDA, MOE_ERR_INJECTED,
                    MOE_NOALLOC_SCRATCH_BYTES, MOE_OK, MoeError, check, lib, moe_params, ptr, stream_handle)
 
 __all__ = ["LIB_PATH", "MoeError", "Scratch", "Layer", "StepBuffers", "expert_bytes", "moe_route", "cold_gather",
-           "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "run_step",
+           "moe_grouped_ffn", "moe_combine", "residency_update", "moe_gather_join", "link_probe", "debug_e2m1_pairs", "debug_e2m1_round", "run_step",
            "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_CUDA", "MOE_ERR_NONFINITE", "MOE_ERR_BAD_EXPERT",
            "MOE_ERR_TIMEOUT", "MOE_ERR_NOMEM", "MOE_ERR_INJECTED", "MOE_ERR_SCRATCH_TOO_SMALL",
            "moe_grouped_ffn_noalloc", "residency_plan", "quant_mxfp4", "mxf4_peak_probe"]
@@ -224,6 +224,12 @@ def mxf4_peak_probe(iters, status_dev, ctas=0, stream=None):
 
 def debug_e2m1_pairs(out_dev, stream=None):
     check(lib.moe_debug_e2m1_pairs(ptr(out_dev), stream_handle(stream)), "moe_debug_e2m1_pairs")
+
+
+def debug_e2m1_round(v_dev, out_dev, stream=None):
+    """Both E2M1 roundings of every value of fp32 tensor v_dev into uint32 out_dev [2n]."""
+    check(lib.moe_debug_e2m1_round(ptr(v_dev), int(v_dev.numel()), ptr(out_dev), stream_handle(stream)),
+          "moe_debug_e2m1_round")
 
 
 class StepBuffers:

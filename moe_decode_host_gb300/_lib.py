@@ -76,6 +76,7 @@ _SIGS = {
     "moe_layer_profile_read_ffn": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "moe_link_probe": (_I, [_P, _P, _Z, _I, _P]),
     "moe_debug_e2m1_pairs": (_I, [_P, _P]),
+    "moe_debug_e2m1_round": (_I, [_P, _I, _P, _P]),
     "moe_debug_wait_timeout": (_I, [_P, _P, _P]),
 }
 

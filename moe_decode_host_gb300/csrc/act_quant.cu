@@ -35,7 +35,25 @@ __global__ void __launch_bounds__(kQuantThreads) quant_mxfp4_kernel(const uint16
     if (lane == 0) scale[blk] = (uint8_t)(e + 127);
 }
 
+// Both E2M1 roundings of each value: out[2i] from the hardware pair conversion the
+// block-scaled kernels use, out[2i + 1] from the comparison rule (sign in bit 3).
+__global__ void e2m1_round_kernel(const float* __restrict__ v, int n, uint32_t* __restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float x = v[i];
+    const uint32_t bits = __float_as_uint(x);
+    out[2 * i] = moe::e2m1_pair(x, 0.0f) & 0xFu;
+    out[2 * i + 1] = moe::e2m1_code(__uint_as_float(bits & 0x7fffffffu)) | ((bits >> 31) << 3);
+}
+
 }  // namespace
+
+extern "C" int moe_debug_e2m1_round(const float* v_dev, int n, uint32_t* out_dev, void* stream) {
+    if (n < 0 || (n > 0 && (!v_dev || !out_dev))) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    e2m1_round_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(v_dev, n, out_dev);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 extern "C" int moe_quant_mxfp4(const void* x_bf16, int rows, int K, uint8_t* nib, uint8_t* scales, void* stream) {
     if (rows < 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;

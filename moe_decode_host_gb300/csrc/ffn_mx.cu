@@ -74,7 +74,12 @@ constexpr int kMxEpiWarps = 16;  // four per lane quarter, taking every fourth 1
 constexpr int kMxMaxE = 1024;
 constexpr int kMxTaskQ = 4;
 constexpr uint32_t kMxTmemCols = 512;
-constexpr int kMxEpiStage = 16 * 16;      // epilogue staging per warp: 16 tokens x 16 bytes of h
+// epilogue staging per warp in the gate/up phase: with four terms, 16 activation rows
+// x 16 bytes of h codes; with one term, an 8-column slice of h transposed (32 rows x
+// 8 columns of fp32, rows padded to 33 words so that both the row-wise writes and the
+// column-wise reads are free of bank conflicts)
+template <int P, int TERMS>
+__host__ __device__ constexpr int mx_epi_stage() { return P == 1 ? 0 : (TERMS == 1 ? 8 * 33 * 4 : 16 * 16); }
 
 template <int P>
 __host__ __device__ constexpr int mx_mats() { return P == 0 ? 2 : 1; }  // weight matrices per stage
@@ -146,7 +151,7 @@ template <int P, int TERMS>
 struct MxSmem {
     static constexpr size_t kB = (size_t)mx_astages<P, TERMS>() * mx_mats<P>() * kMxASlot;  // after the weight ring
     static constexpr size_t kStg = kB + (size_t)mx_bstages<P, TERMS>() * mx_bstage<TERMS>();
-    static constexpr size_t kHead = kStg + kMxEpiWarps * kMxEpiStage;
+    static constexpr size_t kHead = kStg + (size_t)kMxEpiWarps * mx_epi_stage<P, TERMS>();
     static constexpr size_t kTotal = 1024 + kHead + sizeof(MxHead);
 };
 static_assert(MxSmem<0, 1>::kTotal <= 232448 && MxSmem<1, 1>::kTotal <= 232448 && MxSmem<0, 4>::kTotal <= 232448 &&
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
         const int q = warp & 3;  // tensor-memory lane quarter: weight rows 32 q ..
         const int half = (warp - kMxFirstEpi) >> 2;  // this warp's 16-token chunks: 4 i + half
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        uint8_t* stg = base + MxSmem<P, TERMS>::kStg + (size_t)(warp - kMxFirstEpi) * kMxEpiStage;
+        uint8_t* stg = base + MxSmem<P, TERMS>::kStg + (size_t)(warp - kMxFirstEpi) * mx_epi_stage<P, TERMS>();
         int buf = 0;
         unsigned accph = 0;
         bool ok = true;
@@ -623,7 +628,60 @@ __global__ void __launch_bounds__(kMxThreads, 1) ffn_mx_kernel(FfnArgs a, const 
                 const uint32_t d = lane_addr + (uint32_t)buf * ACC;
                 for (int cb = 16 * half; cb < ncol; cb += 64) {
                     constexpr int TOK = 16 / TERMS;  // tokens of a 16-column chunk
-                    if constexpr (P == 0) {
+                    if constexpr (P == 0 && TERMS == 1) {
+                        // one term: h of the 16 columns (this lane's row), then per 8-column
+                        // slice a transpose through shared memory, so that the four lanes
+                        // 4c..4c+3 hold column c's 32-element block, 8 elements each: the
+                        // block maximum takes two shuffles, the hardware conversion rounds
+                        // element pairs, and each lane stores 4 bytes of the column's row
+                        float g[16], u[16];
+                        tc_ld16x2(d + cb, d + ACC + cb, g, u);
+                        float* tile = reinterpret_cast<float*>(stg);
+                        const int col = lane >> 2, part = lane & 3;
+#pragma unroll
+                        for (int h8 = 0; h8 < 2; ++h8) {
+                            __syncwarp();
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float gs = g[8 * h8 + c];
+                                // the fast exponential and division: relative error about 1e-6
+                                // for |g| up to 10, far below the quantisation step of h
+                                tile[c * 33 + lane] = __fdividef(gs, 1.0f + __expf(-gs)) * u[8 * h8 + c];
+                            }
+                            __syncwarp();
+                            float v[8];
+                            uint32_t amax = 0;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                v[i] = tile[col * 33 + part * 8 + i];
+                                amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+                            }
+                            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                            amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                            const int e = mx_block_exp(amax);
+                            uint32_t word = 0;
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const uint32_t b0 = __float_as_uint(v[2 * m]), b1 = __float_as_uint(v[2 * m + 1]);
+                                const float s0 = __uint_as_float(__float_as_uint(mx_scaled(b0 & 0x7fffffffu, e)) |
+                                                                 (b0 & 0x80000000u));
+                                const float s1 = __uint_as_float(__float_as_uint(mx_scaled(b1 & 0x7fffffffu, e)) |
+                                                                 (b1 & 0x80000000u));
+                                word |= e2m1_pair(s0, s1) << (8 * m);
+                            }
+                            const int cc = cb + 8 * h8 + col;  // accumulator column = activation row offset
+                            if (cc < ncol) {
+                                const int row = (t.off + tb) + cc;
+                                *reinterpret_cast<uint32_t*>(a.hq + (size_t)row * (I / 2) + (r0 + 32 * q) / 2 +
+                                                             4 * part) = word;
+                                // block (r0 + 32 q) / 32 is byte q of word r0 / 128
+                                if (part == 0)
+                                    reinterpret_cast<uint8_t*>(a.hs)[((size_t)(r0 / 128) * Rs + row) * 4 + q] =
+                                        (uint8_t)(e + 127);
+                            }
+                        }
+                        __syncwarp();
+                    } else if constexpr (P == 0) {
                         float g[16], u[16];
                         tc_ld16x2(d + cb, d + ACC + cb, g, u);
                         int es[16];

@@ -41,6 +41,19 @@ __device__ __forceinline__ uint32_t e2m1_code(float r) {
            (uint32_t)(r > 2.5f) + (uint32_t)(r >= 3.5f) + (uint32_t)(r > 5.0f);
 }
 
+// E2M1 codes (sign in bit 3) of two values already divided by their block scale
+// (|v| < 8), packed as one byte with `lo` in the low nibble: the hardware
+// conversion rounds to nearest with ties to the even code and saturates at 6, the
+// rule e2m1_code implements with comparisons (a sign on a value that rounds to 0
+// gives code 8).
+__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
 }  // namespace moe
 
 namespace moe {

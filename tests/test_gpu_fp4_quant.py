@@ -66,3 +66,26 @@ def test_quant_mxfp4_arguments():
     assert lib.moe_quant_mxfp4(x.data_ptr(), 2, 48, nib.data_ptr(), sc.data_ptr(), None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_mxfp4(x.data_ptr(), -1, 64, nib.data_ptr(), sc.data_ptr(), None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_mxfp4(None, 2, 64, nib.data_ptr(), sc.data_ptr(), None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_hardware_e2m1_rounding_matches_the_comparison_rule():
+    """The block-scaled kernels round h with the hardware pair conversion; it must
+    take the same code as the comparison rule (the OCP rule: nearest, ties to the
+    even code, saturating at 6) for every value below 8: each tie point and its two
+    float neighbours, a dense grid, tiny and subnormal values, both signs, +-0."""
+    import moe_decode_host_gb300 as m
+
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 7.0, 7.999999], np.float32)
+    near = np.concatenate([np.nextafter(ties, np.float32(0)), ties, np.nextafter(ties, np.float32(8))])
+    dense = np.linspace(0, 7.99, 200001, dtype=np.float32)
+    tiny = np.array([1e-45, 1e-38, 1e-20, 1e-3, 0.2499], np.float32)
+    v = np.concatenate([ties, grid, near, dense, tiny]).astype(np.float32)
+    v = np.concatenate([v, -v, np.array([-0.0], np.float32)])
+    d = torch.from_numpy(v).cuda()
+    out = torch.zeros(2 * v.size, dtype=torch.int32, device="cuda")
+    m.debug_e2m1_round(d, out)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy().reshape(-1, 2)
+    bad = np.nonzero(o[:, 0] != o[:, 1])[0]
+    assert bad.size == 0, [(float(v[i]), int(o[i, 0]), int(o[i, 1])) for i in bad[:10]]
