@@ -36,7 +36,7 @@ NCU_TRAFFIC = {
     "cold_copy": (11776 + 11776) / 1,                       # per cold expert copied (both launches)
     "ffn_decode": (66932992 + 728576 + 33495040) / 5,      # dequant-GEMV, per distinct expert, both phases
     "ffn_mx_decode": (536729344 + 3894528 + 268741632 + 4389120) / 40,  # 4-term block-scaled, per distinct expert
-    "ffn_mx": (895477248 + 5763840 + 473281536 + 80008960) / 64,       # all-FP4 prefill, per expert at ~128 tokens
+    "ffn_mx": (891086080 + 6049792 + 472940544 + 79744768) / 64,       # all-FP4 prefill, per expert at ~128 tokens
     "ffn_tc": (934021120 + 93158656 + 482610432 + 114407680) / 64,     # f16 prefill, per expert at ~128 tokens
 }
 

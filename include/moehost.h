@@ -373,7 +373,7 @@ const char* moe_strerror(int code);
 
 /* Number of CTAs the cold copy kernel runs on (0 = the default, 3/16 of the SMs:
  * enough to keep the host link busy on GB300).  A zero-copy layer's cold FFN chain
- * runs on the same number of CTAs.
+ * runs on the same number of CTAs, or a quarter of the SMs if that is more.
  * The copy shares the GPU with the FFN over HBM-resident experts. */
 int moe_layer_set_copy_ctas(moe_layer* L, int ctas);
 

@@ -574,23 +574,26 @@ int moe_grouped_ffn(moe_layer* L, const void* x, int T, const int32_t* phys_ids,
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     if (terms == 0 && L->p.zero_copy && L->p.n_cold > 0 && T <= kTcMinTokens) {
         // zero copy: the cold experts' chain (gate/up, prescale, down) reads their
-        // weights in place over the host link on the layer's copy stream, with as
-        // many CTAs as the cold copy would use, while the experts in HBM run here;
+        // weights in place over the host link on the layer's copy stream, on at least
+        // a quarter of the SMs (its kernels stream less per CTA than the copy: 28 CTAs
+        // reached 131 GB/s, 38 about 170), while the experts in HBM run on the rest;
         // profiled calls record the cold chain as the layer's copy
+        const int zc_ctas = L->copy_ctas > L->sm_count / 4 ? L->copy_ctas : (L->sm_count / 4 > 0 ? L->sm_count / 4 : 1);
+        const int zc_hot = L->sm_count > zc_ctas ? L->sm_count - zc_ctas : L->sm_count;
         a.cold_host = L->d_cold_src;
         err = cudaEventRecord(L->ev_fork, st);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(L->copy_stream, L->ev_fork, 0);
         const bool prof = L->prof_n < (int)L->prof_ev.size() / 2;
         if (err == cudaSuccess && prof) err = cudaEventRecord(L->prof_ev[2 * L->prof_n], L->copy_stream);
-        if (err == cudaSuccess) err = phase(0, 2, L->copy_ctas, L->copy_stream, true);
-        if (err == cudaSuccess) err = phase(1, 2, L->copy_ctas, L->copy_stream, true);
+        if (err == cudaSuccess) err = phase(0, 2, zc_ctas, L->copy_stream, true);
+        if (err == cudaSuccess) err = phase(1, 2, zc_ctas, L->copy_stream, true);
         if (err == cudaSuccess && prof) {
             err = cudaEventRecord(L->prof_ev[2 * L->prof_n + 1], L->copy_stream);
             ++L->prof_n;
         }
         if (err == cudaSuccess) err = cudaEventRecord(L->ev_join, L->copy_stream);
-        if (err == cudaSuccess) err = phase(0, 1, hot_sms, st, false);
-        if (err == cudaSuccess) err = phase(1, 1, hot_sms, st, false);
+        if (err == cudaSuccess) err = phase(0, 1, zc_hot, st, false);
+        if (err == cudaSuccess) err = phase(1, 1, zc_hot, st, false);
         mark(1);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(st, L->ev_join, 0);
         mark(2);
