@@ -793,12 +793,18 @@ __global__ void __launch_bounds__(128) mx_xprep_kernel(const __nv_bfloat16* __re
             const int e = TERMS == 1 ? mx_block_exp(amax) : mx_term_exp(amax);
             uint32_t o[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                // element j -> byte j / 2, low nibble when j is even
-                const uint32_t bits = __float_as_uint(r[j]);
-                const uint32_t c = e2m1_code(mx_scaled(bits & 0x7fffffffu, e)) | ((bits >> 31) << 3);
-                o[j >> 3] |= c << (4 * (j & 7));
-                if (TERMS > 1) r[j] -= mx_decode(c, e);  // exact: the next term's input
+            for (int j = 0; j < 32; j += 2) {
+                // elements j, j + 1 -> byte j / 2 (j in the low nibble), rounded in pairs
+                // by the hardware conversion (the same codes as e2m1_code, tested)
+                const uint32_t b0 = __float_as_uint(r[j]), b1 = __float_as_uint(r[j + 1]);
+                const float s0 = __uint_as_float(__float_as_uint(mx_scaled(b0 & 0x7fffffffu, e)) | (b0 & 0x80000000u));
+                const float s1 = __uint_as_float(__float_as_uint(mx_scaled(b1 & 0x7fffffffu, e)) | (b1 & 0x80000000u));
+                const uint32_t pair = e2m1_pair(s0, s1);
+                o[j >> 3] |= pair << (4 * (j & 7));
+                if (TERMS > 1) {  // exact: the next term's input
+                    r[j] -= mx_decode(pair & 0xFu, e);
+                    r[j + 1] -= mx_decode(pair >> 4, e);
+                }
             }
             const size_t row = (size_t)TERMS * i + tt;
             *reinterpret_cast<uint4*>(xq + row * (H / 2) + 16 * b) = make_uint4(o[0], o[1], o[2], o[3]);
