@@ -929,7 +929,7 @@ def run_ours(args):
     line = {"metric": "MoE layer tokens/s (decode)", "value": res.pop("value"), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e2m1xe2m1->f32" if (c["T"] > 64 and c["prefill"] == "fp4") else "e2m1xf16->f32",
+            "dtype": "e2m1xe2m1->f32" if ffn_terms(c) > 0 else "e2m1xf16->f32",
             "data": "synthetic", "config": _config_json(c, args, pool_steps)}
     line.update(res)
     default_run = (args.config == "c1" and args.batch is None and args.experts is None and not args.zero_copy
